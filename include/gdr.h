@@ -1,0 +1,161 @@
+/*
+ * gdr.h -- C ABI of the GB300 chunkwise gated delta rule forward library.
+ *
+ * The operation. For each batch row b and value head hv, with the state S a
+ * K x V matrix (rows = key channels) that starts at initial_state[b, hv] (or 0),
+ * every token t applies
+ *     S <- exp(g_t) * S                        (decay: one scalar per token and head,
+ *                                               or one factor per key channel)
+ *     S <- S + beta_t k_t (v_t - S^T k_t)^T    (delta-rule write)
+ *     o_t = S^T (scale * q_t)
+ * where q_t, k_t are L2-normalised first when use_qk_l2norm is set
+ * (x / sqrt(sum x^2 + 1e-6)). Value head hv reads query/key head hv / (HV / H).
+ * This is the recurrence of the "分块并行计算（Chunkwise）" lecture notes
+ * (section "为什么需要分块？") with the gate of Gated DeltaNet / KDA, the L2 norm
+ * and default scale of "DeltaNet chunk kernel optimization" (_l2norm,
+ * 1/sqrt(K)), and the tensor shapes of the notes' shape table (形状流水线).
+ *
+ * The library computes it in the chunk form of the same notes (section
+ * "chunk 内的 cumsum 与下三角解" and the inter-chunk loop): per chunk of C tokens
+ * a gate cumsum, the decayed dots A_kk and A_qk, the unit lower-triangular
+ * system M = I + tril(A_kk * beta, -1) solved for W = M^-1 (exp(G) k) and
+ * U = M^-1 v, then the state recurrence across chunks. A sequence whose length
+ * is not a multiple of C is handled as if zero-padded (q = k = v = g = beta = 0
+ * on the padding, "Pad to chunk boundary" of the optimisation script); padded
+ * rows are never written.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are dense, row-major, contiguous, in the layouts given below.
+ *  - Pointers marked (device) are device pointers on the current CUDA device;
+ *    pointers marked (host) are host pointers (pinned memory gives asynchronous
+ *    copies; pageable memory works but the copies then block the host).
+ *  - Every device or host tensor base must be 16-byte aligned
+ *    (GDR_ERR_ALIGNMENT otherwise).
+ *  - The caller owns every buffer. The library allocates no device memory
+ *    and frees nothing; it keeps no state between calls except the
+ *    per-device cache of kernel attributes.
+ *  - Work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *    stream). Argument errors are reported synchronously and enqueue nothing.
+ *  - Launch failures return GDR_ERR_CUDA. A device-side bounded wait that
+ *    gives up records an error word in the workspace; gdr_stream_status then
+ *    returns GDR_ERR_TIMEOUT.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared here so that this header
+ * needs no CUDA include. */
+typedef struct CUstream_st* gdr_stream_t;
+
+typedef enum {
+  GDR_OK = 0,
+  GDR_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size, HV % H != 0, bad scale */
+  GDR_ERR_UNSUPPORTED = 2,  /* valid but not implemented: head dim, chunk size, dtype combination */
+  GDR_ERR_ALIGNMENT = 3,    /* a tensor base is not 16-byte aligned */
+  GDR_ERR_WORKSPACE = 4,    /* workspace missing or smaller than gdr_chunk_fwd_workspace_size */
+  GDR_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+  GDR_ERR_TIMEOUT = 6       /* a device-side bounded wait gave up (see gdr_stream_status) */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+typedef enum {
+  GDR_GATE_SCALAR = 0,   /* g [B, T, HV]: one log-decay per token and value head (Gated DeltaNet) */
+  GDR_GATE_PER_KEY = 1   /* g [B, T, HV, K]: one log-decay per key channel (KDA) */
+} gdr_gate_mode;
+
+/* Problem sizes. q, k have H heads of K channels; v, o have HV value heads of
+ * V channels (HV a multiple of H); B batch rows of T tokens. */
+typedef struct {
+  int B, T, H, HV, K, V;
+  int in_dtype;   /* gdr_dtype of q, k, v */
+  int out_dtype;  /* gdr_dtype of o */
+} gdr_dims;
+
+/*
+ * gdr_chunk_fwd -- chunkwise gated delta rule forward pass on the GPU.
+ *
+ *   q, k           (device) [B, T, H, K]   in_dtype
+ *   v              (device) [B, T, HV, V]  in_dtype
+ *   g              (device) fp32, [B, T, HV] (GDR_GATE_SCALAR) or [B, T, HV, K] (GDR_GATE_PER_KEY);
+ *                  natural-log decay per token (any sign; |in-chunk cumsum span| must stay
+ *                  below ~80 so that exp() of it is finite in fp32)
+ *   beta           (device) fp32 [B, T, HV]
+ *   initial_state  (device) fp32 [B, HV, K, V], or NULL for a zero state
+ *   chunk_size     C: 16, 32 or 64 (64 is the tensor-core path)
+ *   scale          multiplies q after the optional L2 norm; finite and > 0
+ *                  (the usual choice is 1/sqrt(K))
+ *   use_qk_l2norm  nonzero: L2-normalise q and k per token and head first
+ *   gate_mode      gdr_gate_mode
+ *   out            (device) [B, T, HV, V] out_dtype
+ *   final_state    (device) fp32 [B, HV, K, V], or NULL to skip it; may alias
+ *                  initial_state (each state is read before it is written)
+ *   workspace      (device) scratch of at least gdr_chunk_fwd_workspace_size()
+ *                  bytes, 256-byte aligned; contents on entry do not matter
+ *
+ * Supported: K, V in 1..128 with K + V <= 256 on the general path; bf16 inputs
+ * with K = V = 128 and C = 64 take the tcgen05 tensor-core path.
+ * T == 0 writes final_state = initial_state (or zeros) and nothing else.
+ * Concurrent calls must use distinct workspaces.
+ */
+gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* initial_state, int chunk_size,
+                         float scale, int use_qk_l2norm, int gate_mode, void* out,
+                         float* final_state, const gdr_dims* dims, void* workspace,
+                         size_t workspace_bytes, gdr_stream_t stream);
+
+/* Bytes of device workspace gdr_chunk_fwd needs for these sizes (0 if the
+ * arguments are invalid or unsupported). */
+size_t gdr_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode);
+
+/*
+ * gdr_chunk_fwd_host -- the same forward pass on HOST tensors.
+ *
+ * Copies q, k, v, g, beta and initial_state (host, same layouts and dtypes as
+ * above) into `device_buffer`, runs gdr_chunk_fwd there, and copies o and
+ * final_state back to `out` and `final_state` (host), all enqueued on `stream`.
+ * The call returns once the work is enqueued; synchronise `stream` (or call
+ * gdr_stream_status) before reading the outputs. device_buffer (device) must
+ * hold gdr_chunk_fwd_host_buffer_size() bytes and be 256-byte aligned.
+ */
+gdr_status gdr_chunk_fwd_host(const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, const float* initial_state, int chunk_size,
+                              float scale, int use_qk_l2norm, int gate_mode, void* out,
+                              float* final_state, const gdr_dims* dims, void* device_buffer,
+                              size_t device_buffer_bytes, gdr_stream_t stream);
+
+size_t gdr_chunk_fwd_host_buffer_size(const gdr_dims* dims, int chunk_size, int gate_mode,
+                                      int with_initial_state, int with_final_state);
+
+/*
+ * gdr_stream_status -- synchronise `stream`, then report errors.
+ * Returns GDR_ERR_CUDA if the stream reports an error, GDR_ERR_TIMEOUT if a
+ * kernel that ran with this workspace recorded a bounded-wait timeout (the
+ * word is cleared by the next gdr_chunk_fwd on that workspace), else GDR_OK.
+ * `workspace` may be NULL to check only the stream.
+ */
+gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace);
+
+/* Static, human-readable name of a status code. */
+const char* gdr_status_string(gdr_status s);
+
+/* Which kernel path gdr_chunk_fwd takes for these arguments:
+ * 0 = general fp32 CUDA-core path, 1 = tcgen05 tensor-core path,
+ * -1 = arguments rejected (the status is written to *status if non-NULL). */
+int gdr_chunk_fwd_path(const gdr_dims* dims, int chunk_size, int gate_mode, gdr_status* status);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

@@ -1,0 +1,120 @@
+"""C-ABI tests that need no GPU: the library builds, loads, exports every
+function include/gdr.h declares, and rejects bad arguments before it touches
+the device (argument errors return synchronously and enqueue nothing)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunkwise_gated_delta_gdr_gb300 as gdr
+from chunkwise_gated_delta_gdr_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdr.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(gdr_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"gdr_chunk_fwd", "gdr_chunk_fwd_workspace_size", "gdr_stream_status",
+            "gdr_status_string"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(gdr.EXPORTED) <= names
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = gdr.status_string(code)
+        assert s.startswith("GDR_")
+    assert "unknown" in gdr.status_string(99)
+
+
+def test_version(lib):
+    assert lib.gdr_version() >= (0 << 16) | (1 << 8)
+
+
+def dims(**kw):
+    base = dict(B=1, T=256, H=2, HV=4, K=128, V=128, in_dtype=gdr.GDR_BF16,
+                out_dtype=gdr.GDR_F32)
+    base.update(kw)
+    return gdr.make_dims(**base)
+
+
+def test_workspace_size_valid_and_invalid(lib):
+    assert gdr.chunk_fwd_workspace_size(dims(), 64, 0) > 256
+    assert gdr.chunk_fwd_workspace_size(dims(), 48, 0) == 0          # bad chunk size
+    assert gdr.chunk_fwd_workspace_size(dims(HV=3), 64, 0) == 0      # HV % H != 0
+    assert gdr.chunk_fwd_workspace_size(dims(K=256), 64, 0) == 0     # head dim
+    assert gdr.chunk_fwd_workspace_size(dims(T=-1), 64, 0) == 0
+    assert gdr.chunk_fwd_workspace_size(dims(), 64, 2) == 0          # gate mode
+    small = gdr.chunk_fwd_workspace_size(dims(T=64), 64, 0)
+    big = gdr.chunk_fwd_workspace_size(dims(T=4096), 64, 0)
+    assert big > small
+
+
+def test_path_choice(lib):
+    assert gdr.chunk_fwd_path(dims(K=32, V=32), 16, 0) == 0
+    assert gdr.chunk_fwd_path(dims(in_dtype=gdr.GDR_F32), 64, 0) == 0
+    with pytest.raises(gdr.GdrError):
+        gdr.chunk_fwd_path(dims(HV=3), 64, 0)
+
+
+def _call(lib, d, q=16, k=16, v=16, g=16, beta=16, s0=None, out=16, sT=None, C=64, scale=0.1,
+          gate=0, ws=None, ws_bytes=0):
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdr_chunk_fwd(P(q), P(k), P(v), P(g), P(beta), P(s0), C, ctypes.c_float(scale), 1,
+                             gate, P(out), P(sT), ctypes.byref(d), P(ws), ctypes.c_size_t(ws_bytes),
+                             None)
+
+
+def test_argument_errors_are_synchronous(lib):
+    # Fake, never-dereferenced addresses: every case is rejected before any CUDA call.
+    A = 1 << 20
+    d = dims()
+    assert _call(lib, d, q=None, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A + 8, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_ALIGNMENT
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, scale=0.0) == gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, scale=float("nan")) == \
+        gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=48) == gdr.GDR_ERR_UNSUPPORTED
+    assert _call(lib, dims(HV=3), q=A, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, dims(V=200), q=A, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_UNSUPPORTED
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, ws=None) == gdr.GDR_ERR_WORKSPACE
+    need = gdr.chunk_fwd_workspace_size(d, 64, 0)
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, ws=A, ws_bytes=need - 1) == \
+        gdr.GDR_ERR_WORKSPACE
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, ws=A + 16, ws_bytes=need) == \
+        gdr.GDR_ERR_ALIGNMENT
+    assert _call(lib, dims(B=0), q=None, k=None, v=None, g=None, beta=None, out=None) == gdr.GDR_OK
+
+
+def test_host_buffer_size(lib):
+    d = dims()
+    base = gdr.chunk_fwd_host_buffer_size(d, 64, 0, False, False)
+    with_states = gdr.chunk_fwd_host_buffer_size(d, 64, 0, True, True)
+    assert base > gdr.chunk_fwd_workspace_size(d, 64, 0)
+    assert with_states - base == 2 * 4 * 128 * 128 * 4
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        gdr.load_library(str(tmp_path / "nope.so"))

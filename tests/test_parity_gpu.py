@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA library against the float64 oracle, element by element.
+
+Tolerances (the accuracy bound the method's statement sets for this forward
+pass): max|o_gpu - o_ref| <= tol * rms(o_ref) and, separately,
+max|S_gpu - S_ref| <= tol * rms(S_ref), with tol = 2e-3 for bf16 q/k/v and
+1e-4 for fp32 q/k/v. o is compared in fp32 (rounding o itself to bf16 moves it
+by up to half a bf16 ulp, about 8x more than the bound allows; the bf16-output
+path is checked against the fp32-output path instead).
+
+Sizes: every named workload shrunk so the oracle finishes in seconds while the
+sequence still spans several chunks and ends in a ragged chunk, and every
+named workload at full size with a sample of its (batch, head) sequences
+recomputed by the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import chunkwise_gated_delta_gdr_gb300 as gdr
+from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def tol_for(w):
+    return 2e-3 if w.dtype == torch.bfloat16 else 1e-4
+
+
+def relerr(a, b):
+    rms = math.sqrt(float(np.mean(np.asarray(b, np.float64) ** 2)))
+    return float(np.max(np.abs(np.asarray(a, np.float64) - b))) / (rms if rms > 0 else 1.0)
+
+
+def gpu_run(x, w, out_dtype=torch.float32, **kw):
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["s0"], chunk_size=w.C,
+                         scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=out_dtype, **kw)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), S.cpu().numpy()
+
+
+def check_against_oracle(w, x, sel=None, out_dtype=torch.float32):
+    o, S = gpu_run(x, w, out_dtype)
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale,
+                              use_qk_l2norm=w.use_qk_l2norm, sel=sel)
+    if sel is not None:
+        o = np.stack([o[s // w.HV, :, s % w.HV] for s in sel])
+        S = np.stack([S[s // w.HV, s % w.HV] for s in sel])
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    eo, es = relerr(o, ro), relerr(S, rS)
+    tol = tol_for(w)
+    assert eo <= tol, f"{w.name}: output error {eo:.3e} > {tol}"
+    assert es <= tol, f"{w.name}: final-state error {es:.3e} > {tol}"
+    return eo, es
+
+
+SMALL = {
+    "tiny_fp32": {},
+    "gdn_t4096_h12": dict(T=300, H=2, HV=2),
+    "kda_gqa_t8192": dict(B=1, T=200, H=2, HV=4),
+    "gdn_long_t65000": dict(T=333, H=2, HV=2),
+    "kda_many_b64": dict(B=3, T=130, H=2, HV=2),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workloads(name):
+    w = gin.shrink(gin.WORKLOADS[name], **SMALL[name])
+    check_against_oracle(w, gin.make_inputs(w))
+
+
+FULL_SAMPLES = {
+    "tiny_fp32": None,
+    "gdn_t4096_h12": None,                       # all 12 sequences
+    "kda_gqa_t8192": [0, 1, 33, 63],             # (b, hv) = (0,0) (0,1) (1,1) (1,31)
+    "gdn_long_t65000": [0, 31],
+    "kda_many_b64": [0, 17, 512, 1023],
+}
+
+
+@pytest.mark.parametrize("name", list(FULL_SAMPLES))
+def test_full_workloads_sampled(name):
+    w = gin.WORKLOADS[name]
+    check_against_oracle(w, gin.make_inputs(w), sel=FULL_SAMPLES[name])
+
+
+def test_bf16_output_is_fp32_output_rounded():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=257, H=2, HV=2)
+    x = gin.make_inputs(w)
+    o32, S32 = gpu_run(x, w, torch.float32)
+    o16, S16 = gpu_run(x, w, torch.bfloat16)
+    ref = torch.from_numpy(o32).to(torch.bfloat16).float().numpy()
+    ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(o16 - ref) <= ulp)
+    assert np.array_equal(S16, S32)
+
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 129])
+def test_short_and_boundary_lengths(T):
+    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=T, H=1, HV=2)
+    check_against_oracle(w, gin.make_inputs(w))
+
+
+@pytest.mark.parametrize("name", ["gdn_t4096_h12", "kda_many_b64"])
+def test_zero_length_returns_initial_state(name):
+    w = gin.shrink(gin.WORKLOADS[name], T=0, B=2, H=2, HV=2)
+    x = gin.make_inputs(w)
+    s0 = torch.randn(2, 2, w.K, w.V)
+    x["s0"] = s0
+    o, S = gpu_run(x, w)
+    assert o.shape == (2, 0, 2, w.V)
+    assert np.array_equal(S, s0.numpy())
+    x["s0"] = None
+    _, S = gpu_run(x, w)
+    assert np.all(S == 0)
+
+
+def test_final_state_may_alias_initial_state():
+    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=150, H=2, HV=2)
+    x = gin.make_inputs(w)
+    o_ref, S_ref = gpu_run(x, w)
+    dev = torch.device("cuda:0")
+    d = {n: t.to(dev) for n, t in x.items()}
+    state = d["s0"].clone()
+    o, S = gdr.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], state, chunk_size=w.C,
+                         scale=w.scale, out_dtype=torch.float32, final_state=state)
+    torch.cuda.synchronize()
+    assert np.array_equal(S.cpu().numpy(), S_ref)
+    assert np.array_equal(o.cpu().numpy(), o_ref)
+
+
+def test_without_l2norm_prenormalised_keys():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=200, H=2, HV=2, use_qk_l2norm=False)
+    x = gin.make_inputs(w)
+    for n in ("q", "k"):
+        f = x[n].float()
+        x[n] = (f / f.norm(dim=-1, keepdim=True)).to(w.dtype)
+    check_against_oracle(w, x)
+
+
+def test_reset_limit_gate():
+    """g = -1000: every decay is exactly 0; nothing may turn into NaN."""
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=200, H=2, HV=2)
+    x = gin.make_inputs(w)
+    x["g"] = torch.full_like(x["g"], -1000.0)
+    check_against_oracle(w, x)
+
+
+def test_positive_small_gate():
+    """g = 0.1 N(0,1) (gates may exceed 1, as in the optimisation script's smoke run)."""
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=256, H=2, HV=2)
+    x = gin.make_inputs(w)
+    x["g"] = torch.randn(x["g"].shape, generator=torch.Generator().manual_seed(9)) * 0.1
+    check_against_oracle(w, x)
+
+
+def test_split_sequence_matches_single_call():
+    w = gin.shrink(gin.WORKLOADS["kda_gqa_t8192"], B=1, T=320, H=1, HV=2)
+    x = gin.make_inputs(w)
+    o, S = gpu_run(x, w)
+    t1 = 100
+    first = {n: (t[:, :t1].contiguous() if n != "s0" and t is not None else t) for n, t in x.items()}
+    o1, S1 = gpu_run(first, w)
+    second = {n: (t[:, t1:].contiguous() if n != "s0" and t is not None else t) for n, t in x.items()}
+    second["s0"] = torch.from_numpy(S1)
+    o2, S2 = gpu_run(second, w)
+    tol = tol_for(w)
+    assert relerr(np.concatenate([o1, o2], axis=1), o) <= tol
+    assert relerr(S2, S) <= tol
+
+
+def test_host_entry_point_matches_device_call():
+    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=200, H=2, HV=2)
+    x = gin.make_inputs(w)
+    o_ref, S_ref = gpu_run(x, w)
+    pin = {n: t.pin_memory() for n, t in x.items()}
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    nbytes = gdr.chunk_fwd_host_buffer_size(dims, w.C, w.gate_mode, True, True)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda:0")
+    out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32).pin_memory()
+    fin = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32).pin_memory()
+    gdr.chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], pin["s0"], out=out,
+                       final_state=fin, device_buffer=buf, chunk_size=w.C, scale=w.scale)
+    assert gdr.stream_status() == gdr.GDR_OK
+    assert np.array_equal(out.numpy(), o_ref)
+    assert np.array_equal(fin.numpy(), S_ref)
+
+
+def test_stream_status_ok_after_call():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=128, H=1, HV=1)
+    x = {n: (t.cuda() if t is not None else None) for n, t in gin.make_inputs(w).items()}
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims, w.C, w.gate_mode), dtype=torch.uint8,
+                     device="cuda:0")
+    gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, chunk_size=w.C,
+                  out_dtype=torch.float32, workspace=ws)
+    assert gdr.stream_status(workspace=ws) == gdr.GDR_OK
