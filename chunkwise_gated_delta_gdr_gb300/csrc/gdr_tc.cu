@@ -1,12 +1,42 @@
-// gdr_tc.cu -- tcgen05 tensor-core path (bf16, K = V = 128, C = 64).
-#include "gdr_internal.cuh"
+// gdr_tc.cu -- dispatch of the fast path (bf16 inputs, K = V = 128, C = 64).
+#include "gdr_fast.cuh"
 
 namespace gdr {
 
-bool tc_supported(const Problem&) { return false; }
-size_t tc_workspace_bytes(const Problem&) { return 0; }
-gdr_status launch_tc(const Problem&, void*, unsigned int*, cudaStream_t) {
-  return GDR_ERR_UNSUPPORTED;
+bool tc_supported(const Problem& p) {
+  return p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
+}
+
+size_t tc_workspace_bytes(const Problem& p) {
+  return (size_t)p.B * p.HV * p.N * fast::Slab::bytes(p.gate_mode);
+}
+
+gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
+                     cudaStream_t stream) {
+  fast::Params f;
+  f.q = static_cast<const __nv_bfloat16*>(p.q);
+  f.k = static_cast<const __nv_bfloat16*>(p.k);
+  f.v = static_cast<const __nv_bfloat16*>(p.v);
+  f.g = p.g;
+  f.beta = p.beta;
+  f.s0 = p.s0;
+  f.out = p.out;
+  f.sT = p.sT;
+  f.slabs = static_cast<uint8_t*>(ws_body);
+  f.error_word = error_word;
+  f.B = p.B;
+  f.T = p.T;
+  f.H = p.H;
+  f.HV = p.HV;
+  f.N = p.N;
+  f.out_bf16 = p.out_bf16;
+  f.gate_mode = p.gate_mode;
+  f.use_l2 = p.use_l2;
+  f.scale = p.scale;
+  f.slab_bytes = fast::Slab::bytes(p.gate_mode);
+  gdr_status st = fast::launch_chunk_simt(f, stream);
+  if (st != GDR_OK) return st;
+  return fast::launch_state(f, stream);
 }
 
 }  // namespace gdr
