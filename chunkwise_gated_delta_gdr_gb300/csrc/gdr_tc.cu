@@ -34,7 +34,7 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.use_l2 = p.use_l2;
   f.scale = p.scale;
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
-  gdr_status st = fast::launch_chunk_simt(f, stream);
+  gdr_status st = fast::launch_chunk_tc(f, stream);
   if (st != GDR_OK) return st;
   return fast::launch_state(f, stream);
 }
