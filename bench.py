@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the chunkwise gated delta rule forward pass.
+
+One step = one full forward pass (chunk-local kernel + state recurrence) over
+the headline workload: B=1, T=4096, H=HV=12 heads, K=V=128, C=64, bf16 q/k/v,
+fp32 gate and beta, q/k L2-normalised in the kernel, fp32 output and fp32
+final state. Inputs are seeded synthetic tensors already resident in HBM; the
+L2 cache is flushed (a 512 MiB write) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs the same
+workload on its own GPU as a shard of 12 value heads of a 12N-head layer
+(independent sequences, no collective on the data path): weak scaling. Rank 0
+prints one JSON line. ``--impl reference`` times the float64 CPU oracle on the
+host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s for chunked gated-delta fwd (T=4096,H=12,K=V=128,C=64); % of roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# Algorithmic FLOPs per token per value head at C=64, K=V=128: decayed dots
+# A_kk, A_qk (4CK), M^-1 applied to [exp(G)k | v] (2C(K+V)), W S, q S and
+# k^T r (6KV), A_qk r (2CV) and the C x C inverse (~C^2/3).
+FLOP_PER_TOKEN_HEAD = 181589
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def workload(name):
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    return gin.WORKLOADS[name or gin.HEADLINE]
+
+
+def config_of(w, world):
+    return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
+            "C": w.C, "gate": "scalar" if w.gate_mode == 0 else "per-key",
+            "in_dtype": "bf16" if str(w.dtype).endswith("bfloat16") else "fp32",
+            "out_dtype": "fp32", "use_qk_l2norm": w.use_qk_l2norm,
+            "initial_state": w.s0_std is not None, "l2_flush": "512MiB write before each step",
+            "parallelism": f"{world} rank(s), value heads sharded, no collective"}
+
+
+def algorithmic_bytes(w):
+    BT = w.B * w.T
+    qk = 2 * BT * w.H * w.K * 2
+    v = BT * w.HV * w.V * 2
+    g = BT * w.HV * (w.K if w.gate_mode else 1) * 4
+    beta = BT * w.HV * 4
+    o = BT * w.HV * w.V * 4
+    state = w.B * w.HV * w.K * w.V * 4
+    return qk + v + g + beta + o + state + (state if w.s0_std is not None else 0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "chunkwise_gated_delta_gdr_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(wname):
+    """DRAM bytes per step from the committed ncu summary, if it was taken on
+    the kernels as they are now (same source hash); else None."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{wname}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None, None
+    mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not mh or mh.group(1) != source_hash():
+        return None, None
+    per = {}
+    for m in re.finditer(r"^kernel\s+(\S+)\s+dram_bytes_per_launch:\s*([0-9.]+)", text, re.M):
+        per[m.group(1)] = float(m.group(2))
+    return (sum(per.values()) if per else None), per
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        try:
+            import torch
+            bus = getattr(torch.cuda.get_device_properties(device_index), "pci_bus_id", None)
+        except Exception:
+            bus = None
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        if bus:
+            cmd.insert(1, f"--id={bus}")
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(w, x):
+    """The float64 oracle (as it stands) on the host cores, on the full workload."""
+    import oracle
+    ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    nseq = w.B * w.HV
+    threads = max(1, min(ncpu, nseq))
+    times = []
+    for _ in range(2):
+        t0 = time.perf_counter()
+        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale,
+                         use_qk_l2norm=w.use_qk_l2norm, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+        if times[-1] > 10:
+            break
+    t = min(times)
+    return {"value": w.B * w.T / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full workload ({w.B}x{w.T} tokens x {w.HV} heads), float64 token "
+                      f"recurrence, OpenMP over {nseq} sequences, best of {len(times)}",
+            "seconds": t}
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle, as it stands, timed on the host cores. Each step is a
+    bounded sample of the workload: the first `ts` tokens of one (batch, head)
+    sequence, with `ts` sized so that the whole warm-up + timed run stays near
+    90 s of CPU time; the throughput is scaled to the full workload (the
+    recurrence costs the same per token and per sequence)."""
+    if rank != 0:
+        return 0
+    import oracle
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    w = workload(args.workload)
+    x = gin.make_inputs(w)
+    cut = lambda ts: {n: (t[:, :ts].contiguous() if (t is not None and n != "s0") else t)
+                      for n, t in x.items()}
+    # Calibrate: seconds per token of one sequence on one core.
+    cal = cut(min(w.T, 256))
+    t0 = time.perf_counter()
+    oracle.recurrent(cal["q"], cal["k"], cal["v"], cal["g"], cal["beta"], cal["s0"], scale=w.scale,
+                     use_qk_l2norm=w.use_qk_l2norm, sel=[0], nthreads=1)
+    per_token = (time.perf_counter() - t0) / min(w.T, 256)
+    budget = 90.0 / max(1, args.warmup + args.steps)
+    ts = int(max(32, min(w.T, budget / per_token)))
+    xs = cut(ts)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.recurrent(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], xs["s0"], scale=w.scale,
+                         use_qk_l2norm=w.use_qk_l2norm, sel=[0], nthreads=1)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = statistics.mean(times) * (w.T / ts) * (w.B * w.HV)   # seconds for the workload
+    value = w.B * w.T / per_step
+    sample = (f"first {ts} tokens of 1 of {w.B * w.HV} (batch, head) sequences per step, float64 "
+              f"token recurrence on 1 core, scaled to the full workload ({w.B}x{w.T} tokens x "
+              f"{w.HV} heads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import chunkwise_gated_delta_gdr_gb300 as gdr
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = workload(args.workload)
+    wr = gin.shrink(w, seed=w.seed + 1000 * rank)        # this rank's head shard
+    x_cpu = gin.make_inputs(wr)
+    x = {n: (t.to(dev) if t is not None else None) for n, t in x_cpu.items()}
+    gate = w.gate_mode
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims, w.C, gate), dtype=torch.uint8, device=dev)
+    out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32, device=dev)
+    fin = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdr.chunk_prepare(x["q"], x["k"], x["v"], x["g"], x["beta"], workspace=ws,
+                          chunk_size=w.C, scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                          out_dtype=torch.float32, stream=stream)
+        mid.record(stream)
+        gdr.chunk_recur(x["q"], x["k"], x["s0"], workspace=ws, out=out, final_state=fin, HV=w.HV,
+                        V=w.V, gate_mode=gate, chunk_size=w.C, scale=w.scale,
+                        use_qk_l2norm=w.use_qk_l2norm, stream=stream)
+
+    mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.2)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, m, b in evs:
+        flush.zero_()
+        a.record(stream)
+        mid = m
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    tot = [a.elapsed_time(b) for a, m, b in evs]
+    prep = [a.elapsed_time(m) for a, m, b in evs]
+    rec = [m.elapsed_time(b) for a, m, b in evs]
+    ms = statistics.mean(tot)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # End to end through the C ABI with host buffers: pinned inputs copied in,
+    # o and the final state copied out, every step.
+    pin = {n: (t.pin_memory() if t is not None else None) for n, t in x_cpu.items()}
+    out_h = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32).pin_memory()
+    fin_h = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32).pin_memory()
+    hbuf = torch.empty(gdr.chunk_fwd_host_buffer_size(dims, w.C, gate, pin["s0"] is not None, True),
+                       dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for n, t in pin.items() if t is not None)
+    d2h = out_h.numel() * 4 + fin_h.numel() * 4
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        gdr.chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], pin["s0"],
+                           out=out_h, final_state=fin_h, device_buffer=hbuf, chunk_size=w.C,
+                           scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, stream=stream)
+    torch.cuda.synchronize()
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_a.record(stream)
+    for _ in range(e2e_steps):
+        gdr.chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], pin["s0"],
+                           out=out_h, final_state=fin_h, device_buffer=hbuf, chunk_size=w.C,
+                           scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, stream=stream)
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_a.elapsed_time(e_b) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert gdr.stream_status(stream, ws) == gdr.GDR_OK
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    hbm, tflops, peak_kind = load_peaks()
+    bytes_alg = algorithmic_bytes(w)
+    flops_alg = FLOP_PER_TOKEN_HEAD * w.B * w.T * w.HV
+    achieved = bytes_alg / (ms * 1e-3) / 1e9
+    traffic, traffic_per = recorded_traffic(w.name)
+    tokens = world * w.B * w.T
+    line = {
+        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, world),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "scope": "one forward call = chunk-local kernel + state kernel",
+                     "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs",
+                     "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
+                     "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
+        "kernels": {"chunk_local": {"ms": statistics.mean(prep),
+                                    "traffic": (traffic_per or {}).get("chunk_tc_kernel")},
+                    "state": {"ms": statistics.mean(rec),
+                              "traffic": (traffic_per or {}).get("state_kernel")}},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": t_wall,
+    }
+    line["cpu_baseline"] = cpu_baseline(w, x_cpu)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -28,7 +28,8 @@ GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_PER_KEY = 0, 1
 
 EXPORTED = (
-    "gdr_chunk_fwd", "gdr_chunk_fwd_workspace_size", "gdr_chunk_fwd_host",
+    "gdr_chunk_fwd", "gdr_chunk_prepare", "gdr_chunk_recur", "gdr_chunk_fwd_workspace_size",
+    "gdr_chunk_fwd_host",
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
     "gdr_chunk_fwd_path", "gdr_version",
 )
@@ -67,6 +68,10 @@ def load_library(path: Optional[str] = None):
         lib.gdr_chunk_fwd.restype = ip
         lib.gdr_chunk_fwd_host.argtypes = fwd_args
         lib.gdr_chunk_fwd_host.restype = ip
+        lib.gdr_chunk_prepare.argtypes = [vp, vp, vp, vp, vp, ip, fp, ip, ip, dp, vp, sz, vp]
+        lib.gdr_chunk_prepare.restype = ip
+        lib.gdr_chunk_recur.argtypes = [vp, vp, vp, ip, fp, ip, ip, vp, vp, dp, vp, sz, vp]
+        lib.gdr_chunk_recur.restype = ip
         lib.gdr_chunk_fwd_workspace_size.argtypes = [dp, ip, ip]
         lib.gdr_chunk_fwd_workspace_size.restype = sz
         lib.gdr_chunk_fwd_host_buffer_size.argtypes = [dp, ip, ip, ip, ip]
@@ -170,6 +175,38 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, chunk_size: int = 64,
         _stream_handle(stream))
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_fwd")
+    return out, final_state
+
+
+def chunk_prepare(q, k, v, g, beta, *, workspace, chunk_size: int = 64,
+                  scale: Optional[float] = None, use_qk_l2norm: bool = True, out_dtype=None,
+                  stream=None):
+    """First stage of chunk_fwd: the chunk-local kernel fills ``workspace``."""
+    B, T, H, HV, K, V, gate_mode = _shapes(q, v, g)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out_dtype))
+    st = load_library().gdr_chunk_prepare(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), int(chunk_size), ctypes.c_float(scale),
+        int(bool(use_qk_l2norm)), gate_mode, ctypes.byref(dims), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_chunk_prepare")
+
+
+def chunk_recur(q, k, initial_state=None, *, workspace, out, final_state=None, HV: int, V: int,
+                gate_mode: int, chunk_size: int = 64, scale: Optional[float] = None,
+                use_qk_l2norm: bool = True, stream=None):
+    """Second stage of chunk_fwd: the state recurrence over a prepared workspace."""
+    B, T, H, K = q.shape
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out.dtype))
+    st = load_library().gdr_chunk_recur(
+        _ptr(q), _ptr(k), _ptr(initial_state), int(chunk_size), ctypes.c_float(scale),
+        int(bool(use_qk_l2norm)), int(gate_mode), _ptr(out), _ptr(final_state), ctypes.byref(dims),
+        _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_chunk_recur")
     return out, final_state
 
 

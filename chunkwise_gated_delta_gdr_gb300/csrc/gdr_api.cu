@@ -118,16 +118,24 @@ int gdr_chunk_fwd_path(const gdr_dims* dims, int chunk_size, int gate_mode, gdr_
   return tc_supported(p) ? 1 : 0;
 }
 
-gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                         const float* beta, const float* initial_state, int chunk_size,
-                         float scale, int use_qk_l2norm, int gate_mode, void* out,
-                         float* final_state, const gdr_dims* dims, void* workspace,
-                         size_t workspace_bytes, gdr_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of gdr_chunk_fwd (stage 3), gdr_chunk_prepare (1) and
+// gdr_chunk_recur (2).
+gdr_status run(int stage, const void* q, const void* k, const void* v, const float* g,
+               const float* beta, const float* initial_state, int chunk_size, float scale,
+               int use_qk_l2norm, int gate_mode, void* out, float* final_state,
+               const gdr_dims* dims, void* workspace, size_t workspace_bytes,
+               gdr_stream_t stream) {
   gdr_status st = check_dims(dims, chunk_size, gate_mode);
   if (st != GDR_OK) return st;
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
   const bool work = dims->B > 0 && dims->T > 0;
-  if (work && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_INVALID_ARG;
+  if (work && (!q || !k)) return GDR_ERR_INVALID_ARG;
+  if (work && (stage & 1) && (!v || !g || !beta)) return GDR_ERR_INVALID_ARG;
+  if (work && (stage & 2) && !out) return GDR_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, g, beta, initial_state, out, final_state};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return GDR_ERR_ALIGNMENT;
@@ -135,7 +143,7 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
   const size_t state_bytes = (size_t)dims->B * dims->HV * dims->K * dims->V * sizeof(float);
   if (dims->B == 0) return GDR_OK;
   if (dims->T == 0) {
-    if (!final_state) return GDR_OK;
+    if (!(stage & 2) || !final_state) return GDR_OK;
     cudaError_t e = initial_state
                         ? (final_state == initial_state
                                ? cudaSuccess
@@ -151,11 +159,41 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
   Problem p = make_problem(q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm,
                            gate_mode, out, final_state, dims);
   auto* hdr = static_cast<WorkspaceHeader*>(workspace);
-  if (cudaMemsetAsync(&hdr->error_word, 0, sizeof(unsigned int), s) != cudaSuccess)
+  if ((stage & 1) &&
+      cudaMemsetAsync(&hdr->error_word, 0, sizeof(unsigned int), s) != cudaSuccess)
     return GDR_ERR_CUDA;
   void* body = static_cast<char*>(workspace) + sizeof(WorkspaceHeader);
-  if (tc_supported(p)) return launch_tc(p, body, &hdr->error_word, s);
-  return launch_general(p, body, s);
+  if (tc_supported(p)) return launch_tc(p, body, &hdr->error_word, s, stage);
+  return launch_general(p, body, s, stage);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* initial_state, int chunk_size,
+                         float scale, int use_qk_l2norm, int gate_mode, void* out,
+                         float* final_state, const gdr_dims* dims, void* workspace,
+                         size_t workspace_bytes, gdr_stream_t stream) {
+  return run(3, q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm, gate_mode,
+             out, final_state, dims, workspace, workspace_bytes, stream);
+}
+
+gdr_status gdr_chunk_prepare(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, int chunk_size, float scale, int use_qk_l2norm,
+                             int gate_mode, const gdr_dims* dims, void* workspace,
+                             size_t workspace_bytes, gdr_stream_t stream) {
+  return run(1, q, k, v, g, beta, nullptr, chunk_size, scale, use_qk_l2norm, gate_mode, nullptr,
+             nullptr, dims, workspace, workspace_bytes, stream);
+}
+
+gdr_status gdr_chunk_recur(const void* q, const void* k, const float* initial_state,
+                           int chunk_size, float scale, int use_qk_l2norm, int gate_mode,
+                           void* out, float* final_state, const gdr_dims* dims, void* workspace,
+                           size_t workspace_bytes, gdr_stream_t stream) {
+  return run(2, q, k, nullptr, nullptr, nullptr, initial_state, chunk_size, scale, use_qk_l2norm,
+             gate_mode, out, final_state, dims, workspace, workspace_bytes, stream);
 }
 
 size_t gdr_chunk_fwd_host_buffer_size(const gdr_dims* dims, int chunk_size, int gate_mode,

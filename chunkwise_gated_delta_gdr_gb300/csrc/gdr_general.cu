@@ -345,7 +345,7 @@ size_t general_workspace_bytes(const Problem& p) {
          align_up(s.nchunks * s.gm * sizeof(float));
 }
 
-gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream) {
+gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream, int stage) {
   Args a;
   a.p = p;
   a.s = carve(p, ws_body);
@@ -357,12 +357,16 @@ gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream) 
   if (cudaFuncSetAttribute(general_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)state_smem) != cudaSuccess)
     return GDR_ERR_CUDA;
-  dim3 g1(p.N, p.HV, p.B);
-  general_prep_kernel<<<g1, kThreads, prep_smem, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
-  dim3 g2((p.V + kVt - 1) / kVt, p.HV, p.B);
-  general_state_kernel<<<g2, kThreads, state_smem, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+  if (stage & 1) {
+    dim3 g1(p.N, p.HV, p.B);
+    general_prep_kernel<<<g1, kThreads, prep_smem, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+  }
+  if (stage & 2) {
+    dim3 g2((p.V + kVt - 1) / kVt, p.HV, p.B);
+    general_state_kernel<<<g2, kThreads, state_smem, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GDR_ERR_CUDA;
+  }
   return GDR_OK;
 }
 

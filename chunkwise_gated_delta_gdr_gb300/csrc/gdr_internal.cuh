@@ -36,14 +36,16 @@ static_assert(sizeof(WorkspaceHeader) == 256, "header must stay 256 bytes");
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
-// General fp32 CUDA-core path (any supported shape).
+// General fp32 CUDA-core path (any supported shape). stage: 1 = chunk-local
+// kernel, 2 = state recurrence, 3 = both.
 size_t general_workspace_bytes(const Problem& p);
-gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream);
+gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream, int stage);
 
-// tcgen05 tensor-core path (bf16, K = V = 128, C = 64).
+// Fast path (bf16, K = V = 128, C = 64): tcgen05 chunk-local kernel and
+// mma.sync state recurrence.
 bool tc_supported(const Problem& p);
 size_t tc_workspace_bytes(const Problem& p);
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int stage);
 
 }  // namespace gdr

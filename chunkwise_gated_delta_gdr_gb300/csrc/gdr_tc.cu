@@ -12,7 +12,7 @@ size_t tc_workspace_bytes(const Problem& p) {
 }
 
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, int stage) {
   fast::Params f;
   f.q = static_cast<const __nv_bfloat16*>(p.q);
   f.k = static_cast<const __nv_bfloat16*>(p.k);
@@ -34,9 +34,12 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.use_l2 = p.use_l2;
   f.scale = p.scale;
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
-  gdr_status st = fast::launch_chunk_tc(f, stream);
-  if (st != GDR_OK) return st;
-  return fast::launch_state(f, stream);
+  if (stage & 1) {
+    gdr_status st = fast::launch_chunk_tc(f, stream);
+    if (st != GDR_OK) return st;
+  }
+  if (stage & 2) return fast::launch_state(f, stream);
+  return GDR_OK;
 }
 
 }  // namespace gdr

@@ -111,6 +111,34 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          float* final_state, const gdr_dims* dims, void* workspace,
                          size_t workspace_bytes, gdr_stream_t stream);
 
+/*
+ * gdr_chunk_prepare / gdr_chunk_recur -- gdr_chunk_fwd in its two stages.
+ *
+ * gdr_chunk_prepare runs the chunk-local kernel: per chunk, the gate cumsum,
+ * the decayed dots A_kk / A_qk, the triangular solve for W and U, written into
+ * `workspace` (the "chunk 内的 cumsum 与下三角解" section of the notes).
+ * gdr_chunk_recur then runs the state recurrence across chunks (the notes'
+ * inter-chunk loop) and writes out / final_state. gdr_chunk_fwd is exactly
+ * prepare followed by recur on the same stream.
+ *
+ * The prepared workspace does not depend on the initial state: after one
+ * prepare, recur may run any number of times with different initial states
+ * (each run overwrites out / final_state). Every recur must use the q, k,
+ * chunk_size, scale, use_qk_l2norm, gate_mode and dims of the prepare that
+ * filled the workspace, and q / k must still hold the same values. Argument
+ * meaning, layouts, alignment and errors are those of gdr_chunk_fwd; prepare
+ * ignores out / final_state, recur ignores v / g / beta.
+ */
+gdr_status gdr_chunk_prepare(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, int chunk_size, float scale, int use_qk_l2norm,
+                             int gate_mode, const gdr_dims* dims, void* workspace,
+                             size_t workspace_bytes, gdr_stream_t stream);
+
+gdr_status gdr_chunk_recur(const void* q, const void* k, const float* initial_state,
+                           int chunk_size, float scale, int use_qk_l2norm, int gate_mode,
+                           void* out, float* final_state, const gdr_dims* dims, void* workspace,
+                           size_t workspace_bytes, gdr_stream_t stream);
+
 /* Bytes of device workspace gdr_chunk_fwd needs for these sizes (0 if the
  * arguments are invalid or unsupported). */
 size_t gdr_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode);

@@ -199,3 +199,30 @@ def test_stream_status_ok_after_call():
     gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, chunk_size=w.C,
                   out_dtype=torch.float32, workspace=ws)
     assert gdr.stream_status(workspace=ws) == gdr.GDR_OK
+
+
+@pytest.mark.parametrize("name", ["gdn_t4096_h12", "kda_gqa_t8192", "tiny_fp32"])
+def test_prepare_then_recur_with_two_states(name):
+    """prepare + recur equals chunk_fwd, and one prepared workspace serves two
+    different initial states (the slabs do not depend on the state)."""
+    w = gin.shrink(gin.WORKLOADS[name], B=1, T=150, H=1, HV=2)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16 if w.dtype == torch.bfloat16
+                         else gdr.GDR_F32, gdr.GDR_F32)
+    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims, w.C, w.gate_mode), dtype=torch.uint8,
+                     device=dev)
+    gdr.chunk_prepare(d["q"], d["k"], d["v"], d["g"], d["beta"], workspace=ws, chunk_size=w.C,
+                      scale=w.scale, out_dtype=torch.float32)
+    for seed in (1, 2):
+        s0 = torch.randn(w.B, w.HV, w.K, w.V, generator=torch.Generator().manual_seed(seed)) * 0.1
+        out = torch.empty(w.B, w.T, w.HV, w.V, device=dev)
+        fin = torch.empty(w.B, w.HV, w.K, w.V, device=dev)
+        gdr.chunk_recur(d["q"], d["k"], s0.to(dev), workspace=ws, out=out, final_state=fin,
+                        HV=w.HV, V=w.V, gate_mode=w.gate_mode, chunk_size=w.C, scale=w.scale)
+        x2 = dict(x, s0=s0)
+        o_ref, S_ref = gpu_run(x2, w)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), o_ref)
+        assert np.array_equal(fin.cpu().numpy(), S_ref)
