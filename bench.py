@@ -244,6 +244,7 @@ def run_ours(args, rank, local_rank, world):
     import torch
     import chunkwise_gated_delta_gdr_gb300 as gdr
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    from chunkwise_gated_delta_gdr_gb300 import shard
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -302,11 +303,7 @@ def run_ours(args, rank, local_rank, world):
     tot = [a.elapsed_time(b) for a, m, b in evs]
     prep = [a.elapsed_time(m) for a, m, b in evs]
     rec = [m.elapsed_time(b) for a, m, b in evs]
-    ms = statistics.mean(tot)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = shard.step_time_across_ranks(statistics.mean(tot), pg)
 
     # End to end through the C ABI with host buffers: pinned inputs copied in,
     # o and the final state copied out, every step.
@@ -331,11 +328,7 @@ def run_ours(args, rank, local_rank, world):
                            scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, stream=stream)
     e_b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_a.elapsed_time(e_b) / e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = shard.step_time_across_ranks(e_a.elapsed_time(e_b) / e2e_steps, pg)
     assert gdr.stream_status(stream, ws) == gdr.GDR_OK
 
     if rank != 0:

@@ -33,20 +33,39 @@ constexpr long kWaitLimit = 1L << 24;   // bounded spin: ~tens of ms, then error
 constexpr unsigned int kErrTmaWait = 1u, kErrMmaWait = 2u;
 
 // Shared-memory map (bytes from a 1024-aligned base).
-constexpr int OFF_K0 = 0;          // k cols 0-63   (8 KB, SW128)
+constexpr int OFF_K0 = 0;          // k cols 0-63   (8 KB, 128-byte swizzle, from TMA)
 constexpr int OFF_Q0 = 8192;       // q cols 0-63
 constexpr int OFF_K1 = 16384;      // k cols 64-127
 constexpr int OFF_Q1 = 24576;      // q cols 64-127
 constexpr int OFF_V0 = 32768;      // v cols 0-63
 constexpr int OFF_V1 = 40960;      // v cols 64-127
-constexpr int OFF_L = 49152;       // L fp32 [64][64]; later XW = [X'hi; X'lo] (M=128, K=64)
-constexpr int OFF_X = 65536;       // X fp32 [64][64]; later XU = [Xhi; Xlo]
-constexpr int OFF_SMALL = 81920;   // G, nq, nk, beta (4 x 64 fp32)
-constexpr int OFF_BAR = 82944;     // mbarriers + TMEM slot
+constexpr int LDL = 68;            // fp32 row stride of L (272 B: float4 rows, conflict-free)
+constexpr int OFF_L = 49152;       // L [64][LDL] fp32; later XW (16 KB)
+constexpr int LDQ = 72;            // bf16 row stride of the A_qk staging tiles
+constexpr int OFF_AQS = 66560;     // A_qk hi / lo staging [2][64][LDQ] bf16
+constexpr int OFF_XU = 65536;      // XU (16 KB), written once L and the A_qk staging are dead
+constexpr int LDX = 68;            // fp32 row stride of X
+constexpr int OFF_X = 84992;       // X = (I + L)^-1 [64][LDX] fp32
+constexpr int OFF_T = 8192;        // block-product scratch [32][36] fp32 (in the dead q tile)
+constexpr int OFF_SMALL = 102400;  // G, nq, nk, beta, column factor (5 x 64 fp32)
+constexpr int OFF_BAR = 103680;    // mbarriers + TMEM slot
 constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
-// After the W / U MMAs complete, [0, 65536) holds the two fp32 exchange tiles.
-constexpr int OFF_XCH_W = 0;       // [64][128] fp32
-constexpr int OFF_XCH_U = 32768;   // [64][128] fp32
+// Epilogue-2 staging (after the W / U MMAs, over the dead operand tiles).
+constexpr int LDWS = 136;          // bf16 row stride of the -W staging tiles
+constexpr int OFF_WS = 0;          // -W hi / lo [2][64][LDWS] bf16 (34816 B)
+constexpr int LDUS = 132;          // fp32 row stride of the U staging tile
+constexpr int OFF_US = 34816;      // U [64][LDUS] fp32 (33792 B)
+static_assert(OFF_AQS + 2 * 64 * LDQ * 2 <= OFF_SMALL, "A_qk staging overlaps");
+static_assert(OFF_L + 64 * LDL * 4 <= OFF_AQS, "L overlaps");
+static_assert(OFF_US + 64 * LDUS * 4 <= OFF_X, "U staging overlaps X");
+static_assert(OFF_X + 64 * LDX * 4 <= OFF_SMALL, "X overlaps");
+static_assert(OFF_T + 32 * 36 * 4 <= OFF_K1, "scratch overlaps the k tile");
+
+// Rows of the stacked A operands [X_hi; X_lo] of the W / U MMAs are
+// interleaved in blocks of 16 so that the hi and lo products of output row i
+// land in the same warp's TMEM lanes (lanes 32 w + t and 32 w + 16 + t):
+//   row i, hi part -> A row 32 (i / 16) + (i % 16); lo part -> that + 16.
+__host__ __device__ constexpr int stacked_row(int i, int lo) { return 32 * (i >> 4) + (i & 15) + 16 * lo; }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -146,10 +165,13 @@ __global__ void __launch_bounds__(THREADS, 2)
 
   float* L = reinterpret_cast<float*>(sm + OFF_L);
   float* X = reinterpret_cast<float*>(sm + OFF_X);
+  float* T = reinterpret_cast<float*>(sm + OFF_T);
+  __nv_bfloat16* aqs = reinterpret_cast<__nv_bfloat16*>(sm + OFF_AQS);
   float* G = reinterpret_cast<float*>(sm + OFF_SMALL);
   float* nq = G + C;
   float* nk = nq + C;
   float* bb = nk + C;
+  float* cfac = bb + C;
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
@@ -182,7 +204,13 @@ __global__ void __launch_bounds__(THREADS, 2)
     tma_load4(smem_u32(sm + OFF_V0), &map_v, 0, hv, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_V1), &map_v, 64, hv, t0, b, bar_tma);
   }
-  // beta (plain loads; zero past the end of the sequence).
+  // Gate and beta (plain loads, issued before the TMA wait; zero past the end).
+  float ga = 0.f, gb = 0.f;
+  if (warp == 0) {
+    const int ta = t0 + 2 * lane;
+    if (ta < p.T) ga = p.g[((size_t)b * p.T + ta) * p.HV + hv];
+    if (ta + 1 < p.T) gb = p.g[((size_t)b * p.T + ta + 1) * p.HV + hv];
+  }
   if (tid < C) {
     const int t = t0 + tid;
     bb[tid] = (t < p.T) ? p.beta[((size_t)b * p.T + t) * p.HV + hv] : 0.f;
@@ -190,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tma, 0));
   if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
 
-  // ---- MMA 1: D[0:128, 0:64] = [k; q] k^T ------------------------------------
+  // ---- MMA 1: D[0:128, 0:64] = [k; q] k^T -------------------------------------
   if (ok && tid == 0) {
     fence_after();
     const uint32_t id = idesc_bf16(128, 64, 0, 0);
@@ -202,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     umma_commit(bar_mma);
   }
-  // Row norms (threads 0-63: k rows, 64-127: q rows) and the gate cumsum, while
+  // Row norms (threads 0-63: k rows, 64-127: q rows) and the gate cumsum while
   // the MMA runs.
   {
     const int r = tid & 63;
@@ -225,24 +253,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (tid < 64) nk[r] = inv; else nq[r] = inv;
   }
   if (warp == 0) {
-    // Inclusive scan of the 64 gate values of the chunk, two per lane (zero
-    // past the end of the sequence).
-    const int ta = t0 + 2 * lane;
-    const float a0 = (ta < p.T) ? p.g[((size_t)b * p.T + ta) * p.HV + hv] : 0.f;
-    const float a1 = (ta + 1 < p.T) ? p.g[((size_t)b * p.T + ta + 1) * p.HV + hv] : 0.f;
-    float s = a0 + a1;
+    // Inclusive scan of the chunk's 64 gate values, two per lane.
+    float s = ga + gb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    const float excl = s - (a0 + a1);
-    G[2 * lane] = excl + a0;
-    G[2 * lane + 1] = excl + a0 + a1;
+    const float excl = s - (ga + gb);
+    G[2 * lane] = excl + ga;
+    G[2 * lane + 1] = excl + ga + gb;
   }
   __syncthreads();
 
-  // ---- epilogue 1: A_kk -> L (smem), A_qk -> slab ------------------------------
+  // ---- epilogue 1: A_kk -> L (fp32, smem), A_qk -> bf16 hi/lo staging -----------
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 0));
   if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
   fence_after();
@@ -251,16 +275,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     const bool is_q = tid >= 64;
     const float Gi = G[r];
     const float rowf = is_q ? p.scale * nq[r] : nk[r];
-    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
-#pragma unroll
+#pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc * 32, v);
       if (!is_q) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = cc * 32 + e;
-          L[r * C + j] = (j < r) ? v[e] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
+        for (int e = 0; e < 32; e += 4) {
+          float a4[4];
+#pragma unroll
+          for (int z = 0; z < 4; ++z) {
+            const int j = cc * 32 + e + z;
+            a4[z] = (j < r) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
+          }
+          *reinterpret_cast<float4*>(L + r * LDL + cc * 32 + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       } else {
 #pragma unroll
@@ -280,8 +308,9 @@ __global__ void __launch_bounds__(THREADS, 2)
             lo[f / 2] = pack_bf16(a2[0] - hf.x, a2[1] - hf.y);
           }
           const int j0 = cc * 32 + e;
-          *reinterpret_cast<uint4*>(aq + r * C + j0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(aq + C * C + r * C + j0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(aqs + r * LDQ + j0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(aqs + 64 * LDQ + r * LDQ + j0) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
@@ -289,95 +318,153 @@ __global__ void __launch_bounds__(THREADS, 2)
   fence_before();
   __syncthreads();
 
-  // ---- X = (I + L)^-1 ---------------------------------------------------------
-  // Diagonal 16x16 blocks: thread (blk, col) runs forward substitution down one column.
+  // A_qk slab rows out (coalesced) and the per-row factors of the state pass.
+  {
+    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
+#pragma unroll 2
+    for (int idx = tid; idx < 2 * C * (C / 8); idx += THREADS) {
+      const int half = idx / (C * C / 8), rem = idx % (C * C / 8);
+      const int r = rem >> 3, c8 = (rem & 7) * 8;
+      *reinterpret_cast<uint4*>(aq + half * C * C + r * C + c8) =
+          *reinterpret_cast<const uint4*>(aqs + half * 64 * LDQ + r * LDQ + c8);
+    }
+    float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
+    const float gl = G[C - 1];
+    if (tid < C) {
+      vec[tid] = p.scale * nq[tid] * __expf(G[tid]);
+      vec[C + tid] = bb[tid] * nk[tid] * __expf(gl - G[tid]);
+      cfac[tid] = __expf(G[tid]) * nk[tid];   // column factor of X' = X diag(exp(G) |k|^-1)
+    }
+    vec[2 * C + tid] = __expf(gl);
+  }
+
+  // ---- X = (I + L)^-1, blocked --------------------------------------------------
+  // Level 0: the four 16x16 diagonal blocks, one column per thread (threads 0-63),
+  // by forward substitution x_i = delta_ij - sum_{m<i} L_im x_m.
   if (tid < 64) {
-    const int blk = tid >> 4, col = tid & 15, o = blk * 16;
-    float x[16];
+    const int o = (tid >> 4) * 16, col = tid & 15;
+    float xd[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float acc = (i == col) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(-L[(o + i) * C + o + m], x[m], acc);
-      x[i] = acc;
+      for (int m = 0; m < i; ++m) acc = fmaf(-L[(o + i) * LDL + o + m], xd[m], acc);
+      xd[i] = acc;
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) X[(o + i) * C + o + col] = x[i];
-  } else {
-    // Zero the strictly upper blocks of X.
-    for (int idx = tid - 64; idx < C * C; idx += 64) {
-      const int i = idx / C, j = idx % C;
-      if ((j >> 4) > (i >> 4)) X[idx] = 0.f;
-    }
+    for (int i = 0; i < 16; ++i) X[(o + i) * LDX + o + col] = xd[i];
   }
   __syncthreads();
-  // Off-diagonal blocks, by distance d = I - J: X_IJ = -X_II sum_{m=J}^{I-1} L_Im X_mJ.
-  // T_IJ is staged in the strictly upper blocks of L (unused by then).
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    const int nblk = 4 - d;
-    for (int idx = tid; idx < nblk * 256; idx += THREADS) {
-      const int J = idx >> 8, e = idx & 255, i = e >> 4, j = e & 15, I = J + d;
-      float acc = 0.f;
-      for (int m = 16 * J; m < 16 * I; ++m) acc = fmaf(L[(16 * I + i) * C + m], X[m * C + 16 * J + j], acc);
-      L[(16 * J + i) * C + 16 * I + j] = acc;   // block (J, I) of L is above the diagonal
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += THREADS) {
-      const int J = idx >> 8, e = idx & 255, i = e >> 4, j = e & 15, I = J + d;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        acc = fmaf(X[(16 * I + i) * C + 16 * I + m], L[(16 * J + m) * C + 16 * I + j], acc);
-      X[(16 * I + i) * C + 16 * J + j] = -acc;
-    }
-    __syncthreads();
-  }
-
-  // ---- A operands of the W / U MMAs: XW = [X'hi; X'lo], XU = [Xhi; Xlo] ---------
-  // X' = X diag(exp(G_j) |k_j|^-1). Thread: row r = tid >> 1, columns 32 (tid & 1) ..
+  // Level 1: X_10 = -X_11 (L_10 X_00) and X_32 = -X_33 (L_32 X_22), 16x16 blocks;
+  // each thread one row segment of 4 columns.
   {
-    const int r = tid >> 1, c0 = (tid & 1) * 32;
-    float xv[32];
+    const int which = tid >> 6, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
+    const int I = 16 * (2 * which + 1), J = I - 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) xv[e] = X[r * C + c0 + e];
-    __syncthreads();   // X and L are overwritten below
+    for (int m = 0; m < 16; ++m) {
+      const float l = L[(I + i) * LDL + J + m];
+      const float4 xv = *reinterpret_cast<const float4*>(X + (J + m) * LDX + J + j0);
+      acc.x = fmaf(l, xv.x, acc.x); acc.y = fmaf(l, xv.y, acc.y);
+      acc.z = fmaf(l, xv.z, acc.z); acc.w = fmaf(l, xv.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(T + (which * 16 + i) * 36 + j0) = acc;
+    __syncthreads();
+    float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float xv = X[(I + i) * LDX + I + m];
+      const float4 t4 = *reinterpret_cast<const float4*>(T + (which * 16 + m) * 36 + j0);
+      r4.x = fmaf(xv, t4.x, r4.x); r4.y = fmaf(xv, t4.y, r4.y);
+      r4.z = fmaf(xv, t4.z, r4.z); r4.w = fmaf(xv, t4.w, r4.w);
+    }
+    *reinterpret_cast<float4*>(X + (I + i) * LDX + J + j0) = make_float4(-r4.x, -r4.y, -r4.z, -r4.w);
+  }
+  __syncthreads();
+  // Level 2: X[32:64, 0:32] = -X[32:64, 32:64] (L[32:64, 0:32] X[0:32, 0:32]); each
+  // thread one row segment of 8 columns. Entries above the diagonal of X are
+  // never written and read as zero through the masks below.
+  {
+    const int i = tid >> 2, j0 = (tid & 3) * 8;
+    float a[8];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) a[z] = 0.f;
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float l = L[(32 + i) * LDL + m];
+      const float4 x0 = *reinterpret_cast<const float4*>(X + m * LDX + j0);
+      const float4 x1 = *reinterpret_cast<const float4*>(X + m * LDX + j0 + 4);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int z = 0; z < 8; ++z) a[z] = fmaf(l, (j0 + z <= m) ? xs[z] : 0.f, a[z]);
+    }
+    __syncthreads();   // every thread is past its reads of the level-1 scratch
+#pragma unroll
+    for (int z = 0; z < 8; z += 4)
+      *reinterpret_cast<float4*>(T + i * 36 + j0 + z) = make_float4(a[z], a[z + 1], a[z + 2], a[z + 3]);
+    __syncthreads();
+    float r8[8];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) r8[z] = 0.f;
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float xv = (m <= i) ? X[(32 + i) * LDX + 32 + m] : 0.f;
+      const float4 t0 = *reinterpret_cast<const float4*>(T + m * 36 + j0);
+      const float4 t1 = *reinterpret_cast<const float4*>(T + m * 36 + j0 + 4);
+      const float ts[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+      for (int z = 0; z < 8; ++z) r8[z] = fmaf(xv, ts[z], r8[z]);
+    }
+#pragma unroll
+    for (int z = 0; z < 8; z += 4)
+      *reinterpret_cast<float4*>(X + (32 + i) * LDX + j0 + z) =
+          make_float4(-r8[z], -r8[z + 1], -r8[z + 2], -r8[z + 3]);
+  }
+  __syncthreads();   // X complete; L and the A_qk staging are dead from here on
+
+  // ---- A operands XW = [X' hi/lo], XU = [X hi/lo] (rows interleaved, see stacked_row)
+  // Each thread: one row i, 8 consecutive columns, 4 items.
+  {
     uint8_t* xw = sm + OFF_L;
-    uint8_t* xu = sm + OFF_X;
-#pragma unroll
-    for (int e = 0; e < 32; e += 8) {
+    uint8_t* xu = sm + OFF_XU;
+#pragma unroll 2
+    for (int it = tid; it < C * 8; it += THREADS) {
+      const int i = it >> 3, c8 = (it & 7) * 8;
+      const float4 x0 = *reinterpret_cast<const float4*>(X + i * LDX + c8);
+      const float4 x1 = *reinterpret_cast<const float4*>(X + i * LDX + c8 + 4);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       uint32_t whi[4], wlo[4], uhi[4], ulo[4];
 #pragma unroll
-      for (int f = 0; f < 8; f += 2) {
-        const int j = c0 + e + f;
-        const float w0 = xv[e + f] * __expf(G[j]) * nk[j];
-        const float w1 = xv[e + f + 1] * __expf(G[j + 1]) * nk[j + 1];
+      for (int z = 0; z < 8; z += 2) {
+        const float u0 = (c8 + z <= i) ? xs[z] : 0.f;
+        const float u1 = (c8 + z + 1 <= i) ? xs[z + 1] : 0.f;
+        const float w0 = u0 * cfac[c8 + z], w1 = u1 * cfac[c8 + z + 1];
         __nv_bfloat162 wb = __floats2bfloat162_rn(w0, w1);
-        float2 wf = __bfloat1622float2(wb);
-        whi[f / 2] = *reinterpret_cast<uint32_t*>(&wb);
-        wlo[f / 2] = pack_bf16(w0 - wf.x, w1 - wf.y);
-        __nv_bfloat162 ub = __floats2bfloat162_rn(xv[e + f], xv[e + f + 1]);
-        float2 uf = __bfloat1622float2(ub);
-        uhi[f / 2] = *reinterpret_cast<uint32_t*>(&ub);
-        ulo[f / 2] = pack_bf16(xv[e + f] - uf.x, xv[e + f + 1] - uf.y);
+        const float2 wf = __bfloat1622float2(wb);
+        whi[z / 2] = *reinterpret_cast<uint32_t*>(&wb);
+        wlo[z / 2] = pack_bf16(w0 - wf.x, w1 - wf.y);
+        __nv_bfloat162 ub = __floats2bfloat162_rn(u0, u1);
+        const float2 uf = __bfloat1622float2(ub);
+        uhi[z / 2] = *reinterpret_cast<uint32_t*>(&ub);
+        ulo[z / 2] = pack_bf16(u0 - uf.x, u1 - uf.y);
       }
-      const uint32_t off_hi = swz128((uint32_t)(r * 128 + (c0 + e) * 2));
-      const uint32_t off_lo = swz128((uint32_t)((r + 64) * 128 + (c0 + e) * 2));
-      *reinterpret_cast<uint4*>(xw + off_hi) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-      *reinterpret_cast<uint4*>(xw + off_lo) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-      *reinterpret_cast<uint4*>(xu + off_hi) = make_uint4(uhi[0], uhi[1], uhi[2], uhi[3]);
-      *reinterpret_cast<uint4*>(xu + off_lo) = make_uint4(ulo[0], ulo[1], ulo[2], ulo[3]);
+      const uint32_t o_hi = swz128((uint32_t)(stacked_row(i, 0) * 128 + c8 * 2));
+      const uint32_t o_lo = swz128((uint32_t)(stacked_row(i, 1) * 128 + c8 * 2));
+      *reinterpret_cast<uint4*>(xw + o_hi) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+      *reinterpret_cast<uint4*>(xw + o_lo) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+      *reinterpret_cast<uint4*>(xu + o_hi) = make_uint4(uhi[0], uhi[1], uhi[2], uhi[3]);
+      *reinterpret_cast<uint4*>(xu + o_lo) = make_uint4(ulo[0], ulo[1], ulo[2], ulo[3]);
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   fence_before();
   __syncthreads();
 
-  // ---- MMA 2/3: D_W = [X'hi; X'lo] k (cols 0-127), D_U = [Xhi; Xlo] v (cols 128-255) --
+  // ---- MMA 2/3: D_W = XW k (TMEM cols 0-127), D_U = XU v (cols 128-255) ----------
   if (ok && tid == 0) {
     fence_after();
     const uint32_t id = idesc_bf16(128, 128, 0, 1);
-    const uint32_t xw = smem_u32(sm + OFF_L), xu = smem_u32(sm + OFF_X);
+    const uint32_t xw = smem_u32(sm + OFF_L), xu = smem_u32(sm + OFF_XU);
     const uint32_t kb = smem_u32(sm + OFF_K0), vb = smem_u32(sm + OFF_V0);
 #pragma unroll
     for (int s = 0; s < C / 16; ++s) {
@@ -386,77 +473,75 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     umma_commit(bar_mma);
   }
-  // Per-row factors of the state pass, while the MMAs run.
-  {
-    float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
-    const float gl = G[C - 1];
-    if (tid < C) {
-      vec[tid] = p.scale * nq[tid] * __expf(G[tid]);
-      vec[C + tid] = bb[tid] * nk[tid] * __expf(gl - G[tid]);
-    }
-    vec[2 * C + tid] = __expf(gl);
-  }
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 1));
   if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
   fence_after();
 
-  // ---- epilogue 2: W = D_W[0:64] + D_W[64:128], U = D_U[0:64] + D_U[64:128] ------
-  // Warps 2-3 hand their W halves to warps 0-1 through shared memory; warps 0-1
-  // hand their U halves to warps 2-3.
-  float* xch_w = reinterpret_cast<float*>(sm + OFF_XCH_W);
-  float* xch_u = reinterpret_cast<float*>(sm + OFF_XCH_U);
-  const int r = tid & 63;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  // ---- epilogue 2: W = hi + lo rows, U likewise; -W hi/lo and U staged in smem ----
+  // Lane t < 16 of warp w holds the hi product of row r = 16 w + t, lane t + 16
+  // the lo product of the same row: one shuffle per value sums them, after which
+  // lane t keeps columns [0,16) and lane t + 16 columns [16,32) of each 32-block.
+  __nv_bfloat16* ws_hi = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WS);
+  __nv_bfloat16* ws_lo = ws_hi + 64 * LDWS;
+  float* us = reinterpret_cast<float*>(sm + OFF_US);
   if (ok) {
+    const int r = 16 * warp + (lane & 15);
+    const int half = lane >> 4;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int blk = 0; blk < 8; ++blk) {
+      const bool is_u = blk >= 4;
+      const int cc = blk & 3;
       float v[32];
-      tmem_ld32(tmem + lane_base + (tid < 64 ? 128 : 0) + cc * 32, v);
-      float* dst = (tid < 64 ? xch_u : xch_w) + r * 128 + cc * 32;
+      tmem_ld32(tmem + lane_base + (is_u ? 128 : 0) + cc * 32, v);
+      float s[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-    }
-  }
-  fence_before();
-  __syncthreads();
-  if (ok) {
-    __nv_bfloat16* w2 = reinterpret_cast<__nv_bfloat16*>(slab + Slab::W2);
-    float* u = reinterpret_cast<float*>(slab + Slab::U);
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      float v[32];
-      tmem_ld32(tmem + lane_base + (tid < 64 ? 0 : 128) + cc * 32, v);
-      const float* other = (tid < 64 ? xch_w : xch_u) + r * 128 + cc * 32;
-      if (tid < 64) {
+      for (int e = 0; e < 16; ++e) {
+        const float send = half ? v[e] : v[16 + e];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        s[e] = (half ? v[16 + e] : v[e]) + recv;
+      }
+      const int c0 = cc * 32 + half * 16;
+      if (!is_u) {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int f = 0; f < 8; f += 2) {
-            const float w0 = -(v[e + f] + other[e + f]);
-            const float w1 = -(v[e + f + 1] + other[e + f + 1]);
-            __nv_bfloat162 hb = __floats2bfloat162_rn(w0, w1);
-            const float2 hf = __bfloat1622float2(hb);
-            hi[f / 2] = *reinterpret_cast<uint32_t*>(&hb);
-            lo[f / 2] = pack_bf16(w0 - hf.x, w1 - hf.y);
-          }
-          const int c = cc * 32 + e;
-          *reinterpret_cast<uint4*>(w2 + r * K + c) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(w2 + C * K + r * K + c) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int e = 0; e < 16; e += 2) {
+          const float w0 = -s[e], w1 = -s[e + 1];
+          __nv_bfloat162 hb = __floats2bfloat162_rn(w0, w1);
+          const float2 hf = __bfloat1622float2(hb);
+          hi[e / 2] = *reinterpret_cast<uint32_t*>(&hb);
+          lo[e / 2] = pack_bf16(w0 - hf.x, w1 - hf.y);
         }
+        *reinterpret_cast<uint4*>(ws_hi + r * LDWS + c0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(ws_hi + r * LDWS + c0 + 8) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        *reinterpret_cast<uint4*>(ws_lo + r * LDWS + c0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(ws_lo + r * LDWS + c0 + 8) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 s4 = make_float4(v[e] + other[e], v[e + 1] + other[e + 1],
-                                        v[e + 2] + other[e + 2], v[e + 3] + other[e + 3]);
-          *reinterpret_cast<float4*>(u + r * V + cc * 32 + e) = s4;
-        }
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(us + r * LDUS + c0 + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
       }
     }
   }
   fence_before();
   __syncthreads();
+  // Coalesced copy-out of the staged -W (hi, lo) and U rows into the slab.
+  {
+    __nv_bfloat16* w2 = reinterpret_cast<__nv_bfloat16*>(slab + Slab::W2);
+    float* u = reinterpret_cast<float*>(slab + Slab::U);
+#pragma unroll 4
+    for (int idx = tid; idx < 2 * C * (K / 8); idx += THREADS) {
+      const int half = idx / (C * K / 8), rem = idx % (C * K / 8);
+      const int r = rem >> 4, c8 = (rem & 15) * 8;
+      *reinterpret_cast<uint4*>(w2 + half * C * K + r * K + c8) =
+          *reinterpret_cast<const uint4*>(ws_hi + half * 64 * LDWS + r * LDWS + c8);
+    }
+#pragma unroll 4
+    for (int idx = tid; idx < C * (V / 4); idx += THREADS) {
+      const int r = idx >> 5, c4 = (idx & 31) * 4;
+      *reinterpret_cast<float4*>(u + r * V + c4) = *reinterpret_cast<const float4*>(us + r * LDUS + c4);
+    }
+  }
   if (warp == 0) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
