@@ -1,6 +1,6 @@
 // gdr_state.cu -- inter-chunk state recurrence of the fast path.
 //
-// One CTA per (batch b, value head hv, 16-column V tile), 4 warps, serial over
+// One CTA per (batch b, value head hv, 16-column V tile), 8 warps, serial over
 // the chunks of the sequence. Per chunk n it applies the inter-chunk loop of
 // the "分块并行计算（Chunkwise）" notes (listing of the chunk 间递推 section):
 //     r   = U - W S
@@ -13,10 +13,13 @@
 //     o^T  = diag-scaled S^T q^T + r^T A_qk^T   (16 x 64)
 //     S^T <- gamma S^T + (kscale r)^T k    (16 x 128, K = 64)
 // The state S^T stays in fp32 registers for the whole sequence (each warp owns
-// 32 of its 128 key channels). Products run on the tensor cores with
+// 16 of its 128 key channels). Products run on the tensor cores with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate); an fp32-valued operand x is
 // fed as x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi), and the
 // lo * lo term is dropped, which keeps about 16 significant bits per product.
+// Every split term accumulates into its own register tile, so no chain of
+// dependent mma.sync is longer than one product's k-steps; two warps per SM
+// sub-partition hide the remaining latency.
 // The only exchanges are two shared-memory tiles per chunk (S^T and r^T) and
 // two CTA barriers. Chunk operands are staged in shared memory with cp.async,
 // one chunk ahead.
@@ -28,7 +31,8 @@ namespace gdr {
 namespace fast {
 namespace {
 
-constexpr int THREADS = 128;
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
 constexpr int LDW = K + 8;  // bf16 row stride of [*, 128] tiles (272 B: ldmatrix conflict-free)
 constexpr int LDA = C + 8;  // bf16 row stride of [*, 64] tiles (144 B)
 
@@ -40,10 +44,10 @@ struct Smem {
   __host__ __device__ static constexpr int stage_bytes(int gate) { return TILE_W * (2 + (gate ? 4 : 2)) + 2 * TILE_A; }
   // Small double-buffered part: U tile [64][16] fp32 and VEC.
   static constexpr int SMALL = C * VT * 4 + (2 * C + K) * 4;
-  // Exchange tiles: S^T hi/lo [16][136]; r^T, rho^T hi/lo [16][72]; o staging 4 x [16][16] fp32.
+  // Exchange tiles: S^T hi/lo [16][136]; r^T, rho^T hi/lo [16][72]; o staging 8 x [8][16] fp32.
   static constexpr int XS = 2 * VT * LDW * 2;
   static constexpr int XR = 4 * VT * LDA * 2;
-  static constexpr int XO = 4 * 16 * 16 * 4;
+  static constexpr int XO = WARPS * 8 * 16 * 4;
   __host__ __device__ static constexpr int total(int gate, int stages) {
     return stages * stage_bytes(gate) + 2 * SMALL + XS + XR + XO;
   }
@@ -228,16 +232,20 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
   __nv_bfloat16* xp_hi = xr_lo + VT * LDA;
   __nv_bfloat16* xp_lo = xp_hi + VT * LDA;
   sp += Smem::XR;
-  float* xo = reinterpret_cast<float*>(sp) + warp * 256;
+  float* xo = reinterpret_cast<float*>(sp) + warp * 128;
 
   const size_t seq = (size_t)b * p.HV + hv;
   const uint8_t* slabs = p.slabs + seq * p.N * p.slab_bytes;
 
-  // State S^T[v][c]: this warp owns c in [32 warp, 32 warp + 32), 4 n-tiles of 8.
-  float S[4][4];
+  // Warp roles per chunk: r^T and o^T columns j, i in [8 warp, 8 warp + 8);
+  // S^T key channels c in [16 warp, 16 warp + 16) (two n-tiles of 8).
+  const int jw = 8 * warp, cw = 16 * warp;
+
+  // State S^T[v][c] (fp32) of this warp's channels.
+  float S[2][4];
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int c = 32 * warp + 8 * nt + 2 * t4;
+  for (int nt = 0; nt < 2; ++nt) {
+    const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int vv = g + (e >> 1) * 8, cc = c + (e & 1);
@@ -257,16 +265,24 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
     load_group2(st0, slabs, tid);
   }
 
+  // ldmatrix lane addressing.
+  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;   // A fragments (16 rows)
+  const int acol = (lane >> 4) * 8;
+  const int brow = (lane & 7);                           // B from [n][k] tiles, 2 k-steps per x4
+  const int bcol = (lane >> 3) * 8;
+  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // B from the [j][c] k tile (.trans)
+  const int kcol = cw + (lane >> 4) * 8;
+
   for (int n = 0; n < p.N; ++n) {
     const uint8_t* slab = slabs + (size_t)n * p.slab_bytes;
     Stage<GATE> st(stage_at(n));
     Small sm(small_at(n));
     const int t0 = n * C;
 
-    // ---- A: publish this warp's S^T slice as bf16 hi/lo ----------------------
+    // ---- A: publish this warp's S^T slice as bf16 hi/lo -------------------------
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int c = 32 * warp + 8 * nt + 2 * t4;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int c = cw + 8 * nt + 2 * t4;
       uint32_t hi, lo;
       split_pair(S[nt][0], S[nt][1], hi, lo);
       *reinterpret_cast<uint32_t*>(xs_hi + g * LDW + c) = hi;
@@ -282,10 +298,10 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
     }
     __syncthreads();          // #1: S^T tiles and chunk-n operands visible to all
 
-    if (n + 1 < p.N) {
-      const uint8_t* nslab = slab + p.slab_bytes;
-      if constexpr (STAGES == 2) {
+    if constexpr (STAGES == 2) {
+      if (n + 1 < p.N) {
         // Both buffers of chunk n+1 were last read in chunk n-1, before barrier #1.
+        const uint8_t* nslab = slab + p.slab_bytes;
         Stage<GATE> nst(stage_at(n + 1));
         load_big<GATE>(p, nst, nslab, b, h, n + 1, tid);
         load_small(Small(small_at(n + 1)), nslab, v0, tid);
@@ -293,146 +309,134 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
       }
     }
 
-    // ---- B: r^T = U^T - S^T W^T (this warp: j in [16 warp, +16)), o part 1 ----
-    float R[2][4], O[2][4];
-#pragma unroll
-    for (int jt = 0; jt < 2; ++jt) {
-      const int j = 16 * warp + 8 * jt + 2 * t4;
-      R[jt][0] = sm.u[j * VT + g];
-      R[jt][1] = sm.u[(j + 1) * VT + g];
-      R[jt][2] = sm.u[j * VT + g + 8];
-      R[jt][3] = sm.u[(j + 1) * VT + g + 8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) O[jt][e] = 0.f;
-    }
+    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T q^T (one n-tile each) --------
+    float Rhh[4], Rlh[4], Rhl[4], Oh[4], Ol[4], Ox[4];
     {
-      const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int acol = (lane >> 4) * 8;
-      const int brow = 16 * warp + (lane & 7) + (lane >> 4) * 8;
-      const int bcol = ((lane >> 3) & 1) * 8;
+      const int j = jw + 2 * t4;
+      Rhh[0] = sm.u[j * VT + g];
+      Rhh[1] = sm.u[(j + 1) * VT + g];
+      Rhh[2] = sm.u[j * VT + g + 8];
+      Rhh[3] = sm.u[(j + 1) * VT + g + 8];
 #pragma unroll
-      for (int ks = 0; ks < K / 16; ++ks) {
-        uint32_t ah[4], al[4], wh[4], wl[4], qh[4];
-        ldsm_x4(ah, smem_u32(xs_hi + arow * LDW + 16 * ks + acol));
-        ldsm_x4(al, smem_u32(xs_lo + arow * LDW + 16 * ks + acol));
-        ldsm_x4(wh, smem_u32(st.w_hi + brow * LDW + 16 * ks + bcol));
-        ldsm_x4(wl, smem_u32(st.w_lo + brow * LDW + 16 * ks + bcol));
-        ldsm_x4(qh, smem_u32(st.q_hi + brow * LDW + 16 * ks + bcol));
+      for (int e = 0; e < 4; ++e) Rlh[e] = Rhl[e] = Oh[e] = Ol[e] = Ox[e] = 0.f;
+    }
 #pragma unroll
-        for (int jt = 0; jt < 2; ++jt) {
-          mma(R[jt], ah, wh[2 * jt], wh[2 * jt + 1]);
-          mma(R[jt], al, wh[2 * jt], wh[2 * jt + 1]);
-          mma(R[jt], ah, wl[2 * jt], wl[2 * jt + 1]);
-          mma(O[jt], ah, qh[2 * jt], qh[2 * jt + 1]);
-          mma(O[jt], al, qh[2 * jt], qh[2 * jt + 1]);
-        }
-        if (GATE) {
-          uint32_t ql[4];
-          ldsm_x4(ql, smem_u32(st.q_lo + brow * LDW + 16 * ks + bcol));
+    for (int ks = 0; ks < K / 16; ks += 2) {
+      uint32_t wh[4], wl[4], qh[4];
+      ldsm_x4(wh, smem_u32(st.w_hi + (jw + brow) * LDW + 16 * ks + bcol));
+      ldsm_x4(wl, smem_u32(st.w_lo + (jw + brow) * LDW + 16 * ks + bcol));
+      ldsm_x4(qh, smem_u32(st.q_hi + (jw + brow) * LDW + 16 * ks + bcol));
+      uint32_t ql[4];
+      if (GATE) ldsm_x4(ql, smem_u32(st.q_lo + (jw + brow) * LDW + 16 * ks + bcol));
 #pragma unroll
-          for (int jt = 0; jt < 2; ++jt) mma(O[jt], ah, ql[2 * jt], ql[2 * jt + 1]);
-        }
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t ah[4], al[4];
+        ldsm_x4(ah, smem_u32(xs_hi + arow * LDW + 16 * (ks + h2) + acol));
+        ldsm_x4(al, smem_u32(xs_lo + arow * LDW + 16 * (ks + h2) + acol));
+        mma(Rhh, ah, wh[2 * h2], wh[2 * h2 + 1]);
+        mma(Rlh, al, wh[2 * h2], wh[2 * h2 + 1]);
+        mma(Rhl, ah, wl[2 * h2], wl[2 * h2 + 1]);
+        mma(Oh, ah, qh[2 * h2], qh[2 * h2 + 1]);
+        mma(Ol, al, qh[2 * h2], qh[2 * h2 + 1]);
+        if (GATE) mma(Ox, ah, ql[2 * h2], ql[2 * h2 + 1]);
       }
     }
 
-    // ---- C: publish r^T and rho^T = r^T diag(kscale) slices; scale o part 1 ----
+    // ---- C: publish r^T and rho^T = r^T diag(kscale); scale o part 1 -------------
+    float O[4];
+    {
+      const int j = jw + 2 * t4;
+      float R[4];
 #pragma unroll
-    for (int jt = 0; jt < 2; ++jt) {
-      const int j = 16 * warp + 8 * jt + 2 * t4;
+      for (int e = 0; e < 4; ++e) R[e] = Rhh[e] + (Rlh[e] + Rhl[e]);
       uint32_t hi, lo;
-      split_pair(R[jt][0], R[jt][1], hi, lo);
+      split_pair(R[0], R[1], hi, lo);
       *reinterpret_cast<uint32_t*>(xr_hi + g * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xr_lo + g * LDA + j) = lo;
-      split_pair(R[jt][2], R[jt][3], hi, lo);
+      split_pair(R[2], R[3], hi, lo);
       *reinterpret_cast<uint32_t*>(xr_hi + (g + 8) * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xr_lo + (g + 8) * LDA + j) = lo;
       const float k0 = sm.ks[j], k1 = sm.ks[j + 1];
-      split_pair(R[jt][0] * k0, R[jt][1] * k1, hi, lo);
+      split_pair(R[0] * k0, R[1] * k1, hi, lo);
       *reinterpret_cast<uint32_t*>(xp_hi + g * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xp_lo + g * LDA + j) = lo;
-      split_pair(R[jt][2] * k0, R[jt][3] * k1, hi, lo);
+      split_pair(R[2] * k0, R[3] * k1, hi, lo);
       *reinterpret_cast<uint32_t*>(xp_hi + (g + 8) * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
       const float q0 = sm.qs[j], q1 = sm.qs[j + 1];
-      O[jt][0] *= q0;
-      O[jt][1] *= q1;
-      O[jt][2] *= q0;
-      O[jt][3] *= q1;
+      O[0] = (Oh[0] + (Ol[0] + Ox[0])) * q0;
+      O[1] = (Oh[1] + (Ol[1] + Ox[1])) * q1;
+      O[2] = (Oh[2] + (Ol[2] + Ox[2])) * q0;
+      O[3] = (Oh[3] + (Ol[3] + Ox[3])) * q1;
     }
     if constexpr (STAGES == 1) cp_wait<0>();  // group 2 (K, A_qk) of chunk n landed
-    __syncthreads();                // #2: r^T / rho^T tiles visible
+    __syncthreads();                           // #2: r^T / rho^T tiles visible
 
-    // ---- D: S^T = gamma S^T + rho^T k (this warp: c in [32 warp, +32)), o part 2 ----
+    // ---- D: S^T = gamma S^T + rho^T k (channels of this warp), o^T part 2 -----------
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int c = 32 * warp + 8 * nt + 2 * t4;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int c = cw + 8 * nt + 2 * t4;
       const float g0 = sm.gam[c], g1 = sm.gam[c + 1];
       S[nt][0] *= g0;
       S[nt][1] *= g1;
       S[nt][2] *= g0;
       S[nt][3] *= g1;
     }
-    {
-      const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int acol = (lane >> 4) * 8;
-      // k stored [j][c]: .trans gives the col-major B fragment (k = j, n = c).
-      const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int kcol = 32 * warp + (lane >> 4) * 8;
-      // A_qk stored [i][j]: plain ldmatrix gives B (k = j, n = i).
-      const int brow = 16 * warp + (lane & 7) + (lane >> 4) * 8;
-      const int bcol = ((lane >> 3) & 1) * 8;
+    float Dl[2][4], Dx[2][4], Phh[4], Plh[4], Phl[4];
 #pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) {
-        uint32_t ph[4], pl[4], rh[4], rl[4], k01[4], k23[4], ah[4], al[4];
-        ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * ks + acol));
-        ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
-        ldsm_x4_t(k01, smem_u32(st.k_hi + (16 * ks + krow) * LDW + kcol));
-        ldsm_x4_t(k23, smem_u32(st.k_hi + (16 * ks + krow) * LDW + kcol + 16));
-        mma(S[0], ph, k01[0], k01[1]);
-        mma(S[1], ph, k01[2], k01[3]);
-        mma(S[2], ph, k23[0], k23[1]);
-        mma(S[3], ph, k23[2], k23[3]);
-        mma(S[0], pl, k01[0], k01[1]);
-        mma(S[1], pl, k01[2], k01[3]);
-        mma(S[2], pl, k23[0], k23[1]);
-        mma(S[3], pl, k23[2], k23[3]);
-        if (GATE) {
-          uint32_t l01[4], l23[4];
-          ldsm_x4_t(l01, smem_u32(st.k_lo + (16 * ks + krow) * LDW + kcol));
-          ldsm_x4_t(l23, smem_u32(st.k_lo + (16 * ks + krow) * LDW + kcol + 16));
-          mma(S[0], ph, l01[0], l01[1]);
-          mma(S[1], ph, l01[2], l01[3]);
-          mma(S[2], ph, l23[0], l23[1]);
-          mma(S[3], ph, l23[2], l23[3]);
-        }
-        ldsm_x4(rh, smem_u32(xr_hi + arow * LDA + 16 * ks + acol));
-        ldsm_x4(rl, smem_u32(xr_lo + arow * LDA + 16 * ks + acol));
-        ldsm_x4(ah, smem_u32(st.aq_hi + brow * LDA + 16 * ks + bcol));
-        ldsm_x4(al, smem_u32(st.aq_lo + brow * LDA + 16 * ks + bcol));
+    for (int e = 0; e < 4; ++e) {
+      Dl[0][e] = Dl[1][e] = Dx[0][e] = Dx[1][e] = 0.f;
+      Phh[e] = Plh[e] = Phl[e] = 0.f;
+    }
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-          mma(O[it], rh, ah[2 * it], ah[2 * it + 1]);
-          mma(O[it], rl, ah[2 * it], ah[2 * it + 1]);
-          mma(O[it], rh, al[2 * it], al[2 * it + 1]);
-        }
+    for (int ks = 0; ks < C / 16; ++ks) {
+      uint32_t ph[4], pl[4], kh[4];
+      ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * ks + acol));
+      ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
+      ldsm_x4_t(kh, smem_u32(st.k_hi + (16 * ks + krow) * LDW + kcol));
+      mma(S[0], ph, kh[0], kh[1]);
+      mma(S[1], ph, kh[2], kh[3]);
+      mma(Dl[0], pl, kh[0], kh[1]);
+      mma(Dl[1], pl, kh[2], kh[3]);
+      if (GATE) {
+        uint32_t kl[4];
+        ldsm_x4_t(kl, smem_u32(st.k_lo + (16 * ks + krow) * LDW + kcol));
+        mma(Dx[0], ph, kl[0], kl[1]);
+        mma(Dx[1], ph, kl[2], kl[3]);
       }
     }
-
-    // ---- E: o rows of this warp (i in [16 warp, +16)) -> global -------------------
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
-      const int i = 8 * it + 2 * t4;
-      xo[i * 16 + g] = O[it][0];
-      xo[(i + 1) * 16 + g] = O[it][1];
-      xo[i * 16 + g + 8] = O[it][2];
-      xo[(i + 1) * 16 + g + 8] = O[it][3];
+    for (int ks = 0; ks < C / 16; ks += 2) {
+      uint32_t ah[4], al[4];
+      ldsm_x4(ah, smem_u32(st.aq_hi + (jw + brow) * LDA + 16 * ks + bcol));
+      ldsm_x4(al, smem_u32(st.aq_lo + (jw + brow) * LDA + 16 * ks + bcol));
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t rh[4], rl[4];
+        ldsm_x4(rh, smem_u32(xr_hi + arow * LDA + 16 * (ks + h2) + acol));
+        ldsm_x4(rl, smem_u32(xr_lo + arow * LDA + 16 * (ks + h2) + acol));
+        mma(Phh, rh, ah[2 * h2], ah[2 * h2 + 1]);
+        mma(Plh, rl, ah[2 * h2], ah[2 * h2 + 1]);
+        mma(Phl, rh, al[2 * h2], al[2 * h2 + 1]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S[nt][e] += Dl[nt][e] + Dx[nt][e];
+
+    // ---- E: o rows of this warp (i in [8 warp, +8)) -> global -------------------
+    {
+      const int i = 2 * t4;
+      xo[i * 16 + g] = O[0] + (Phh[0] + (Plh[0] + Phl[0]));
+      xo[(i + 1) * 16 + g] = O[1] + (Phh[1] + (Plh[1] + Phl[1]));
+      xo[i * 16 + g + 8] = O[2] + (Phh[2] + (Plh[2] + Phl[2]));
+      xo[(i + 1) * 16 + g + 8] = O[3] + (Phh[3] + (Plh[3] + Phl[3]));
     }
     __syncwarp();
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int idx = lane + 32 * rep;           // 16 rows x 4 float4
-      const int i = idx >> 2, c4 = (idx & 3) * 4;
-      const int t = t0 + 16 * warp + i;
+    {
+      const int i = lane >> 2, c4 = (lane & 3) * 4;   // 8 rows x 4 float4
+      const int t = t0 + jw + i;
       if (t < p.T) {
         const float4 val = *reinterpret_cast<const float4*>(xo + i * 16 + c4);
         const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0 + c4;
@@ -463,8 +467,8 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
 
   if (p.sT) {
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int c = 32 * warp + 8 * nt + 2 * t4;
+    for (int nt = 0; nt < 2; ++nt) {
+      const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int vv = g + (e >> 1) * 8, cc = c + (e & 1);
