@@ -31,8 +31,10 @@ EXPORTED = (
     "gdr_chunk_fwd", "gdr_chunk_prepare", "gdr_chunk_recur", "gdr_chunk_fwd_workspace_size",
     "gdr_chunk_fwd_host",
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
-    "gdr_chunk_fwd_path", "gdr_version",
+    "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc",
 )
+# Size of the library-owned scratch used by gdr_chunk_fwd_noalloc (per device).
+GDR_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class GdrError(RuntimeError):
@@ -68,6 +70,8 @@ def load_library(path: Optional[str] = None):
         lib.gdr_chunk_fwd.restype = ip
         lib.gdr_chunk_fwd_host.argtypes = fwd_args
         lib.gdr_chunk_fwd_host.restype = ip
+        lib.gdr_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ip, fp, ip, ip, vp, vp, dp, vp]
+        lib.gdr_chunk_fwd_noalloc.restype = ip
         lib.gdr_chunk_prepare.argtypes = [vp, vp, vp, vp, vp, ip, fp, ip, ip, dp, vp, sz, vp]
         lib.gdr_chunk_prepare.restype = ip
         lib.gdr_chunk_recur.argtypes = [vp, vp, vp, ip, fp, ip, ip, vp, vp, dp, vp, sz, vp]
@@ -207,6 +211,25 @@ def chunk_recur(q, k, initial_state=None, *, workspace, out, final_state=None, H
         _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream_handle(stream))
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_recur")
+    return out, final_state
+
+
+def chunk_fwd_noalloc(q, k, v, g, beta, initial_state=None, *, out, final_state=None,
+                      chunk_size: int = 64, scale: Optional[float] = None,
+                      use_qk_l2norm: bool = True, stream=None):
+    """chunk_fwd on the library's own fixed scratch (no workspace is passed or
+    allocated). For callers that cannot provide device memory; limited to
+    problems whose workspace fits GDR_NOALLOC_SCRATCH_BYTES. Calls on one device
+    share that scratch, so they must not overlap on the GPU."""
+    B, T, H, HV, K, V, gate_mode = _shapes(q, v, g)
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out.dtype))
+    st = load_library().gdr_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), int(chunk_size),
+        ctypes.c_float(scale), int(bool(use_qk_l2norm)), gate_mode, _ptr(out), _ptr(final_state),
+        ctypes.byref(dims), _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_chunk_fwd_noalloc")
     return out, final_state
 
 

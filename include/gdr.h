@@ -171,6 +171,40 @@ size_t gdr_chunk_fwd_host_buffer_size(const gdr_dims* dims, int chunk_size, int 
  */
 gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace);
 
+/*
+ * gdr_chunk_fwd_noalloc -- gdr_chunk_fwd without a caller workspace.
+ *
+ * There is no counterpart of this entry point in the method's sources; it
+ * exists for callers that cannot hand the library a device buffer. Examples:
+ * code that runs under an allocator other than CUDA's (or none), plug-ins that
+ * must not touch the device heap, and callers in a region where cudaMalloc is
+ * not allowed (it synchronises the device and is illegal while a stream is
+ * being captured). Such callers still pass their inputs and outputs; the
+ * scratch space comes from a fixed array in device global memory owned by the
+ * library: GDR_NOALLOC_SCRATCH_BYTES per device that loads the library, held
+ * until the process exits. Neither this call nor anything it calls allocates
+ * or frees memory.
+ *
+ * Arguments, layouts and errors are those of gdr_chunk_fwd, minus the
+ * workspace. Sizes whose gdr_chunk_fwd_workspace_size() exceeds
+ * GDR_NOALLOC_SCRATCH_BYTES are rejected with GDR_ERR_WORKSPACE before
+ * anything is enqueued (64 MiB fits, for example, B=1, T=4096, 12 value heads,
+ * K=V=128, C=64).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. All calls on a device share the one array, which keeps whatever
+ * the last call left in it (each call rewrites everything it reads, and clears
+ * the error word itself). Calls that can overlap on the GPU (different streams
+ * without ordering) race on the array and must not be issued.
+ */
+#define GDR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* initial_state, int chunk_size,
+                                 float scale, int use_qk_l2norm, int gate_mode, void* out,
+                                 float* final_state, const gdr_dims* dims, gdr_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status s);
 
