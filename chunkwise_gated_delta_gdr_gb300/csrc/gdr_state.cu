@@ -9,239 +9,164 @@
 // in the transposed form, so that every product has the 16 value columns of
 // the tile as its M dimension and each accumulator can feed the next product
 // straight from registers:
-//     r^T  = U^T - S^T W^T                 (16 x 64,  K = 128)
+//     r^T  = U^T - S^T W^T                      (16 x 64,  K = 128)
 //     o^T  = diag-scaled S^T q^T + r^T A_qk^T   (16 x 64)
-//     S^T <- gamma S^T + (kscale r)^T k    (16 x 128, K = 64)
+//     S^T <- gamma S^T + (kscale r)^T k         (16 x 128, K = 64)
 // The state S^T stays in fp32 registers for the whole sequence (each warp owns
 // 16 of its 128 key channels). Products run on the tensor cores with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate); an fp32-valued operand x is
 // fed as x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi), and the
 // lo * lo term is dropped, which keeps about 16 significant bits per product.
-// Every split term accumulates into its own register tile, so no chain of
-// dependent mma.sync is longer than one product's k-steps; two warps per SM
-// sub-partition hide the remaining latency.
-// The only exchanges are two shared-memory tiles per chunk (S^T and r^T) and
-// two CTA barriers. Chunk operands are staged in shared memory with cp.async,
-// one chunk ahead.
+// Every split term accumulates into its own register tile.
+//
+// Chunk operands arrive by TMA (128-byte swizzled tiles, read conflict-free
+// by ldmatrix), one chunk ahead, counted on mbarriers; the only per-chunk
+// exchanges are two shared-memory tiles (S^T and r^T) and two CTA barriers.
+#include <string.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "gdr_fast.cuh"
+#include "gdr_ptx.cuh"
 
 namespace gdr {
 namespace fast {
 namespace {
 
+using namespace ptx;
+
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
-constexpr int LDW = K + 8;  // bf16 row stride of [*, 128] tiles (272 B: ldmatrix conflict-free)
-constexpr int LDA = C + 8;  // bf16 row stride of [*, 64] tiles (144 B)
+constexpr int LDW = K + 8;   // bf16 row stride of the S^T exchange tiles (272 B)
+constexpr int LDA = C + 8;   // bf16 row stride of the r^T exchange tiles (144 B)
+constexpr long kWaitLimit = 1L << 24;
+constexpr unsigned int kErrStateWait = 4u;
 
-// Shared-memory plan (bytes). "Big" operand tiles are staged STAGES times.
-struct Smem {
-  static constexpr int TILE_W = C * LDW * 2;      // one [64][136] bf16 tile
-  static constexpr int TILE_A = C * LDA * 2;      // one [64][72] bf16 tile
-  // Per stage: W hi, W lo, Q (hi[, lo]), K (hi[, lo]), AQ hi, AQ lo.
-  __host__ __device__ static constexpr int stage_bytes(int gate) { return TILE_W * (2 + (gate ? 4 : 2)) + 2 * TILE_A; }
-  // Small double-buffered part: U tile [64][16] fp32 and VEC.
-  static constexpr int SMALL = C * VT * 4 + (2 * C + K) * 4;
-  // Exchange tiles: S^T hi/lo [16][136]; r^T, rho^T hi/lo [16][72]; o staging 8 x [8][16] fp32.
-  static constexpr int XS = 2 * VT * LDW * 2;
-  static constexpr int XR = 4 * VT * LDA * 2;
-  static constexpr int XO = WARPS * 8 * 16 * 4;
-  __host__ __device__ static constexpr int total(int gate, int stages) {
-    return stages * stage_bytes(gate) + 2 * SMALL + XS + XR + XO;
-  }
+// Operand tiles of one chunk, 1024-byte aligned, 128-byte swizzled. A
+// [64][128] bf16 tile is two 8 KB boxes (columns 0-63, 64-127).
+struct Big {
+  static constexpr int W_HI = 0, W_LO = 16384, Q_HI = 32768;
+  static constexpr int Q_LO_PK = 49152, K_LO_PK = 81920;   // per-key gate only
+  __host__ __device__ static constexpr int k_hi(int gate) { return gate ? 65536 : 49152; }
+  __host__ __device__ static constexpr int aq_hi(int gate) { return gate ? 98304 : 65536; }
+  __host__ __device__ static constexpr int aq_lo(int gate) { return aq_hi(gate) + 8192; }
+  __host__ __device__ static constexpr int bytes(int gate) { return aq_hi(gate) + 16384; }
+};
+// U tile [64][16] fp32 (unswizzled) and VEC, double-buffered.
+constexpr int SMALL_U = 0, SMALL_VEC = 4096, SMALL_BYTES = 5120;
+// Bytes a scalar-gate chunk brings in: W hi/lo, q, k, A_qk hi/lo, U tile, VEC.
+constexpr uint32_t kScalarChunkBytes = 32768 + 16384 + 16384 + 16384 + 4096 + 1024;
+// Per-key gate: group 1 = W hi/lo, q hi/lo, U tile, VEC; group 2 = k hi/lo, A_qk hi/lo.
+constexpr uint32_t kPerKeyGroup1Bytes = 32768 + 32768 + 4096 + 1024;
+constexpr uint32_t kPerKeyGroup2Bytes = 32768 + 16384;
+
+struct Layout {
+  int big, small, xs, xr, xo, bars, total;
+  __host__ __device__ constexpr Layout(int gate, int stages)
+      : big(0),
+        small(stages * Big::bytes(gate)),
+        xs(small + 2 * SMALL_BYTES),
+        xr(xs + 2 * 16 * LDW * 2),
+        xo(xr + 4 * 16 * LDA * 2),
+        bars(xo + WARPS * 8 * 16 * 4),
+        total(bars + 64 + 1024) {}
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
+// Byte address of element (r, c) (c a multiple of 8) of a swizzled bf16 tile
+// stored as 64-column boxes of 8 KB.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int c) {
+  return base + (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// D += A (16x16, row) * B (16x8, col), bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// bf16 pair (lo half = x) and the hi/lo split of an fp32 pair.
-__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& lo) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  float2 hf = __bfloat1622float2(h);
-  hi = *reinterpret_cast<uint32_t*>(&h);
-  lo = pack_bf16(x - hf.x, y - hf.y);
-}
-
-// Stage pointers inside the dynamic shared memory block.
-template <int GATE>
-struct Stage {
-  __nv_bfloat16 *w_hi, *w_lo, *q_hi, *q_lo, *k_hi, *k_lo, *aq_hi, *aq_lo;
-  __device__ Stage(uint8_t* base) {
-    uint8_t* p = base;
-    w_hi = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W;
-    w_lo = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W;
-    q_hi = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W;
-    if (GATE) { q_lo = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W; } else { q_lo = nullptr; }
-    k_hi = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W;
-    if (GATE) { k_lo = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_W; } else { k_lo = nullptr; }
-    aq_hi = reinterpret_cast<__nv_bfloat16*>(p); p += Smem::TILE_A;
-    aq_lo = reinterpret_cast<__nv_bfloat16*>(p);
-  }
+struct Maps {
+  CUtensorMap q, k, w2, aq2, u, qb2, kb2;
 };
-
-struct Small {
-  float* u;      // [64][16]
-  float* qs;     // [64]
-  float* ks;     // [64]
-  float* gam;    // [128]
-  __device__ Small(uint8_t* base) {
-    u = reinterpret_cast<float*>(base);
-    qs = u + C * VT;
-    ks = qs + C;
-    gam = ks + C;
-  }
-};
-
-// Copy a [64][128] bf16 tile whose rows are `row_stride` elements apart into a
-// [64][LDW] shared tile; rows >= valid_rows are zero-filled.
-__device__ __forceinline__ void load_tile128(__nv_bfloat16* dst, const __nv_bfloat16* src,
-                                             size_t row_stride, int valid_rows, int tid) {
-  for (int idx = tid; idx < C * (K / 8); idx += THREADS) {
-    const int r = idx >> 4, c8 = (idx & 15) * 8;
-    const bool ok = r < valid_rows;
-    const __nv_bfloat16* s = src + (ok ? (size_t)r * row_stride + c8 : 0);
-    cp_async16(smem_u32(dst + r * LDW + c8), s, ok);
-  }
-}
-__device__ __forceinline__ void load_tile64(__nv_bfloat16* dst, const __nv_bfloat16* src, int tid) {
-  for (int idx = tid; idx < C * (C / 8); idx += THREADS) {
-    const int r = idx >> 3, c8 = (idx & 7) * 8;
-    cp_async16(smem_u32(dst + r * LDA + c8), src + r * C + c8, true);
-  }
-}
-
-// Operands of chunk n from its slab (and, for the scalar gate, raw q / k).
-template <int GATE>
-__device__ __forceinline__ void load_big(const Params& p, const Stage<GATE>& st, const uint8_t* slab,
-                                         int b, int h, int n, int tid) {
-  const __nv_bfloat16* w2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::W2);
-  load_tile128(st.w_hi, w2, K, C, tid);
-  load_tile128(st.w_lo, w2 + C * K, K, C, tid);
-  if (GATE) {
-    const __nv_bfloat16* q2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::QB2);
-    const __nv_bfloat16* k2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::KB2);
-    load_tile128(st.q_hi, q2, K, C, tid);
-    load_tile128(st.q_lo, q2 + C * K, K, C, tid);
-    load_tile128(st.k_hi, k2, K, C, tid);
-    load_tile128(st.k_lo, k2 + C * K, K, C, tid);
-  } else {
-    const int t0 = n * C;
-    const int valid = min(C, p.T - t0);
-    const size_t rs = (size_t)p.H * K;
-    const size_t off = (((size_t)b * p.T + t0) * p.H + h) * K;
-    load_tile128(st.q_hi, p.q + off, rs, valid, tid);
-    load_tile128(st.k_hi, p.k + off, rs, valid, tid);
-  }
-  const __nv_bfloat16* aq = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::AQ2);
-  load_tile64(st.aq_hi, aq, tid);
-  load_tile64(st.aq_lo, aq + C * C, tid);
-}
-
-__device__ __forceinline__ void load_small(const Small& sm, const uint8_t* slab, int v0, int tid) {
-  const float* u = reinterpret_cast<const float*>(slab + Slab::U);
-  for (int idx = tid; idx < C * (VT / 4); idx += THREADS) {
-    const int r = idx / (VT / 4), c4 = (idx % (VT / 4)) * 4;
-    cp_async16(smem_u32(sm.u + r * VT + c4), u + r * V + v0 + c4, true);
-  }
-  const float* vec = reinterpret_cast<const float*>(slab + Slab::VEC);
-  for (int idx = tid; idx < (2 * C + K) / 4; idx += THREADS)
-    cp_async16(smem_u32(sm.qs + idx * 4), vec + idx * 4, true);
-}
-
-// Single-stage protocol (per-key gate): group 1 = W, Q and the small part,
-// group 2 = K and A_qk.
-__device__ __forceinline__ void load_group1(const Stage<1>& st, const Small& sm, const uint8_t* slab,
-                                            int v0, int tid) {
-  const __nv_bfloat16* w2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::W2);
-  load_tile128(st.w_hi, w2, K, C, tid);
-  load_tile128(st.w_lo, w2 + C * K, K, C, tid);
-  const __nv_bfloat16* q2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::QB2);
-  load_tile128(st.q_hi, q2, K, C, tid);
-  load_tile128(st.q_lo, q2 + C * K, K, C, tid);
-  load_small(sm, slab, v0, tid);
-  cp_commit();
-}
-__device__ __forceinline__ void load_group2(const Stage<1>& st, const uint8_t* slab, int tid) {
-  const __nv_bfloat16* k2 = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::KB2);
-  load_tile128(st.k_hi, k2, K, C, tid);
-  load_tile128(st.k_lo, k2 + C * K, K, C, tid);
-  const __nv_bfloat16* aq = reinterpret_cast<const __nv_bfloat16*>(slab + Slab::AQ2);
-  load_tile64(st.aq_hi, aq, tid);
-  load_tile64(st.aq_lo, aq + C * C, tid);
-  cp_commit();
-}
 
 template <int GATE, int STAGES>
-__global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ Maps maps, Params p) {
+  constexpr Layout LY(GATE, STAGES);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
   const int h = hv / (p.HV / p.H);
   const int v0 = vt * VT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
 
-  uint8_t* sp = smem;
-  uint8_t* const stage0 = sp;
-  sp += STAGES * Smem::stage_bytes(GATE);
-  uint8_t* const small0 = sp;
-  sp += 2 * Smem::SMALL;
-  auto stage_at = [&](int n) { return stage0 + (STAGES == 2 ? (n & 1) : 0) * Smem::stage_bytes(GATE); };
-  auto small_at = [&](int n) { return small0 + (n & 1) * Smem::SMALL; };
-  __nv_bfloat16* xs_hi = reinterpret_cast<__nv_bfloat16*>(sp);
-  __nv_bfloat16* xs_lo = xs_hi + VT * LDW;
-  sp += Smem::XS;
-  __nv_bfloat16* xr_hi = reinterpret_cast<__nv_bfloat16*>(sp);
-  __nv_bfloat16* xr_lo = xr_hi + VT * LDA;
-  __nv_bfloat16* xp_hi = xr_lo + VT * LDA;
-  __nv_bfloat16* xp_lo = xp_hi + VT * LDA;
-  sp += Smem::XR;
-  float* xo = reinterpret_cast<float*>(sp) + warp * 128;
+  __nv_bfloat16* xs_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY.xs);
+  __nv_bfloat16* xs_lo = xs_hi + 16 * LDW;
+  __nv_bfloat16* xr_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY.xr);
+  __nv_bfloat16* xr_lo = xr_hi + 16 * LDA;
+  __nv_bfloat16* xp_hi = xr_lo + 16 * LDA;
+  __nv_bfloat16* xp_lo = xp_hi + 16 * LDA;
+  float* xo = reinterpret_cast<float*>(sm + LY.xo) + warp * 128;
+  // Scalar gate: bars[s] = stage s. Per-key gate: bars[0] = group 1, bars[1] = group 2.
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY.bars);
 
   const size_t seq = (size_t)b * p.HV + hv;
-  const uint8_t* slabs = p.slabs + seq * p.N * p.slab_bytes;
+  const int chunk0 = (int)(seq * p.N);
+
+  auto big_at = [&](int n) { return sm + LY.big + (STAGES == 2 ? (n & 1) : 0) * Big::bytes(GATE); };
+  auto small_at = [&](int n) { return sm + LY.small + (n & 1) * SMALL_BYTES; };
+
+  // Loads of chunk n (issued by one thread). Scalar gate: everything on one
+  // barrier. Per-key gate: group 1 here, group 2 in issue_group2.
+  auto issue_group1 = [&](int n, uint64_t* bar) {
+    const int idx = chunk0 + n;
+    const uint32_t big = smem_u32(big_at(n));
+    const uint32_t small = smem_u32(small_at(n));
+    mbar_expect_tx(bar, GATE ? kPerKeyGroup1Bytes : kScalarChunkBytes);
+    tma_load3(big + Big::W_HI, &maps.w2, 0, 0, idx, bar);
+    tma_load3(big + Big::W_HI + 8192, &maps.w2, 64, 0, idx, bar);
+    tma_load3(big + Big::W_LO, &maps.w2, 0, 64, idx, bar);
+    tma_load3(big + Big::W_LO + 8192, &maps.w2, 64, 64, idx, bar);
+    if (GATE) {
+      tma_load3(big + Big::Q_HI, &maps.qb2, 0, 0, idx, bar);
+      tma_load3(big + Big::Q_HI + 8192, &maps.qb2, 64, 0, idx, bar);
+      tma_load3(big + Big::Q_LO_PK, &maps.qb2, 0, 64, idx, bar);
+      tma_load3(big + Big::Q_LO_PK + 8192, &maps.qb2, 64, 64, idx, bar);
+    } else {
+      const int t0 = n * C;
+      tma_load4(big + Big::Q_HI, &maps.q, 0, h, t0, b, bar);
+      tma_load4(big + Big::Q_HI + 8192, &maps.q, 64, h, t0, b, bar);
+      tma_load4(big + Big::k_hi(GATE), &maps.k, 0, h, t0, b, bar);
+      tma_load4(big + Big::k_hi(GATE) + 8192, &maps.k, 64, h, t0, b, bar);
+      tma_load3(big + Big::aq_hi(GATE), &maps.aq2, 0, 0, idx, bar);
+      tma_load3(big + Big::aq_lo(GATE), &maps.aq2, 0, 64, idx, bar);
+    }
+    tma_load3(small + SMALL_U, &maps.u, v0, 0, idx, bar);
+    bulk_load(small + SMALL_VEC, p.slabs + (size_t)idx * p.slab_bytes + Slab::VEC, 1024, bar);
+  };
+  auto issue_group2 = [&](int n, uint64_t* bar) {
+    const int idx = chunk0 + n;
+    const uint32_t big = smem_u32(big_at(n));
+    mbar_expect_tx(bar, kPerKeyGroup2Bytes);
+    tma_load3(big + Big::k_hi(GATE), &maps.kb2, 0, 0, idx, bar);
+    tma_load3(big + Big::k_hi(GATE) + 8192, &maps.kb2, 64, 0, idx, bar);
+    tma_load3(big + Big::K_LO_PK, &maps.kb2, 0, 64, idx, bar);
+    tma_load3(big + Big::K_LO_PK + 8192, &maps.kb2, 64, 64, idx, bar);
+    tma_load3(big + Big::aq_hi(GATE), &maps.aq2, 0, 0, idx, bar);
+    tma_load3(big + Big::aq_lo(GATE), &maps.aq2, 0, 64, idx, bar);
+  };
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    issue_group1(0, &bars[0]);
+    if (GATE) issue_group2(0, &bars[1]);
+  }
 
   // Warp roles per chunk: r^T and o^T columns j, i in [8 warp, 8 warp + 8);
   // S^T key channels c in [16 warp, 16 warp + 16) (two n-tiles of 8).
   const int jw = 8 * warp, cw = 16 * warp;
 
-  // State S^T[v][c] (fp32) of this warp's channels.
   float S[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
@@ -253,18 +178,6 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
     }
   }
 
-  // Prologue: the operands of chunk 0, in the groups the loop expects.
-  if constexpr (STAGES == 2) {
-    Stage<GATE> st0(stage_at(0));
-    load_big<GATE>(p, st0, slabs, b, h, 0, tid);
-    load_small(Small(small_at(0)), slabs, v0, tid);
-    cp_commit();
-  } else {
-    Stage<1> st0(stage_at(0));
-    load_group1(st0, Small(small_at(0)), slabs, v0, tid);
-    load_group2(st0, slabs, tid);
-  }
-
   // ldmatrix lane addressing.
   const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;   // A fragments (16 rows)
   const int acol = (lane >> 4) * 8;
@@ -272,11 +185,21 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
   const int bcol = (lane >> 3) * 8;
   const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // B from the [j][c] k tile (.trans)
   const int kcol = cw + (lane >> 4) * 8;
+  bool ok = true;
 
   for (int n = 0; n < p.N; ++n) {
-    const uint8_t* slab = slabs + (size_t)n * p.slab_bytes;
-    Stage<GATE> st(stage_at(n));
-    Small sm(small_at(n));
+    uint8_t* bigp = big_at(n);
+    const uint32_t w_hi = smem_u32(bigp + Big::W_HI), w_lo = smem_u32(bigp + Big::W_LO);
+    const uint32_t q_hi = smem_u32(bigp + Big::Q_HI);
+    const uint32_t q_lo = smem_u32(bigp + Big::Q_LO_PK);       // read only for the per-key gate
+    const uint32_t k_hi = smem_u32(bigp + Big::k_hi(GATE));
+    const uint32_t k_lo = smem_u32(bigp + Big::K_LO_PK);       // read only for the per-key gate
+    const uint32_t aq_hi = smem_u32(bigp + Big::aq_hi(GATE));
+    const uint32_t aq_lo = smem_u32(bigp + Big::aq_lo(GATE));
+    const float* su = reinterpret_cast<const float*>(small_at(n) + SMALL_U);
+    const float* qs = reinterpret_cast<const float*>(small_at(n) + SMALL_VEC);
+    const float* ks = qs + C;
+    const float* gam = ks + C;
     const int t0 = n * C;
 
     // ---- A: publish this warp's S^T slice as bf16 hi/lo -------------------------
@@ -291,54 +214,45 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
       *reinterpret_cast<uint32_t*>(xs_hi + (g + 8) * LDW + c) = hi;
       *reinterpret_cast<uint32_t*>(xs_lo + (g + 8) * LDW + c) = lo;
     }
-    if constexpr (STAGES == 2) {
-      cp_wait<0>();           // chunk n operands landed (this thread's copies)
-    } else {
-      cp_wait<1>();           // group 1 (W, Q, small part) of chunk n landed
-    }
-    __syncthreads();          // #1: S^T tiles and chunk-n operands visible to all
+    // Chunk n's operands (scalar gate) / first group (per-key gate).
+    const uint32_t par = STAGES == 2 ? ((n >> 1) & 1) : (n & 1);
+    ok = ok && mbar_wait(&bars[STAGES == 2 ? (n & 1) : 0], par, kWaitLimit);
+    __syncthreads();          // #1: S^T tiles visible; chunk n-1's tiles are free
 
-    if constexpr (STAGES == 2) {
-      if (n + 1 < p.N) {
-        // Both buffers of chunk n+1 were last read in chunk n-1, before barrier #1.
-        const uint8_t* nslab = slab + p.slab_bytes;
-        Stage<GATE> nst(stage_at(n + 1));
-        load_big<GATE>(p, nst, nslab, b, h, n + 1, tid);
-        load_small(Small(small_at(n + 1)), nslab, v0, tid);
-        cp_commit();
-      }
+    if (tid == 0) {
+      if (!ok) atomicOr(p.error_word, kErrStateWait);
+      if (STAGES == 2 && n + 1 < p.N) issue_group1(n + 1, &bars[(n + 1) & 1]);
     }
 
     // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T q^T (one n-tile each) --------
     float Rhh[4], Rlh[4], Rhl[4], Oh[4], Ol[4], Ox[4];
     {
       const int j = jw + 2 * t4;
-      Rhh[0] = sm.u[j * VT + g];
-      Rhh[1] = sm.u[(j + 1) * VT + g];
-      Rhh[2] = sm.u[j * VT + g + 8];
-      Rhh[3] = sm.u[(j + 1) * VT + g + 8];
+      Rhh[0] = su[j * VT + g];
+      Rhh[1] = su[(j + 1) * VT + g];
+      Rhh[2] = su[j * VT + g + 8];
+      Rhh[3] = su[(j + 1) * VT + g + 8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) Rlh[e] = Rhl[e] = Oh[e] = Ol[e] = Ox[e] = 0.f;
     }
 #pragma unroll
-    for (int ks = 0; ks < K / 16; ks += 2) {
-      uint32_t wh[4], wl[4], qh[4];
-      ldsm_x4(wh, smem_u32(st.w_hi + (jw + brow) * LDW + 16 * ks + bcol));
-      ldsm_x4(wl, smem_u32(st.w_lo + (jw + brow) * LDW + 16 * ks + bcol));
-      ldsm_x4(qh, smem_u32(st.q_hi + (jw + brow) * LDW + 16 * ks + bcol));
-      uint32_t ql[4];
-      if (GATE) ldsm_x4(ql, smem_u32(st.q_lo + (jw + brow) * LDW + 16 * ks + bcol));
+    for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
+      uint32_t wh[4], wl[4], qh[4], ql[4];
+      ldsm_x4(wh, tile_addr(w_hi, jw + brow, 16 * ks2 + bcol));
+      ldsm_x4(wl, tile_addr(w_lo, jw + brow, 16 * ks2 + bcol));
+      ldsm_x4(qh, tile_addr(q_hi, jw + brow, 16 * ks2 + bcol));
+      if (GATE) ldsm_x4(ql, tile_addr(q_lo, jw + brow, 16 * ks2 + bcol));
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t ah[4], al[4];
-        ldsm_x4(ah, smem_u32(xs_hi + arow * LDW + 16 * (ks + h2) + acol));
-        ldsm_x4(al, smem_u32(xs_lo + arow * LDW + 16 * (ks + h2) + acol));
-        mma(Rhh, ah, wh[2 * h2], wh[2 * h2 + 1]);
-        mma(Rlh, al, wh[2 * h2], wh[2 * h2 + 1]);
-        mma(Rhl, ah, wl[2 * h2], wl[2 * h2 + 1]);
-        mma(Oh, ah, qh[2 * h2], qh[2 * h2 + 1]);
-        mma(Ol, al, qh[2 * h2], qh[2 * h2 + 1]);
-        if (GATE) mma(Ox, ah, ql[2 * h2], ql[2 * h2 + 1]);
+        ldsm_x4(ah, smem_u32(xs_hi + arow * LDW + 16 * (ks2 + h2) + acol));
+        ldsm_x4(al, smem_u32(xs_lo + arow * LDW + 16 * (ks2 + h2) + acol));
+        mma_bf16_16816(Rhh, ah, wh[2 * h2], wh[2 * h2 + 1]);
+        mma_bf16_16816(Rlh, al, wh[2 * h2], wh[2 * h2 + 1]);
+        mma_bf16_16816(Rhl, ah, wl[2 * h2], wl[2 * h2 + 1]);
+        mma_bf16_16816(Oh, ah, qh[2 * h2], qh[2 * h2 + 1]);
+        mma_bf16_16816(Ol, al, qh[2 * h2], qh[2 * h2 + 1]);
+        if (GATE) mma_bf16_16816(Ox, ah, ql[2 * h2], ql[2 * h2 + 1]);
       }
     }
 
@@ -356,27 +270,27 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
       split_pair(R[2], R[3], hi, lo);
       *reinterpret_cast<uint32_t*>(xr_hi + (g + 8) * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xr_lo + (g + 8) * LDA + j) = lo;
-      const float k0 = sm.ks[j], k1 = sm.ks[j + 1];
+      const float k0 = ks[j], k1 = ks[j + 1];
       split_pair(R[0] * k0, R[1] * k1, hi, lo);
       *reinterpret_cast<uint32_t*>(xp_hi + g * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xp_lo + g * LDA + j) = lo;
       split_pair(R[2] * k0, R[3] * k1, hi, lo);
       *reinterpret_cast<uint32_t*>(xp_hi + (g + 8) * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
-      const float q0 = sm.qs[j], q1 = sm.qs[j + 1];
+      const float q0 = qs[j], q1 = qs[j + 1];
       O[0] = (Oh[0] + (Ol[0] + Ox[0])) * q0;
       O[1] = (Oh[1] + (Ol[1] + Ox[1])) * q1;
       O[2] = (Oh[2] + (Ol[2] + Ox[2])) * q0;
       O[3] = (Oh[3] + (Ol[3] + Ox[3])) * q1;
     }
-    if constexpr (STAGES == 1) cp_wait<0>();  // group 2 (K, A_qk) of chunk n landed
+    if (GATE) ok = ok && mbar_wait(&bars[1], n & 1, kWaitLimit);   // k, A_qk of chunk n
     __syncthreads();                           // #2: r^T / rho^T tiles visible
 
     // ---- D: S^T = gamma S^T + rho^T k (channels of this warp), o^T part 2 -----------
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int c = cw + 8 * nt + 2 * t4;
-      const float g0 = sm.gam[c], g1 = sm.gam[c + 1];
+      const float g0 = gam[c], g1 = gam[c + 1];
       S[nt][0] *= g0;
       S[nt][1] *= g1;
       S[nt][2] *= g0;
@@ -393,31 +307,31 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
       uint32_t ph[4], pl[4], kh[4];
       ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * ks + acol));
       ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
-      ldsm_x4_t(kh, smem_u32(st.k_hi + (16 * ks + krow) * LDW + kcol));
-      mma(S[0], ph, kh[0], kh[1]);
-      mma(S[1], ph, kh[2], kh[3]);
-      mma(Dl[0], pl, kh[0], kh[1]);
-      mma(Dl[1], pl, kh[2], kh[3]);
+      ldsm_x4_t(kh, tile_addr(k_hi, 16 * ks + krow, kcol));
+      mma_bf16_16816(S[0], ph, kh[0], kh[1]);
+      mma_bf16_16816(S[1], ph, kh[2], kh[3]);
+      mma_bf16_16816(Dl[0], pl, kh[0], kh[1]);
+      mma_bf16_16816(Dl[1], pl, kh[2], kh[3]);
       if (GATE) {
         uint32_t kl[4];
-        ldsm_x4_t(kl, smem_u32(st.k_lo + (16 * ks + krow) * LDW + kcol));
-        mma(Dx[0], ph, kl[0], kl[1]);
-        mma(Dx[1], ph, kl[2], kl[3]);
+        ldsm_x4_t(kl, tile_addr(k_lo, 16 * ks + krow, kcol));
+        mma_bf16_16816(Dx[0], ph, kl[0], kl[1]);
+        mma_bf16_16816(Dx[1], ph, kl[2], kl[3]);
       }
     }
 #pragma unroll
-    for (int ks = 0; ks < C / 16; ks += 2) {
+    for (int ks2 = 0; ks2 < C / 16; ks2 += 2) {
       uint32_t ah[4], al[4];
-      ldsm_x4(ah, smem_u32(st.aq_hi + (jw + brow) * LDA + 16 * ks + bcol));
-      ldsm_x4(al, smem_u32(st.aq_lo + (jw + brow) * LDA + 16 * ks + bcol));
+      ldsm_x4(ah, tile_addr(aq_hi, jw + brow, 16 * ks2 + bcol));
+      ldsm_x4(al, tile_addr(aq_lo, jw + brow, 16 * ks2 + bcol));
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t rh[4], rl[4];
-        ldsm_x4(rh, smem_u32(xr_hi + arow * LDA + 16 * (ks + h2) + acol));
-        ldsm_x4(rl, smem_u32(xr_lo + arow * LDA + 16 * (ks + h2) + acol));
-        mma(Phh, rh, ah[2 * h2], ah[2 * h2 + 1]);
-        mma(Plh, rl, ah[2 * h2], ah[2 * h2 + 1]);
-        mma(Phl, rh, al[2 * h2], al[2 * h2 + 1]);
+        ldsm_x4(rh, smem_u32(xr_hi + arow * LDA + 16 * (ks2 + h2) + acol));
+        ldsm_x4(rl, smem_u32(xr_lo + arow * LDA + 16 * (ks2 + h2) + acol));
+        mma_bf16_16816(Phh, rh, ah[2 * h2], ah[2 * h2 + 1]);
+        mma_bf16_16816(Plh, rl, ah[2 * h2], ah[2 * h2 + 1]);
+        mma_bf16_16816(Phl, rh, al[2 * h2], al[2 * h2 + 1]);
       }
     }
 #pragma unroll
@@ -452,15 +366,13 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
     }
     __syncwarp();
 
-    if constexpr (STAGES == 1) {
-      if (n + 1 < p.N) {
-        // Every warp must be done with this chunk's tiles before they are
-        // overwritten: a CTA barrier, then the next chunk in two groups.
-        __syncthreads();
-        const uint8_t* nslab = slab + p.slab_bytes;
-        Stage<1> nst(stage_at(n + 1));
-        load_group1(nst, Small(small_at(n + 1)), nslab, v0, tid);
-        load_group2(nst, nslab, tid);
+    if (STAGES == 1 && n + 1 < p.N) {
+      // Single stage: every warp must be done with this chunk's tiles before
+      // the next chunk's loads overwrite them.
+      __syncthreads();
+      if (tid == 0) {
+        issue_group1(n + 1, &bars[0]);
+        issue_group2(n + 1, &bars[1]);
       }
     }
   }
@@ -478,14 +390,75 @@ __global__ void __launch_bounds__(THREADS) state_kernel(Params p) {
   }
 }
 
+// ---------------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapSwizzle swz) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(map, type, rank, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Slab array viewed as [nchunks][rows][cols] of `esize`-byte elements.
+bool encode_slab(CUtensorMap* map, const Params& p, size_t offset, CUtensorMapDataType type,
+                 int esize, int cols, int rows, int box_cols, CUtensorMapSwizzle swz) {
+  const cuuint64_t nch = (cuuint64_t)p.B * p.HV * p.N;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, nch};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * esize, (cuuint64_t)p.slab_bytes};
+  const cuuint32_t box[3] = {(cuuint32_t)box_cols, 64, 1};
+  return encode(map, type, 3, p.slabs + offset, dims, strides, box, swz);
+}
+
+bool encode_bthd(CUtensorMap* map, const void* base, int B, int T, int heads) {
+  const cuuint64_t dims[4] = {128, (cuuint64_t)heads, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {128 * 2, (cuuint64_t)heads * 128 * 2,
+                                 (cuuint64_t)T * heads * 128 * 2};
+  const cuuint32_t box[4] = {64, 1, 64, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 template <int GATE, int STAGES>
 gdr_status launch_one(const Params& p, cudaStream_t stream) {
-  const int smem = Smem::total(GATE, STAGES);
+  Maps m;
+  memset(&m, 0, sizeof m);
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = encode_slab(&m.w2, p, Slab::W2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_slab(&m.aq2, p, Slab::AQ2, BF, 2, C, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_slab(&m.u, p, Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, VT,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (GATE) {
+    ok = ok && encode_slab(&m.qb2, p, Slab::QB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_slab(&m.kb2, p, Slab::KB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok = ok && encode_bthd(&m.q, p.q, p.B, p.T, p.H) && encode_bthd(&m.k, p.k, p.B, p.T, p.H);
+  }
+  if (!ok) return GDR_ERR_CUDA;
+  constexpr Layout LY(GATE, STAGES);
   auto kern = state_kernel<GATE, STAGES>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total) !=
+      cudaSuccess)
     return GDR_ERR_CUDA;
   dim3 grid(V / VT, p.HV, p.B);
-  kern<<<grid, THREADS, smem, stream>>>(p);
+  kern<<<grid, THREADS, LY.total, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
