@@ -37,10 +37,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int THREADS = 256;
-constexpr int WARPS = THREADS / 32;
 constexpr int LDW = K + 8;   // bf16 row stride of the S^T exchange tiles (272 B)
 constexpr int LDA = C + 8;   // bf16 row stride of the r^T exchange tiles (144 B)
+#ifndef STATE_WARPS
+#define STATE_WARPS 4
+#endif
 constexpr long kWaitLimit = 1L << 24;
 constexpr unsigned int kErrStateWait = 4u;
 
@@ -70,7 +71,7 @@ struct Layout {
         xs(small + 2 * SMALL_BYTES),
         xr(xs + 2 * 16 * LDW * 2),
         xo(xr + 4 * 16 * LDA * 2),
-        bars(xo + WARPS * 8 * 16 * 4),
+        bars(xo + C * 16 * 4),
         total(bars + 64 + 1024) {}
 };
 
@@ -84,9 +85,13 @@ struct Maps {
   CUtensorMap q, k, w2, aq2, u, qb2, kb2;
 };
 
-template <int GATE, int STAGES>
-__global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ Maps maps, Params p) {
+// WARPS warps split the per-chunk work: warp w produces JT 8-column tiles of
+// r^T and of o^T (j, i in [8 JT w, 8 JT (w + 1))) and owns CT 8-channel tiles
+// of the state (c in [8 CT w, 8 CT (w + 1))).
+template <int GATE, int STAGES, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant__ Maps maps, Params p) {
   constexpr Layout LY(GATE, STAGES);
+  constexpr int JT = C / 8 / WARPS, CT = K / 8 / WARPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
   __nv_bfloat16* xr_lo = xr_hi + 16 * LDA;
   __nv_bfloat16* xp_hi = xr_lo + 16 * LDA;
   __nv_bfloat16* xp_lo = xp_hi + 16 * LDA;
-  float* xo = reinterpret_cast<float*>(sm + LY.xo) + warp * 128;
+  float* xo = reinterpret_cast<float*>(sm + LY.xo) + warp * (8 * JT * 16);
   // Scalar gate: bars[s] = stage s. Per-key gate: bars[0] = group 1, bars[1] = group 2.
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY.bars);
 
@@ -163,13 +168,11 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
     if (GATE) issue_group2(0, &bars[1]);
   }
 
-  // Warp roles per chunk: r^T and o^T columns j, i in [8 warp, 8 warp + 8);
-  // S^T key channels c in [16 warp, 16 warp + 16) (two n-tiles of 8).
-  const int jw = 8 * warp, cw = 16 * warp;
+  const int jw = 8 * JT * warp, cw = 8 * CT * warp;
 
-  float S[2][4];
+  float S[CT][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < CT; ++nt) {
     const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
   const int brow = (lane & 7);                           // B from [n][k] tiles, 2 k-steps per x4
   const int bcol = (lane >> 3) * 8;
   const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // B from the [j][c] k tile (.trans)
-  const int kcol = cw + (lane >> 4) * 8;
+  const int kcol = cw + (lane >> 4) * 8;                 // two c-tiles per x4
   bool ok = true;
 
   for (int n = 0; n < p.N; ++n) {
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
 
     // ---- A: publish this warp's S^T slice as bf16 hi/lo -------------------------
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < CT; ++nt) {
       const int c = cw + 8 * nt + 2 * t4;
       uint32_t hi, lo;
       split_pair(S[nt][0], S[nt][1], hi, lo);
@@ -224,45 +227,54 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
       if (STAGES == 2 && n + 1 < p.N) issue_group1(n + 1, &bars[(n + 1) & 1]);
     }
 
-    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T q^T (one n-tile each) --------
-    float Rhh[4], Rlh[4], Rhl[4], Oh[4], Ol[4], Ox[4];
-    {
-      const int j = jw + 2 * t4;
-      Rhh[0] = su[j * VT + g];
-      Rhh[1] = su[(j + 1) * VT + g];
-      Rhh[2] = su[j * VT + g + 8];
-      Rhh[3] = su[(j + 1) * VT + g + 8];
+    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T q^T (JT n-tiles each) -------
+    float Rhh[JT][4], Rlh[JT][4], Rhl[JT][4], Oh[JT][4], Ol[JT][4], Ox[JT][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) Rlh[e] = Rhl[e] = Oh[e] = Ol[e] = Ox[e] = 0.f;
+    for (int jt = 0; jt < JT; ++jt) {
+      const int j = jw + 8 * jt + 2 * t4;
+      Rhh[jt][0] = su[j * VT + g];
+      Rhh[jt][1] = su[(j + 1) * VT + g];
+      Rhh[jt][2] = su[j * VT + g + 8];
+      Rhh[jt][3] = su[(j + 1) * VT + g + 8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = Oh[jt][e] = Ol[jt][e] = Ox[jt][e] = 0.f;
     }
 #pragma unroll
     for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
-      uint32_t wh[4], wl[4], qh[4], ql[4];
-      ldsm_x4(wh, tile_addr(w_hi, jw + brow, 16 * ks2 + bcol));
-      ldsm_x4(wl, tile_addr(w_lo, jw + brow, 16 * ks2 + bcol));
-      ldsm_x4(qh, tile_addr(q_hi, jw + brow, 16 * ks2 + bcol));
-      if (GATE) ldsm_x4(ql, tile_addr(q_lo, jw + brow, 16 * ks2 + bcol));
+      uint32_t ah[2][4], al[2][4];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t ah[4], al[4];
-        ldsm_x4(ah, smem_u32(xs_hi + arow * LDW + 16 * (ks2 + h2) + acol));
-        ldsm_x4(al, smem_u32(xs_lo + arow * LDW + 16 * (ks2 + h2) + acol));
-        mma_bf16_16816(Rhh, ah, wh[2 * h2], wh[2 * h2 + 1]);
-        mma_bf16_16816(Rlh, al, wh[2 * h2], wh[2 * h2 + 1]);
-        mma_bf16_16816(Rhl, ah, wl[2 * h2], wl[2 * h2 + 1]);
-        mma_bf16_16816(Oh, ah, qh[2 * h2], qh[2 * h2 + 1]);
-        mma_bf16_16816(Ol, al, qh[2 * h2], qh[2 * h2 + 1]);
-        if (GATE) mma_bf16_16816(Ox, ah, ql[2 * h2], ql[2 * h2 + 1]);
+        ldsm_x4(ah[h2], smem_u32(xs_hi + arow * LDW + 16 * (ks2 + h2) + acol));
+        ldsm_x4(al[h2], smem_u32(xs_lo + arow * LDW + 16 * (ks2 + h2) + acol));
+      }
+#pragma unroll
+      for (int jt = 0; jt < JT; ++jt) {
+        const int rb = jw + 8 * jt + brow;
+        uint32_t wh[4], wl[4], qh[4], ql[4];
+        ldsm_x4(wh, tile_addr(w_hi, rb, 16 * ks2 + bcol));
+        ldsm_x4(wl, tile_addr(w_lo, rb, 16 * ks2 + bcol));
+        ldsm_x4(qh, tile_addr(q_hi, rb, 16 * ks2 + bcol));
+        if (GATE) ldsm_x4(ql, tile_addr(q_lo, rb, 16 * ks2 + bcol));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          mma_bf16_16816(Rhh[jt], ah[h2], wh[2 * h2], wh[2 * h2 + 1]);
+          mma_bf16_16816(Rlh[jt], al[h2], wh[2 * h2], wh[2 * h2 + 1]);
+          mma_bf16_16816(Rhl[jt], ah[h2], wl[2 * h2], wl[2 * h2 + 1]);
+          mma_bf16_16816(Oh[jt], ah[h2], qh[2 * h2], qh[2 * h2 + 1]);
+          mma_bf16_16816(Ol[jt], al[h2], qh[2 * h2], qh[2 * h2 + 1]);
+          if (GATE) mma_bf16_16816(Ox[jt], ah[h2], ql[2 * h2], ql[2 * h2 + 1]);
+        }
       }
     }
 
     // ---- C: publish r^T and rho^T = r^T diag(kscale); scale o part 1 -------------
-    float O[4];
-    {
-      const int j = jw + 2 * t4;
+    float O[JT][4];
+#pragma unroll
+    for (int jt = 0; jt < JT; ++jt) {
+      const int j = jw + 8 * jt + 2 * t4;
       float R[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) R[e] = Rhh[e] + (Rlh[e] + Rhl[e]);
+      for (int e = 0; e < 4; ++e) R[e] = Rhh[jt][e] + (Rlh[jt][e] + Rhl[jt][e]);
       uint32_t hi, lo;
       split_pair(R[0], R[1], hi, lo);
       *reinterpret_cast<uint32_t*>(xr_hi + g * LDA + j) = hi;
@@ -278,17 +290,17 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
       *reinterpret_cast<uint32_t*>(xp_hi + (g + 8) * LDA + j) = hi;
       *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
       const float q0 = qs[j], q1 = qs[j + 1];
-      O[0] = (Oh[0] + (Ol[0] + Ox[0])) * q0;
-      O[1] = (Oh[1] + (Ol[1] + Ox[1])) * q1;
-      O[2] = (Oh[2] + (Ol[2] + Ox[2])) * q0;
-      O[3] = (Oh[3] + (Ol[3] + Ox[3])) * q1;
+      O[jt][0] = (Oh[jt][0] + (Ol[jt][0] + Ox[jt][0])) * q0;
+      O[jt][1] = (Oh[jt][1] + (Ol[jt][1] + Ox[jt][1])) * q1;
+      O[jt][2] = (Oh[jt][2] + (Ol[jt][2] + Ox[jt][2])) * q0;
+      O[jt][3] = (Oh[jt][3] + (Ol[jt][3] + Ox[jt][3])) * q1;
     }
     if (GATE) ok = ok && mbar_wait(&bars[1], n & 1, kWaitLimit);   // k, A_qk of chunk n
     __syncthreads();                           // #2: r^T / rho^T tiles visible
 
     // ---- D: S^T = gamma S^T + rho^T k (channels of this warp), o^T part 2 -----------
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < CT; ++nt) {
       const int c = cw + 8 * nt + 2 * t4;
       const float g0 = gam[c], g1 = gam[c + 1];
       S[nt][0] *= g0;
@@ -296,60 +308,74 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
       S[nt][2] *= g0;
       S[nt][3] *= g1;
     }
-    float Dl[2][4], Dx[2][4], Phh[4], Plh[4], Phl[4];
+    float Dl[CT][4], Dx[CT][4], Phh[JT][4], Plh[JT][4], Phl[JT][4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      Dl[0][e] = Dl[1][e] = Dx[0][e] = Dx[1][e] = 0.f;
-      Phh[e] = Plh[e] = Phl[e] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < CT; ++nt) Dl[nt][e] = Dx[nt][e] = 0.f;
+#pragma unroll
+      for (int jt = 0; jt < JT; ++jt) Phh[jt][e] = Plh[jt][e] = Phl[jt][e] = 0.f;
     }
 #pragma unroll
     for (int ks = 0; ks < C / 16; ++ks) {
-      uint32_t ph[4], pl[4], kh[4];
+      uint32_t ph[4], pl[4];
       ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * ks + acol));
       ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
-      ldsm_x4_t(kh, tile_addr(k_hi, 16 * ks + krow, kcol));
-      mma_bf16_16816(S[0], ph, kh[0], kh[1]);
-      mma_bf16_16816(S[1], ph, kh[2], kh[3]);
-      mma_bf16_16816(Dl[0], pl, kh[0], kh[1]);
-      mma_bf16_16816(Dl[1], pl, kh[2], kh[3]);
-      if (GATE) {
-        uint32_t kl[4];
-        ldsm_x4_t(kl, tile_addr(k_lo, 16 * ks + krow, kcol));
-        mma_bf16_16816(Dx[0], ph, kl[0], kl[1]);
-        mma_bf16_16816(Dx[1], ph, kl[2], kl[3]);
+#pragma unroll
+      for (int np = 0; np < CT / 2; ++np) {
+        uint32_t kh[4];
+        ldsm_x4_t(kh, tile_addr(k_hi, 16 * ks + krow, kcol + 16 * np));
+        mma_bf16_16816(S[2 * np], ph, kh[0], kh[1]);
+        mma_bf16_16816(S[2 * np + 1], ph, kh[2], kh[3]);
+        mma_bf16_16816(Dl[2 * np], pl, kh[0], kh[1]);
+        mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
+        if (GATE) {
+          uint32_t kl[4];
+          ldsm_x4_t(kl, tile_addr(k_lo, 16 * ks + krow, kcol + 16 * np));
+          mma_bf16_16816(Dx[2 * np], ph, kl[0], kl[1]);
+          mma_bf16_16816(Dx[2 * np + 1], ph, kl[2], kl[3]);
+        }
       }
     }
 #pragma unroll
     for (int ks2 = 0; ks2 < C / 16; ks2 += 2) {
-      uint32_t ah[4], al[4];
-      ldsm_x4(ah, tile_addr(aq_hi, jw + brow, 16 * ks2 + bcol));
-      ldsm_x4(al, tile_addr(aq_lo, jw + brow, 16 * ks2 + bcol));
+      uint32_t rh[2][4], rl[2][4];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t rh[4], rl[4];
-        ldsm_x4(rh, smem_u32(xr_hi + arow * LDA + 16 * (ks2 + h2) + acol));
-        ldsm_x4(rl, smem_u32(xr_lo + arow * LDA + 16 * (ks2 + h2) + acol));
-        mma_bf16_16816(Phh, rh, ah[2 * h2], ah[2 * h2 + 1]);
-        mma_bf16_16816(Plh, rl, ah[2 * h2], ah[2 * h2 + 1]);
-        mma_bf16_16816(Phl, rh, al[2 * h2], al[2 * h2 + 1]);
+        ldsm_x4(rh[h2], smem_u32(xr_hi + arow * LDA + 16 * (ks2 + h2) + acol));
+        ldsm_x4(rl[h2], smem_u32(xr_lo + arow * LDA + 16 * (ks2 + h2) + acol));
+      }
+#pragma unroll
+      for (int jt = 0; jt < JT; ++jt) {
+        uint32_t ah[4], al[4];
+        ldsm_x4(ah, tile_addr(aq_hi, jw + 8 * jt + brow, 16 * ks2 + bcol));
+        ldsm_x4(al, tile_addr(aq_lo, jw + 8 * jt + brow, 16 * ks2 + bcol));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          mma_bf16_16816(Phh[jt], rh[h2], ah[2 * h2], ah[2 * h2 + 1]);
+          mma_bf16_16816(Plh[jt], rl[h2], ah[2 * h2], ah[2 * h2 + 1]);
+          mma_bf16_16816(Phl[jt], rh[h2], al[2 * h2], al[2 * h2 + 1]);
+        }
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < CT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[nt][e] += Dl[nt][e] + Dx[nt][e];
 
-    // ---- E: o rows of this warp (i in [8 warp, +8)) -> global -------------------
-    {
-      const int i = 2 * t4;
-      xo[i * 16 + g] = O[0] + (Phh[0] + (Plh[0] + Phl[0]));
-      xo[(i + 1) * 16 + g] = O[1] + (Phh[1] + (Plh[1] + Phl[1]));
-      xo[i * 16 + g + 8] = O[2] + (Phh[2] + (Plh[2] + Phl[2]));
-      xo[(i + 1) * 16 + g + 8] = O[3] + (Phh[3] + (Plh[3] + Phl[3]));
+    // ---- E: o rows of this warp (i in [jw, jw + 8 JT)) -> global ---------------
+#pragma unroll
+    for (int jt = 0; jt < JT; ++jt) {
+      const int i = 8 * jt + 2 * t4;
+      xo[i * 16 + g] = O[jt][0] + (Phh[jt][0] + (Plh[jt][0] + Phl[jt][0]));
+      xo[(i + 1) * 16 + g] = O[jt][1] + (Phh[jt][1] + (Plh[jt][1] + Phl[jt][1]));
+      xo[i * 16 + g + 8] = O[jt][2] + (Phh[jt][2] + (Plh[jt][2] + Phl[jt][2]));
+      xo[(i + 1) * 16 + g + 8] = O[jt][3] + (Phh[jt][3] + (Plh[jt][3] + Phl[jt][3]));
     }
     __syncwarp();
-    {
-      const int i = lane >> 2, c4 = (lane & 3) * 4;   // 8 rows x 4 float4
+#pragma unroll
+    for (int rep = 0; rep < JT; ++rep) {
+      const int i = 8 * rep + (lane >> 2), c4 = (lane & 3) * 4;   // 8 JT rows x 4 float4
       const int t = t0 + jw + i;
       if (t < p.T) {
         const float4 val = *reinterpret_cast<const float4*>(xo + i * 16 + c4);
@@ -379,7 +405,7 @@ __global__ void __launch_bounds__(THREADS) state_kernel(const __grid_constant__ 
 
   if (p.sT) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < CT; ++nt) {
       const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -436,7 +462,7 @@ bool encode_bthd(CUtensorMap* map, const void* base, int B, int T, int heads) {
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int GATE, int STAGES>
+template <int GATE, int STAGES, int WARPS>
 gdr_status launch_one(const Params& p, cudaStream_t stream) {
   Maps m;
   memset(&m, 0, sizeof m);
@@ -453,20 +479,20 @@ gdr_status launch_one(const Params& p, cudaStream_t stream) {
   }
   if (!ok) return GDR_ERR_CUDA;
   constexpr Layout LY(GATE, STAGES);
-  auto kern = state_kernel<GATE, STAGES>;
+  auto kern = state_kernel<GATE, STAGES, WARPS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total) !=
       cudaSuccess)
     return GDR_ERR_CUDA;
   dim3 grid(V / VT, p.HV, p.B);
-  kern<<<grid, THREADS, LY.total, stream>>>(m, p);
+  kern<<<grid, WARPS * 32, LY.total, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 }  // namespace
 
 gdr_status launch_state(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode) return launch_one<1, 1>(p, stream);
-  return launch_one<0, 2>(p, stream);
+  if (p.gate_mode) return launch_one<1, 1, STATE_WARPS>(p, stream);
+  return launch_one<0, 2, STATE_WARPS>(p, stream);
 }
 
 }  // namespace fast
