@@ -27,6 +27,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+// Plain arrival (no transaction bytes) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // Bounded wait on an mbarrier phase: false after `limit` unsuccessful polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long limit) {
   for (long i = 0; i < limit; ++i) {

@@ -428,7 +428,9 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
 //   5+s: r^T tile s ready (chain arrives, output waits);
 //   7+s: chunk in buffer s consumed by the output warps (output arrives, chain waits).
 namespace ws {
-constexpr int CW = 4, OW = 4, THREADS = (CW + OW) * 32;
+// Chain warps, output warps, and two producer warps that only issue TMA loads
+// (one for each buffer ring), so that no compute warp waits on the issue.
+constexpr int CW = 4, OW = 4, PW = 2, XT = (CW + OW) * 32, THREADS = XT + PW * 32;
 // Chain-side buffer: W hi, W lo, k, U tile [64][16] fp32, VEC.
 constexpr int C_W_HI = 0, C_W_LO = 16384, C_K = 32768, C_U = 49152, C_VEC = 53248, C_BYTES = 55296;
 constexpr uint32_t C_TX = 32768 + 16384 + 4096 + 1024;
@@ -466,6 +468,8 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
   const int chunk0 = (int)(seq * p.N);
   uint64_t* cfull = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* ofull = cfull + 2;
+  uint64_t* cempty = cfull + 4;
+  uint64_t* oempty = cfull + 6;
   const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int acol = (lane >> 4) * 8;
   const int brow = (lane & 7);
@@ -506,17 +510,37 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(&cfull[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&cempty[i], CW);
+      mbar_init(&oempty[i], OW);
+    }
     mbar_fence_init();
   }
   __syncthreads();
   bool ok = true;
 
-  if (warp < CW) {
+  if (warp >= CW + OW) {
+    // ============================== producer warps ===============================
+    // Stage s of a ring is refilled with chunk n once the consumers have released
+    // chunk n - 2 from it (completion (n >> 1) - 1 of its empty barrier).
+    if (lane == 0) {
+      const bool chain = warp == CW + OW;
+      uint64_t* empty = chain ? cempty : oempty;
+      for (int n = 0; n < p.N; ++n) {
+        if (n >= 2) ok = ok && mbar_wait(&empty[n & 1], ((n >> 1) - 1) & 1, kWaitLimit);
+        if (!ok) break;
+        if (chain)
+          issue_chain(n);
+        else
+          issue_output(n);
+      }
+      if (!ok) atomicOr(p.error_word, kErrStateWait);
+    }
+  } else if (warp < CW) {
     // ================================ chain warps ================================
     const int jw = 16 * warp, cw = 32 * warp;          // r^T j-tiles, state channels
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
     const int kcol = cw + (lane >> 4) * 8;
-    if (tid == 0) issue_chain(0);
     float S[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -535,7 +559,7 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
       const float* su = reinterpret_cast<const float*>(cb + C_U);
       const float* ks = reinterpret_cast<const float*>(cb + C_VEC) + C;
       const float* gam = ks + C;
-      if (n >= 2) nb_sync(7 + s, THREADS);             // output done with chunk n-2's tiles
+      if (n >= 2) nb_sync(7 + s, XT);                  // output done with chunk n-2's tiles
       __nv_bfloat16* xsh = xs(s, 0);
       __nv_bfloat16* xsl = xs(s, 1);
 #pragma unroll
@@ -550,12 +574,8 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
         *reinterpret_cast<uint32_t*>(xsl + (g + 8) * LDW + c) = lo;
       }
       ok = ok && mbar_wait(&cfull[s], (n >> 1) & 1, kWaitLimit);
-      nb_sync(1, CW * 32);                             // S^T complete; chunk n-1 tiles free
-      nb_arrive(3 + s, THREADS);
-      if (tid == 0) {
-        if (!ok) atomicOr(p.error_word, kErrStateWait);
-        if (n + 1 < p.N) issue_chain(n + 1);
-      }
+      nb_sync(1, CW * 32);                             // S^T complete
+      nb_arrive(3 + s, XT);
       // r^T = U^T - S^T W^T, j in [jw, jw + 16)
       float Rhh[2][4], Rlh[2][4], Rhl[2][4];
 #pragma unroll
@@ -613,7 +633,7 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
         *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
       }
       nb_sync(1, CW * 32);                             // r^T, rho^T complete
-      nb_arrive(5 + s, THREADS);
+      nb_arrive(5 + s, XT);
       // S^T = gamma S^T + rho^T k, c in [cw, cw + 32)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
@@ -648,9 +668,12 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[nt][e] += Dl[nt][e];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cempty[s]);          // this warp is done with the stage
     }
+    if (!ok) atomicOr(p.error_word, kErrStateWait);
     // Balance the consumed-barrier generations of the last two chunks.
-    for (int n = (p.N >= 2 ? p.N - 2 : 0); n < p.N; ++n) nb_sync(7 + (n & 1), THREADS);
+    for (int n = (p.N >= 2 ? p.N - 2 : 0); n < p.N; ++n) nb_sync(7 + (n & 1), XT);
     if (p.sT) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
@@ -666,10 +689,6 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
     // ================================ output warps ===============================
     const int ow = warp - CW, iw = 16 * ow;            // o^T rows i in [iw, iw + 16)
     float* xo = reinterpret_cast<float*>(sm + OFF_XO) + ow * 256;
-    if (tid == CW * 32) {
-      issue_output(0);
-      if (p.N > 1) issue_output(1);
-    }
     for (int n = 0; n < p.N; ++n) {
       const int s = n & 1;
       uint8_t* ob = sm + OFF_O + s * O_BYTES;
@@ -677,7 +696,7 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
       const uint32_t aq_hi = smem_u32(ob + O_AQ_HI), aq_lo = smem_u32(ob + O_AQ_LO);
       const float* qs = reinterpret_cast<const float*>(ob + O_QS);
       ok = ok && mbar_wait(&ofull[s], (n >> 1) & 1, kWaitLimit);
-      nb_sync(3 + s, THREADS);                         // S^T of chunk n published
+      nb_sync(3 + s, XT);                              // S^T of chunk n published
       const __nv_bfloat16* xsh = xs(s, 0);
       const __nv_bfloat16* xsl = xs(s, 1);
       float Oh[2][4], Ol[2][4];
@@ -714,7 +733,7 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
         O[it][2] = (Oh[it][2] + Ol[it][2]) * q0;
         O[it][3] = (Oh[it][3] + Ol[it][3]) * q1;
       }
-      nb_sync(5 + s, THREADS);                         // r^T of chunk n published
+      nb_sync(5 + s, XT);                              // r^T of chunk n published
       const __nv_bfloat16* xrh = xr(s, 0);
       const __nv_bfloat16* xrl = xr(s, 1);
       float Phh[2][4], Plh[2][4], Phl[2][4];
@@ -744,12 +763,10 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
         }
       }
       // The S^T, r^T copies and this chunk's output tiles are no longer read.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&oempty[s]);          // q, A_qk, qscale of the stage read
       nb_sync(2, OW * 32);
-      nb_arrive(7 + s, THREADS);
-      if (tid == CW * 32) {
-        if (!ok) atomicOr(p.error_word, kErrStateWait);
-        if (n + 2 < p.N) issue_output(n + 2);
-      }
+      nb_arrive(7 + s, XT);
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int i = 8 * it + 2 * t4;
@@ -778,6 +795,7 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
       }
       __syncwarp();
     }
+    if (!ok) atomicOr(p.error_word, kErrStateWait);
   }
 }
 
