@@ -49,6 +49,20 @@ static_assert(Slab::AQ2 % 16 == 0 && Slab::U % 16 == 0 && Slab::VEC % 16 == 0 &&
                   Slab::QB2 % 16 == 0 && Slab::KB2 % 16 == 0,
               "slab arrays must stay 16-byte aligned");
 
+// Exchange block of one chunk (scalar gate): the state at the chunk start and
+// the chunk's corrected values, published by the state chain for the output
+// stage, as bf16 hi / lo planes, value-major (the layout the output products
+// read as their K-major B operands).
+//   S_HI, S_LO  [V][K] bf16   S^T at the start of the chunk
+//   R_HI, R_LO  [V][C] bf16   r^T = (U - W S)^T
+struct Xchg {
+  static constexpr size_t S_HI = 0;
+  static constexpr size_t S_LO = S_HI + (size_t)V * K * 2;
+  static constexpr size_t R_HI = S_LO + (size_t)V * K * 2;
+  static constexpr size_t R_LO = R_HI + (size_t)V * C * 2;
+  static constexpr size_t BYTES = R_LO + (size_t)V * C * 2;
+};
+
 // Everything both kernels of the fast path need.
 struct Params {
   const __nv_bfloat16* q;   // [B, T, H, K]
@@ -60,6 +74,8 @@ struct Params {
   void* out;                // [B, T, HV, V]
   float* sT;                // [B, HV, K, V] or null
   uint8_t* slabs;           // N * B * HV slabs
+  uint8_t* xchg;            // N * B * HV exchange blocks (scalar gate), else null
+  unsigned int* flags;      // [B * HV][V / VT] chunks published per chain (scalar gate)
   unsigned int* error_word;
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;
@@ -73,6 +89,8 @@ inline __host__ __device__ size_t slab_index(const Params& p, int b, int hv, int
 
 // Launchers (gdr_state.cu, gdr_chunk.cu).
 gdr_status launch_state(const Params& p, cudaStream_t stream);
+// Scalar gate: state chain and chunk outputs in one launch (gdr_recur.cu).
+gdr_status launch_recur(const Params& p, cudaStream_t stream);
 gdr_status launch_chunk_simt(const Params& p, cudaStream_t stream);
 gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream);
 

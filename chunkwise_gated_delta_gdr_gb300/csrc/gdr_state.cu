@@ -894,7 +894,10 @@ gdr_status launch_ws(const Params& p, cudaStream_t stream) {
 
 gdr_status launch_state(const Params& p, cudaStream_t stream) {
   if (p.gate_mode) return launch_one<1, 1, STATE_WARPS>(p, stream);
-  return launch_ws(p, stream);
+  // Scalar gate: the fused chain + output launch when the chains leave SMs
+  // for the outputs, else chain and outputs in the same CTAs.
+  const gdr_status st = launch_recur(p, stream);
+  return st == GDR_ERR_UNSUPPORTED ? launch_ws(p, stream) : st;
 }
 
 }  // namespace fast

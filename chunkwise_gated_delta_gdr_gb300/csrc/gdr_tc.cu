@@ -7,9 +7,33 @@ bool tc_supported(const Problem& p) {
   return p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
 }
 
-size_t tc_workspace_bytes(const Problem& p) {
-  return (size_t)p.B * p.HV * p.N * fast::Slab::bytes(p.gate_mode);
+namespace {
+
+// Workspace body of the fast path: the chunk slabs, then (scalar gate) the
+// exchange blocks of the state chain and its per-chain progress flags.
+struct TcLayout {
+  size_t xchg = 0, flags = 0, total = 0;
+};
+
+TcLayout tc_layout(const Problem& p) {
+  const size_t nch = (size_t)p.B * p.HV * p.N;
+  TcLayout L;
+  size_t off = nch * fast::Slab::bytes(p.gate_mode);
+  if (p.gate_mode == 0) {
+    off = align_up(off, 1024);
+    L.xchg = off;
+    off += nch * fast::Xchg::BYTES;
+    off = align_up(off, 256);
+    L.flags = off;
+    off += (size_t)p.B * p.HV * (fast::V / fast::VT) * sizeof(unsigned int);
+  }
+  L.total = off;
+  return L;
 }
+
+}  // namespace
+
+size_t tc_workspace_bytes(const Problem& p) { return tc_layout(p).total; }
 
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
                      cudaStream_t stream, int stage) {
@@ -23,6 +47,9 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.out = p.out;
   f.sT = p.sT;
   f.slabs = static_cast<uint8_t*>(ws_body);
+  const TcLayout L = tc_layout(p);
+  f.xchg = p.gate_mode == 0 ? f.slabs + L.xchg : nullptr;
+  f.flags = p.gate_mode == 0 ? reinterpret_cast<unsigned int*>(f.slabs + L.flags) : nullptr;
   f.error_word = error_word;
   f.B = p.B;
   f.T = p.T;
