@@ -183,11 +183,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          (1ull << 46) | (2ull << 61);
 }
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, dense.
-__host__ __device__ constexpr uint32_t idesc_bf16_kk(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Same with an explicit leading-dimension byte offset (LBO): for an MN-major
+// operand, the distance between consecutive 64-element blocks along M / N.
+__device__ __forceinline__ uint64_t sdesc_sw128_lbo(uint32_t saddr, uint32_t lbo) {
+  return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
+// kind::f16 instruction descriptor: D fp32, A and B bf16, dense; a_mn / b_mn
+// set when the operand is MN-major instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_kk(int M, int N) { return idesc_bf16(M, N, 0, 0); }
 // D (TMEM) = A * B (+ D when acc != 0), issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
   asm volatile(
