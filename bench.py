@@ -348,14 +348,14 @@ def run_ours(args, rank, local_rank, world):
         "config": config_of(w, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "scope": "one forward call = chunk-local kernel + state kernel",
+                     "scope": "one forward call = chunk-local kernel + recurrence kernel",
                      "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs",
                      "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
         "kernels": {"chunk_local": {"ms": statistics.mean(prep),
                                     "traffic": (traffic_per or {}).get("chunk_tc_kernel")},
-                    "state": {"ms": statistics.mean(rec),
-                              "traffic": (traffic_per or {}).get("state_kernel")}},
+                    "recurrence": {"ms": statistics.mean(rec),
+                                   "traffic": (traffic_per or {}).get("recur_kernel")}},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
