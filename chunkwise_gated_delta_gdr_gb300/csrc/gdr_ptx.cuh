@@ -96,6 +96,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
 }
+// Stores four 8x8 b16 matrices; lanes 8 i .. 8 i + 7 give the row addresses of
+// matrix i, register i holds this lane's pair of matrix i (mma C-fragment order).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
 // D += A (16x16, row) * B (16x8, col): bf16 in, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -75,16 +75,17 @@ constexpr int CW = 4;
 constexpr int W_HI = 0, W_LO = 16384, KT = 32768, U = 49152, VEC = 53248, STAGE = 55296;
 constexpr uint32_t TX = 32768 + 16384 + 4096 + 1024;
 constexpr int NST = 3;
-// Published tiles (double-buffered), 128-byte swizzled: S^T hi, lo as two
+// Published tiles (three buffers), 128-byte swizzled: S^T hi, lo as two
 // [16 v][64 k] boxes each; r^T hi, lo as one [16 v][64 j] box each. rho^T
 // (chain-internal) is a padded [2][16][LDA] bf16 tile.
 constexpr int XS_BUF = 2 * 2 * 2048, XR_BUF = 2 * 2048, XP_BYTES = 2 * 16 * LDA * 2;
-constexpr int XS = NST * STAGE, XR = XS + 2 * XS_BUF, XP = XR + 2 * XR_BUF, BAR = XP + XP_BYTES;
+constexpr int NXB = 3;                     // published-tile buffers
+constexpr int XS = NST * STAGE, XR = XS + NXB * XS_BUF, XP = XR + NXB * XR_BUF, BAR = XP + XP_BYTES;
 constexpr int DONE = BAR + 2 * NST * 8;     // chunks copied out (u32)
 constexpr int BYTES = DONE + 16;
 constexpr int SYNC = CW * 32 + 32;         // chain warps + copy warp
-// Named barriers: 1 chain warps; 2 + s S^T of buffer s published; 4 + s r^T
-// of buffer s published; 6 + s buffer s copied out.
+// Named barriers: 1 chain warps; 2 + s S^T of buffer s published; 5 + s r^T
+// of buffer s published; 8 + s buffer s copied out (s < NXB).
 }  // namespace ch
 
 // ----------------------------------------------------------------- output role
@@ -184,7 +185,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
     // queue behind possibly aliasing stores). Row r of a published tile keeps
     // its 16-byte chunk c at chunk c ^ (r % 8); the exchange block is plain.
     for (int n = 0; n < p.N; ++n) {
-      const int s = n & 1;
+      const int s = n % NXB;
       uint8_t* blk = p.xchg + (size_t)(chunk0 + n) * Xchg::BYTES;
       nb_sync(2 + s, SYNC);
       const uint8_t* xs = sm + XS + s * XS_BUF;
@@ -201,7 +202,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         *reinterpret_cast<uint4*>(blk + Xchg::S_HI + pl * (Xchg::S_LO - Xchg::S_HI) +
                                   (size_t)(v0 + row) * (K * 2) + c * 16) = val[i];
       }
-      nb_sync(4 + s, SYNC);
+      nb_sync(5 + s, SYNC);
       const uint8_t* xr = sm + XR + s * XR_BUF;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {                    // 2 planes x 16 rows x 8 chunks
@@ -214,7 +215,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         *reinterpret_cast<uint4*>(blk + Xchg::R_HI + pl * (Xchg::R_LO - Xchg::R_HI) +
                                   (size_t)(v0 + row) * (C * 2) + c * 16) = val[i];
       }
-      nb_arrive(6 + s, SYNC);                          // buffer s may be overwritten
+      nb_arrive(8 + s, SYNC);                          // buffer s may be overwritten
       __syncwarp();                                    // orders the lanes' stores before:
       if (lane == 0) st_release_cta_shared(done, (unsigned int)(n + 1));
     }
@@ -260,7 +261,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       }
     }
     for (int n = 0; n < p.N; ++n) {
-      const int s = n & 1, st = n % NST;               // exchange buffer, operand stage
+      const int s = n % NXB, st = n % NST;             // published-tile buffer, operand stage
       uint8_t* cb = sm + st * STAGE;
       const uint32_t w_hi = smem_u32(cb + W_HI), w_lo = smem_u32(cb + W_LO);
       const uint32_t k_t = smem_u32(cb + KT);
@@ -269,17 +270,20 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       const float* gam = ks + C;
       uint8_t* xsh = sm + XS + s * XS_BUF;             // S^T hi; lo at + 4096
       uint8_t* xrh = sm + XR + s * XR_BUF;             // r^T hi; lo at + 2048
-      if (n >= 2) nb_sync(6 + s, SYNC);                // chunk n - 2 stored from buffer s
+      if (n >= NXB) nb_sync(8 + s, SYNC);              // chunk n - NXB copied out of buffer s
+      // S^T hi / lo by stmatrix: matrix i of call q is channel tile 2 q + i / 2,
+      // value rows 8 (i % 2) .. + 8.
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int c = cw + 8 * nt + 2 * t4;
-        uint32_t hi, lo;
-        split_pair(S[nt][0], S[nt][1], hi, lo);
-        *reinterpret_cast<uint32_t*>(xsh + tile16_off(g, c)) = hi;
-        *reinterpret_cast<uint32_t*>(xsh + 4096 + tile16_off(g, c)) = lo;
-        split_pair(S[nt][2], S[nt][3], hi, lo);
-        *reinterpret_cast<uint32_t*>(xsh + tile16_off(g + 8, c)) = hi;
-        *reinterpret_cast<uint32_t*>(xsh + 4096 + tile16_off(g + 8, c)) = lo;
+      for (int q = 0; q < 2; ++q) {
+        uint32_t hi[4], lo[4];
+        split_pair(S[2 * q][0], S[2 * q][1], hi[0], lo[0]);
+        split_pair(S[2 * q][2], S[2 * q][3], hi[1], lo[1]);
+        split_pair(S[2 * q + 1][0], S[2 * q + 1][1], hi[2], lo[2]);
+        split_pair(S[2 * q + 1][2], S[2 * q + 1][3], hi[3], lo[3]);
+        const int mi = lane >> 3;
+        const uint32_t a = smem_u32(xsh) + tile16_off(8 * (mi & 1) + (lane & 7), cw + 16 * q + 8 * (mi >> 1));
+        stsm_x4(a, hi[0], hi[1], hi[2], hi[3]);
+        stsm_x4(a + 4096, lo[0], lo[1], lo[2], lo[3]);
       }
       ok = ok && mbar_wait(&full[st], (n / NST) & 1, kWaitLimit);
       nb_sync(1, CW * 32);                             // S^T complete
@@ -317,39 +321,39 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
           }
         }
       }
+      {
+        // r^T and rho^T = (kscale r)^T hi / lo by stmatrix: matrix i is j tile
+        // i / 2, value rows 8 (i % 2) .. + 8.
+        uint32_t rh[4], rl[4], ph[4], pl[4];
 #pragma unroll
-      for (int jt = 0; jt < 2; ++jt) {
-        const int j = jw + 8 * jt + 2 * t4;
-        float R[4];
+        for (int jt = 0; jt < 2; ++jt) {
+          const int j = jw + 8 * jt + 2 * t4;
+          float R[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) R[e] = Rhh[jt][e] + (Rlh[jt][e] + Rhl[jt][e]);
-        uint32_t hi, lo;
-        split_pair(R[0], R[1], hi, lo);
-        *reinterpret_cast<uint32_t*>(xrh + tile16_off(g, j)) = hi;
-        *reinterpret_cast<uint32_t*>(xrh + 2048 + tile16_off(g, j)) = lo;
-        split_pair(R[2], R[3], hi, lo);
-        *reinterpret_cast<uint32_t*>(xrh + tile16_off(g + 8, j)) = hi;
-        *reinterpret_cast<uint32_t*>(xrh + 2048 + tile16_off(g + 8, j)) = lo;
-        const float k0 = ks[j], k1 = ks[j + 1];
-        split_pair(R[0] * k0, R[1] * k1, hi, lo);
-        *reinterpret_cast<uint32_t*>(xp_hi + g * LDA + j) = hi;
-        *reinterpret_cast<uint32_t*>(xp_lo + g * LDA + j) = lo;
-        split_pair(R[2] * k0, R[3] * k1, hi, lo);
-        *reinterpret_cast<uint32_t*>(xp_hi + (g + 8) * LDA + j) = hi;
-        *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
+          for (int e = 0; e < 4; ++e) R[e] = Rhh[jt][e] + (Rlh[jt][e] + Rhl[jt][e]);
+          const float k0 = ks[j], k1 = ks[j + 1];
+          split_pair(R[0], R[1], rh[2 * jt], rl[2 * jt]);
+          split_pair(R[2], R[3], rh[2 * jt + 1], rl[2 * jt + 1]);
+          split_pair(R[0] * k0, R[1] * k1, ph[2 * jt], pl[2 * jt]);
+          split_pair(R[2] * k0, R[3] * k1, ph[2 * jt + 1], pl[2 * jt + 1]);
+        }
+        const int mi = lane >> 3, row = 8 * (mi & 1) + (lane & 7), col = jw + 8 * (mi >> 1);
+        const uint32_t a = smem_u32(xrh) + tile16_off(row, col);
+        stsm_x4(a, rh[0], rh[1], rh[2], rh[3]);
+        stsm_x4(a + 2048, rl[0], rl[1], rl[2], rl[3]);
+        const uint32_t b = smem_u32(xp_hi + row * LDA + col);
+        stsm_x4(b, ph[0], ph[1], ph[2], ph[3]);
+        stsm_x4(b + 16 * LDA * 2, pl[0], pl[1], pl[2], pl[3]);
       }
       nb_sync(1, CW * 32);                             // r^T, rho^T complete
-      nb_arrive(4 + s, SYNC);
-      // S^T = gamma S^T + rho^T k, c in [cw, cw + 32)
+      nb_arrive(5 + s, SYNC);
+      // S^T = gamma S^T + rho^T k, c in [cw, cw + 32); the scalar gate's decay
+      // gamma is the same on every channel.
+      const float gm = gam[0];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int c = cw + 8 * nt + 2 * t4;
-        const float g0 = gam[c], g1 = gam[c + 1];
-        S[nt][0] *= g0;
-        S[nt][1] *= g1;
-        S[nt][2] *= g0;
-        S[nt][3] *= g1;
-      }
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[nt][e] *= gm;
       float Dl[4][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
@@ -377,8 +381,8 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);          // this warp is done with stage st
     }
-    // Balance the store-read barrier generations of the last two chunks.
-    for (int n = (p.N >= 2 ? p.N - 2 : 0); n < p.N; ++n) nb_sync(6 + (n & 1), SYNC);
+    // Balance the copy-out barrier generations of the last NXB chunks.
+    for (int n = (p.N >= NXB ? p.N - NXB : 0); n < p.N; ++n) nb_sync(8 + n % NXB, SYNC);
     if (p.sT) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
