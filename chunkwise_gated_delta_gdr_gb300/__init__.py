@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libgdr.so")
 GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_ALIGNMENT = 0, 1, 2, 3
 GDR_ERR_WORKSPACE, GDR_ERR_CUDA, GDR_ERR_TIMEOUT = 4, 5, 6
 GDR_F32, GDR_BF16 = 0, 1
-GDR_GATE_SCALAR, GDR_GATE_PER_KEY = 0, 1
+GDR_GATE_SCALAR, GDR_GATE_PER_KEY, GDR_GATE_NONE = 0, 1, 2
 
 EXPORTED = (
     "gdr_chunk_fwd", "gdr_chunk_prepare", "gdr_chunk_recur", "gdr_chunk_fwd_workspace_size",
@@ -139,7 +139,10 @@ def _stream_handle(stream):
 def _shapes(q, v, g):
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[3]
-    gate_mode = GDR_GATE_PER_KEY if g.dim() == 4 else GDR_GATE_SCALAR
+    if g is None:
+        gate_mode = GDR_GATE_NONE               # ungated delta rule
+    else:
+        gate_mode = GDR_GATE_PER_KEY if g.dim() == 4 else GDR_GATE_SCALAR
     return B, T, H, HV, K, V, gate_mode
 
 
@@ -149,8 +152,8 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, chunk_size: int = 64,
               workspace=None, stream=None):
     """Chunkwise gated delta rule forward on CUDA tensors.
 
-    q, k [B,T,H,K], v [B,T,HV,V] (bf16 or fp32); g fp32 [B,T,HV] (scalar gate) or
-    [B,T,HV,K] (per-key gate); beta fp32 [B,T,HV]; initial_state fp32 [B,HV,K,V]
+    q, k [B,T,H,K], v [B,T,HV,V] (bf16 or fp32); g fp32 [B,T,HV] (scalar gate),
+    [B,T,HV,K] (per-key gate) or None (ungated); beta fp32 [B,T,HV]; initial_state fp32 [B,HV,K,V]
     or None. scale defaults to 1/sqrt(K), out_dtype to q's dtype. Returns
     (o [B,T,HV,V], final_state [B,HV,K,V] fp32 or None). Buffers not passed in
     are allocated with torch on q's device; the call is asynchronous on

@@ -17,12 +17,17 @@ gdr_status check_dims(const gdr_dims* d, int chunk_size, int gate_mode) {
   if (d->B < 0 || d->T < 0 || d->H <= 0 || d->HV <= 0 || d->K <= 0 || d->V <= 0)
     return GDR_ERR_INVALID_ARG;
   if (d->HV % d->H != 0) return GDR_ERR_INVALID_ARG;
-  if (gate_mode != GDR_GATE_SCALAR && gate_mode != GDR_GATE_PER_KEY) return GDR_ERR_INVALID_ARG;
+  if (gate_mode != GDR_GATE_SCALAR && gate_mode != GDR_GATE_PER_KEY && gate_mode != GDR_GATE_NONE)
+    return GDR_ERR_INVALID_ARG;
   if ((d->in_dtype != GDR_F32 && d->in_dtype != GDR_BF16) ||
       (d->out_dtype != GDR_F32 && d->out_dtype != GDR_BF16))
     return GDR_ERR_INVALID_ARG;
-  if (chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDR_ERR_UNSUPPORTED;
+  if (chunk_size != 16 && chunk_size != 32 && chunk_size != 64 && chunk_size != 128)
+    return GDR_ERR_UNSUPPORTED;
   if (d->K > 128 || d->V > 128 || d->K + d->V > 256) return GDR_ERR_UNSUPPORTED;
+  // C = 128 runs on the general path, whose per-chunk tiles fit shared memory
+  // for head dims up to 64.
+  if (chunk_size == 128 && (d->K > 64 || d->V > 64)) return GDR_ERR_UNSUPPORTED;
   if (d->HV > 65535 || d->B > 65535) return GDR_ERR_UNSUPPORTED;
   // Element counts must fit the kernels' 64-bit indexing and the grid limits.
   if ((long long)d->T * d->HV * (d->V > d->K ? d->V : d->K) > (1LL << 46)) return GDR_ERR_UNSUPPORTED;
@@ -39,7 +44,9 @@ Problem make_problem(const void* q, const void* k, const void* v, const float* g
   p.N = (d->T + chunk_size - 1) / chunk_size;
   p.in_bf16 = d->in_dtype == GDR_BF16;
   p.out_bf16 = d->out_dtype == GDR_BF16;
-  p.gate_mode = gate_mode;
+  // Ungated: the scalar-gate path with g identically zero (g is never read).
+  p.gate_mode = gate_mode == GDR_GATE_NONE ? GDR_GATE_SCALAR : gate_mode;
+  if (gate_mode == GDR_GATE_NONE) p.g = nullptr;
   p.use_l2 = use_l2 != 0;
   p.scale = scale;
   return p;
@@ -51,6 +58,11 @@ size_t body_bytes(const Problem& p) {
 }
 
 size_t elem_in(const gdr_dims* d) { return d->in_dtype == GDR_BF16 ? 2 : 4; }
+// Bytes of g for a gate mode (none for the ungated mode).
+size_t gate_bytes(const gdr_dims* d, int gate_mode) {
+  if (gate_mode == GDR_GATE_NONE) return 0;
+  return (size_t)d->B * d->T * d->HV * (gate_mode == GDR_GATE_PER_KEY ? d->K : 1) * sizeof(float);
+}
 size_t elem_out(const gdr_dims* d) { return d->out_dtype == GDR_BF16 ? 2 : 4; }
 
 struct HostLayout {
@@ -62,7 +74,7 @@ HostLayout host_layout(const gdr_dims* d, int chunk_size, int gate_mode, int wit
   const size_t BT = (size_t)d->B * d->T;
   const size_t qk = BT * d->H * d->K * elem_in(d);
   const size_t vv = BT * d->HV * d->V * elem_in(d);
-  const size_t gg = BT * d->HV * (gate_mode ? d->K : 1) * sizeof(float);
+  const size_t gg = gate_bytes(d, gate_mode);
   const size_t bb = BT * d->HV * sizeof(float);
   const size_t st = (size_t)d->B * d->HV * d->K * d->V * sizeof(float);
   const size_t oo = BT * d->HV * d->V * elem_out(d);
@@ -134,7 +146,8 @@ gdr_status run(int stage, const void* q, const void* k, const void* v, const flo
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
   const bool work = dims->B > 0 && dims->T > 0;
   if (work && (!q || !k)) return GDR_ERR_INVALID_ARG;
-  if (work && (stage & 1) && (!v || !g || !beta)) return GDR_ERR_INVALID_ARG;
+  if (work && (stage & 1) && (!v || (!g && gate_mode != GDR_GATE_NONE) || !beta))
+    return GDR_ERR_INVALID_ARG;
   if (work && (stage & 2) && !out) return GDR_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, g, beta, initial_state, out, final_state};
   for (const void* ptr : ptrs)
@@ -211,7 +224,8 @@ gdr_status gdr_chunk_fwd_host(const void* q, const void* k, const void* v, const
   if (st != GDR_OK) return st;
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
   const bool work = dims->B > 0 && dims->T > 0;
-  if (work && (!q || !k || !v || !g || !beta || !out)) return GDR_ERR_INVALID_ARG;
+  if (work && (!q || !k || !v || (!g && gate_mode != GDR_GATE_NONE) || !beta || !out))
+    return GDR_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, g, beta, initial_state, out, final_state};
   for (const void* ptr : ptrs)
     if (ptr && !aligned16(ptr)) return GDR_ERR_ALIGNMENT;
@@ -224,7 +238,7 @@ gdr_status gdr_chunk_fwd_host(const void* q, const void* k, const void* v, const
   const size_t BT = (size_t)dims->B * dims->T;
   const size_t qk = BT * dims->H * dims->K * elem_in(dims);
   const size_t vv = BT * dims->HV * dims->V * elem_in(dims);
-  const size_t gg = BT * dims->HV * (gate_mode ? dims->K : 1) * sizeof(float);
+  const size_t gg = gate_bytes(dims, gate_mode);
   const size_t bb = BT * dims->HV * sizeof(float);
   const size_t stb = (size_t)dims->B * dims->HV * dims->K * dims->V * sizeof(float);
   const size_t oo = BT * dims->HV * dims->V * elem_out(dims);

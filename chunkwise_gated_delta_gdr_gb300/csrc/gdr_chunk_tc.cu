@@ -125,12 +125,13 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
     tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_tma);
   }
-  // Gate and beta (plain loads, issued before the TMA wait; zero past the end).
+  // Gate and beta (plain loads, issued before the TMA wait; zero past the end
+  // and for the ungated mode).
   float ga = 0.f, gb = 0.f;
   if (warp == 0) {
     const int ta = t0 + 2 * lane;
-    if (ta < p.T) ga = p.g[((size_t)b * p.T + ta) * p.HV + hv];
-    if (ta + 1 < p.T) gb = p.g[((size_t)b * p.T + ta + 1) * p.HV + hv];
+    if (p.g && ta < p.T) ga = p.g[((size_t)b * p.T + ta) * p.HV + hv];   // g == NULL: ungated
+    if (p.g && ta + 1 < p.T) gb = p.g[((size_t)b * p.T + ta + 1) * p.HV + hv];
   }
   if (tid < C) {
     const int t = t0 + tid;

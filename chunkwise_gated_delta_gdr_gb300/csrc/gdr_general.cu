@@ -1,7 +1,8 @@
 // gdr_general.cu -- general chunkwise gated delta rule forward on CUDA cores (fp32).
 //
 // Two kernels, for any head dims K, V <= 128 (K + V <= 256), chunk sizes
-// 16/32/64, fp32 or bf16 inputs and both gate kinds. All arithmetic is fp32,
+// 16/32/64 (and 128 for K, V <= 64), fp32 or bf16 inputs, both gate kinds and
+// the ungated mode (g == NULL reads as zero). All arithmetic is fp32,
 // which is what the fp32-input accuracy bound needs; the bf16 K = V = 128,
 // C = 64 workloads take the tensor-core path instead (gdr_tc.cu).
 //
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   }
   for (int idx = tid; idx < C * KG; idx += kThreads) {
     const int i = idx / KG, c = idx % KG, t = t0 + i;
-    G[i * GP + c] = (t < p.T) ? p.g[(((long)b * p.T + t) * p.HV + hv) * KG + c] : 0.f;
+    G[i * GP + c] = (p.g && t < p.T) ? p.g[(((long)b * p.T + t) * p.HV + hv) * KG + c] : 0.f;
   }
   for (int i = tid; i < C; i += kThreads) {
     const int t = t0 + i;

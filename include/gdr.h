@@ -68,7 +68,9 @@ typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
 
 typedef enum {
   GDR_GATE_SCALAR = 0,   /* g [B, T, HV]: one log-decay per token and value head (Gated DeltaNet) */
-  GDR_GATE_PER_KEY = 1   /* g [B, T, HV, K]: one log-decay per key channel (KDA) */
+  GDR_GATE_PER_KEY = 1,  /* g [B, T, HV, K]: one log-decay per key channel (KDA) */
+  GDR_GATE_NONE = 2      /* ungated delta rule (DeltaNet): g is not read and may be NULL;
+                            every decay factor is 1, i.e. g identically 0 */
 } gdr_gate_mode;
 
 /* Problem sizes. q, k have H heads of K channels; v, o have HV value heads of
@@ -86,10 +88,12 @@ typedef struct {
  *   v              (device) [B, T, HV, V]  in_dtype
  *   g              (device) fp32, [B, T, HV] (GDR_GATE_SCALAR) or [B, T, HV, K] (GDR_GATE_PER_KEY);
  *                  natural-log decay per token (any sign; |in-chunk cumsum span| must stay
- *                  below ~80 so that exp() of it is finite in fp32)
+ *                  below ~80 so that exp() of it is finite in fp32); not read, and may be
+ *                  NULL, with GDR_GATE_NONE
  *   beta           (device) fp32 [B, T, HV]
  *   initial_state  (device) fp32 [B, HV, K, V], or NULL for a zero state
- *   chunk_size     C: 16, 32 or 64 (64 is the tensor-core path)
+ *   chunk_size     C: 16, 32, 64 (64 is the tensor-core path) or 128 (general path,
+ *                  K <= 64 and V <= 64; larger head dims return GDR_ERR_UNSUPPORTED)
  *   scale          multiplies q after the optional L2 norm; finite and > 0
  *                  (the usual choice is 1/sqrt(K))
  *   use_qk_l2norm  nonzero: L2-normalise q and k per token and head first

@@ -64,7 +64,7 @@ def test_workspace_size_valid_and_invalid(lib):
     assert gdr.chunk_fwd_workspace_size(dims(HV=3), 64, 0) == 0      # HV % H != 0
     assert gdr.chunk_fwd_workspace_size(dims(K=256), 64, 0) == 0     # head dim
     assert gdr.chunk_fwd_workspace_size(dims(T=-1), 64, 0) == 0
-    assert gdr.chunk_fwd_workspace_size(dims(), 64, 2) == 0          # gate mode
+    assert gdr.chunk_fwd_workspace_size(dims(), 64, 3) == 0          # gate mode
     small = gdr.chunk_fwd_workspace_size(dims(T=64), 64, 0)
     big = gdr.chunk_fwd_workspace_size(dims(T=4096), 64, 0)
     assert big > small
@@ -118,3 +118,30 @@ def test_host_buffer_size(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         gdr.load_library(str(tmp_path / "nope.so"))
+
+
+def test_ungated_mode_and_chunk_size_128_sizes(lib):
+    d = dims()
+    scalar = gdr.chunk_fwd_workspace_size(d, 64, gdr.GDR_GATE_SCALAR)
+    assert gdr.chunk_fwd_workspace_size(d, 64, gdr.GDR_GATE_NONE) == scalar
+    assert gdr.chunk_fwd_workspace_size(d, 64, 3) == 0
+    # The ungated host buffer carries no gate array.
+    g_bytes = 1 * 256 * 4 * 4
+    assert (gdr.chunk_fwd_host_buffer_size(d, 64, gdr.GDR_GATE_SCALAR, False, False) -
+            gdr.chunk_fwd_host_buffer_size(d, 64, gdr.GDR_GATE_NONE, False, False)) == g_bytes
+    # C = 128: general path, head dims up to 64 only.
+    assert gdr.chunk_fwd_workspace_size(dims(K=64, V=64), 128, 0) > 0
+    assert gdr.chunk_fwd_path(dims(K=64, V=64), 128, 1) == 0
+    assert gdr.chunk_fwd_workspace_size(dims(), 128, 0) == 0
+    assert gdr.chunk_fwd_workspace_size(dims(K=64, V=128), 128, 0) == 0
+
+
+def test_gate_array_required_unless_ungated(lib):
+    A = 1 << 20
+    d = dims()
+    assert _call(lib, d, q=A, k=A, v=A, g=None, beta=A, out=A, gate=gdr.GDR_GATE_SCALAR) == \
+        gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=None, beta=A, out=A, gate=gdr.GDR_GATE_PER_KEY) == \
+        gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, gate=3) == gdr.GDR_ERR_INVALID_ARG
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=128) == gdr.GDR_ERR_UNSUPPORTED

@@ -128,6 +128,37 @@ def test_bruteforce_products(gate_mode, T):
     assert relerr(s_r, s_b) <= 1e-12
 
 
+# ---------------------------------------------------------------- ungated mode
+@pytest.mark.parametrize("C", [1, 16, 128])
+def test_ungated_is_householder_deltanet(C):
+    """With g = 0 (the library's ungated mode) the method is plain DeltaNet:
+    in the value-by-key convention of the Chunkwise blog (section 2.1),
+    S_t = S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and o_t = S_t q_t.
+    Computed here in that transposed form, per head, and compared with the
+    oracle's recurrence and chunk form run with a zero gate."""
+    p = rand_problem(71, T=150, K=8, V=6, H=1, HV=2)
+    p["g"] = np.zeros_like(p["g"])
+    B, T, H, K = p["q"].shape
+    HV, V = p["v"].shape[2], p["v"].shape[3]
+    scale = 1.0 / math.sqrt(K)
+    o_ref = np.zeros((B, T, HV, V))
+    s_ref = np.zeros((B, HV, K, V))
+    for hv in range(HV):
+        St = p["s0"][0, hv].T.copy()                       # V x K
+        for t in range(T):
+            kk = p["k"][0, t, 0] / math.sqrt(np.sum(p["k"][0, t, 0] ** 2) + 1e-6)
+            qq = p["q"][0, t, 0] / math.sqrt(np.sum(p["q"][0, t, 0] ** 2) + 1e-6)
+            b = p["beta"][0, t, hv]
+            St = St @ (np.eye(K) - b * np.outer(kk, kk)) + b * np.outer(p["v"][0, t, hv], kk)
+            o_ref[0, t, hv] = St @ (scale * qq)
+        s_ref[0, hv] = St.T
+    o_r, s_r = run(oracle.recurrent, p, scale=scale)
+    assert o_r.shape == o_ref.shape and relerr(o_r, o_ref) <= 1e-12
+    assert relerr(s_r, s_ref) <= 1e-12
+    o_c, s_c = run(oracle.chunkwise, p, scale=scale, chunk_size=C)
+    assert relerr(o_c, o_r) <= 1e-10 and relerr(s_c, s_r) <= 1e-10
+
+
 # ---------------------------------------------------------------- P-9, hand-worked cases
 def test_single_token_closed_form():
     """T = 1: S_1 = (I - beta k k^T) D S_0 + beta k v^T, o = S_1^T (scale q)."""

@@ -226,3 +226,76 @@ def test_prepare_then_recur_with_two_states(name):
         torch.cuda.synchronize()
         assert np.array_equal(out.cpu().numpy(), o_ref)
         assert np.array_equal(fin.cpu().numpy(), S_ref)
+
+
+# ---- ungated delta rule (gate_mode none) and chunk size 128 ----------------------
+# Ungated: the call passes g = None; the oracle runs the recurrence with g = 0,
+# i.e. every decay factor 1 (plain DeltaNet).
+
+def check_ungated(w, x):
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd(d["q"], d["k"], d["v"], None, d["beta"], d["s0"], chunk_size=w.C,
+                         scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    g0 = torch.zeros(w.B, w.T, w.HV, dtype=torch.float32)
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], g0, x["beta"], x["s0"], scale=w.scale,
+                              use_qk_l2norm=w.use_qk_l2norm)
+    o, S = o.cpu().numpy(), S.cpu().numpy()
+    tol = tol_for(w)
+    assert relerr(o, ro) <= tol and relerr(S, rS) <= tol, (relerr(o, ro), relerr(S, rS))
+
+
+@pytest.mark.parametrize("name,ov", [
+    ("gdn_t4096_h12", dict(T=300, H=2, HV=2)),                   # tensor-core path
+    ("gdn_long_t65000", dict(T=200, H=2, HV=4)),                 # with an initial state
+    ("tiny_fp32", {}),                                           # general fp32 path
+])
+def test_ungated(name, ov):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    x = gin.make_inputs(w)
+    assert gdr.chunk_fwd_path(gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V,
+                                            gdr.GDR_BF16 if w.dtype == torch.bfloat16 else gdr.GDR_F32,
+                                            gdr.GDR_F32), w.C, gdr.GDR_GATE_NONE) == \
+        (1 if name != "tiny_fp32" else 0)
+    check_ungated(w, x)
+
+
+def test_ungated_equals_zero_gate():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=200, H=2, HV=2)
+    x = gin.make_inputs(w)
+    x0 = dict(x, g=torch.zeros_like(x["g"]))
+    o0, S0 = gpu_run(x0, w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o1, S1 = gdr.chunk_fwd(d["q"], d["k"], d["v"], None, d["beta"], None, chunk_size=w.C,
+                           scale=w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert np.array_equal(o0, o1.cpu().numpy()) and np.array_equal(S0, S1.cpu().numpy())
+
+
+@pytest.mark.parametrize("name,ov", [
+    ("gdn_t4096_h12", dict(T=300, H=2, HV=2, K=64, V=64, C=128)),
+    ("gdn_long_t65000", dict(T=260, H=1, HV=2, K=64, V=48, C=128)),     # K != V, carried state
+    ("kda_gqa_t8192", dict(B=1, T=200, H=1, HV=2, K=64, V=64, C=128)),
+    ("tiny_fp32", dict(T=300, C=128)),
+])
+def test_chunk_size_128(name, ov):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V,
+                         gdr.GDR_BF16 if w.dtype == torch.bfloat16 else gdr.GDR_F32, gdr.GDR_F32)
+    assert gdr.chunk_fwd_path(dims, 128, w.gate_mode) == 0          # general path
+    check_against_oracle(w, gin.make_inputs(w))
+
+
+def test_chunk_size_128_equals_64():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=256, H=1, HV=1, K=64, V=64, C=128)
+    x = gin.make_inputs(w)
+    o128, S128 = gpu_run(x, w)
+    o64, S64 = gpu_run(x, dataclasses_replace(w, C=64))
+    assert relerr(o128, o64) <= 2e-3 and relerr(S128, S64) <= 2e-3
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
