@@ -31,7 +31,7 @@ EXPORTED = (
     "gdr_chunk_fwd", "gdr_chunk_prepare", "gdr_chunk_recur", "gdr_chunk_fwd_workspace_size",
     "gdr_chunk_fwd_host",
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
-    "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc",
+    "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
 )
 # Size of the library-owned scratch used by gdr_chunk_fwd_noalloc (per device).
 GDR_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -86,6 +86,8 @@ def load_library(path: Optional[str] = None):
         lib.gdr_status_string.restype = ctypes.c_char_p
         lib.gdr_chunk_fwd_path.argtypes = [dp, ip, ip, ctypes.POINTER(ctypes.c_int)]
         lib.gdr_chunk_fwd_path.restype = ip
+        lib.gdr_recurrent_fwd.argtypes = [vp, vp, vp, vp, vp, vp, fp, ip, ip, vp, dp, vp]
+        lib.gdr_recurrent_fwd.restype = ip
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ip
         if path is None:
@@ -234,6 +236,31 @@ def chunk_fwd_noalloc(q, k, v, g, beta, initial_state=None, *, out, final_state=
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_fwd_noalloc")
     return out, final_state
+
+
+def recurrent_fwd(q, k, v, g, beta, state, *, scale: Optional[float] = None,
+                  use_qk_l2norm: bool = True, out=None, out_dtype=None, stream=None):
+    """Token-by-token recurrence (decode step for T = 1) on CUDA tensors.
+
+    Shapes as for chunk_fwd; ``state`` fp32 [B,HV,K,V] is updated in place
+    (the state before the first token on entry, after the last token on
+    return). Returns o [B,T,HV,V]."""
+    import torch
+    B, T, H, HV, K, V, gate_mode = _shapes(q, v, g)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out_dtype))
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty(B, T, HV, V, dtype=out_dtype, device=q.device)
+    st = load_library().gdr_recurrent_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), ctypes.c_float(scale),
+        int(bool(use_qk_l2norm)), gate_mode, _ptr(out), ctypes.byref(dims), _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_recurrent_fwd")
+    return out
 
 
 def chunk_fwd_host_buffer_size(dims: gdr_dims, chunk_size: int, gate_mode: int,

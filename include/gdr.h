@@ -209,6 +209,32 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  float scale, int use_qk_l2norm, int gate_mode, void* out,
                                  float* final_state, const gdr_dims* dims, gdr_stream_t stream);
 
+/*
+ * gdr_recurrent_fwd -- the token-by-token (recurrent) form, for decoding.
+ *
+ * Applies, for each (b, hv) and token t = 0 .. T-1 in order, the recurrence
+ * of the "分块并行计算（Chunkwise）" notes (section "为什么需要分块？"):
+ *   S <- diag(exp(g_t)) S;  S <- S + beta_t k_t (v_t - S^T k_t)^T;  o_t = S^T (scale q_t)
+ * with q_t, k_t L2-normalised when use_qk_l2norm is nonzero. T = 1 is the
+ * single-token decode step; T > 1 runs the tokens one after another with the
+ * state held on chip (one read and one write of each state per call). The
+ * result equals gdr_chunk_fwd on the same tokens up to rounding.
+ *
+ *   q, k     (device) [B, T, H, K]   in_dtype
+ *   v        (device) [B, T, HV, V]  in_dtype
+ *   g, beta  as for gdr_chunk_fwd (g may be NULL with GDR_GATE_NONE)
+ *   state    (device) fp32 [B, HV, K, V]: read as the state before token 0 and
+ *            overwritten with the state after token T-1 (caller-owned)
+ *   out      (device) [B, T, HV, V] out_dtype; must not overlap the inputs
+ *   dims     as for gdr_chunk_fwd; K <= 128, any V
+ *
+ * Errors: invalid arguments return synchronously and enqueue nothing;
+ * B == 0 or T == 0 is a no-op. No workspace and no device waits.
+ */
+gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* state, float scale, int use_qk_l2norm,
+                             int gate_mode, void* out, const gdr_dims* dims, gdr_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status s);
 

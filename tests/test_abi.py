@@ -145,3 +145,20 @@ def test_gate_array_required_unless_ungated(lib):
         gdr.GDR_ERR_INVALID_ARG
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, gate=3) == gdr.GDR_ERR_INVALID_ARG
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=128) == gdr.GDR_ERR_UNSUPPORTED
+
+
+def test_recurrent_argument_errors(lib):
+    A = 1 << 20
+    P = ctypes.c_void_p
+    def rec(d, g=A, gate=0, scale=0.1, q=A):
+        return lib.gdr_recurrent_fwd(P(q) if q else None, P(A), P(A), P(g) if g else None, P(A),
+                                     P(A), ctypes.c_float(scale), 1, gate, P(A), ctypes.byref(d),
+                                     None)
+    assert rec(dims(T=1), q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert rec(dims(T=1), g=None) == gdr.GDR_ERR_INVALID_ARG
+    assert rec(dims(T=1), gate=3) == gdr.GDR_ERR_INVALID_ARG
+    assert rec(dims(T=1), scale=0.0) == gdr.GDR_ERR_INVALID_ARG
+    assert rec(dims(T=1, HV=3)) == gdr.GDR_ERR_INVALID_ARG
+    assert rec(dims(T=1, K=256)) == gdr.GDR_ERR_UNSUPPORTED
+    assert rec(dims(T=0)) == gdr.GDR_OK
+    assert rec(dims(B=0, T=1)) == gdr.GDR_OK
