@@ -60,6 +60,8 @@ def dist_env():
 
 def workload(name):
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    if name in gin.DECODE_WORKLOADS:
+        return gin.DECODE_WORKLOADS[name]
     return gin.WORKLOADS[name or gin.HEADLINE]
 
 
@@ -369,11 +371,121 @@ def run_ours(args, rank, local_rank, world):
     return 0
 
 
+def run_decode(args, rank, local_rank, world):
+    """The recurrent (decode) form on a decode workload: every step applies one
+    token per sequence to states resident in HBM (read and written in place)."""
+    import torch
+    import chunkwise_gated_delta_gdr_gb300 as gdr
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    from chunkwise_gated_delta_gdr_gb300 import shard
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = workload(args.workload)
+    wr = gin.shrink(w, seed=w.seed + 1000 * rank)
+    x_cpu = gin.make_inputs(wr)
+    x = {n: (t.to(dev) if t is not None else None) for n, t in x_cpu.items()}
+    state = x["s0"].clone()
+    out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdr.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], state, scale=w.scale,
+                          use_qk_l2norm=w.use_qk_l2norm, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.2)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    ms = shard.step_time_across_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), pg)
+    assert torch.isfinite(out).all() and torch.isfinite(state).all()
+
+    # End to end: the token inputs come from pinned host memory and o goes back
+    # every step; the states stay resident on the device (as in decoding).
+    names = ("q", "k", "v", "g", "beta")
+    pin = {n: x_cpu[n].pin_memory() for n in names}
+    dbuf = {n: torch.empty_like(x[n]) for n in names}
+    out_h = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32).pin_memory()
+    h2d = sum(pin[n].numel() * pin[n].element_size() for n in names)
+    d2h = out_h.numel() * 4
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 200))
+    e_a.record(stream)
+    for _ in range(n_e2e):
+        for n in names:
+            dbuf[n].copy_(pin[n], non_blocking=True)
+        gdr.recurrent_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], state,
+                          scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out=out, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = shard.step_time_across_ranks(e_a.elapsed_time(e_b) / n_e2e, pg)
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    hbm, _, peak_kind = load_peaks()
+    sbytes = 2 * w.B * w.HV * w.K * w.V * 4                      # state read + write
+    io = (2 * w.B * w.T * w.H * w.K * 2 + w.B * w.T * w.HV * w.V * 2 + 2 * w.B * w.T * w.HV * 4 +
+          w.B * w.T * w.HV * w.V * 4)
+    bytes_alg = sbytes + io
+    achieved = bytes_alg / (ms * 1e-3) / 1e9
+    tokens = world * w.B * w.T
+    line = {
+        "metric": f"tokens/s of the recurrent decode step ({w.name}); % of HBM roofline",
+        "value": tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
+                   "V": w.V, "gate": "scalar", "in_dtype": "bf16", "out_dtype": "fp32",
+                   "state": "fp32 in place", "l2_flush": "512MiB write before each step",
+                   "parallelism": f"{world} rank(s), value heads sharded, no collective"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "scope": "one gdr_recurrent_fwd call (recurrent_kernel)",
+                     "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    line["cpu_baseline"] = cpu_baseline(w, x_cpu)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    if args.workload in gin.DECODE_WORKLOADS:
+        return run_decode(args, rank, local_rank, world)
     return run_ours(args, rank, local_rank, world)
 
 

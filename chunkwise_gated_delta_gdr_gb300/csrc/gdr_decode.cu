@@ -11,9 +11,10 @@
 // back once, in place: the per-token HBM traffic is the token's q, k, v, gate
 // and o, and a call's total is one read and one write of every state.
 //
-// One CTA per (V tile of 32 columns, hv, b), 8 warps: warp w holds state rows
-// [16 w, 16 w + 16) of the tile's columns (lane = column), so every state
-// access is a coalesced 128-byte row segment. Per token the column sums
+// One CTA per (V tile of 32 columns, hv, b), 16 warps: warp w holds state rows
+// [8 w, 8 w + 8) of the tile's columns (lane = column), so every state access
+// is a coalesced 128-byte row segment; 64 registers per thread keep two CTAs
+// (32 warps) per SM in flight, which the HBM stream needs. Per token the column sums
 // (S^T k and S^T q over all rows) are combined across the warps through
 // shared memory; everything else is per element.
 #include <math.h>
@@ -23,7 +24,7 @@
 namespace gdr {
 namespace {
 
-constexpr int kWarps = 8, kRows = 16, kThreads = kWarps * 32, kCols = 32;
+constexpr int kWarps = 16, kRows = 128 / kWarps, kThreads = kWarps * 32, kCols = 32;
 static_assert(kWarps * kRows == 128, "rows per CTA must cover K <= 128");
 
 struct DecodeArgs {
@@ -44,7 +45,7 @@ __device__ __forceinline__ float ld_x(const void* p, size_t i, int bf16) {
   return static_cast<const float*>(p)[i];
 }
 
-__global__ void __launch_bounds__(kThreads) recurrent_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(DecodeArgs a) {
   __shared__ float kr[128], qr[128], dec[128];
   __shared__ float red_u[kWarps][kCols], red_o[kWarps][kCols];
   __shared__ float tok[4];   // |k|^-1, scale |q|^-1, beta, q~ . k^
@@ -66,6 +67,9 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(DecodeArgs a) {
 
   for (int t = 0; t < a.T; ++t) {
     const size_t bt = (size_t)b * a.T + t;
+    // Every load of the token is issued up front, beside the state loads.
+    const float vv = cok ? ld_x(a.v, (bt * a.HV + hv) * V + col, a.in_bf16) : 0.f;
+    const float bet = tid == 0 ? a.beta[bt * a.HV + hv] : 0.f;
     if (tid < K) {
       const size_t qk = (bt * a.H + h) * K + tid;
       kr[tid] = ld_x(a.k, qk, a.in_bf16);
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(DecodeArgs a) {
         const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
         tok[0] = nk;
         tok[1] = nq;
-        tok[2] = a.beta[bt * a.HV + hv];
+        tok[2] = bet;
         tok[3] = nq * nk * sqk;
       }
     }
@@ -119,7 +123,6 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(DecodeArgs a) {
       u += red_u[w][lane];
       oq += red_o[w][lane];
     }
-    const float vv = cok ? ld_x(a.v, (bt * a.HV + hv) * V + col, a.in_bf16) : 0.f;
     const float wv = beta * (vv - u);                 // delta-rule write of this column
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {

@@ -85,6 +85,14 @@ WORKLOADS = {
 }
 
 # The workload the throughput figure is quoted on.
+# The token-by-token (decode) form: one new token per sequence, carried state.
+DECODE_WORKLOADS = {
+    "decode_b64_h16": Workload(
+        "decode_b64_h16", B=64, T=1, H=16, HV=16, K=128, V=128, C=64, dtype=torch.bfloat16,
+        gate_mode=0, g_mean=0.0, g_std=1.0, s0_std=0.02, seed=5,
+        description="decode step: 64 sequences x 16 heads, one token each, fp32 state in place"),
+}
+
 HEADLINE = "gdn_t4096_h12"
 
 
