@@ -66,9 +66,11 @@ def _load():
         lib.gdr_oracle_chunkwise_rowbeta.argtypes = common + [ip, ip, vp, ip, vp, vp, ip]
         lib.gdr_oracle_bruteforce.argtypes = common + [vp, vp]
         lib.gdr_oracle_unit_lower_inverse.argtypes = [vp, ip, ip, vp]
+        lib.gdr_oracle_ssd_recurrent.argtypes = [vp] * 5 + [ip] * 2 + [ip] * 7 + [dp, ip] + \
+            [vp, ip, vp, vp, ip]
         for f in (lib.gdr_oracle_recurrent, lib.gdr_oracle_chunkwise,
                   lib.gdr_oracle_chunkwise_rowbeta, lib.gdr_oracle_bruteforce,
-                  lib.gdr_oracle_unit_lower_inverse):
+                  lib.gdr_oracle_unit_lower_inverse, lib.gdr_oracle_ssd_recurrent):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -108,7 +110,7 @@ def _prepare(q, k, v, g, beta, s0):
     sa, sd = _as_array(s0, (F64, F32))
     # g, beta and s0 share one element-type code in the C interface.
     gate_dtype = gd
-    if bd != gd:
+    if ba is not None and bd != gd:
         ba = ba.astype(np.float64) if gd == F64 else ba.astype(np.float32)
     if sa is not None and sd != gd:
         sa = sa.astype(np.float64) if gd == F64 else sa.astype(np.float32)
@@ -156,6 +158,22 @@ def recurrent(q, k, v, g, beta, s0=None, *, scale=None, use_qk_l2norm=True, sel=
                                       scale, int(bool(use_qk_l2norm)), _ptr(sarr), nseq,
                                       _ptr(o), _ptr(S), int(nthreads), int(mutation))
     _check(rc, "gdr_oracle_recurrent")
+    return _reshape_out(o, S, sel, B, T, HV, K, V)
+
+
+def ssd_recurrent(q, k, v, g, s0=None, *, scale=None, use_qk_l2norm=True, sel=None, nthreads=0):
+    """The Mamba2 SSD recurrence in float64: S <- diag(exp g_t) S + k_t v_t^T,
+    o_t = S^T (scale q_t), with no delta erase and no beta."""
+    arrs, qd, gd, (B, T, H, HV, K, V), gm = _prepare(q, k, v, g, None, s0)
+    qa, ka, va, ga, _, sa = arrs
+    scale = K ** -0.5 if scale is None else float(scale)
+    sarr, nseq = _sel_array(sel, B, HV)
+    o = np.zeros((nseq, T, V), np.float64)
+    S = np.zeros((nseq, K, V), np.float64)
+    rc = _load().gdr_oracle_ssd_recurrent(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(sa), qd, gd,
+                                          B, T, H, HV, K, V, gm, scale, int(bool(use_qk_l2norm)),
+                                          _ptr(sarr), nseq, _ptr(o), _ptr(S), int(nthreads))
+    _check(rc, "gdr_oracle_ssd_recurrent")
     return _reshape_out(o, S, sel, B, T, HV, K, V)
 
 

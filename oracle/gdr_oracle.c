@@ -13,7 +13,7 @@
  *            "为什么需要分块？", "chunk 内的 cumsum 与下三角解", the listings
  *            "naive_chunk_kda" (代码对照) and the inter-chunk loop (chunk 间递推),
  *            the shape table (形状流水线) and "_decayed_dot" (Decayed dot 函数).
- *   [blog]   "Chunkwise 并行算法 —— 线性注意力": §2.1 (Householder form),
+ *   [blog]   "Chunkwise 并行算法 —— 线性注意力": §1.1-1.2 (Mamba2 SSD), §2.1 (Householder form),
  *            §2.3 (UT transform, Neumann series, row recursion), §2.4.
  *   [optim]  "DeltaNet chunk kernel optimization" (deltanet_chunk_optimize.py):
  *            _l2norm, the padding and trimming steps, the row-beta weighted
@@ -27,6 +27,9 @@
  *                               right-hand sides ([blog] §2.3, [optim]).
  *   gdr_oracle_bruteforce       explicit products of the one-step maps
  *                               (I - beta k k^T) D_t ([blog] §2.1), for tiny T, K.
+ *   gdr_oracle_ssd_recurrent    the Mamba2 SSD recurrence S_t = diag(alpha_t) S_{t-1}
+ *                               + k_t v_t^T, o_t = S_t^T q_t (no delta erase, no
+ *                               beta; [blog] §1.1), token by token.
  *   gdr_oracle_unit_lower_inverse  (I + L)^{-1} three ways ([notes] solve,
  *                               [blog] §2.3 Neumann series and row recursion).
  *
@@ -218,6 +221,53 @@ int gdr_oracle_recurrent(const void* q, const void* k, const void* v, const void
     }
     if (s_out) memcpy(s_out + s * (long)K * V, S, sizeof(double) * K * V);
     free(S); free(qt); free(kt); free(u); free(pre);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Mamba2 SSD ([blog] §1.1): per (b, hv), S <- diag(exp(g_t)) S + k_t v_t^T,
+ * o_t = S^T (scale q_t), token by token; q_t, k_t L2-normalised when asked.
+ * Same tensor conventions as gdr_oracle_recurrent; there is no beta.
+ * ------------------------------------------------------------------------- */
+int gdr_oracle_ssd_recurrent(const void* q, const void* k, const void* v, const void* g,
+                             const void* s0, int qkv_dtype, int gate_dtype, int B, int T, int H,
+                             int HV, int K, int V, int gate_mode, double scale, int use_qk_l2norm,
+                             const int* sel, int nsel, double* o_out, double* s_out,
+                             int nthreads) {
+  /* beta is never read: g stands in for it so that the shared checks apply. */
+  problem p = {q, k, v, g, g, s0, qkv_dtype, gate_dtype, B, T, H, HV, K, V,
+               gate_mode, use_qk_l2norm, scale};
+  int rc = check_problem(&p);
+  if (rc) return rc;
+  long nseq = sel ? nsel : (long)B * HV;
+  int group = HV / H;
+
+#pragma omp parallel for num_threads(resolve_threads(nthreads)) schedule(dynamic, 1)
+  for (long s = 0; s < nseq; ++s) {
+    long bh = sel ? sel[s] : s;
+    int b = (int)(bh / HV), hv = (int)(bh % HV);
+    int h = hv / group;
+    double* S = malloc(sizeof(double) * K * V);
+    double* qt = malloc(sizeof(double) * K);
+    double* kt = malloc(sizeof(double) * K);
+    load_s0(&p, b, hv, S);
+    for (int t = 0; t < T; ++t) {
+      load_qk(&p, q, b, t, h, qt);
+      load_qk(&p, k, b, t, h, kt);
+      for (int c = 0; c < K; ++c) {
+        double d = exp(load_g(&p, b, t, hv, c));
+        for (int j = 0; j < V; ++j)
+          S[(long)c * V + j] = d * S[(long)c * V + j] + kt[c] * load_v(&p, b, t, hv, j);
+      }
+      for (int j = 0; j < V; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < K; ++c) acc += S[(long)c * V + j] * scale * qt[c];
+        o_out[((long)s * T + t) * V + j] = acc;
+      }
+    }
+    if (s_out) memcpy(s_out + s * (long)K * V, S, sizeof(double) * K * V);
+    free(S); free(qt); free(kt);
   }
   return 0;
 }

@@ -159,6 +159,55 @@ def test_ungated_is_householder_deltanet(C):
     assert relerr(o_c, o_r) <= 1e-10 and relerr(s_c, s_r) <= 1e-10
 
 
+# ---------------------------------------------------------------- Mamba2 SSD (NEXT row)
+def _ssd_block_expansion(p, hv, scale, per_key):
+    """Block expansion of the SSD recurrence (Chunkwise blog, section 1.2),
+    written as whole-sequence matrix algebra for one head:
+      O   = ((Q~ K^T) (.) Gamma) V + (Q~ (.) exp G) S0,  Gamma_ij = exp(G_i - G_j), j <= i
+      S_T = K^T diag(exp(G_T - G)) V + diag(exp G_T) S0
+    with G the cumulative sum of the log-decays (per key channel if per_key)."""
+    q = p["q"][0, :, 0]
+    k = p["k"][0, :, 0]
+    qn = q / np.sqrt(np.sum(q ** 2, 1, keepdims=True) + 1e-6) * scale
+    kn = k / np.sqrt(np.sum(k ** 2, 1, keepdims=True) + 1e-6)
+    v = p["v"][0, :, hv]
+    S0 = p["s0"][0, hv]
+    T = q.shape[0]
+    if not per_key:
+        G = np.cumsum(p["g"][0, :, hv])
+        Gam = np.tril(np.exp(G[:, None] - G[None, :]))
+        O = ((qn @ kn.T) * Gam) @ v + (qn * np.exp(G)[:, None]) @ S0
+        ST = kn.T @ (np.exp(G[-1] - G)[:, None] * v) + np.exp(G[-1]) * S0
+    else:
+        G = np.cumsum(p["g"][0, :, hv], axis=0)                     # T x K
+        A = np.einsum("ic,jc,ijc->ij", qn, kn, np.exp(G[:, None, :] - G[None, :, :]))
+        O = np.tril(A) @ v + (qn * np.exp(G)) @ S0
+        ST = (kn * np.exp(G[-1][None, :] - G)).T @ v + np.exp(G[-1])[:, None] * S0
+    return O, ST
+
+
+@pytest.mark.parametrize("gate_mode", [0, 1])
+def test_ssd_equals_block_expansion(gate_mode):
+    p = rand_problem(91, T=33, K=7, V=5, H=1, HV=2, gate_mode=gate_mode)
+    scale = 0.37
+    o, S = oracle.ssd_recurrent(p["q"], p["k"], p["v"], p["g"], p["s0"], scale=scale)
+    for hv in range(2):
+        O, ST = _ssd_block_expansion(p, hv, scale, gate_mode == 1)
+        assert relerr(o[0, :, hv], O) <= 1e-12
+        assert relerr(S[0, hv], ST) <= 1e-12
+
+
+def test_ssd_without_decay_is_causal_linear_attention():
+    """alpha = 1 and a zero initial state: O = tril(Q K^T) V (no normalisation)."""
+    p = rand_problem(92, T=20, K=6, V=4, H=1, HV=1, s0=False)
+    p["g"] = np.zeros_like(p["g"])
+    o, S = oracle.ssd_recurrent(p["q"], p["k"], p["v"], p["g"], None, scale=1.0,
+                                use_qk_l2norm=False)
+    q, k, v = p["q"][0, :, 0], p["k"][0, :, 0], p["v"][0, :, 0]
+    assert relerr(o[0, :, 0], np.tril(q @ k.T) @ v) <= 1e-12
+    assert relerr(S[0, 0], k.T @ v) <= 1e-12
+
+
 # ---------------------------------------------------------------- P-9, hand-worked cases
 def test_single_token_closed_form():
     """T = 1: S_1 = (I - beta k k^T) D S_0 + beta k v^T, o = S_1^T (scale q)."""
