@@ -32,6 +32,7 @@ EXPORTED = (
     "gdr_chunk_fwd_host",
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
     "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
+    "gdr_ssd_chunk_fwd", "gdr_ssd_chunk_fwd_workspace_size",
 )
 # Size of the library-owned scratch used by gdr_chunk_fwd_noalloc (per device).
 GDR_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -88,6 +89,10 @@ def load_library(path: Optional[str] = None):
         lib.gdr_chunk_fwd_path.restype = ip
         lib.gdr_recurrent_fwd.argtypes = [vp, vp, vp, vp, vp, vp, fp, ip, ip, vp, dp, vp]
         lib.gdr_recurrent_fwd.restype = ip
+        lib.gdr_ssd_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, ip, fp, ip, ip, vp, vp, dp, vp, sz, vp]
+        lib.gdr_ssd_chunk_fwd.restype = ip
+        lib.gdr_ssd_chunk_fwd_workspace_size.argtypes = [dp, ip, ip]
+        lib.gdr_ssd_chunk_fwd_workspace_size.restype = sz
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ip
         if path is None:
@@ -235,6 +240,35 @@ def chunk_fwd_noalloc(q, k, v, g, beta, initial_state=None, *, out, final_state=
         ctypes.byref(dims), _stream_handle(stream))
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_fwd_noalloc")
+    return out, final_state
+
+
+def ssd_chunk_fwd(q, k, v, g, initial_state=None, *, chunk_size: int = 64,
+                  scale: Optional[float] = None, use_qk_l2norm: bool = True, out_dtype=None,
+                  output_final_state: bool = True, stream=None):
+    """Chunkwise Mamba2 SSD forward (S <- diag(exp g) S + k v^T, o = S^T scale q):
+    the gated recurrence without the delta erase and without beta. Shapes as
+    for chunk_fwd. Returns (o, final_state)."""
+    import torch
+    B, T, H, HV, K, V, gate_mode = _shapes(q, v, g)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out_dtype))
+    out = torch.empty(B, T, HV, V, dtype=out_dtype, device=q.device)
+    final_state = (torch.empty(B, HV, K, V, dtype=torch.float32, device=q.device)
+                   if output_final_state else None)
+    lib = load_library()
+    ws_bytes = lib.gdr_ssd_chunk_fwd_workspace_size(ctypes.byref(dims), int(chunk_size), gate_mode)
+    if ws_bytes == 0 and B * T > 0:
+        raise GdrError(GDR_ERR_UNSUPPORTED, "gdr_ssd_chunk_fwd_workspace_size")
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.gdr_ssd_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(initial_state), int(chunk_size),
+        ctypes.c_float(scale), int(bool(use_qk_l2norm)), gate_mode, _ptr(out), _ptr(final_state),
+        ctypes.byref(dims), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_ssd_chunk_fwd")
     return out, final_state
 
 

@@ -121,6 +121,14 @@ size_t gdr_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int ga
   return sizeof(WorkspaceHeader) + align_up(body_bytes(p));
 }
 
+size_t gdr_ssd_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode) {
+  if (check_dims(dims, chunk_size, gate_mode) != GDR_OK) return 0;
+  Problem p = make_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, chunk_size,
+                           1.f, 0, gate_mode, nullptr, nullptr, dims);
+  p.ssd = 1;
+  return sizeof(WorkspaceHeader) + align_up(body_bytes(p));
+}
+
 int gdr_chunk_fwd_path(const gdr_dims* dims, int chunk_size, int gate_mode, gdr_status* status) {
   gdr_status st = check_dims(dims, chunk_size, gate_mode);
   if (status) *status = st;
@@ -140,13 +148,13 @@ gdr_status run(int stage, const void* q, const void* k, const void* v, const flo
                const float* beta, const float* initial_state, int chunk_size, float scale,
                int use_qk_l2norm, int gate_mode, void* out, float* final_state,
                const gdr_dims* dims, void* workspace, size_t workspace_bytes,
-               gdr_stream_t stream) {
+               gdr_stream_t stream, int ssd = 0) {
   gdr_status st = check_dims(dims, chunk_size, gate_mode);
   if (st != GDR_OK) return st;
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
   const bool work = dims->B > 0 && dims->T > 0;
   if (work && (!q || !k)) return GDR_ERR_INVALID_ARG;
-  if (work && (stage & 1) && (!v || (!g && gate_mode != GDR_GATE_NONE) || !beta))
+  if (work && (stage & 1) && (!v || (!g && gate_mode != GDR_GATE_NONE) || (!beta && !ssd)))
     return GDR_ERR_INVALID_ARG;
   if (work && (stage & 2) && !out) return GDR_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, g, beta, initial_state, out, final_state};
@@ -165,12 +173,14 @@ gdr_status run(int stage, const void* q, const void* k, const void* v, const flo
                         : cudaMemsetAsync(final_state, 0, state_bytes, s);
     return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
   }
-  const size_t need = gdr_chunk_fwd_workspace_size(dims, chunk_size, gate_mode);
+  const size_t need = ssd ? gdr_ssd_chunk_fwd_workspace_size(dims, chunk_size, gate_mode)
+                          : gdr_chunk_fwd_workspace_size(dims, chunk_size, gate_mode);
   if (!workspace || workspace_bytes < need) return GDR_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return GDR_ERR_ALIGNMENT;
 
   Problem p = make_problem(q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm,
                            gate_mode, out, final_state, dims);
+  p.ssd = ssd;
   auto* hdr = static_cast<WorkspaceHeader*>(workspace);
   if ((stage & 1) &&
       cudaMemsetAsync(&hdr->error_word, 0, sizeof(unsigned int), s) != cudaSuccess)
@@ -199,6 +209,15 @@ gdr_status gdr_chunk_prepare(const void* q, const void* k, const void* v, const 
                              size_t workspace_bytes, gdr_stream_t stream) {
   return run(1, q, k, v, g, beta, nullptr, chunk_size, scale, use_qk_l2norm, gate_mode, nullptr,
              nullptr, dims, workspace, workspace_bytes, stream);
+}
+
+gdr_status gdr_ssd_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                             const float* initial_state, int chunk_size, float scale,
+                             int use_qk_l2norm, int gate_mode, void* out, float* final_state,
+                             const gdr_dims* dims, void* workspace, size_t workspace_bytes,
+                             gdr_stream_t stream) {
+  return run(3, q, k, v, g, nullptr, initial_state, chunk_size, scale, use_qk_l2norm, gate_mode,
+             out, final_state, dims, workspace, workspace_bytes, stream, 1);
 }
 
 gdr_status gdr_chunk_recur(const void* q, const void* k, const float* initial_state,

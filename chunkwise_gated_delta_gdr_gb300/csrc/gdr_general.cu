@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   }
   for (int i = tid; i < C; i += kThreads) {
     const int t = t0 + i;
-    bb[i] = (t < p.T) ? p.beta[((long)b * p.T + t) * p.HV + hv] : 0.f;
+    // SSD: beta = 1 everywhere (padded rows carry k = v = 0).
+    bb[i] = p.ssd ? 1.f : (t < p.T) ? p.beta[((long)b * p.T + t) * p.HV + hv] : 0.f;
   }
   __syncthreads();
 
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
         }
       }
     }
-    L[idx] = (j < i) ? akk * bb[j] : 0.f;
+    L[idx] = (j < i && !p.ssd) ? akk * bb[j] : 0.f;   // SSD: no erase, M = I
     AQ[idx] = (j <= i) ? aqk * bb[j] : 0.f;
   }
 
@@ -243,7 +244,8 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   __syncthreads();
   float* W = a.s.W + chunk * (long)C * K;
   float* U = a.s.U + chunk * (long)C * V;
-  for (int idx = tid; idx < C * K; idx += kThreads) W[idx] = ks[(idx / K) * KP + idx % K];
+  for (int idx = tid; idx < C * K; idx += kThreads)
+    W[idx] = p.ssd ? 0.f : ks[(idx / K) * KP + idx % K];   // SSD: r = U - W S = v
   for (int idx = tid; idx < C * V; idx += kThreads) U[idx] = vs[(idx / V) * VP + idx % V];
 }
 

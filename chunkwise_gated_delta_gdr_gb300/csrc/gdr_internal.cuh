@@ -24,6 +24,7 @@ struct Problem {
   int N;                 // chunks per sequence, ceil(T / C)
   int in_bf16, out_bf16, gate_mode, use_l2;
   float scale;
+  int ssd = 0;           // Mamba2 SSD update: no delta erase, no beta (general path only)
 };
 
 // Workspace header: first 256 bytes of every workspace.

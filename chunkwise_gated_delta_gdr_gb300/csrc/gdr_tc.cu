@@ -4,7 +4,7 @@
 namespace gdr {
 
 bool tc_supported(const Problem& p) {
-  return p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
+  return !p.ssd && p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
 }
 
 namespace {

@@ -235,6 +235,23 @@ gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void* v, const 
                              const float* beta, float* state, float scale, int use_qk_l2norm,
                              int gate_mode, void* out, const gdr_dims* dims, gdr_stream_t stream);
 
+/*
+ * gdr_ssd_chunk_fwd -- chunkwise forward of the Mamba2 SSD recurrence, the
+ * second workload of the "Chunkwise 并行算法 —— 线性注意力" page (§1.1-1.2):
+ *   S <- diag(exp(g_t)) S + k_t v_t^T,   o_t = S^T (scale q_t)
+ * i.e. the gated recurrence without the delta erase and without beta. It
+ * runs on the same chunk machinery with the triangular solve dropped
+ * (M = I, W = 0, U = v) on the general fp32 path. Arguments as for
+ * gdr_chunk_fwd, minus beta; the workspace must hold
+ * gdr_ssd_chunk_fwd_workspace_size() bytes.
+ */
+gdr_status gdr_ssd_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                             const float* initial_state, int chunk_size, float scale,
+                             int use_qk_l2norm, int gate_mode, void* out, float* final_state,
+                             const gdr_dims* dims, void* workspace, size_t workspace_bytes,
+                             gdr_stream_t stream);
+size_t gdr_ssd_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode);
+
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status s);
 

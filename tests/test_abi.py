@@ -162,3 +162,14 @@ def test_recurrent_argument_errors(lib):
     assert rec(dims(T=1, K=256)) == gdr.GDR_ERR_UNSUPPORTED
     assert rec(dims(T=0)) == gdr.GDR_OK
     assert rec(dims(B=0, T=1)) == gdr.GDR_OK
+
+
+def test_ssd_workspace_and_arguments(lib):
+    d = dims()
+    assert lib.gdr_ssd_chunk_fwd_workspace_size(ctypes.byref(d), 64, 0) > 256
+    assert lib.gdr_ssd_chunk_fwd_workspace_size(ctypes.byref(d), 48, 0) == 0
+    A = 1 << 20
+    P = ctypes.c_void_p
+    st = lib.gdr_ssd_chunk_fwd(P(A), P(A), P(A), None, None, 64, ctypes.c_float(0.1), 1, 0, P(A),
+                               None, ctypes.byref(d), P(A), ctypes.c_size_t(1 << 40), None)
+    assert st == gdr.GDR_ERR_INVALID_ARG                    # g required for a gated mode

@@ -299,3 +299,27 @@ def test_chunk_size_128_equals_64():
 def dataclasses_replace(w, **kw):
     import dataclasses
     return dataclasses.replace(w, **kw)
+
+
+# ---- Mamba2 SSD (no delta erase, no beta) on the chunk machinery ------------------
+
+@pytest.mark.parametrize("name,ov", [
+    ("gdn_t4096_h12", dict(T=300, H=2, HV=2)),                 # bf16, scalar gate, C = 64
+    ("gdn_long_t65000", dict(T=200, H=2, HV=4)),               # carried state
+    ("kda_gqa_t8192", dict(B=1, T=150, H=1, HV=2)),            # per-key gate
+    ("tiny_fp32", {}),                                         # fp32, C = 16
+    ("gdn_t4096_h12", dict(T=260, H=1, HV=2, K=64, V=64, C=128)),
+])
+def test_ssd_matches_oracle(name, ov):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.ssd_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["s0"], chunk_size=w.C,
+                             scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rS = oracle.ssd_recurrent(x["q"], x["k"], x["v"], x["g"], x["s0"], scale=w.scale,
+                                  use_qk_l2norm=w.use_qk_l2norm)
+    tol = tol_for(w)
+    eo, es = relerr(o.cpu().numpy(), ro), relerr(S.cpu().numpy(), rS)
+    assert eo <= tol and es <= tol, (eo, es)
