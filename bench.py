@@ -62,6 +62,8 @@ def workload(name):
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
     if name in gin.DECODE_WORKLOADS:
         return gin.DECODE_WORKLOADS[name]
+    if name in gin.SSD_WORKLOADS:
+        return gin.SSD_WORKLOADS[name]
     return gin.WORKLOADS[name or gin.HEADLINE]
 
 
@@ -174,7 +176,7 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(w, x):
+def cpu_baseline(w, x, ssd=False):
     """The float64 oracle (as it stands) on the host cores, on the full workload."""
     import oracle
     ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -183,8 +185,12 @@ def cpu_baseline(w, x):
     times = []
     for _ in range(2):
         t0 = time.perf_counter()
-        oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale,
-                         use_qk_l2norm=w.use_qk_l2norm, nthreads=threads)
+        if ssd:
+            oracle.ssd_recurrent(x["q"], x["k"], x["v"], x["g"], x["s0"], scale=w.scale,
+                                 use_qk_l2norm=w.use_qk_l2norm, nthreads=threads)
+        else:
+            oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale,
+                             use_qk_l2norm=w.use_qk_l2norm, nthreads=threads)
         times.append(time.perf_counter() - t0)
         if times[-1] > 10:
             break
@@ -371,9 +377,10 @@ def run_ours(args, rank, local_rank, world):
     return 0
 
 
-def run_decode(args, rank, local_rank, world):
+def run_decode(args, rank, local_rank, world, kind="decode"):
     """The recurrent (decode) form on a decode workload: every step applies one
-    token per sequence to states resident in HBM (read and written in place)."""
+    token per sequence to states resident in HBM (read and written in place).
+    kind "ssd": the chunkwise Mamba2 SSD forward on an SSD workload instead."""
     import torch
     import chunkwise_gated_delta_gdr_gb300 as gdr
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
@@ -390,14 +397,24 @@ def run_decode(args, rank, local_rank, world):
     wr = gin.shrink(w, seed=w.seed + 1000 * rank)
     x_cpu = gin.make_inputs(wr)
     x = {n: (t.to(dev) if t is not None else None) for n, t in x_cpu.items()}
-    state = x["s0"].clone()
+    state = x["s0"].clone() if x["s0"] is not None else None
     out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32, device=dev)
+    last = {}
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def call(q, k, v, g, beta):
+        if kind == "ssd":
+            last["o"], _ = gdr.ssd_chunk_fwd(q, k, v, g, None, chunk_size=w.C, scale=w.scale,
+                                             use_qk_l2norm=w.use_qk_l2norm,
+                                             out_dtype=torch.float32, output_final_state=False,
+                                             stream=stream)
+        else:
+            gdr.recurrent_fwd(q, k, v, g, beta, state, scale=w.scale,
+                              use_qk_l2norm=w.use_qk_l2norm, out=out, stream=stream)
+
     def step():
-        gdr.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], state, scale=w.scale,
-                          use_qk_l2norm=w.use_qk_l2norm, out=out, stream=stream)
+        call(x["q"], x["k"], x["v"], x["g"], x["beta"])
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -420,7 +437,10 @@ def run_decode(args, rank, local_rank, world):
         pg.barrier()
     clocks = sampler.stop()
     ms = shard.step_time_across_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), pg)
-    assert torch.isfinite(out).all() and torch.isfinite(state).all()
+    if kind == "ssd":
+        assert torch.isfinite(last["o"]).all()
+    else:
+        assert torch.isfinite(out).all() and torch.isfinite(state).all()
 
     # End to end: the token inputs come from pinned host memory and o goes back
     # every step; the states stay resident on the device (as in decoding).
@@ -436,9 +456,8 @@ def run_decode(args, rank, local_rank, world):
     for _ in range(n_e2e):
         for n in names:
             dbuf[n].copy_(pin[n], non_blocking=True)
-        gdr.recurrent_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], state,
-                          scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out=out, stream=stream)
-        out_h.copy_(out, non_blocking=True)
+        call(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"])
+        out_h.copy_(last["o"] if kind == "ssd" else out, non_blocking=True)
     e_b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = shard.step_time_across_ranks(e_a.elapsed_time(e_b) / n_e2e, pg)
@@ -447,31 +466,35 @@ def run_decode(args, rank, local_rank, world):
             pg.destroy_process_group()
         return 0
     hbm, _, peak_kind = load_peaks()
-    sbytes = 2 * w.B * w.HV * w.K * w.V * 4                      # state read + write
+    sbytes = 0 if kind == "ssd" else 2 * w.B * w.HV * w.K * w.V * 4   # state read + write
     io = (2 * w.B * w.T * w.H * w.K * 2 + w.B * w.T * w.HV * w.V * 2 + 2 * w.B * w.T * w.HV * 4 +
           w.B * w.T * w.HV * w.V * 4)
     bytes_alg = sbytes + io
     achieved = bytes_alg / (ms * 1e-3) / 1e9
     tokens = world * w.B * w.T
     line = {
-        "metric": f"tokens/s of the recurrent decode step ({w.name}); % of HBM roofline",
+        "metric": (f"tokens/s of the chunkwise SSD forward ({w.name}); % of HBM roofline"
+                   if kind == "ssd" else
+                   f"tokens/s of the recurrent decode step ({w.name}); % of HBM roofline"),
         "value": tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K,
                    "V": w.V, "gate": "scalar", "in_dtype": "bf16", "out_dtype": "fp32",
-                   "state": "fp32 in place", "l2_flush": "512MiB write before each step",
+                   "state": "none" if kind == "ssd" else "fp32 in place",
+                   "l2_flush": "512MiB write before each step",
                    "parallelism": f"{world} rank(s), value heads sharded, no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,
-                     "scope": "one gdr_recurrent_fwd call (recurrent_kernel)",
+                     "scope": ("one gdr_ssd_chunk_fwd call (general prep + state kernels)"
+                               if kind == "ssd" else "one gdr_recurrent_fwd call (recurrent_kernel)"),
                      "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": (2 if kind == "ssd" else 1) * args.steps,
         "clocks": clocks,
     }
-    line["cpu_baseline"] = cpu_baseline(w, x_cpu)
+    line["cpu_baseline"] = cpu_baseline(w, x_cpu, ssd=kind == "ssd")
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -486,6 +509,8 @@ def main():
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
     if args.workload in gin.DECODE_WORKLOADS:
         return run_decode(args, rank, local_rank, world)
+    if args.workload in gin.SSD_WORKLOADS:
+        return run_decode(args, rank, local_rank, world, kind="ssd")
     return run_ours(args, rank, local_rank, world)
 
 

@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   }
   if (tid < C) {
     const int t = t0 + tid;
-    bb[tid] = (t < p.T) ? p.beta[((size_t)b * p.T + t) * p.HV + hv] : 0.f;
+    // SSD: beta = 1 on real rows.
+    bb[tid] = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
   }
   bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tma, 0, kWaitLimit));
   if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
 #pragma unroll
         for (int z = 0; z < 4; ++z) {
           const int j = jb + e + z;
-          a4[z] = (j < rr) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
+          a4[z] = (j < rr && !p.ssd) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
         }
         *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
@@ -407,7 +408,9 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
       if (!is_u) {
         uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) split_pair(-s[e], -s[e + 1], hi[e / 2], lo[e / 2]);
+        // SSD keeps no erase term: W = 0 (then X = I and U = v).
+        const float ws = p.ssd ? 0.f : -1.f;
+        for (int e = 0; e < 16; e += 2) split_pair(ws * s[e], ws * s[e + 1], hi[e / 2], lo[e / 2]);
         const int bx = c0 >> 6, c = (c0 & 63) >> 3;
         uint8_t* wh = sm + OFF_WS + bx * 8192;
         uint8_t* wl = wh + 16384;

@@ -79,6 +79,7 @@ struct Params {
   unsigned int* error_word;
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;
+  int ssd;                  // Mamba2 SSD update: no delta erase (W = 0), beta = 1
   float scale;
   size_t slab_bytes;
 };

@@ -168,11 +168,13 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         if (n >= NST) ok = ok && mbar_wait(&empty[s], (n / NST - 1) & 1, kWaitLimit);
         if (!ok) break;
         const uint32_t base = smem_u32(sm + s * STAGE);
-        mbar_expect_tx(&full[s], TX);
-        tma_load3(base + W_HI, &maps.w2, 0, 0, idx, &full[s]);
-        tma_load3(base + W_HI + 8192, &maps.w2, 64, 0, idx, &full[s]);
-        tma_load3(base + W_LO, &maps.w2, 0, 64, idx, &full[s]);
-        tma_load3(base + W_LO + 8192, &maps.w2, 64, 64, idx, &full[s]);
+        mbar_expect_tx(&full[s], p.ssd ? TX - 32768 : TX);
+        if (!p.ssd) {                                  // SSD: W = 0, not loaded
+          tma_load3(base + W_HI, &maps.w2, 0, 0, idx, &full[s]);
+          tma_load3(base + W_HI + 8192, &maps.w2, 64, 0, idx, &full[s]);
+          tma_load3(base + W_LO, &maps.w2, 0, 64, idx, &full[s]);
+          tma_load3(base + W_LO + 8192, &maps.w2, 64, 64, idx, &full[s]);
+        }
         tma_load4(base + KT, &maps.k, 0, h, n * C, b, &full[s]);
         tma_load4(base + KT + 8192, &maps.k, 64, h, n * C, b, &full[s]);
         tma_load3(base + U, &maps.u, v0, 0, idx, &full[s]);
@@ -300,24 +302,26 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
 #pragma unroll
         for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = 0.f;
       }
+      if (!p.ssd) {                                    // SSD: r = U
 #pragma unroll
-      for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
-        uint32_t ah[2][4], al[2][4];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          ldsm_x4(ah[h2], smem_u32(xsh) + tile16_off(arow, 16 * (ks2 + h2) + acol));
-          ldsm_x4(al[h2], smem_u32(xsh) + 4096 + tile16_off(arow, 16 * (ks2 + h2) + acol));
-        }
-#pragma unroll
-        for (int jt = 0; jt < 2; ++jt) {
-          uint32_t wh[4], wl[4];
-          ldsm_x4(wh, tile_addr(w_hi, jw + 8 * jt + brow, 16 * ks2 + bcol));
-          ldsm_x4(wl, tile_addr(w_lo, jw + 8 * jt + brow, 16 * ks2 + bcol));
+        for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
+          uint32_t ah[2][4], al[2][4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            mma_bf16_16816(Rhh[jt], ah[h2], wh[2 * h2], wh[2 * h2 + 1]);
-            mma_bf16_16816(Rlh[jt], al[h2], wh[2 * h2], wh[2 * h2 + 1]);
-            mma_bf16_16816(Rhl[jt], ah[h2], wl[2 * h2], wl[2 * h2 + 1]);
+            ldsm_x4(ah[h2], smem_u32(xsh) + tile16_off(arow, 16 * (ks2 + h2) + acol));
+            ldsm_x4(al[h2], smem_u32(xsh) + 4096 + tile16_off(arow, 16 * (ks2 + h2) + acol));
+          }
+#pragma unroll
+          for (int jt = 0; jt < 2; ++jt) {
+            uint32_t wh[4], wl[4];
+            ldsm_x4(wh, tile_addr(w_hi, jw + 8 * jt + brow, 16 * ks2 + bcol));
+            ldsm_x4(wl, tile_addr(w_lo, jw + 8 * jt + brow, 16 * ks2 + bcol));
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              mma_bf16_16816(Rhh[jt], ah[h2], wh[2 * h2], wh[2 * h2 + 1]);
+              mma_bf16_16816(Rlh[jt], al[h2], wh[2 * h2], wh[2 * h2 + 1]);
+              mma_bf16_16816(Rhl[jt], ah[h2], wl[2 * h2], wl[2 * h2 + 1]);
+            }
           }
         }
       }

@@ -4,7 +4,8 @@
 namespace gdr {
 
 bool tc_supported(const Problem& p) {
-  return !p.ssd && p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
+  // SSD with the per-key gate stays on the general path.
+  return !(p.ssd && p.gate_mode) && p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
 }
 
 namespace {
@@ -59,6 +60,7 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.out_bf16 = p.out_bf16;
   f.gate_mode = p.gate_mode;
   f.use_l2 = p.use_l2;
+  f.ssd = p.ssd;
   f.scale = p.scale;
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
   if (stage & 1) {

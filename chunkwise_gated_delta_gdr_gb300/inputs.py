@@ -93,6 +93,14 @@ DECODE_WORKLOADS = {
         description="decode step: 64 sequences x 16 heads, one token each, fp32 state in place"),
 }
 
+# The Mamba2 SSD recurrence on the headline shape (beta is drawn but not used).
+SSD_WORKLOADS = {
+    "ssd_t4096_h12": Workload(
+        "ssd_t4096_h12", B=1, T=4096, H=12, HV=12, K=128, V=128, C=64, dtype=torch.bfloat16,
+        gate_mode=0, g_mean=0.0, g_std=1.0, s0_std=None, seed=6,
+        description="Mamba2 SSD forward on the headline shape"),
+}
+
 HEADLINE = "gdn_t4096_h12"
 
 
