@@ -51,6 +51,8 @@ CASES = [
     ("gdn_long_t65000", dict(T=3, H=2, HV=2, K=64, V=96)),       # K != V
     ("tiny_fp32", dict(T=11)),                                   # fp32 inputs, K = V = 32
     ("tiny_fp32", dict(T=4, K=20, V=40)),                        # ragged rows and columns
+    ("tiny_fp32", dict(T=3, K=16, V=30)),                        # V % 4 != 0: fallback kernel
+    ("gdn_t4096_h12", dict(B=2, T=2, H=3, HV=6, K=128, V=72)),   # ragged last V tile
 ]
 
 
