@@ -323,3 +323,37 @@ def test_ssd_matches_oracle(name, ov):
     tol = tol_for(w)
     eo, es = relerr(o.cpu().numpy(), ro), relerr(S.cpu().numpy(), rS)
     assert eo <= tol and es <= tol, (eo, es)
+
+
+# ---- the fused recurrence on further shapes ---------------------------------------
+
+@pytest.mark.parametrize("ov", [
+    dict(B=3, T=200, H=2, HV=4),            # batch > 1, GQA, carried state below
+    dict(B=2, T=64, H=1, HV=3),             # exactly one chunk
+    dict(B=1, T=1000, H=4, HV=8),           # 64 chains, 16 chunks, ragged tail
+])
+def test_fused_recurrence_shapes(ov):
+    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], **ov)
+    check_against_oracle(w, gin.make_inputs(w))
+
+
+def test_fused_recurrence_reuses_its_flags():
+    """One prepare, then three recurrences on the same workspace: each must wait
+    for its own chains (the progress flags are reset per launch)."""
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=700, H=3, HV=3)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims, w.C, 0), dtype=torch.uint8, device=dev)
+    gdr.chunk_prepare(d["q"], d["k"], d["v"], d["g"], d["beta"], workspace=ws, scale=w.scale,
+                      out_dtype=torch.float32)
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], None, scale=w.scale)
+    for rep in range(3):
+        o = torch.full((w.B, w.T, w.HV, w.V), float("nan"), device=dev)
+        S = torch.empty(w.B, w.HV, w.K, w.V, device=dev)
+        gdr.chunk_recur(d["q"], d["k"], None, workspace=ws, out=o, final_state=S, HV=w.HV, V=w.V,
+                        gate_mode=0, scale=w.scale)
+        torch.cuda.synchronize()
+        assert gdr.stream_status(None, ws) == gdr.GDR_OK
+        assert relerr(o.cpu().numpy(), ro) <= 2e-3 and relerr(S.cpu().numpy(), rS) <= 2e-3
