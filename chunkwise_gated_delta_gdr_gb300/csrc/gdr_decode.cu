@@ -11,12 +11,13 @@
 // back once, in place: the per-token HBM traffic is the token's q, k, v, gate
 // and o, and a call's total is one read and one write of every state.
 //
-// Main kernel (state V a multiple of 4, 16-byte aligned): persistent CTAs walk
-// the (b, hv, 32-column V tile) tiles. A producer warp streams the state tiles
-// (K x 32 fp32, 16 KB) through a four-stage shared-memory ring by TMA and
-// stores each finished tile back by TMA, so several tiles per SM are in
-// flight; 8 compute warps each hold 16 rows of the tile (lane = column) in
-// registers while they apply the tokens.
+// Main kernel (V <= 128 and a multiple of 4, state 16-byte aligned): one
+// persistent CTA per SM walks the heads. A producer warp streams each head's
+// whole state (K x V fp32, one TMA box of up to 512-byte rows) through a
+// three-stage shared-memory ring and stores the finished state back by TMA, so
+// about 190 KB per SM are in flight; 16 compute warps each hold 8 rows x 4
+// columns in registers while they apply the tokens. (Boxes of 128-byte rows
+// were served several times slower.)
 //
 // Fallback kernel (any V): one CTA per (V tile of 32 columns, hv, b), 16 warps: warp w holds state rows
 // [8 w, 8 w + 8) of the tile's columns (lane = column), so every state access
@@ -161,30 +162,34 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(DecodeArgs a) {
 }
 
 // ------------------------------------------------------------ pipelined kernel
+// Whole-head tiles: the K x V state of one (b, hv) is one TMA box of V-element
+// (up to 512-byte) rows, streamed through a three-stage ring.
 namespace pipe {
-constexpr int CW = 8, ROWS = 16, STAGES = 4, TILE = 128 * kCols * 4;   // 16 KB stage
+constexpr int CW = 16, ROWS = 8, CPL = 4;          // compute warps, rows per warp, columns per lane
+constexpr int STAGES = 3, TILE = 128 * 128 * 4;    // 64 KB stage
 constexpr int THREADS = (CW + 1) * 32;
 constexpr int OFF_BAR = STAGES * TILE, SMEM = OFF_BAR + 2 * STAGES * 8 + 1024;
 constexpr long kWaitLimit = 1L << 24;
+static_assert(CW * ROWS == 128 && CPL * 32 == 128, "tile covers K, V <= 128");
 __device__ __forceinline__ void nb_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 }  // namespace pipe
 
-__global__ void __launch_bounds__(pipe::THREADS, 2)
-    recurrent_pipe_kernel(const __grid_constant__ CUtensorMap smap, DecodeArgs a, int ntiles) {
+__global__ void __launch_bounds__(pipe::THREADS, 1)
+    recurrent_pipe_kernel(const __grid_constant__ CUtensorMap smap, DecodeArgs a, int nplanes) {
   using namespace pipe;
   using namespace ptx;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   __shared__ __align__(16) float kr[128], qr[128], dec[128];   // zero past K
-  __shared__ float2 red[CW][kCols];                            // (k^T D S, q^T D S) partials
+  __shared__ float2 red[CW][128];                              // (k^T D S, q^T D S) partials
+  __shared__ float wcol[128];                                  // delta-rule write per column
   __shared__ float tok[4];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* done = full + STAGES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int vtiles = (a.V + kCols - 1) / kCols;
   const int K = a.K, V = a.V;
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -195,86 +200,62 @@ __global__ void __launch_bounds__(pipe::THREADS, 2)
   }
   __syncthreads();
   bool ok = true;
-  // Tile i of this CTA: global tile blockIdx.x + i * gridDim.x -> (plane = b HV + hv, vt).
-  const int my = ntiles > (int)blockIdx.x ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  // Plane i of this CTA: blockIdx.x + i * gridDim.x (= b * HV + hv).
+  const int my = nplanes > (int)blockIdx.x ? (nplanes - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (warp == CW) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint32_t tbytes = (uint32_t)K * kCols * 4;
-      auto coords = [&](int i, int& plane, int& vt) {
-        const int t = blockIdx.x + i * gridDim.x;
-        plane = t / vtiles;
-        vt = t % vtiles;
-      };
+      const uint32_t tbytes = (uint32_t)K * V * 4;
       for (int i = 0; i < my + STAGES && ok; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES) {
-          // Tile i - STAGES is finished in stage s: store it, then reuse the stage.
+          // Plane i - STAGES is finished in stage s: store it, then reuse the stage.
           ok = mbar_wait(&done[s], ((i / STAGES) - 1) & 1, kWaitLimit);
           if (!ok) break;
-          int plane, vt;
-          coords(i - STAGES, plane, vt);
-          tma_store3(&smap, smem_u32(sm + s * TILE), vt * kCols, 0, plane);
+          tma_store3(&smap, smem_u32(sm + s * TILE), 0, 0, blockIdx.x + (i - STAGES) * gridDim.x);
           bulk_commit();
           bulk_wait_read<0>();
         }
         if (i < my) {
-          int plane, vt;
-          coords(i, plane, vt);
           mbar_expect_tx(&full[s], tbytes);
-          tma_load3(smem_u32(sm + s * TILE), &smap, vt * kCols, 0, plane, &full[s]);
+          tma_load3(smem_u32(sm + s * TILE), &smap, 0, 0, blockIdx.x + i * gridDim.x, &full[s]);
         }
       }
       bulk_wait<0>();
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    // The inputs of a tile's first token are loaded into registers while the
-    // previous tile is still being processed (and before the TMA wait).
+    // Warp w holds rows [8 w, 8 w + 8) of columns lane + 32 m (m < 4).
     const int r0 = warp * ROWS;
-    struct Tok {
-      float v, beta, k, q, g;
-    };
-    auto load_tok = [&](int i, int tk, Tok& x) {
-      const int t = blockIdx.x + i * gridDim.x;
-      const int plane = t / vtiles, vt = t % vtiles;
-      const int b = plane / a.HV, hv = plane % a.HV, h = hv / (a.HV / a.H);
-      const int col = vt * kCols + lane;
-      const size_t bt = (size_t)b * a.T + tk;
-      x.v = col < V ? ld_x(a.v, (bt * a.HV + hv) * V + col, a.in_bf16) : 0.f;
-      x.beta = tid == 0 ? a.beta[bt * a.HV + hv] : 0.f;
-      x.k = x.q = x.g = 0.f;
-      if (tid < K) {
-        const size_t qk = (bt * a.H + h) * K + tid;
-        x.k = ld_x(a.k, qk, a.in_bf16);
-        x.q = ld_x(a.q, qk, a.in_bf16);
-        if (a.g) x.g = a.per_key ? a.g[(bt * a.HV + hv) * K + tid] : a.g[bt * a.HV + hv];
-      }
-    };
-    Tok nx;
-    if (my > 0) load_tok(0, 0, nx);
     for (int i = 0; i < my; ++i) {
       const int s = i % STAGES;
-      const int t = blockIdx.x + i * gridDim.x;
-      const int plane = t / vtiles, vt = t % vtiles;
-      const int b = plane / a.HV, hv = plane % a.HV;
-      const int col = vt * kCols + lane;
-      const bool cok = col < V;
-      float* tile = reinterpret_cast<float*>(sm + s * TILE);   // [K][32] fp32, row = key channel
+      const int plane = blockIdx.x + i * gridDim.x;
+      const int b = plane / a.HV, hv = plane % a.HV, h = hv / (a.HV / a.H);
+      const float* tile = reinterpret_cast<const float*>(sm + s * TILE);   // [K][V] fp32
+      float* tilew = reinterpret_cast<float*>(sm + s * TILE);
       ok = ok && mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit);
-      float S[ROWS];
+      float S[ROWS][CPL];
 #pragma unroll
-      for (int r = 0; r < ROWS; ++r) S[r] = (r0 + r < K) ? tile[(r0 + r) * kCols + lane] : 0.f;
+      for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+          const int c = lane + 32 * m;
+          S[r][m] = (r0 + r < K && c < V) ? tile[(r0 + r) * V + c] : 0.f;
+        }
       for (int tk = 0; tk < a.T; ++tk) {
         const size_t bt = (size_t)b * a.T + tk;
-        Tok x = nx;
-        if (tk > 0) load_tok(i, tk, x);
-        const float vv = x.v, bet = x.beta;
         if (tid < 128) {
-          kr[tid] = tid < K ? x.k : 0.f;
-          qr[tid] = tid < K ? x.q : 0.f;
-          dec[tid] = tid < K ? expf(x.g) : 0.f;
+          float kx = 0.f, qx = 0.f, gx = 0.f;
+          if (tid < K) {
+            const size_t qk = (bt * a.H + h) * K + tid;
+            kx = ld_x(a.k, qk, a.in_bf16);
+            qx = ld_x(a.q, qk, a.in_bf16);
+            if (a.g) gx = a.per_key ? a.g[(bt * a.HV + hv) * K + tid] : a.g[bt * a.HV + hv];
+          }
+          kr[tid] = kx;
+          qr[tid] = qx;
+          dec[tid] = tid < K ? expf(gx) : 0.f;
         }
         nb_sync(1, CW * 32);
         if (warp == 0) {
@@ -296,70 +277,74 @@ __global__ void __launch_bounds__(pipe::THREADS, 2)
             const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
             tok[0] = nk;
             tok[1] = nq;
-            tok[2] = bet;
+            tok[2] = a.beta[bt * a.HV + hv];
             tok[3] = nq * nk * sqk;
           }
         }
         nb_sync(1, CW * 32);
         const float nk = tok[0], nq = tok[1], beta = tok[2], qk = tok[3];
-        // Decay, then this warp's share of k^T (D S) and q^T (D S) (raw k, q: the
-        // norms are applied to the sums). Rows past K hold zeros throughout.
-        const float4* k4 = reinterpret_cast<const float4*>(kr + r0);
-        const float4* q4 = reinterpret_cast<const float4*>(qr + r0);
-        const float4* d4 = reinterpret_cast<const float4*>(dec + r0);
-        float pu = 0.f, po = 0.f;
+        // Decay, then this warp's share of k^T (D S) and q^T (D S) per column.
+        const float4 kk0 = *reinterpret_cast<const float4*>(kr + r0);
+        const float4 kk1 = *reinterpret_cast<const float4*>(kr + r0 + 4);
+        const float4 qq0 = *reinterpret_cast<const float4*>(qr + r0);
+        const float4 qq1 = *reinterpret_cast<const float4*>(qr + r0 + 4);
+        const float4 dd0 = *reinterpret_cast<const float4*>(dec + r0);
+        const float4 dd1 = *reinterpret_cast<const float4*>(dec + r0 + 4);
+        const float kv[ROWS] = {kk0.x, kk0.y, kk0.z, kk0.w, kk1.x, kk1.y, kk1.z, kk1.w};
+        const float qv[ROWS] = {qq0.x, qq0.y, qq0.z, qq0.w, qq1.x, qq1.y, qq1.z, qq1.w};
+        const float dv[ROWS] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
 #pragma unroll
-        for (int r = 0; r < ROWS / 4; ++r) {
-          const float4 kk = k4[r], qq = q4[r], dd = d4[r];
-          S[4 * r + 0] *= dd.x;
-          S[4 * r + 1] *= dd.y;
-          S[4 * r + 2] *= dd.z;
-          S[4 * r + 3] *= dd.w;
-          pu = fmaf(kk.x, S[4 * r + 0], pu);
-          po = fmaf(qq.x, S[4 * r + 0], po);
-          pu = fmaf(kk.y, S[4 * r + 1], pu);
-          po = fmaf(qq.y, S[4 * r + 1], po);
-          pu = fmaf(kk.z, S[4 * r + 2], pu);
-          po = fmaf(qq.z, S[4 * r + 2], po);
-          pu = fmaf(kk.w, S[4 * r + 3], pu);
-          po = fmaf(qq.w, S[4 * r + 3], po);
+        for (int m = 0; m < CPL; ++m) {
+          float pu = 0.f, po = 0.f;
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) {
+            S[r][m] *= dv[r];
+            pu = fmaf(kv[r], S[r][m], pu);
+            po = fmaf(qv[r], S[r][m], po);
+          }
+          red[warp][lane + 32 * m] = make_float2(pu, po);
         }
-        red[warp][lane] = make_float2(pu, po);
         nb_sync(1, CW * 32);
-        float u = 0.f, oq = 0.f;
+        if (tid < 128) {
+          // Column tid: sum the warps' partials, form the write and the output.
+          float u = 0.f, oq = 0.f;
 #pragma unroll
-        for (int w = 0; w < CW; ++w) {
-          const float2 pr = red[w][lane];
-          u += pr.x;
-          oq += pr.y;
+          for (int w = 0; w < CW; ++w) {
+            const float2 pr = red[w][tid];
+            u += pr.x;
+            oq += pr.y;
+          }
+          const float vv = tid < V ? ld_x(a.v, (bt * a.HV + hv) * V + tid, a.in_bf16) : 0.f;
+          const float wv = beta * (vv - nk * u);
+          wcol[tid] = nk * wv;                              // times k^ = nk k
+          if (tid < V) {
+            const float o = fmaf(qk, wv, nq * oq);         // S'^T q~ = (D S)^T q~ + (q~ . k^) w
+            const size_t off = (bt * a.HV + hv) * V + tid;
+            if (a.out_bf16)
+              static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(o);
+            else
+              static_cast<float*>(a.out)[off] = o;
+          }
         }
-        const float wv = beta * (vv - nk * u);           // delta-rule write of this column
-        const float wk = nk * wv;                        // times k^ = nk k
+        nb_sync(1, CW * 32);
 #pragma unroll
-        for (int r = 0; r < ROWS / 4; ++r) {
-          const float4 kk = k4[r];
-          S[4 * r + 0] = fmaf(kk.x, wk, S[4 * r + 0]);
-          S[4 * r + 1] = fmaf(kk.y, wk, S[4 * r + 1]);
-          S[4 * r + 2] = fmaf(kk.z, wk, S[4 * r + 2]);
-          S[4 * r + 3] = fmaf(kk.w, wk, S[4 * r + 3]);
+        for (int m = 0; m < CPL; ++m) {
+          const float wk = wcol[lane + 32 * m];
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) S[r][m] = fmaf(kv[r], wk, S[r][m]);
         }
-        if (warp == 0 && cok) {
-          const float o = fmaf(qk, wv, nq * oq);        // S'^T q~ = (D S)^T q~ + (q~ . k^) w
-          const size_t off = (bt * a.HV + hv) * V + col;
-          if (a.out_bf16)
-            static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(o);
-          else
-            static_cast<float*>(a.out)[off] = o;
-        }
-        nb_sync(1, CW * 32);   // kr / qr / dec / red are rewritten by the next token
+        nb_sync(1, CW * 32);   // kr / qr / dec / red / wcol are rewritten by the next token
       }
 #pragma unroll
       for (int r = 0; r < ROWS; ++r)
-        if (r0 + r < K) tile[(r0 + r) * kCols + lane] = S[r];
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+          const int c = lane + 32 * m;
+          if (r0 + r < K && c < V) tilew[(r0 + r) * V + c] = S[r][m];
+        }
       fence_async_shared();                            // the TMA store reads the tile
       __syncwarp();
       if (lane == 0) mbar_arrive(&done[s]);
-      if (i + 1 < my) load_tok(i + 1, 0, nx);
     }
   }
   if (!ok && a.error_word) atomicOr(a.error_word, 16u);
@@ -410,13 +395,13 @@ extern "C" gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void
   a.scale = scale;
   a.error_word = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (d->V % 4 == 0 && (reinterpret_cast<uintptr_t>(state) & 15) == 0) {
-    // State viewed as [B HV][K][V] fp32; box = all K rows x 32 columns.
+  if (d->V % 4 == 0 && d->V <= 128 && (reinterpret_cast<uintptr_t>(state) & 15) == 0) {
+    // State viewed as [B HV][K][V] fp32; box = one whole head (K rows x V columns).
     CUtensorMap m;
     memset(&m, 0, sizeof m);
     const cuuint64_t dims[3] = {(cuuint64_t)d->V, (cuuint64_t)d->K, (cuuint64_t)d->B * d->HV};
     const cuuint64_t strides[2] = {(cuuint64_t)d->V * 4, (cuuint64_t)d->K * d->V * 4};
-    const cuuint32_t box[3] = {(cuuint32_t)kCols, (cuuint32_t)d->K, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)d->V, (cuuint32_t)d->K, 1};
     if (fast::tmap_encode(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, state, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) {
       static int sms = 0;
@@ -429,10 +414,10 @@ extern "C" gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void
       if (cudaFuncSetAttribute(recurrent_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                pipe::SMEM) != cudaSuccess)
         return GDR_ERR_CUDA;
-      const long long tiles = (long long)d->B * d->HV * ((d->V + kCols - 1) / kCols);
-      if (tiles <= (1LL << 30)) {
-        const int grid = (int)(tiles < 2LL * sms ? tiles : 2LL * sms);
-        recurrent_pipe_kernel<<<grid, pipe::THREADS, pipe::SMEM, st>>>(m, a, (int)tiles);
+      const long long planes = (long long)d->B * d->HV;
+      if (planes <= (1LL << 30)) {
+        const int grid = (int)(planes < sms ? planes : sms);
+        recurrent_pipe_kernel<<<grid, pipe::THREADS, pipe::SMEM, st>>>(m, a, (int)planes);
         return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
       }
     }
