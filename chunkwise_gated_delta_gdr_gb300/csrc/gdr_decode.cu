@@ -227,11 +227,34 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
   } else {
     // ------------------------------------------------------------ compute warps
     // Warp w holds rows [8 w, 8 w + 8) of columns lane + 32 m (m < 4).
+    // Threads 0-127 load a token's inputs (channel / column tid) into registers
+    // one head ahead: the next head's first token while this head finishes.
+    // (Staging them in the producer warp, or two heads ahead in registers,
+    // measured slower.)
     const int r0 = warp * ROWS;
+    struct Tok {
+      float k, q, g, v, beta;
+    };
+    auto load_tok = [&](int plane, int tk, Tok& x) {
+      x.k = x.q = x.g = x.v = x.beta = 0.f;
+      if (tid >= 128) return;
+      const int b = plane / a.HV, hv = plane % a.HV, h = hv / (a.HV / a.H);
+      const size_t bt = (size_t)b * a.T + tk;
+      if (tid < K) {
+        const size_t qk = (bt * a.H + h) * K + tid;
+        x.k = ld_x(a.k, qk, a.in_bf16);
+        x.q = ld_x(a.q, qk, a.in_bf16);
+        if (a.g) x.g = a.per_key ? a.g[(bt * a.HV + hv) * K + tid] : a.g[bt * a.HV + hv];
+      }
+      if (tid < V) x.v = ld_x(a.v, (bt * a.HV + hv) * V + tid, a.in_bf16);
+      if (tid == 0) x.beta = a.beta[bt * a.HV + hv];
+    };
+    Tok nx;
+    if (my > 0) load_tok(blockIdx.x, 0, nx);
     for (int i = 0; i < my; ++i) {
       const int s = i % STAGES;
       const int plane = blockIdx.x + i * gridDim.x;
-      const int b = plane / a.HV, hv = plane % a.HV, h = hv / (a.HV / a.H);
+      const int b = plane / a.HV, hv = plane % a.HV;
       const float* tile = reinterpret_cast<const float*>(sm + s * TILE);   // [K][V] fp32
       float* tilew = reinterpret_cast<float*>(sm + s * TILE);
       ok = ok && mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit);
@@ -245,17 +268,13 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
         }
       for (int tk = 0; tk < a.T; ++tk) {
         const size_t bt = (size_t)b * a.T + tk;
+        Tok x = nx;
+        if (tk > 0) load_tok(plane, tk, x);
         if (tid < 128) {
-          float kx = 0.f, qx = 0.f, gx = 0.f;
-          if (tid < K) {
-            const size_t qk = (bt * a.H + h) * K + tid;
-            kx = ld_x(a.k, qk, a.in_bf16);
-            qx = ld_x(a.q, qk, a.in_bf16);
-            if (a.g) gx = a.per_key ? a.g[(bt * a.HV + hv) * K + tid] : a.g[bt * a.HV + hv];
-          }
-          kr[tid] = kx;
-          qr[tid] = qx;
-          dec[tid] = tid < K ? expf(gx) : 0.f;
+          kr[tid] = x.k;
+          qr[tid] = x.q;
+          dec[tid] = tid < K ? expf(x.g) : 0.f;
+          if (tid == 0) tok[2] = x.beta;
         }
         nb_sync(1, CW * 32);
         if (warp == 0) {
@@ -277,7 +296,6 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
             const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
             tok[0] = nk;
             tok[1] = nq;
-            tok[2] = a.beta[bt * a.HV + hv];
             tok[3] = nq * nk * sqk;
           }
         }
@@ -314,8 +332,7 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
             u += pr.x;
             oq += pr.y;
           }
-          const float vv = tid < V ? ld_x(a.v, (bt * a.HV + hv) * V + tid, a.in_bf16) : 0.f;
-          const float wv = beta * (vv - nk * u);
+          const float wv = beta * (x.v - nk * u);
           wcol[tid] = nk * wv;                              // times k^ = nk k
           if (tid < V) {
             const float o = fmaf(qk, wv, nq * oq);         // S'^T q~ = (D S)^T q~ + (q~ . k^) w
@@ -345,6 +362,7 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
       fence_async_shared();                            // the TMA store reads the tile
       __syncwarp();
       if (lane == 0) mbar_arrive(&done[s]);
+      if (i + 1 < my) load_tok(plane + gridDim.x, 0, nx);
     }
   }
   if (!ok && a.error_word) atomicOr(a.error_word, 16u);
