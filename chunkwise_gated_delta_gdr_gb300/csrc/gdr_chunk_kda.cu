@@ -1,0 +1,401 @@
+// gdr_chunk_kda.cu -- chunk-local kernel of the fast path for the per-key gate (KDA).
+//
+// One CTA (8 warps) per chunk (n, hv, b); bf16 inputs, C = 64, K = V = 128.
+// For one chunk of the "分块并行计算（Chunkwise）" notes (section "chunk 内的
+// cumsum 与下三角解" and the naive_chunk_kda listing) it computes
+//   G      = cumsum(g) per key channel
+//   A_qk   = [sum_c q~_ic k^_jc exp(G_ic - G_jc)] beta_j    (j <= i)
+//   A_kk   = [sum_c k^_ic k^_jc exp(G_ic - G_jc)] beta_j    (j <  i)  -> L
+//   X      = (I + L)^-1                                      (gdr_trinv.cuh)
+//   W      = X (exp(G) k^),  U = X v
+//   QB     = q~ exp(G),  KB = beta k^ exp(G_last - G),  gamma = exp(G_last)
+// and writes the slab of gdr_fast.cuh.
+//
+// The decay sits inside the dot product of A, so the dot is factorised per
+// 16-row block I with the block's first row r = 16 I as reference:
+//   exp(G_ic - G_jc) = exp(G_ic - G_rc) * exp(G_rc - G_jc),
+// a product of a left operand (rows of block I) and a right operand (rows
+// j < 16 (I + 1)) that both depend on I only. For a decaying gate (g <= 0) both
+// factors are <= 1 except on the diagonal block, where the right factor grows to
+// exp(span of the block). A block row whose factors would exceed exp(60) is
+// computed element by element instead (exact in fp32, rarely taken).
+// The operands are fp32-valued, so every product is a 3-term split-bf16
+// mma.sync (hi hi + hi lo + lo hi, fp32 accumulation); W and U use the same
+// split for X and for exp(G) k^ (v is exact in bf16: 2 terms).
+#include <cuda_bf16.h>
+
+#include "gdr_fast.cuh"
+#include "gdr_ptx.cuh"
+#include "gdr_trinv.cuh"
+
+namespace gdr {
+namespace fast {
+namespace {
+
+using namespace ptx;
+
+constexpr int THREADS = 256;
+constexpr int LDB = 136;   // bf16 row stride of the q, k, v tiles (272 B: conflict-free fragments)
+constexpr int LDG = 136;   // fp32 row stride of G (544 B)
+constexpr int LDL = 68;    // fp32 row stride of L and X
+constexpr float kFactorLimit = 60.f;   // largest exponent of a factorised operand
+
+// Shared-memory map (bytes).
+constexpr int OFF_Q = 0;                        // q tile; later the lo plane of exp(G) k^
+constexpr int OFF_K = OFF_Q + C * LDB * 2;      // k tile; later the hi plane of exp(G) k^
+constexpr int OFF_V = OFF_K + C * LDB * 2;      // v tile
+constexpr int OFF_L = OFF_V + C * LDB * 2;      // L [64][LDL] fp32; later X hi / lo (2 swizzled 8 KB boxes)
+constexpr int OFF_G = OFF_L + C * LDL * 4;      // G [64][LDG] fp32; later X fp32 and the inverse scratch
+constexpr int OFF_X = OFF_G;
+constexpr int OFF_T = OFF_G + C * LDL * 4;
+constexpr int OFF_SMALL = OFF_G + C * LDG * 4;  // sq, nk, beta [64] fp32, block flags
+constexpr int SMEM_BYTES = OFF_SMALL + 3 * C * 4 + 16;
+static_assert(OFF_T + 32 * 36 * 4 <= OFF_SMALL, "inverse scratch overlaps");
+static_assert(2 * 8192 <= C * LDL * 4, "X hi / lo boxes overlap G");
+static_assert(SMEM_BYTES <= 113 * 1024, "two CTAs per SM");
+
+// Byte offset of 16-byte chunk c of row r in a swizzled box of 128-byte rows.
+__device__ __forceinline__ uint32_t box_off(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int z = 0; z < 4; ++z) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[z]));
+    f[2 * z] = t.x;
+    f[2 * z + 1] = t.y;
+  }
+}
+
+// hi / lo bf16 planes of 8 fp32 values as two 16-byte words.
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int z = 0; z < 4; ++z) split_pair(x[2 * z], x[2 * z + 1], h[z], l[z]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int n = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+  const int h = hv / (p.HV / p.H);
+  const int t0 = n * C;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(sm + OFF_Q);
+  __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(sm + OFF_K);
+  float* L = reinterpret_cast<float*>(sm + OFF_L);
+  float* G = reinterpret_cast<float*>(sm + OFF_G);
+  float* sq = reinterpret_cast<float*>(sm + OFF_SMALL);   // scale |q_i|^-1
+  float* nk = sq + C;                                     // |k_i|^-1
+  float* bs = nk + C;                                     // beta_i
+  unsigned int* flags = reinterpret_cast<unsigned int*>(bs + C);
+  uint8_t* slab = p.slabs + slab_index(p, b, hv, n) * p.slab_bytes;
+
+  // ---- load q, k, v (bf16) and g (fp32) tiles; rows past T are zero-filled ----
+  for (int idx = tid; idx < 3 * C * 16; idx += THREADS) {
+    const int which = idx / (C * 16), e = idx % (C * 16), i = e >> 4, ch = e & 15;
+    const int t = t0 + i;
+    const bool ok = t < p.T;
+    const size_t tt = (size_t)b * p.T + (ok ? t : 0);
+    const __nv_bfloat16* src = (which == 2) ? p.v + (tt * p.HV + hv) * V + ch * 8
+                                            : (which == 0 ? p.q : p.k) + (tt * p.H + h) * K + ch * 8;
+    cp_async16(smem_u32(sm + which * (C * LDB * 2) + i * (LDB * 2) + ch * 16), src, ok ? 16u : 0u);
+  }
+  for (int idx = tid; idx < C * 32; idx += THREADS) {
+    const int i = idx >> 5, ch = idx & 31, t = t0 + i;
+    const bool ok = t < p.T;
+    const float* src = p.g + (((size_t)b * p.T + (ok ? t : 0)) * p.HV + hv) * K + ch * 4;
+    cp_async16(smem_u32(sm + OFF_G + i * (LDG * 4) + ch * 16), src, ok ? 16u : 0u);
+  }
+  if (tid < C) bs[tid] = (t0 + tid < p.T) ? p.beta[((size_t)b * p.T + t0 + tid) * p.HV + hv] : 0.f;
+  if (tid == 0) *flags = 0u;
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- gate cumsum per channel (threads 0-127) | L2 norms (threads 128-255) ----
+  if (tid < K) {
+    const int c = tid;
+    float gv[C];
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      acc += G[i * LDG + c];
+      gv[i] = acc;
+      G[i * LDG + c] = acc;
+    }
+    // Largest exponent among the factorised operands of each block row.
+    unsigned int bad = 0u;
+#pragma unroll
+    for (int I = 0; I < 4; ++I) {
+      const float gr = gv[16 * I];
+      float mx = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16 * I + 16; ++j) mx = fmaxf(mx, gr - gv[j]);
+#pragma unroll
+      for (int i = 16 * I; i < 16 * I + 16; ++i) mx = fmaxf(mx, gv[i] - gr);
+      if (!(mx <= kFactorLimit)) bad |= 1u << I;
+    }
+    if (bad) atomicOr(flags, bad);
+  } else {
+    const int e = tid - K, r = e & (C - 1), which = e >> 6;
+    const __nv_bfloat16* row = (which ? ks : qs) + r * LDB;
+    float s = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 16; ++ch) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(row + ch * 8), f);
+#pragma unroll
+      for (int z = 0; z < 8; ++z) s = fmaf(f[z], f[z], s);
+    }
+    const float nrm = p.use_l2 ? 1.f / sqrtf(s + 1e-6f) : 1.f;
+    if (which == 0) sq[r] = nrm * p.scale;
+    else nk[r] = nrm;
+  }
+  __syncthreads();
+
+  // ---- decayed dots: block row I, q and k m-tiles, n-tiles of 8 columns j ----
+  // Warp -> (I, first n-tile, n-tile count): 20 n-tiles, 5 per SM sub-partition.
+  const int I = (0x01132233u >> (4 * warp)) & 15;
+  const int nt0 = (0x02063030u >> (4 * warp)) & 15;
+  const int ntn = (0x22223333u >> (4 * warp)) & 15;
+  const int r8 = lane >> 2, cq = 2 * (lane & 3);
+  const int ra = 16 * I + r8, rb = ra + 8;
+  {
+    float accq[3][4], acck[3][4];
+#pragma unroll
+    for (int u = 0; u < 3; ++u)
+#pragma unroll
+      for (int z = 0; z < 4; ++z) accq[u][z] = acck[u][z] = 0.f;
+    const float* Gr = G + 16 * I * LDG;
+    const float sqa = sq[ra], sqb = sq[rb], nka = nk[ra], nkb = nk[rb];
+#pragma unroll 1
+    for (int s = 0; s < K / 16; ++s) {
+      const int c0 = 16 * s + cq;
+      const float2 gr0 = *reinterpret_cast<const float2*>(Gr + c0);
+      const float2 gr1 = *reinterpret_cast<const float2*>(Gr + c0 + 8);
+      // A fragments: a0 (ra, c0), a1 (rb, c0), a2 (ra, c0 + 8), a3 (rb, c0 + 8).
+      uint32_t aqh[4], aql[4], akh[4], akl[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int row = (x & 1) ? rb : ra;
+        const int col = c0 + ((x & 2) ? 8 : 0);
+        const float2 gref = (x & 2) ? gr1 : gr0;
+        const float2 gg = *reinterpret_cast<const float2*>(G + row * LDG + col);
+        const float e0 = __expf(gg.x - gref.x), e1 = __expf(gg.y - gref.y);
+        const float2 qv = ld_bf2(qs + row * LDB + col), kv = ld_bf2(ks + row * LDB + col);
+        const float fq = (x & 1) ? sqb : sqa, fk = (x & 1) ? nkb : nka;
+        split_pair(qv.x * fq * e0, qv.y * fq * e1, aqh[x], aql[x]);
+        split_pair(kv.x * fk * e0, kv.y * fk * e1, akh[x], akl[x]);
+      }
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (u < ntn) {
+          // B fragment (16 channels x 8 columns): b0 (c0, j), b1 (c0 + 8, j).
+          const int j = 8 * (nt0 + u) + r8;
+          const float nj = nk[j];
+          const float2 g0 = *reinterpret_cast<const float2*>(G + j * LDG + c0);
+          const float2 g1 = *reinterpret_cast<const float2*>(G + j * LDG + c0 + 8);
+          const float2 k0 = ld_bf2(ks + j * LDB + c0), k1 = ld_bf2(ks + j * LDB + c0 + 8);
+          uint32_t bh0, bl0, bh1, bl1;
+          split_pair(k0.x * nj * __expf(gr0.x - g0.x), k0.y * nj * __expf(gr0.y - g0.y), bh0, bl0);
+          split_pair(k1.x * nj * __expf(gr1.x - g1.x), k1.y * nj * __expf(gr1.y - g1.y), bh1, bl1);
+          mma_bf16_16816(accq[u], aqh, bh0, bh1);
+          mma_bf16_16816(accq[u], aqh, bl0, bl1);
+          mma_bf16_16816(accq[u], aql, bh0, bh1);
+          mma_bf16_16816(acck[u], akh, bh0, bh1);
+          mma_bf16_16816(acck[u], akh, bl0, bl1);
+          mma_bf16_16816(acck[u], akl, bh0, bh1);
+        }
+      }
+    }
+    // Block rows whose factors would overflow: every element directly.
+    if ((*flags >> I) & 1u) {
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (u < ntn) {
+#pragma unroll
+          for (int z = 0; z < 4; ++z) {
+            const int i = (z & 2) ? rb : ra, j = 8 * (nt0 + u) + cq + (z & 1);
+            float dq = 0.f, dk = 0.f;
+            if (j <= i) {
+#pragma unroll 4
+              for (int c = 0; c < K; ++c) {
+                const float w = __expf(G[i * LDG + c] - G[j * LDG + c]) * __bfloat162float(ks[j * LDB + c]);
+                dq = fmaf(__bfloat162float(qs[i * LDB + c]), w, dq);
+                dk = fmaf(__bfloat162float(ks[i * LDB + c]), w, dk);
+              }
+            }
+            accq[u][z] = dq * sq[i] * nk[j];
+            acck[u][z] = dk * nk[i] * nk[j];
+          }
+        }
+      }
+    }
+    // A_qk (beta on the columns, zero above the diagonal) -> slab; A_kk beta -> L.
+    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {
+      if (u < ntn) {
+        const int j = 8 * (nt0 + u) + cq;
+        const float b0 = bs[j], b1 = bs[j + 1];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int i = hr ? rb : ra;
+          uint32_t hi, lo;
+          split_pair((j <= i) ? accq[u][2 * hr] * b0 : 0.f, (j + 1 <= i) ? accq[u][2 * hr + 1] * b1 : 0.f,
+                     hi, lo);
+          *reinterpret_cast<uint32_t*>(aq + i * C + j) = hi;
+          *reinterpret_cast<uint32_t*>(aq + C * C + i * C + j) = lo;
+          *reinterpret_cast<float2*>(L + i * LDL + j) =
+              make_float2((j < i) ? acck[u][2 * hr] * b0 : 0.f, (j + 1 < i) ? acck[u][2 * hr + 1] * b1 : 0.f);
+        }
+      }
+    }
+  }
+  __syncthreads();   // q, k and G are no longer read by the dots
+
+  // ---- elementwise outputs: QB, KB, gamma; exp(G) k^ split in place ----------
+  {
+    const float* Gl = G + (C - 1) * LDG;
+    __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::QB2);
+    __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::KB2);
+    for (int idx = tid; idx < C * 16; idx += THREADS) {
+      const int i = idx >> 4, c = (idx & 15) * 8;
+      float gi[8], gl[8], qf[8], kf[8];
+      *reinterpret_cast<float4*>(gi) = *reinterpret_cast<const float4*>(G + i * LDG + c);
+      *reinterpret_cast<float4*>(gi + 4) = *reinterpret_cast<const float4*>(G + i * LDG + c + 4);
+      *reinterpret_cast<float4*>(gl) = *reinterpret_cast<const float4*>(Gl + c);
+      *reinterpret_cast<float4*>(gl + 4) = *reinterpret_cast<const float4*>(Gl + c + 4);
+      unpack8(*reinterpret_cast<const uint4*>(qs + i * LDB + c), qf);
+      unpack8(*reinterpret_cast<const uint4*>(ks + i * LDB + c), kf);
+      const float fq = sq[i], fk = nk[i], fb = bs[i] * nk[i];
+      float xq[8], xk[8], xe[8];
+#pragma unroll
+      for (int z = 0; z < 8; ++z) {
+        const float e = __expf(gi[z]);
+        xq[z] = qf[z] * fq * e;
+        xe[z] = kf[z] * fk * e;
+        xk[z] = kf[z] * fb * __expf(gl[z] - gi[z]);
+      }
+      uint4 hi, lo;
+      split8(xq, hi, lo);
+      *reinterpret_cast<uint4*>(qb + i * K + c) = hi;
+      *reinterpret_cast<uint4*>(qb + C * K + i * K + c) = lo;
+      split8(xk, hi, lo);
+      *reinterpret_cast<uint4*>(kb + i * K + c) = hi;
+      *reinterpret_cast<uint4*>(kb + C * K + i * K + c) = lo;
+      split8(xe, hi, lo);
+      *reinterpret_cast<uint4*>(ks + i * LDB + c) = hi;   // same thread read these bytes above
+      *reinterpret_cast<uint4*>(qs + i * LDB + c) = lo;
+    }
+    float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
+    if (tid < K) vec[2 * C + tid] = __expf(Gl[tid]);
+    else vec[tid - K] = 1.f;   // qscale = kscale = 1
+    // A_qk blocks above the diagonal: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3).
+    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
+    for (int idx = tid; idx < 6 * 16 * 4; idx += THREADS) {
+      const int plane = idx & 1, half = (idx >> 1) & 1, rr = (idx >> 2) & 15, blk = idx >> 6;
+      const int Ib = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int Jb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      *reinterpret_cast<uint4*>(aq + plane * C * C + (16 * Ib + rr) * C + 16 * Jb + 8 * half) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __syncthreads();   // G is dead: X and the scratch take its place
+
+  float* X = reinterpret_cast<float*>(sm + OFF_X);
+  unit_lower_inverse64<LDL, LDL>(L, X, reinterpret_cast<float*>(sm + OFF_T), tid);
+  __syncthreads();   // L is dead: the X hi / lo boxes take its place
+
+  // ---- X -> hi / lo bf16 boxes (the 10 blocks on and below the diagonal) ------
+  for (int idx = tid; idx < C * 8; idx += THREADS) {
+    const int i = idx >> 3, ch = idx & 7;
+    if (ch > 2 * (i >> 4) + 1) continue;
+    float x[8];
+    *reinterpret_cast<float4*>(x) = *reinterpret_cast<const float4*>(X + i * LDL + 8 * ch);
+    *reinterpret_cast<float4*>(x + 4) = *reinterpret_cast<const float4*>(X + i * LDL + 8 * ch + 4);
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    *reinterpret_cast<uint4*>(sm + OFF_L + box_off(i, ch)) = hi;
+    *reinterpret_cast<uint4*>(sm + OFF_L + 8192 + box_off(i, ch)) = lo;
+  }
+  __syncthreads();
+
+  // ---- W = X (exp(G) k^), U = X v: warp w owns columns 16 w .. 16 w + 15 -------
+  {
+    const uint32_t xh = smem_u32(sm + OFF_L), xl = xh + 8192;
+    const uint32_t ekh = smem_u32(sm + OFF_K), ekl = smem_u32(sm + OFF_Q), vb = smem_u32(sm + OFF_V);
+    const int cb = 16 * warp;
+    float aw[4][2][4], au[4][2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int z = 0; z < 4; ++z) aw[i][u][z] = au[i][u][z] = 0.f;
+    const int m = lane >> 3;
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+      // B fragments of rows 16 J .. 16 J + 15, two n-tiles, by transposed ldmatrix.
+      const uint32_t boff = (uint32_t)(((16 * J + ((m & 1) << 3) + (lane & 7)) * LDB + cb + ((m >> 1) << 3)) * 2);
+      uint32_t bh[4], bl[4], bv[4];
+      ldsm_x4_t(bh, ekh + boff);
+      ldsm_x4_t(bl, ekl + boff);
+      ldsm_x4_t(bv, vb + boff);
+#pragma unroll
+      for (int Ib = J; Ib < 4; ++Ib) {
+        const uint32_t aoff = box_off(16 * Ib + (lane & 15), 2 * J + (lane >> 4));
+        uint32_t ah[4], al[4];
+        ldsm_x4(ah, xh + aoff);
+        ldsm_x4(al, xl + aoff);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          mma_bf16_16816(aw[Ib][u], ah, bh[2 * u], bh[2 * u + 1]);
+          mma_bf16_16816(aw[Ib][u], ah, bl[2 * u], bl[2 * u + 1]);
+          mma_bf16_16816(aw[Ib][u], al, bh[2 * u], bh[2 * u + 1]);
+          mma_bf16_16816(au[Ib][u], ah, bv[2 * u], bv[2 * u + 1]);
+          mma_bf16_16816(au[Ib][u], al, bv[2 * u], bv[2 * u + 1]);
+        }
+      }
+    }
+    __nv_bfloat16* w2 = reinterpret_cast<__nv_bfloat16*>(slab + Slab::W2);
+    float* uo = reinterpret_cast<float*>(slab + Slab::U);
+#pragma unroll
+    for (int Ib = 0; Ib < 4; ++Ib) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col = cb + 8 * u + cq;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int i = 16 * Ib + r8 + 8 * hr;
+          uint32_t hi, lo;
+          split_pair(-aw[Ib][u][2 * hr], -aw[Ib][u][2 * hr + 1], hi, lo);
+          *reinterpret_cast<uint32_t*>(w2 + i * K + col) = hi;
+          *reinterpret_cast<uint32_t*>(w2 + C * K + i * K + col) = lo;
+          *reinterpret_cast<float2*>(uo + i * V + col) = make_float2(au[Ib][u][2 * hr], au[Ib][u][2 * hr + 1]);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+gdr_status launch_chunk_kda(const Params& p, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(chunk_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+      cudaSuccess)
+    return GDR_ERR_CUDA;
+  dim3 grid(p.N, p.HV, p.B);
+  chunk_kda_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+}  // namespace fast
+}  // namespace gdr

@@ -25,6 +25,7 @@
 #include "gdr_fast.cuh"
 #include "gdr_ptx.cuh"
 #include "gdr_tmap.cuh"
+#include "gdr_trinv.cuh"
 
 namespace gdr {
 namespace fast {
@@ -256,81 +257,8 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
     if (tid < K) vec[2 * C + tid] = __expf(gl);
   }
 
-  // ---- X = (I + L)^-1, blocked --------------------------------------------------
-  // Level 0: the four 16x16 diagonal blocks, one column per thread (threads 0-63),
-  // by forward substitution x_i = delta_ij - sum_{m<i} L_im x_m.
-  if (tid < 64) {
-    const int o = (tid >> 4) * 16, col = tid & 15;
-    float xd[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = (i == col) ? 1.f : 0.f;
-#pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(-L[(o + i) * LDL + o + m], xd[m], acc);
-      xd[i] = acc;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) X[(o + i) * LDX + o + col] = xd[i];
-  }
-  __syncthreads();
-  // Level 1: X_10 = -X_11 (L_10 X_00) and X_32 = -X_33 (L_32 X_22), 16x16 blocks;
-  // threads 0-127, each one row segment of 4 columns.
-  {
-    const int which = (tid >> 6) & 1, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
-    const int I = 16 * (2 * which + 1), J = I - 16;
-    if (tid < 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float l = L[(I + i) * LDL + J + m];
-        const float4 xv = *reinterpret_cast<const float4*>(X + (J + m) * LDX + J + j0);
-        acc.x = fmaf(l, xv.x, acc.x); acc.y = fmaf(l, xv.y, acc.y);
-        acc.z = fmaf(l, xv.z, acc.z); acc.w = fmaf(l, xv.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(T + (which * 16 + i) * 36 + j0) = acc;
-    }
-    __syncthreads();
-    if (tid < 128) {
-      float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float xv = X[(I + i) * LDX + I + m];
-        const float4 t4 = *reinterpret_cast<const float4*>(T + (which * 16 + m) * 36 + j0);
-        r4.x = fmaf(xv, t4.x, r4.x); r4.y = fmaf(xv, t4.y, r4.y);
-        r4.z = fmaf(xv, t4.z, r4.z); r4.w = fmaf(xv, t4.w, r4.w);
-      }
-      *reinterpret_cast<float4*>(X + (I + i) * LDX + J + j0) = make_float4(-r4.x, -r4.y, -r4.z, -r4.w);
-    }
-  }
-  __syncthreads();
-  // Level 2: X[32:64, 0:32] = -X[32:64, 32:64] (L[32:64, 0:32] X[0:32, 0:32]); each
-  // thread one row segment of 4 columns. Entries above the diagonal of X are
-  // never written and read as zero through the masks below.
-  {
-    const int i = tid >> 3, j0 = (tid & 7) * 4;
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float l = L[(32 + i) * LDL + m];
-      const float4 x0 = *reinterpret_cast<const float4*>(X + m * LDX + j0);
-      const float xs[4] = {x0.x, x0.y, x0.z, x0.w};
-#pragma unroll
-      for (int z = 0; z < 4; ++z) a[z] = fmaf(l, (j0 + z <= m) ? xs[z] : 0.f, a[z]);
-    }
-    __syncthreads();   // every thread is past its reads of the level-1 scratch
-    *reinterpret_cast<float4*>(T + i * 36 + j0) = make_float4(a[0], a[1], a[2], a[3]);
-    __syncthreads();
-    float r4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float xv = (m <= i) ? X[(32 + i) * LDX + 32 + m] : 0.f;
-      const float4 t4 = *reinterpret_cast<const float4*>(T + m * 36 + j0);
-      const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-      for (int z = 0; z < 4; ++z) r4[z] = fmaf(xv, ts[z], r4[z]);
-    }
-    *reinterpret_cast<float4*>(X + (32 + i) * LDX + j0) = make_float4(-r4[0], -r4[1], -r4[2], -r4[3]);
-  }
+  // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
+  unit_lower_inverse64<LDL, LDX>(L, X, T, tid);
   if (tid == 0) bulk_wait_read<0>();   // the A_qk staging is read before XU overwrites it
   __syncthreads();   // X complete; L and the A_qk staging are dead from here on
 
@@ -449,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
 }  // namespace
 
 gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode != 0) return launch_chunk_simt(p, stream);
+  if (p.gate_mode != 0) return launch_chunk_kda(p, stream);
   Maps m;
   const size_t nch = (size_t)p.B * p.HV * p.N;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

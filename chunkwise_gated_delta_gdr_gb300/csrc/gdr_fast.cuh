@@ -92,7 +92,8 @@ inline __host__ __device__ size_t slab_index(const Params& p, int b, int hv, int
 gdr_status launch_state(const Params& p, cudaStream_t stream);
 // Scalar gate: state chain and chunk outputs in one launch (gdr_recur.cu).
 gdr_status launch_recur(const Params& p, cudaStream_t stream);
-gdr_status launch_chunk_simt(const Params& p, cudaStream_t stream);
+// Per-key gate: chunk-local kernel on mma.sync (gdr_chunk_kda.cu).
+gdr_status launch_chunk_kda(const Params& p, cudaStream_t stream);
 gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream);
 
 }  // namespace fast

@@ -158,6 +158,26 @@ def test_positive_small_gate():
     check_against_oracle(w, x)
 
 
+# Per-key gate recipes for the factorised decayed dots: a 16-row block whose
+# gate span exceeds the factor limit is computed element by element, so these
+# cover both branches and their mix within one chunk.
+KDA_GATES = {
+    "reset_limit": lambda shape, gen: torch.full(shape, -1000.0),
+    "steep_half_channels": lambda shape, gen: torch.where(
+        torch.arange(shape[-1]) % 2 == 0, torch.tensor(-5.0), torch.tensor(-0.01)).expand(shape).clone(),
+    "mixed_spans": lambda shape, gen: -torch.randn(shape, generator=gen).abs() * 3.0,
+    "positive_small": lambda shape, gen: torch.randn(shape, generator=gen) * 0.1,
+}
+
+
+@pytest.mark.parametrize("recipe", list(KDA_GATES))
+def test_per_key_gate_ranges(recipe):
+    w = gin.shrink(gin.WORKLOADS["kda_gqa_t8192"], B=1, T=200, H=1, HV=2)
+    x = gin.make_inputs(w)
+    x["g"] = KDA_GATES[recipe](tuple(x["g"].shape), torch.Generator().manual_seed(21)).float()
+    check_against_oracle(w, x)
+
+
 def test_split_sequence_matches_single_call():
     w = gin.shrink(gin.WORKLOADS["kda_gqa_t8192"], B=1, T=320, H=1, HV=2)
     x = gin.make_inputs(w)
