@@ -39,41 +39,11 @@ using namespace ptx;
 
 constexpr int LDW = K + 8;   // bf16 row stride of the S^T exchange tiles (272 B)
 constexpr int LDA = C + 8;   // bf16 row stride of the r^T exchange tiles (144 B)
-#ifndef STATE_WARPS
-#define STATE_WARPS 4
+#ifndef KDA_MG
+#define KDA_MG 4
 #endif
 constexpr long kWaitLimit = 1L << 24;
 constexpr unsigned int kErrStateWait = 4u;
-
-// Operand tiles of one chunk, 1024-byte aligned, 128-byte swizzled. A
-// [64][128] bf16 tile is two 8 KB boxes (columns 0-63, 64-127).
-struct Big {
-  static constexpr int W_HI = 0, W_LO = 16384, Q_HI = 32768;
-  static constexpr int Q_LO_PK = 49152, K_LO_PK = 81920;   // per-key gate only
-  __host__ __device__ static constexpr int k_hi(int gate) { return gate ? 65536 : 49152; }
-  __host__ __device__ static constexpr int aq_hi(int gate) { return gate ? 98304 : 65536; }
-  __host__ __device__ static constexpr int aq_lo(int gate) { return aq_hi(gate) + 8192; }
-  __host__ __device__ static constexpr int bytes(int gate) { return aq_hi(gate) + 16384; }
-};
-// U tile [64][16] fp32 (unswizzled) and VEC, double-buffered.
-constexpr int SMALL_U = 0, SMALL_VEC = 4096, SMALL_BYTES = 5120;
-// Bytes a scalar-gate chunk brings in: W hi/lo, q, k, A_qk hi/lo, U tile, VEC.
-constexpr uint32_t kScalarChunkBytes = 32768 + 16384 + 16384 + 16384 + 4096 + 1024;
-// Per-key gate: group 1 = W hi/lo, q hi/lo, U tile, VEC; group 2 = k hi/lo, A_qk hi/lo.
-constexpr uint32_t kPerKeyGroup1Bytes = 32768 + 32768 + 4096 + 1024;
-constexpr uint32_t kPerKeyGroup2Bytes = 32768 + 16384;
-
-struct Layout {
-  int big, small, xs, xr, xo, bars, total;
-  __host__ __device__ constexpr Layout(int gate, int stages)
-      : big(0),
-        small(stages * Big::bytes(gate)),
-        xs(small + 2 * SMALL_BYTES),
-        xr(xs + 2 * 16 * LDW * 2),
-        xo(xr + 4 * 16 * LDA * 2),
-        bars(xo + C * 16 * 4),
-        total(bars + 64 + 1024) {}
-};
 
 // Byte address of element (r, c) (c a multiple of 8) of a swizzled bf16 tile
 // stored as 64-column boxes of 8 KB.
@@ -85,76 +55,95 @@ struct Maps {
   CUtensorMap q, k, w2, aq2, u, qb2, kb2;
 };
 
-// WARPS warps split the per-chunk work: warp w produces JT 8-column tiles of
-// r^T and of o^T (j, i in [8 JT w, 8 JT (w + 1))) and owns CT 8-channel tiles
-// of the state (c in [8 CT w, 8 CT (w + 1))).
-template <int GATE, int STAGES, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant__ Maps maps, Params p) {
-  constexpr Layout LY(GATE, STAGES);
-  constexpr int JT = C / 8 / WARPS, CT = K / 8 / WARPS;
+// ---------------------------------------------------------------------------
+// Per-key gate. One CTA per (b, hv, 16 MG value columns): MG groups of 4 warps,
+// group m owning value rows 16 m .. 16 m + 15 of the CTA's S^T tile. All groups
+// read the same chunk operands from one shared buffer, so a chunk's W, QB, KB
+// and A_qk cross from L2 once per MG 16-column tiles.
+//
+// Operand tiles of one chunk, 128-byte swizzled [64][128] bf16 tiles as two
+// 8 KB boxes. Group 1 (read by the r and o products): W hi/lo, QB hi/lo, plus
+// the U tile and VEC in the small buffer. Group 2 (read by the state update and
+// the second o product): KB hi/lo, A_qk hi/lo.
+namespace kda {
+constexpr int WARPS = 4;                          // per group
+constexpr int JT = C / 8 / WARPS, CT = K / 8 / WARPS;
+constexpr int W_HI = 0, W_LO = 16384, Q_HI = 32768, Q_LO = 49152;
+constexpr int K_HI = 65536, K_LO = 81920, AQ_HI = 98304, AQ_LO = 106496, BIG = 114688;
+constexpr uint32_t kGroup2Bytes = 32768 + 16384;
+
+template <int MG>
+struct Layout {
+  static constexpr int VTK = 16 * MG;                     // value columns per CTA
+  static constexpr int SMALL_U = BIG;                     // U tile [C][VTK] fp32
+  static constexpr int SMALL_VEC = SMALL_U + C * VTK * 4; // qscale, kscale, gamma
+  static constexpr int XS = SMALL_VEC + 1024;             // S^T hi / lo [VTK][LDW]
+  static constexpr int XR = XS + 2 * VTK * LDW * 2;       // r^T, rho^T hi / lo [VTK][LDA]
+  static constexpr int XO = XR + 4 * VTK * LDA * 2;       // o staging, per warp
+  static constexpr int BARS = XO + MG * WARPS * (8 * JT * 16) * 4;
+  static constexpr int TOTAL = BARS + 64 + 1024;
+  static constexpr uint32_t kGroup1Bytes = 32768 + 32768 + C * VTK * 4 + 1024;
+};
+}  // namespace kda
+
+template <int MG>
+__global__ void __launch_bounds__(MG * kda::WARPS * 32, 1)
+    state_kda_kernel(const __grid_constant__ Maps maps, Params p) {
+  using namespace kda;
+  using LY = Layout<MG>;
+  constexpr int VTK = LY::VTK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-  const int h = hv / (p.HV / p.H);
-  const int v0 = vt * VT;
+  const int v0 = vt * VTK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mg = warp / WARPS, wi = warp % WARPS;
+  const int vr = 16 * mg;                                 // this group's rows of S^T
   const int g = lane >> 2, t4 = lane & 3;
 
-  __nv_bfloat16* xs_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY.xs);
-  __nv_bfloat16* xs_lo = xs_hi + 16 * LDW;
-  __nv_bfloat16* xr_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY.xr);
-  __nv_bfloat16* xr_lo = xr_hi + 16 * LDA;
-  __nv_bfloat16* xp_hi = xr_lo + 16 * LDA;
-  __nv_bfloat16* xp_lo = xp_hi + 16 * LDA;
-  float* xo = reinterpret_cast<float*>(sm + LY.xo) + warp * (8 * JT * 16);
-  // Scalar gate: bars[s] = stage s. Per-key gate: bars[0] = group 1, bars[1] = group 2.
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY.bars);
+  __nv_bfloat16* xs_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY::XS);
+  __nv_bfloat16* xs_lo = xs_hi + VTK * LDW;
+  __nv_bfloat16* xr_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY::XR);
+  __nv_bfloat16* xr_lo = xr_hi + VTK * LDA;
+  __nv_bfloat16* xp_hi = xr_lo + VTK * LDA;
+  __nv_bfloat16* xp_lo = xp_hi + VTK * LDA;
+  float* xo = reinterpret_cast<float*>(sm + LY::XO) + warp * (8 * JT * 16);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BARS);   // [0] group 1, [1] group 2
+  const float* su = reinterpret_cast<const float*>(sm + LY::SMALL_U);
+  const float* vec = reinterpret_cast<const float*>(sm + LY::SMALL_VEC);
 
   const size_t seq = (size_t)b * p.HV + hv;
   const int chunk0 = (int)(seq * p.N);
 
-  auto big_at = [&](int n) { return sm + LY.big + (STAGES == 2 ? (n & 1) : 0) * Big::bytes(GATE); };
-  auto small_at = [&](int n) { return sm + LY.small + (n & 1) * SMALL_BYTES; };
-
-  // Loads of chunk n (issued by one thread). Scalar gate: everything on one
-  // barrier. Per-key gate: group 1 here, group 2 in issue_group2.
-  auto issue_group1 = [&](int n, uint64_t* bar) {
+  // Loads of chunk n, issued by one thread. Group 1 is reissued as soon as
+  // every warp is past the products that read it (the CTA barrier after the
+  // r^T tiles), group 2 after the chunk's last product.
+  auto issue_group1 = [&](int n) {
     const int idx = chunk0 + n;
-    const uint32_t big = smem_u32(big_at(n));
-    const uint32_t small = smem_u32(small_at(n));
-    mbar_expect_tx(bar, GATE ? kPerKeyGroup1Bytes : kScalarChunkBytes);
-    tma_load3(big + Big::W_HI, &maps.w2, 0, 0, idx, bar);
-    tma_load3(big + Big::W_HI + 8192, &maps.w2, 64, 0, idx, bar);
-    tma_load3(big + Big::W_LO, &maps.w2, 0, 64, idx, bar);
-    tma_load3(big + Big::W_LO + 8192, &maps.w2, 64, 64, idx, bar);
-    if (GATE) {
-      tma_load3(big + Big::Q_HI, &maps.qb2, 0, 0, idx, bar);
-      tma_load3(big + Big::Q_HI + 8192, &maps.qb2, 64, 0, idx, bar);
-      tma_load3(big + Big::Q_LO_PK, &maps.qb2, 0, 64, idx, bar);
-      tma_load3(big + Big::Q_LO_PK + 8192, &maps.qb2, 64, 64, idx, bar);
-    } else {
-      const int t0 = n * C;
-      tma_load4(big + Big::Q_HI, &maps.q, 0, h, t0, b, bar);
-      tma_load4(big + Big::Q_HI + 8192, &maps.q, 64, h, t0, b, bar);
-      tma_load4(big + Big::k_hi(GATE), &maps.k, 0, h, t0, b, bar);
-      tma_load4(big + Big::k_hi(GATE) + 8192, &maps.k, 64, h, t0, b, bar);
-      tma_load3(big + Big::aq_hi(GATE), &maps.aq2, 0, 0, idx, bar);
-      tma_load3(big + Big::aq_lo(GATE), &maps.aq2, 0, 64, idx, bar);
-    }
-    tma_load3(small + SMALL_U, &maps.u, v0, 0, idx, bar);
-    bulk_load(small + SMALL_VEC, p.slabs + (size_t)idx * p.slab_bytes + Slab::VEC, 1024, bar);
+    const uint32_t big = smem_u32(sm);
+    mbar_expect_tx(&bars[0], LY::kGroup1Bytes);
+    tma_load3(big + W_HI, &maps.w2, 0, 0, idx, &bars[0]);
+    tma_load3(big + W_HI + 8192, &maps.w2, 64, 0, idx, &bars[0]);
+    tma_load3(big + W_LO, &maps.w2, 0, 64, idx, &bars[0]);
+    tma_load3(big + W_LO + 8192, &maps.w2, 64, 64, idx, &bars[0]);
+    tma_load3(big + Q_HI, &maps.qb2, 0, 0, idx, &bars[0]);
+    tma_load3(big + Q_HI + 8192, &maps.qb2, 64, 0, idx, &bars[0]);
+    tma_load3(big + Q_LO, &maps.qb2, 0, 64, idx, &bars[0]);
+    tma_load3(big + Q_LO + 8192, &maps.qb2, 64, 64, idx, &bars[0]);
+    tma_load3(big + LY::SMALL_U, &maps.u, v0, 0, idx, &bars[0]);
+    bulk_load(big + LY::SMALL_VEC, p.slabs + (size_t)idx * p.slab_bytes + Slab::VEC, 1024, &bars[0]);
   };
-  auto issue_group2 = [&](int n, uint64_t* bar) {
+  auto issue_group2 = [&](int n) {
     const int idx = chunk0 + n;
-    const uint32_t big = smem_u32(big_at(n));
-    mbar_expect_tx(bar, kPerKeyGroup2Bytes);
-    tma_load3(big + Big::k_hi(GATE), &maps.kb2, 0, 0, idx, bar);
-    tma_load3(big + Big::k_hi(GATE) + 8192, &maps.kb2, 64, 0, idx, bar);
-    tma_load3(big + Big::K_LO_PK, &maps.kb2, 0, 64, idx, bar);
-    tma_load3(big + Big::K_LO_PK + 8192, &maps.kb2, 64, 64, idx, bar);
-    tma_load3(big + Big::aq_hi(GATE), &maps.aq2, 0, 0, idx, bar);
-    tma_load3(big + Big::aq_lo(GATE), &maps.aq2, 0, 64, idx, bar);
+    const uint32_t big = smem_u32(sm);
+    mbar_expect_tx(&bars[1], kGroup2Bytes);
+    tma_load3(big + K_HI, &maps.kb2, 0, 0, idx, &bars[1]);
+    tma_load3(big + K_HI + 8192, &maps.kb2, 64, 0, idx, &bars[1]);
+    tma_load3(big + K_LO, &maps.kb2, 0, 64, idx, &bars[1]);
+    tma_load3(big + K_LO + 8192, &maps.kb2, 64, 64, idx, &bars[1]);
+    tma_load3(big + AQ_HI, &maps.aq2, 0, 0, idx, &bars[1]);
+    tma_load3(big + AQ_LO, &maps.aq2, 0, 64, idx, &bars[1]);
   };
 
   if (tid == 0) {
@@ -164,11 +153,11 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
   }
   __syncthreads();
   if (tid == 0) {
-    issue_group1(0, &bars[0]);
-    if (GATE) issue_group2(0, &bars[1]);
+    issue_group1(0);
+    issue_group2(0);
   }
 
-  const int jw = 8 * JT * warp, cw = 8 * CT * warp;
+  const int jw = 8 * JT * wi, cw = 8 * CT * wi;
 
   float S[CT][4];
 #pragma unroll
@@ -176,33 +165,22 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
     const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int vv = g + (e >> 1) * 8, cc = c + (e & 1);
+      const int vv = vr + g + (e >> 1) * 8, cc = c + (e & 1);
       S[nt][e] = p.s0 ? p.s0[(seq * K + cc) * V + v0 + vv] : 0.f;
     }
   }
 
   // ldmatrix lane addressing.
-  const int arow = (lane & 7) + ((lane >> 3) & 1) * 8;   // A fragments (16 rows)
+  const int arow = vr + (lane & 7) + ((lane >> 3) & 1) * 8;   // A fragments (this group's 16 rows)
   const int acol = (lane >> 4) * 8;
-  const int brow = (lane & 7);                           // B from [n][k] tiles, 2 k-steps per x4
+  const int brow = (lane & 7);                                // B from [n][k] tiles, 2 k-steps per x4
   const int bcol = (lane >> 3) * 8;
-  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;   // B from the [j][c] k tile (.trans)
-  const int kcol = cw + (lane >> 4) * 8;                 // two c-tiles per x4
+  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;        // B from the [j][c] k tile (.trans)
+  const int kcol = cw + (lane >> 4) * 8;                      // two c-tiles per x4
+  const uint32_t big = smem_u32(sm);
   bool ok = true;
 
   for (int n = 0; n < p.N; ++n) {
-    uint8_t* bigp = big_at(n);
-    const uint32_t w_hi = smem_u32(bigp + Big::W_HI), w_lo = smem_u32(bigp + Big::W_LO);
-    const uint32_t q_hi = smem_u32(bigp + Big::Q_HI);
-    const uint32_t q_lo = smem_u32(bigp + Big::Q_LO_PK);       // read only for the per-key gate
-    const uint32_t k_hi = smem_u32(bigp + Big::k_hi(GATE));
-    const uint32_t k_lo = smem_u32(bigp + Big::K_LO_PK);       // read only for the per-key gate
-    const uint32_t aq_hi = smem_u32(bigp + Big::aq_hi(GATE));
-    const uint32_t aq_lo = smem_u32(bigp + Big::aq_lo(GATE));
-    const float* su = reinterpret_cast<const float*>(small_at(n) + SMALL_U);
-    const float* qs = reinterpret_cast<const float*>(small_at(n) + SMALL_VEC);
-    const float* ks = qs + C;
-    const float* gam = ks + C;
     const int t0 = n * C;
 
     // ---- A: publish this warp's S^T slice as bf16 hi/lo -------------------------
@@ -211,31 +189,25 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       const int c = cw + 8 * nt + 2 * t4;
       uint32_t hi, lo;
       split_pair(S[nt][0], S[nt][1], hi, lo);
-      *reinterpret_cast<uint32_t*>(xs_hi + g * LDW + c) = hi;
-      *reinterpret_cast<uint32_t*>(xs_lo + g * LDW + c) = lo;
+      *reinterpret_cast<uint32_t*>(xs_hi + (vr + g) * LDW + c) = hi;
+      *reinterpret_cast<uint32_t*>(xs_lo + (vr + g) * LDW + c) = lo;
       split_pair(S[nt][2], S[nt][3], hi, lo);
-      *reinterpret_cast<uint32_t*>(xs_hi + (g + 8) * LDW + c) = hi;
-      *reinterpret_cast<uint32_t*>(xs_lo + (g + 8) * LDW + c) = lo;
+      *reinterpret_cast<uint32_t*>(xs_hi + (vr + g + 8) * LDW + c) = hi;
+      *reinterpret_cast<uint32_t*>(xs_lo + (vr + g + 8) * LDW + c) = lo;
     }
-    // Chunk n's operands (scalar gate) / first group (per-key gate).
-    const uint32_t par = STAGES == 2 ? ((n >> 1) & 1) : (n & 1);
-    ok = ok && mbar_wait(&bars[STAGES == 2 ? (n & 1) : 0], par, kWaitLimit);
-    __syncthreads();          // #1: S^T tiles visible; chunk n-1's tiles are free
+    ok = ok && mbar_wait(&bars[0], n & 1, kWaitLimit);   // W, QB, U, VEC of chunk n
+    __syncthreads();          // #1: S^T tiles visible
+    if (tid == 0 && !ok) atomicOr(p.error_word, kErrStateWait);
 
-    if (tid == 0) {
-      if (!ok) atomicOr(p.error_word, kErrStateWait);
-      if (STAGES == 2 && n + 1 < p.N) issue_group1(n + 1, &bars[(n + 1) & 1]);
-    }
-
-    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T q^T (JT n-tiles each) -------
+    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T QB^T (JT n-tiles each) -----
     float Rhh[JT][4], Rlh[JT][4], Rhl[JT][4], Oh[JT][4], Ol[JT][4], Ox[JT][4];
 #pragma unroll
     for (int jt = 0; jt < JT; ++jt) {
       const int j = jw + 8 * jt + 2 * t4;
-      Rhh[jt][0] = su[j * VT + g];
-      Rhh[jt][1] = su[(j + 1) * VT + g];
-      Rhh[jt][2] = su[j * VT + g + 8];
-      Rhh[jt][3] = su[(j + 1) * VT + g + 8];
+      Rhh[jt][0] = su[j * VTK + vr + g];
+      Rhh[jt][1] = su[(j + 1) * VTK + vr + g];
+      Rhh[jt][2] = su[j * VTK + vr + g + 8];
+      Rhh[jt][3] = su[(j + 1) * VTK + vr + g + 8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = Oh[jt][e] = Ol[jt][e] = Ox[jt][e] = 0.f;
     }
@@ -251,10 +223,10 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       for (int jt = 0; jt < JT; ++jt) {
         const int rb = jw + 8 * jt + brow;
         uint32_t wh[4], wl[4], qh[4], ql[4];
-        ldsm_x4(wh, tile_addr(w_hi, rb, 16 * ks2 + bcol));
-        ldsm_x4(wl, tile_addr(w_lo, rb, 16 * ks2 + bcol));
-        ldsm_x4(qh, tile_addr(q_hi, rb, 16 * ks2 + bcol));
-        if (GATE) ldsm_x4(ql, tile_addr(q_lo, rb, 16 * ks2 + bcol));
+        ldsm_x4(wh, tile_addr(big + W_HI, rb, 16 * ks2 + bcol));
+        ldsm_x4(wl, tile_addr(big + W_LO, rb, 16 * ks2 + bcol));
+        ldsm_x4(qh, tile_addr(big + Q_HI, rb, 16 * ks2 + bcol));
+        ldsm_x4(ql, tile_addr(big + Q_LO, rb, 16 * ks2 + bcol));
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           mma_bf16_16816(Rhh[jt], ah[h2], wh[2 * h2], wh[2 * h2 + 1]);
@@ -262,12 +234,14 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
           mma_bf16_16816(Rhl[jt], ah[h2], wl[2 * h2], wl[2 * h2 + 1]);
           mma_bf16_16816(Oh[jt], ah[h2], qh[2 * h2], qh[2 * h2 + 1]);
           mma_bf16_16816(Ol[jt], al[h2], qh[2 * h2], qh[2 * h2 + 1]);
-          if (GATE) mma_bf16_16816(Ox[jt], ah[h2], ql[2 * h2], ql[2 * h2 + 1]);
+          mma_bf16_16816(Ox[jt], ah[h2], ql[2 * h2], ql[2 * h2 + 1]);
         }
       }
     }
 
-    // ---- C: publish r^T and rho^T = r^T diag(kscale); scale o part 1 -------------
+    // ---- C: publish r^T and rho^T = r^T diag(kscale) ------------------------------
+    const float* qs = vec;
+    const float* ks = vec + C;
     float O[JT][4];
 #pragma unroll
     for (int jt = 0; jt < JT; ++jt) {
@@ -277,36 +251,43 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       for (int e = 0; e < 4; ++e) R[e] = Rhh[jt][e] + (Rlh[jt][e] + Rhl[jt][e]);
       uint32_t hi, lo;
       split_pair(R[0], R[1], hi, lo);
-      *reinterpret_cast<uint32_t*>(xr_hi + g * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xr_lo + g * LDA + j) = lo;
+      *reinterpret_cast<uint32_t*>(xr_hi + (vr + g) * LDA + j) = hi;
+      *reinterpret_cast<uint32_t*>(xr_lo + (vr + g) * LDA + j) = lo;
       split_pair(R[2], R[3], hi, lo);
-      *reinterpret_cast<uint32_t*>(xr_hi + (g + 8) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xr_lo + (g + 8) * LDA + j) = lo;
+      *reinterpret_cast<uint32_t*>(xr_hi + (vr + g + 8) * LDA + j) = hi;
+      *reinterpret_cast<uint32_t*>(xr_lo + (vr + g + 8) * LDA + j) = lo;
       const float k0 = ks[j], k1 = ks[j + 1];
       split_pair(R[0] * k0, R[1] * k1, hi, lo);
-      *reinterpret_cast<uint32_t*>(xp_hi + g * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xp_lo + g * LDA + j) = lo;
+      *reinterpret_cast<uint32_t*>(xp_hi + (vr + g) * LDA + j) = hi;
+      *reinterpret_cast<uint32_t*>(xp_lo + (vr + g) * LDA + j) = lo;
       split_pair(R[2] * k0, R[3] * k1, hi, lo);
-      *reinterpret_cast<uint32_t*>(xp_hi + (g + 8) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xp_lo + (g + 8) * LDA + j) = lo;
+      *reinterpret_cast<uint32_t*>(xp_hi + (vr + g + 8) * LDA + j) = hi;
+      *reinterpret_cast<uint32_t*>(xp_lo + (vr + g + 8) * LDA + j) = lo;
       const float q0 = qs[j], q1 = qs[j + 1];
       O[jt][0] = (Oh[jt][0] + (Ol[jt][0] + Ox[jt][0])) * q0;
       O[jt][1] = (Oh[jt][1] + (Ol[jt][1] + Ox[jt][1])) * q1;
       O[jt][2] = (Oh[jt][2] + (Ol[jt][2] + Ox[jt][2])) * q0;
       O[jt][3] = (Oh[jt][3] + (Ol[jt][3] + Ox[jt][3])) * q1;
     }
-    if (GATE) ok = ok && mbar_wait(&bars[1], n & 1, kWaitLimit);   // k, A_qk of chunk n
-    __syncthreads();                           // #2: r^T / rho^T tiles visible
-
-    // ---- D: S^T = gamma S^T + rho^T k (channels of this warp), o^T part 2 -----------
+    // gamma of this warp's channels, read before the group-1 buffer is reloaded.
+    float gam[CT][2];
 #pragma unroll
     for (int nt = 0; nt < CT; ++nt) {
       const int c = cw + 8 * nt + 2 * t4;
-      const float g0 = gam[c], g1 = gam[c + 1];
-      S[nt][0] *= g0;
-      S[nt][1] *= g1;
-      S[nt][2] *= g0;
-      S[nt][3] *= g1;
+      gam[nt][0] = vec[2 * C + c];
+      gam[nt][1] = vec[2 * C + c + 1];
+    }
+    ok = ok && mbar_wait(&bars[1], n & 1, kWaitLimit);   // KB, A_qk of chunk n
+    __syncthreads();                           // #2: r^T / rho^T tiles visible; group 1 is free
+    if (tid == 0 && n + 1 < p.N) issue_group1(n + 1);
+
+    // ---- D: S^T = gamma S^T + rho^T KB (channels of this warp), o^T part 2 ---------
+#pragma unroll
+    for (int nt = 0; nt < CT; ++nt) {
+      S[nt][0] *= gam[nt][0];
+      S[nt][1] *= gam[nt][1];
+      S[nt][2] *= gam[nt][0];
+      S[nt][3] *= gam[nt][1];
     }
     float Dl[CT][4], Dx[CT][4], Phh[JT][4], Plh[JT][4], Phl[JT][4];
 #pragma unroll
@@ -323,18 +304,15 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
 #pragma unroll
       for (int np = 0; np < CT / 2; ++np) {
-        uint32_t kh[4];
-        ldsm_x4_t(kh, tile_addr(k_hi, 16 * ks + krow, kcol + 16 * np));
+        uint32_t kh[4], kl[4];
+        ldsm_x4_t(kh, tile_addr(big + K_HI, 16 * ks + krow, kcol + 16 * np));
+        ldsm_x4_t(kl, tile_addr(big + K_LO, 16 * ks + krow, kcol + 16 * np));
         mma_bf16_16816(S[2 * np], ph, kh[0], kh[1]);
         mma_bf16_16816(S[2 * np + 1], ph, kh[2], kh[3]);
         mma_bf16_16816(Dl[2 * np], pl, kh[0], kh[1]);
         mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
-        if (GATE) {
-          uint32_t kl[4];
-          ldsm_x4_t(kl, tile_addr(k_lo, 16 * ks + krow, kcol + 16 * np));
-          mma_bf16_16816(Dx[2 * np], ph, kl[0], kl[1]);
-          mma_bf16_16816(Dx[2 * np + 1], ph, kl[2], kl[3]);
-        }
+        mma_bf16_16816(Dx[2 * np], ph, kl[0], kl[1]);
+        mma_bf16_16816(Dx[2 * np + 1], ph, kl[2], kl[3]);
       }
     }
 #pragma unroll
@@ -348,8 +326,8 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
 #pragma unroll
       for (int jt = 0; jt < JT; ++jt) {
         uint32_t ah[4], al[4];
-        ldsm_x4(ah, tile_addr(aq_hi, jw + 8 * jt + brow, 16 * ks2 + bcol));
-        ldsm_x4(al, tile_addr(aq_lo, jw + 8 * jt + brow, 16 * ks2 + bcol));
+        ldsm_x4(ah, tile_addr(big + AQ_HI, jw + 8 * jt + brow, 16 * ks2 + bcol));
+        ldsm_x4(al, tile_addr(big + AQ_LO, jw + 8 * jt + brow, 16 * ks2 + bcol));
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           mma_bf16_16816(Phh[jt], rh[h2], ah[2 * h2], ah[2 * h2 + 1]);
@@ -363,7 +341,7 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[nt][e] += Dl[nt][e] + Dx[nt][e];
 
-    // ---- E: o rows of this warp (i in [jw, jw + 8 JT)) -> global ---------------
+    // ---- E: o rows of this warp (i in [jw, jw + 8 JT)), 16 value columns -> global
 #pragma unroll
     for (int jt = 0; jt < JT; ++jt) {
       const int i = 8 * jt + 2 * t4;
@@ -379,7 +357,7 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       const int t = t0 + jw + i;
       if (t < p.T) {
         const float4 val = *reinterpret_cast<const float4*>(xo + i * 16 + c4);
-        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0 + c4;
+        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0 + vr + c4;
         if (p.out_bf16) {
           uint2 pk;
           pk.x = pack_bf16(val.x, val.y);
@@ -392,14 +370,9 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
     }
     __syncwarp();
 
-    if (STAGES == 1 && n + 1 < p.N) {
-      // Single stage: every warp must be done with this chunk's tiles before
-      // the next chunk's loads overwrite them.
-      __syncthreads();
-      if (tid == 0) {
-        issue_group1(n + 1, &bars[0]);
-        issue_group2(n + 1, &bars[1]);
-      }
+    if (n + 1 < p.N) {
+      __syncthreads();   // every warp is done with group 2 of chunk n
+      if (tid == 0) issue_group2(n + 1);
     }
   }
 
@@ -409,7 +382,7 @@ __global__ void __launch_bounds__(WARPS * 32) state_kernel(const __grid_constant
       const int c = cw + 8 * nt + 2 * t4;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int vv = g + (e >> 1) * 8, cc = c + (e & 1);
+        const int vv = vr + g + (e >> 1) * 8, cc = c + (e & 1);
         p.sT[(seq * K + cc) * V + v0 + vv] = S[nt][e];
       }
     }
@@ -845,29 +818,26 @@ bool encode_bthd(CUtensorMap* map, const void* base, int B, int T, int heads) {
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int GATE, int STAGES, int WARPS>
-gdr_status launch_one(const Params& p, cudaStream_t stream) {
+template <int MG>
+gdr_status launch_kda(const Params& p, cudaStream_t stream) {
+  using LY = kda::Layout<MG>;
   Maps m;
   memset(&m, 0, sizeof m);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  bool ok = encode_slab(&m.w2, p, Slab::W2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_slab(&m.aq2, p, Slab::AQ2, BF, 2, C, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_slab(&m.u, p, Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, VT,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (GATE) {
-    ok = ok && encode_slab(&m.qb2, p, Slab::QB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_slab(&m.kb2, p, Slab::KB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    ok = ok && encode_bthd(&m.q, p.q, p.B, p.T, p.H) && encode_bthd(&m.k, p.k, p.B, p.T, p.H);
-  }
+  const bool ok =
+      encode_slab(&m.w2, p, Slab::W2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_slab(&m.aq2, p, Slab::AQ2, BF, 2, C, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_slab(&m.u, p, Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, LY::VTK,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
+      encode_slab(&m.qb2, p, Slab::QB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_slab(&m.kb2, p, Slab::KB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return GDR_ERR_CUDA;
-  constexpr Layout LY(GATE, STAGES);
-  auto kern = state_kernel<GATE, STAGES, WARPS>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total) !=
+  auto kern = state_kda_kernel<MG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
       cudaSuccess)
     return GDR_ERR_CUDA;
-  dim3 grid(V / VT, p.HV, p.B);
-  kern<<<grid, WARPS * 32, LY.total, stream>>>(m, p);
+  dim3 grid(V / LY::VTK, p.HV, p.B);
+  kern<<<grid, MG * kda::WARPS * 32, LY::TOTAL, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
@@ -893,7 +863,7 @@ gdr_status launch_ws(const Params& p, cudaStream_t stream) {
 }  // namespace
 
 gdr_status launch_state(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode) return launch_one<1, 1, STATE_WARPS>(p, stream);
+  if (p.gate_mode) return launch_kda<KDA_MG>(p, stream);
   // Scalar gate: the fused chain + output launch when the chains leave SMs
   // for the outputs, else chain and outputs in the same CTAs.
   const gdr_status st = launch_recur(p, stream);
