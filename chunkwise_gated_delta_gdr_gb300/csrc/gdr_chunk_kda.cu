@@ -99,13 +99,13 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
   uint8_t* slab = p.slabs + slab_index(p, b, hv, n) * p.slab_bytes;
 
   // ---- load q, k, v (bf16) and g (fp32) tiles; rows past T are zero-filled ----
-  for (int idx = tid; idx < 3 * C * 16; idx += THREADS) {
+  // Group 1: q, k, g (read from the start); group 2: v (read by the last products).
+  for (int idx = tid; idx < 2 * C * 16; idx += THREADS) {
     const int which = idx / (C * 16), e = idx % (C * 16), i = e >> 4, ch = e & 15;
     const int t = t0 + i;
     const bool ok = t < p.T;
     const size_t tt = (size_t)b * p.T + (ok ? t : 0);
-    const __nv_bfloat16* src = (which == 2) ? p.v + (tt * p.HV + hv) * V + ch * 8
-                                            : (which == 0 ? p.q : p.k) + (tt * p.H + h) * K + ch * 8;
+    const __nv_bfloat16* src = (which == 0 ? p.q : p.k) + (tt * p.H + h) * K + ch * 8;
     cp_async16(smem_u32(sm + which * (C * LDB * 2) + i * (LDB * 2) + ch * 16), src, ok ? 16u : 0u);
   }
   for (int idx = tid; idx < C * 32; idx += THREADS) {
@@ -114,9 +114,17 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
     const float* src = p.g + (((size_t)b * p.T + (ok ? t : 0)) * p.HV + hv) * K + ch * 4;
     cp_async16(smem_u32(sm + OFF_G + i * (LDG * 4) + ch * 16), src, ok ? 16u : 0u);
   }
+  cp_async_commit();
+  for (int idx = tid; idx < C * 16; idx += THREADS) {
+    const int i = idx >> 4, ch = idx & 15, t = t0 + i;
+    const bool ok = t < p.T;
+    const __nv_bfloat16* src = p.v + (((size_t)b * p.T + (ok ? t : 0)) * p.HV + hv) * V + ch * 8;
+    cp_async16(smem_u32(sm + OFF_V + i * (LDB * 2) + ch * 16), src, ok ? 16u : 0u);
+  }
+  cp_async_commit();
   if (tid < C) bs[tid] = (t0 + tid < p.T) ? p.beta[((size_t)b * p.T + t0 + tid) * p.HV + hv] : 0.f;
   if (tid == 0) *flags = 0u;
-  cp_async_wait_all();
+  cp_async_wait<1>();
   __syncthreads();
 
   // ---- gate cumsum per channel (threads 0-127) | L2 norms (threads 128-255) ----
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
       for (int z = 0; z < 4; ++z) accq[u][z] = acck[u][z] = 0.f;
     const float* Gr = G + 16 * I * LDG;
     const float sqa = sq[ra], sqb = sq[rb], nka = nk[ra], nkb = nk[rb];
-#pragma unroll 1
+#pragma unroll 2
     for (int s = 0; s < K / 16; ++s) {
       const int c0 = 16 * s + cq;
       const float2 gr0 = *reinterpret_cast<const float2*>(Gr + c0);
@@ -261,12 +269,17 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
   }
   __syncthreads();   // q, k and G are no longer read by the dots
 
-  // ---- elementwise outputs: QB, KB, gamma; exp(G) k^ split in place ----------
-  {
+  // ---- warps 0-1: level 0 of the inverse (diagonal blocks, in registers) ------
+  // ---- warps 2-7: QB, KB, gamma; exp(G) k^ split in place --------------------
+  float xd[16];
+  if (tid < 64) {
+    inverse_level0<LDL>(L, xd, tid);
+  } else {
     const float* Gl = G + (C - 1) * LDG;
     __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::QB2);
     __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::KB2);
-    for (int idx = tid; idx < C * 16; idx += THREADS) {
+    constexpr int EW = THREADS - 64;
+    for (int idx = tid - 64; idx < C * 16; idx += EW) {
       const int i = idx >> 4, c = (idx & 15) * 8;
       float gi[8], gl[8], qf[8], kf[8];
       *reinterpret_cast<float4*>(gi) = *reinterpret_cast<const float4*>(G + i * LDG + c);
@@ -296,11 +309,13 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
       *reinterpret_cast<uint4*>(qs + i * LDB + c) = lo;
     }
     float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
-    if (tid < K) vec[2 * C + tid] = __expf(Gl[tid]);
-    else vec[tid - K] = 1.f;   // qscale = kscale = 1
+    for (int e = tid - 64; e < 2 * C + K; e += EW) {
+      if (e < K) vec[2 * C + e] = __expf(Gl[e]);
+      else vec[e - K] = 1.f;   // qscale = kscale = 1
+    }
     // A_qk blocks above the diagonal: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3).
     __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
-    for (int idx = tid; idx < 6 * 16 * 4; idx += THREADS) {
+    for (int idx = tid - 64; idx < 6 * 16 * 4; idx += EW) {
       const int plane = idx & 1, half = (idx >> 1) & 1, rr = (idx >> 2) & 15, blk = idx >> 6;
       const int Ib = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int Jb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -311,7 +326,10 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
   __syncthreads();   // G is dead: X and the scratch take its place
 
   float* X = reinterpret_cast<float*>(sm + OFF_X);
-  unit_lower_inverse64<LDL, LDL>(L, X, reinterpret_cast<float*>(sm + OFF_T), tid);
+  if (tid < 64) inverse_level0_store<LDL>(X, xd, tid);
+  __syncthreads();
+  inverse_levels12<LDL, LDL>(L, X, reinterpret_cast<float*>(sm + OFF_T), tid);
+  cp_async_wait<0>();   // v
   __syncthreads();   // L is dead: the X hi / lo boxes take its place
 
   // ---- X -> hi / lo bf16 boxes (the 10 blocks on and below the diagonal) ------

@@ -335,9 +335,9 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
       const int c0 = cc * 32 + half * 16;   // first column of this lane's 16
       if (!is_u) {
         uint32_t hi[8], lo[8];
-#pragma unroll
         // SSD keeps no erase term: W = 0 (then X = I and U = v).
         const float ws = p.ssd ? 0.f : -1.f;
+#pragma unroll
         for (int e = 0; e < 16; e += 2) split_pair(ws * s[e], ws * s[e + 1], hi[e / 2], lo[e / 2]);
         const int bx = c0 >> 6, c = (c0 & 63) >> 3;
         uint8_t* wh = sm + OFF_WS + bx * 8192;

@@ -17,23 +17,28 @@
 namespace gdr {
 namespace fast {
 
-// L: [64][LDL] fp32; X: [64][LDX] fp32; T: scratch [32][36] fp32.
-template <int LDL, int LDX>
-__device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, float* T, int tid) {
-  if (tid < 64) {
-    const int o = (tid >> 4) * 16, col = tid & 15;
-    float xd[16];
+// Level 0 for threads 0-63: column (tid & 15) of diagonal block tid >> 4, in registers.
+template <int LDL>
+__device__ __forceinline__ void inverse_level0(const float* L, float (&xd)[16], int tid) {
+  const int o = (tid >> 4) * 16, col = tid & 15;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float acc = (i == col) ? 1.f : 0.f;
+  for (int i = 0; i < 16; ++i) {
+    float acc = (i == col) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < i; ++m) acc = fmaf(-L[(o + i) * LDL + o + m], xd[m], acc);
-      xd[i] = acc;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) X[(o + i) * LDX + o + col] = xd[i];
+    for (int m = 0; m < i; ++m) acc = fmaf(-L[(o + i) * LDL + o + m], xd[m], acc);
+    xd[i] = acc;
   }
-  __syncthreads();
+}
+template <int LDX>
+__device__ __forceinline__ void inverse_level0_store(float* X, const float (&xd)[16], int tid) {
+  const int o = (tid >> 4) * 16, col = tid & 15;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) X[(o + i) * LDX + o + col] = xd[i];
+}
+
+// Levels 1 and 2, once the diagonal blocks of X are in place and visible.
+template <int LDL, int LDX>
+__device__ __forceinline__ void inverse_levels12(const float* L, float* X, float* T, int tid) {
   // Level 1: threads 0-127, each one row segment of 4 columns.
   {
     const int which = (tid >> 6) & 1, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
@@ -90,6 +95,18 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, f
     }
     *reinterpret_cast<float4*>(X + (32 + i) * LDX + j0) = make_float4(-r4[0], -r4[1], -r4[2], -r4[3]);
   }
+}
+
+// L: [64][LDL] fp32; X: [64][LDX] fp32; T: scratch [32][36] fp32.
+template <int LDL, int LDX>
+__device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, float* T, int tid) {
+  if (tid < 64) {
+    float xd[16];
+    inverse_level0<LDL>(L, xd, tid);
+    inverse_level0_store<LDX>(X, xd, tid);
+  }
+  __syncthreads();
+  inverse_levels12<LDL, LDX>(L, X, T, tid);
 }
 
 }  // namespace fast
