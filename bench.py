@@ -364,6 +364,9 @@ def run_ours(args, rank, local_rank, world):
     flops_alg = FLOP_PER_TOKEN_HEAD * w.B * w.T * w.HV
     achieved = bytes_alg / (ms * 1e-3) / 1e9
     traffic, traffic_per = recorded_traffic(w.name)
+    # Kernel names in the ncu summaries: tcgen05 chunk kernel + fused recurrence
+    # (scalar gate), mma.sync chunk kernel + tcgen05 state kernel (per-key gate).
+    ck, rk = ("chunk_kda_kernel", "state_kda_tc_kernel") if w.gate_mode else ("chunk_tc_kernel", "recur_kernel")
     tokens = world * w.B * w.T
     line = {
         "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
@@ -377,9 +380,9 @@ def run_ours(args, rank, local_rank, world):
                      "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
         "kernels": {"chunk_local": {"ms": statistics.mean(prep),
-                                    "traffic": (traffic_per or {}).get("chunk_tc_kernel")},
+                                    "traffic": (traffic_per or {}).get(ck)},
                     "recurrence": {"ms": statistics.mean(rec),
-                                   "traffic": (traffic_per or {}).get("recur_kernel")}},
+                                   "traffic": (traffic_per or {}).get(rk)}},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": f"gdr_chunk_fwd_host per step, {E2E_STREAMS} streams alternating"},

@@ -92,6 +92,8 @@ inline __host__ __device__ size_t slab_index(const Params& p, int b, int hv, int
 gdr_status launch_state(const Params& p, cudaStream_t stream);
 // Scalar gate: state chain and chunk outputs in one launch (gdr_recur.cu).
 gdr_status launch_recur(const Params& p, cudaStream_t stream);
+// Per-key gate: the recurrence on tcgen05, 64 value columns per CTA (gdr_state_kda.cu).
+gdr_status launch_state_kda_tc(const Params& p, cudaStream_t stream);
 // Per-key gate: chunk-local kernel on mma.sync (gdr_chunk_kda.cu).
 gdr_status launch_chunk_kda(const Params& p, cudaStream_t stream);
 gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream);

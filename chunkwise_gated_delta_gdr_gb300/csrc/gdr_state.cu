@@ -1,8 +1,9 @@
-// gdr_state.cu -- inter-chunk state recurrence of the fast path.
+// gdr_state.cu -- scalar-gate state recurrence for shapes the fused kernel
+// does not take (fallback of gdr_recur.cu), and the dispatch of the recurrence.
 //
-// One CTA per (batch b, value head hv, 16-column V tile), 8 warps, serial over
-// the chunks of the sequence. Per chunk n it applies the inter-chunk loop of
-// the "分块并行计算（Chunkwise）" notes (listing of the chunk 间递推 section):
+// One CTA per (batch b, value head hv, 16-column V tile), serial over the
+// chunks of the sequence. Per chunk n it applies the inter-chunk loop of the
+// "分块并行计算（Chunkwise）" notes (listing of the chunk 间递推 section):
 //     r   = U - W S
 //     o   = (q exp(G)) S + A_qk r
 //     S   = exp(G_last) S + (exp(G_last - G) k)^T (beta r)
@@ -12,16 +13,15 @@
 //     r^T  = U^T - S^T W^T                      (16 x 64,  K = 128)
 //     o^T  = diag-scaled S^T q^T + r^T A_qk^T   (16 x 64)
 //     S^T <- gamma S^T + (kscale r)^T k         (16 x 128, K = 64)
-// The state S^T stays in fp32 registers for the whole sequence (each warp owns
-// 16 of its 128 key channels). Products run on the tensor cores with
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate); an fp32-valued operand x is
-// fed as x_hi + x_lo with x_hi = bf16(x), x_lo = bf16(x - x_hi), and the
-// lo * lo term is dropped, which keeps about 16 significant bits per product.
-// Every split term accumulates into its own register tile.
+// The state S^T stays in fp32 registers for the whole sequence. Products run
+// on the tensor cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate); an
+// fp32-valued operand x is fed as x_hi + x_lo with x_hi = bf16(x),
+// x_lo = bf16(x - x_hi), and the lo * lo term is dropped, which keeps about 16
+// significant bits per product. Every split term accumulates into its own
+// register tile. The per-key gate runs on tcgen05 instead (gdr_state_kda.cu).
 //
 // Chunk operands arrive by TMA (128-byte swizzled tiles, read conflict-free
-// by ldmatrix), one chunk ahead, counted on mbarriers; the only per-chunk
-// exchanges are two shared-memory tiles (S^T and r^T) and two CTA barriers.
+// by ldmatrix), one chunk ahead, counted on mbarriers.
 #include <string.h>
 
 #include <cuda.h>
@@ -39,9 +39,6 @@ using namespace ptx;
 
 constexpr int LDW = K + 8;   // bf16 row stride of the S^T exchange tiles (272 B)
 constexpr int LDA = C + 8;   // bf16 row stride of the r^T exchange tiles (144 B)
-#ifndef KDA_MG
-#define KDA_MG 4
-#endif
 constexpr long kWaitLimit = 1L << 24;
 constexpr unsigned int kErrStateWait = 4u;
 
@@ -54,340 +51,6 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int c) {
 struct Maps {
   CUtensorMap q, k, w2, aq2, u, qb2, kb2;
 };
-
-// ---------------------------------------------------------------------------
-// Per-key gate. One CTA per (b, hv, 16 MG value columns): MG groups of 4 warps,
-// group m owning value rows 16 m .. 16 m + 15 of the CTA's S^T tile. All groups
-// read the same chunk operands from one shared buffer, so a chunk's W, QB, KB
-// and A_qk cross from L2 once per MG 16-column tiles.
-//
-// Operand tiles of one chunk, 128-byte swizzled [64][128] bf16 tiles as two
-// 8 KB boxes. Group 1 (read by the r and o products): W hi/lo, QB hi/lo, plus
-// the U tile and VEC in the small buffer. Group 2 (read by the state update and
-// the second o product): KB hi/lo, A_qk hi/lo.
-namespace kda {
-constexpr int WARPS = 4;                          // per group
-constexpr int JT = C / 8 / WARPS, CT = K / 8 / WARPS;
-constexpr int W_HI = 0, W_LO = 16384, Q_HI = 32768, Q_LO = 49152;
-constexpr int K_HI = 65536, K_LO = 81920, AQ_HI = 98304, AQ_LO = 106496, BIG = 114688;
-constexpr uint32_t kGroup2Bytes = 32768 + 16384;
-
-template <int MG>
-struct Layout {
-  static constexpr int VTK = 16 * MG;                     // value columns per CTA
-  static constexpr int SMALL_U = BIG;                     // U tile [C][VTK] fp32
-  static constexpr int SMALL_VEC = SMALL_U + C * VTK * 4; // qscale, kscale, gamma
-  static constexpr int XS = SMALL_VEC + 1024;             // S^T hi / lo [VTK][LDW]
-  static constexpr int XR = XS + 2 * VTK * LDW * 2;       // r^T, rho^T hi / lo [VTK][LDA]
-  static constexpr int XO = XR + 4 * VTK * LDA * 2;       // o staging, per warp
-  static constexpr int BARS = XO + MG * WARPS * (8 * JT * 16) * 4;
-  static constexpr int TOTAL = BARS + 64 + 1024;
-  static constexpr uint32_t kGroup1Bytes = 32768 + 32768 + C * VTK * 4 + 1024;
-};
-}  // namespace kda
-
-template <int MG>
-__global__ void __launch_bounds__(MG * kda::WARPS * 32, 1)
-    state_kda_kernel(const __grid_constant__ Maps maps, Params p) {
-  using namespace kda;
-  using LY = Layout<MG>;
-  constexpr int VTK = LY::VTK;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-  const int v0 = vt * VTK;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mg = warp / WARPS, wi = warp % WARPS;
-  const int vr = 16 * mg;                                 // this group's rows of S^T
-  const int g = lane >> 2, t4 = lane & 3;
-
-  __nv_bfloat16* xs_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY::XS);
-  __nv_bfloat16* xs_lo = xs_hi + VTK * LDW;
-  __nv_bfloat16* xr_hi = reinterpret_cast<__nv_bfloat16*>(sm + LY::XR);
-  __nv_bfloat16* xr_lo = xr_hi + VTK * LDA;
-  __nv_bfloat16* xp_hi = xr_lo + VTK * LDA;
-  __nv_bfloat16* xp_lo = xp_hi + VTK * LDA;
-  float* xo = reinterpret_cast<float*>(sm + LY::XO) + warp * (8 * JT * 16);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BARS);   // [0] group 1, [1] group 2
-  const float* su = reinterpret_cast<const float*>(sm + LY::SMALL_U);
-  const float* vec = reinterpret_cast<const float*>(sm + LY::SMALL_VEC);
-
-  const size_t seq = (size_t)b * p.HV + hv;
-  const int chunk0 = (int)(seq * p.N);
-
-  // Loads of chunk n, issued by one thread. Group 1 is reissued as soon as
-  // every warp is past the products that read it (the CTA barrier after the
-  // r^T tiles), group 2 after the chunk's last product.
-  auto issue_group1 = [&](int n) {
-    const int idx = chunk0 + n;
-    const uint32_t big = smem_u32(sm);
-    mbar_expect_tx(&bars[0], LY::kGroup1Bytes);
-    tma_load3(big + W_HI, &maps.w2, 0, 0, idx, &bars[0]);
-    tma_load3(big + W_HI + 8192, &maps.w2, 64, 0, idx, &bars[0]);
-    tma_load3(big + W_LO, &maps.w2, 0, 64, idx, &bars[0]);
-    tma_load3(big + W_LO + 8192, &maps.w2, 64, 64, idx, &bars[0]);
-    tma_load3(big + Q_HI, &maps.qb2, 0, 0, idx, &bars[0]);
-    tma_load3(big + Q_HI + 8192, &maps.qb2, 64, 0, idx, &bars[0]);
-    tma_load3(big + Q_LO, &maps.qb2, 0, 64, idx, &bars[0]);
-    tma_load3(big + Q_LO + 8192, &maps.qb2, 64, 64, idx, &bars[0]);
-    tma_load3(big + LY::SMALL_U, &maps.u, v0, 0, idx, &bars[0]);
-    bulk_load(big + LY::SMALL_VEC, p.slabs + (size_t)idx * p.slab_bytes + Slab::VEC, 1024, &bars[0]);
-  };
-  auto issue_group2 = [&](int n) {
-    const int idx = chunk0 + n;
-    const uint32_t big = smem_u32(sm);
-    mbar_expect_tx(&bars[1], kGroup2Bytes);
-    tma_load3(big + K_HI, &maps.kb2, 0, 0, idx, &bars[1]);
-    tma_load3(big + K_HI + 8192, &maps.kb2, 64, 0, idx, &bars[1]);
-    tma_load3(big + K_LO, &maps.kb2, 0, 64, idx, &bars[1]);
-    tma_load3(big + K_LO + 8192, &maps.kb2, 64, 64, idx, &bars[1]);
-    tma_load3(big + AQ_HI, &maps.aq2, 0, 0, idx, &bars[1]);
-    tma_load3(big + AQ_LO, &maps.aq2, 0, 64, idx, &bars[1]);
-  };
-
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    issue_group1(0);
-    issue_group2(0);
-  }
-
-  const int jw = 8 * JT * wi, cw = 8 * CT * wi;
-
-  float S[CT][4];
-#pragma unroll
-  for (int nt = 0; nt < CT; ++nt) {
-    const int c = cw + 8 * nt + 2 * t4;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int vv = vr + g + (e >> 1) * 8, cc = c + (e & 1);
-      S[nt][e] = p.s0 ? p.s0[(seq * K + cc) * V + v0 + vv] : 0.f;
-    }
-  }
-
-  // ldmatrix lane addressing.
-  const int arow = vr + (lane & 7) + ((lane >> 3) & 1) * 8;   // A fragments (this group's 16 rows)
-  const int acol = (lane >> 4) * 8;
-  const int brow = (lane & 7);                                // B from [n][k] tiles, 2 k-steps per x4
-  const int bcol = (lane >> 3) * 8;
-  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;        // B from the [j][c] k tile (.trans)
-  const int kcol = cw + (lane >> 4) * 8;                      // two c-tiles per x4
-  const uint32_t big = smem_u32(sm);
-  bool ok = true;
-
-  for (int n = 0; n < p.N; ++n) {
-    const int t0 = n * C;
-
-    // ---- A: publish this warp's S^T slice as bf16 hi/lo -------------------------
-#pragma unroll
-    for (int nt = 0; nt < CT; ++nt) {
-      const int c = cw + 8 * nt + 2 * t4;
-      uint32_t hi, lo;
-      split_pair(S[nt][0], S[nt][1], hi, lo);
-      *reinterpret_cast<uint32_t*>(xs_hi + (vr + g) * LDW + c) = hi;
-      *reinterpret_cast<uint32_t*>(xs_lo + (vr + g) * LDW + c) = lo;
-      split_pair(S[nt][2], S[nt][3], hi, lo);
-      *reinterpret_cast<uint32_t*>(xs_hi + (vr + g + 8) * LDW + c) = hi;
-      *reinterpret_cast<uint32_t*>(xs_lo + (vr + g + 8) * LDW + c) = lo;
-    }
-    ok = ok && mbar_wait(&bars[0], n & 1, kWaitLimit);   // W, QB, U, VEC of chunk n
-    __syncthreads();          // #1: S^T tiles visible
-    if (tid == 0 && !ok) atomicOr(p.error_word, kErrStateWait);
-
-    // ---- B: r^T = U^T - S^T W^T and o^T part 1 = S^T QB^T (JT n-tiles each) -----
-    float Rhh[JT][4], Rlh[JT][4], Rhl[JT][4], Oh[JT][4], Ol[JT][4], Ox[JT][4];
-#pragma unroll
-    for (int jt = 0; jt < JT; ++jt) {
-      const int j = jw + 8 * jt + 2 * t4;
-      Rhh[jt][0] = su[j * VTK + vr + g];
-      Rhh[jt][1] = su[(j + 1) * VTK + vr + g];
-      Rhh[jt][2] = su[j * VTK + vr + g + 8];
-      Rhh[jt][3] = su[(j + 1) * VTK + vr + g + 8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = Oh[jt][e] = Ol[jt][e] = Ox[jt][e] = 0.f;
-    }
-#pragma unroll
-    for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
-      uint32_t ah[2][4], al[2][4];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        ldsm_x4(ah[h2], smem_u32(xs_hi + arow * LDW + 16 * (ks2 + h2) + acol));
-        ldsm_x4(al[h2], smem_u32(xs_lo + arow * LDW + 16 * (ks2 + h2) + acol));
-      }
-#pragma unroll
-      for (int jt = 0; jt < JT; ++jt) {
-        const int rb = jw + 8 * jt + brow;
-        uint32_t wh[4], wl[4], qh[4], ql[4];
-        ldsm_x4(wh, tile_addr(big + W_HI, rb, 16 * ks2 + bcol));
-        ldsm_x4(wl, tile_addr(big + W_LO, rb, 16 * ks2 + bcol));
-        ldsm_x4(qh, tile_addr(big + Q_HI, rb, 16 * ks2 + bcol));
-        ldsm_x4(ql, tile_addr(big + Q_LO, rb, 16 * ks2 + bcol));
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          mma_bf16_16816(Rhh[jt], ah[h2], wh[2 * h2], wh[2 * h2 + 1]);
-          mma_bf16_16816(Rlh[jt], al[h2], wh[2 * h2], wh[2 * h2 + 1]);
-          mma_bf16_16816(Rhl[jt], ah[h2], wl[2 * h2], wl[2 * h2 + 1]);
-          mma_bf16_16816(Oh[jt], ah[h2], qh[2 * h2], qh[2 * h2 + 1]);
-          mma_bf16_16816(Ol[jt], al[h2], qh[2 * h2], qh[2 * h2 + 1]);
-          mma_bf16_16816(Ox[jt], ah[h2], ql[2 * h2], ql[2 * h2 + 1]);
-        }
-      }
-    }
-
-    // ---- C: publish r^T and rho^T = r^T diag(kscale) ------------------------------
-    const float* qs = vec;
-    const float* ks = vec + C;
-    float O[JT][4];
-#pragma unroll
-    for (int jt = 0; jt < JT; ++jt) {
-      const int j = jw + 8 * jt + 2 * t4;
-      float R[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) R[e] = Rhh[jt][e] + (Rlh[jt][e] + Rhl[jt][e]);
-      uint32_t hi, lo;
-      split_pair(R[0], R[1], hi, lo);
-      *reinterpret_cast<uint32_t*>(xr_hi + (vr + g) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xr_lo + (vr + g) * LDA + j) = lo;
-      split_pair(R[2], R[3], hi, lo);
-      *reinterpret_cast<uint32_t*>(xr_hi + (vr + g + 8) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xr_lo + (vr + g + 8) * LDA + j) = lo;
-      const float k0 = ks[j], k1 = ks[j + 1];
-      split_pair(R[0] * k0, R[1] * k1, hi, lo);
-      *reinterpret_cast<uint32_t*>(xp_hi + (vr + g) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xp_lo + (vr + g) * LDA + j) = lo;
-      split_pair(R[2] * k0, R[3] * k1, hi, lo);
-      *reinterpret_cast<uint32_t*>(xp_hi + (vr + g + 8) * LDA + j) = hi;
-      *reinterpret_cast<uint32_t*>(xp_lo + (vr + g + 8) * LDA + j) = lo;
-      const float q0 = qs[j], q1 = qs[j + 1];
-      O[jt][0] = (Oh[jt][0] + (Ol[jt][0] + Ox[jt][0])) * q0;
-      O[jt][1] = (Oh[jt][1] + (Ol[jt][1] + Ox[jt][1])) * q1;
-      O[jt][2] = (Oh[jt][2] + (Ol[jt][2] + Ox[jt][2])) * q0;
-      O[jt][3] = (Oh[jt][3] + (Ol[jt][3] + Ox[jt][3])) * q1;
-    }
-    // gamma of this warp's channels, read before the group-1 buffer is reloaded.
-    float gam[CT][2];
-#pragma unroll
-    for (int nt = 0; nt < CT; ++nt) {
-      const int c = cw + 8 * nt + 2 * t4;
-      gam[nt][0] = vec[2 * C + c];
-      gam[nt][1] = vec[2 * C + c + 1];
-    }
-    ok = ok && mbar_wait(&bars[1], n & 1, kWaitLimit);   // KB, A_qk of chunk n
-    __syncthreads();                           // #2: r^T / rho^T tiles visible; group 1 is free
-    if (tid == 0 && n + 1 < p.N) issue_group1(n + 1);
-
-    // ---- D: S^T = gamma S^T + rho^T KB (channels of this warp), o^T part 2 ---------
-#pragma unroll
-    for (int nt = 0; nt < CT; ++nt) {
-      S[nt][0] *= gam[nt][0];
-      S[nt][1] *= gam[nt][1];
-      S[nt][2] *= gam[nt][0];
-      S[nt][3] *= gam[nt][1];
-    }
-    float Dl[CT][4], Dx[CT][4], Phh[JT][4], Plh[JT][4], Phl[JT][4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-#pragma unroll
-      for (int nt = 0; nt < CT; ++nt) Dl[nt][e] = Dx[nt][e] = 0.f;
-#pragma unroll
-      for (int jt = 0; jt < JT; ++jt) Phh[jt][e] = Plh[jt][e] = Phl[jt][e] = 0.f;
-    }
-#pragma unroll
-    for (int ks = 0; ks < C / 16; ++ks) {
-      uint32_t ph[4], pl[4];
-      ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * ks + acol));
-      ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * ks + acol));
-#pragma unroll
-      for (int np = 0; np < CT / 2; ++np) {
-        uint32_t kh[4], kl[4];
-        ldsm_x4_t(kh, tile_addr(big + K_HI, 16 * ks + krow, kcol + 16 * np));
-        ldsm_x4_t(kl, tile_addr(big + K_LO, 16 * ks + krow, kcol + 16 * np));
-        mma_bf16_16816(S[2 * np], ph, kh[0], kh[1]);
-        mma_bf16_16816(S[2 * np + 1], ph, kh[2], kh[3]);
-        mma_bf16_16816(Dl[2 * np], pl, kh[0], kh[1]);
-        mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
-        mma_bf16_16816(Dx[2 * np], ph, kl[0], kl[1]);
-        mma_bf16_16816(Dx[2 * np + 1], ph, kl[2], kl[3]);
-      }
-    }
-#pragma unroll
-    for (int ks2 = 0; ks2 < C / 16; ks2 += 2) {
-      uint32_t rh[2][4], rl[2][4];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        ldsm_x4(rh[h2], smem_u32(xr_hi + arow * LDA + 16 * (ks2 + h2) + acol));
-        ldsm_x4(rl[h2], smem_u32(xr_lo + arow * LDA + 16 * (ks2 + h2) + acol));
-      }
-#pragma unroll
-      for (int jt = 0; jt < JT; ++jt) {
-        uint32_t ah[4], al[4];
-        ldsm_x4(ah, tile_addr(big + AQ_HI, jw + 8 * jt + brow, 16 * ks2 + bcol));
-        ldsm_x4(al, tile_addr(big + AQ_LO, jw + 8 * jt + brow, 16 * ks2 + bcol));
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          mma_bf16_16816(Phh[jt], rh[h2], ah[2 * h2], ah[2 * h2 + 1]);
-          mma_bf16_16816(Plh[jt], rl[h2], ah[2 * h2], ah[2 * h2 + 1]);
-          mma_bf16_16816(Phl[jt], rh[h2], al[2 * h2], al[2 * h2 + 1]);
-        }
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < CT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) S[nt][e] += Dl[nt][e] + Dx[nt][e];
-
-    // ---- E: o rows of this warp (i in [jw, jw + 8 JT)), 16 value columns -> global
-#pragma unroll
-    for (int jt = 0; jt < JT; ++jt) {
-      const int i = 8 * jt + 2 * t4;
-      xo[i * 16 + g] = O[jt][0] + (Phh[jt][0] + (Plh[jt][0] + Phl[jt][0]));
-      xo[(i + 1) * 16 + g] = O[jt][1] + (Phh[jt][1] + (Plh[jt][1] + Phl[jt][1]));
-      xo[i * 16 + g + 8] = O[jt][2] + (Phh[jt][2] + (Plh[jt][2] + Phl[jt][2]));
-      xo[(i + 1) * 16 + g + 8] = O[jt][3] + (Phh[jt][3] + (Plh[jt][3] + Phl[jt][3]));
-    }
-    __syncwarp();
-#pragma unroll
-    for (int rep = 0; rep < JT; ++rep) {
-      const int i = 8 * rep + (lane >> 2), c4 = (lane & 3) * 4;   // 8 JT rows x 4 float4
-      const int t = t0 + jw + i;
-      if (t < p.T) {
-        const float4 val = *reinterpret_cast<const float4*>(xo + i * 16 + c4);
-        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0 + vr + c4;
-        if (p.out_bf16) {
-          uint2 pk;
-          pk.x = pack_bf16(val.x, val.y);
-          pk.y = pack_bf16(val.z, val.w);
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + off) = pk;
-        } else {
-          *reinterpret_cast<float4*>(static_cast<float*>(p.out) + off) = val;
-        }
-      }
-    }
-    __syncwarp();
-
-    if (n + 1 < p.N) {
-      __syncthreads();   // every warp is done with group 2 of chunk n
-      if (tid == 0) issue_group2(n + 1);
-    }
-  }
-
-  if (p.sT) {
-#pragma unroll
-    for (int nt = 0; nt < CT; ++nt) {
-      const int c = cw + 8 * nt + 2 * t4;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int vv = vr + g + (e >> 1) * 8, cc = c + (e & 1);
-        p.sT[(seq * K + cc) * V + v0 + vv] = S[nt][e];
-      }
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Scalar gate, warp-specialised. Warps 0-3 ("chain") run the serial part:
@@ -818,29 +481,6 @@ bool encode_bthd(CUtensorMap* map, const void* base, int B, int T, int heads) {
                 CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MG>
-gdr_status launch_kda(const Params& p, cudaStream_t stream) {
-  using LY = kda::Layout<MG>;
-  Maps m;
-  memset(&m, 0, sizeof m);
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const bool ok =
-      encode_slab(&m.w2, p, Slab::W2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_slab(&m.aq2, p, Slab::AQ2, BF, 2, C, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_slab(&m.u, p, Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, LY::VTK,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) &&
-      encode_slab(&m.qb2, p, Slab::QB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-      encode_slab(&m.kb2, p, Slab::KB2, BF, 2, K, 2 * C, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return GDR_ERR_CUDA;
-  auto kern = state_kda_kernel<MG>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL) !=
-      cudaSuccess)
-    return GDR_ERR_CUDA;
-  dim3 grid(V / LY::VTK, p.HV, p.B);
-  kern<<<grid, MG * kda::WARPS * 32, LY::TOTAL, stream>>>(m, p);
-  return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
-}
-
 gdr_status launch_ws(const Params& p, cudaStream_t stream) {
   Maps m;
   memset(&m, 0, sizeof m);
@@ -863,7 +503,7 @@ gdr_status launch_ws(const Params& p, cudaStream_t stream) {
 }  // namespace
 
 gdr_status launch_state(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode) return launch_kda<KDA_MG>(p, stream);
+  if (p.gate_mode) return launch_state_kda_tc(p, stream);
   // Scalar gate: the fused chain + output launch when the chains leave SMs
   // for the outputs, else chain and outputs in the same CTAs.
   const gdr_status st = launch_recur(p, stream);
