@@ -24,10 +24,9 @@ gdr_status check_dims(const gdr_dims* d, int chunk_size, int gate_mode) {
     return GDR_ERR_INVALID_ARG;
   if (chunk_size != 16 && chunk_size != 32 && chunk_size != 64 && chunk_size != 128)
     return GDR_ERR_UNSUPPORTED;
-  if (d->K > 128 || d->V > 128 || d->K + d->V > 256) return GDR_ERR_UNSUPPORTED;
-  // C = 128 runs on the general path, whose per-chunk tiles fit shared memory
-  // for head dims up to 64.
-  if (chunk_size == 128 && (d->K > 64 || d->V > 64)) return GDR_ERR_UNSUPPORTED;
+  // The general path streams K and V in tiles; its state kernel keeps a K x 32
+  // state tile (and the next one) in shared memory.
+  if (d->K > 256 || d->V > 256) return GDR_ERR_UNSUPPORTED;
   if (d->HV > 65535 || d->B > 65535) return GDR_ERR_UNSUPPORTED;
   // Element counts must fit the kernels' 64-bit indexing and the grid limits.
   if ((long long)d->T * d->HV * (d->V > d->K ? d->V : d->K) > (1LL << 46)) return GDR_ERR_UNSUPPORTED;

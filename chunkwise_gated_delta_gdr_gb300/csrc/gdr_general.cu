@@ -1,16 +1,17 @@
 // gdr_general.cu -- general chunkwise gated delta rule forward on CUDA cores (fp32).
 //
-// Two kernels, for any head dims K, V <= 128 (K + V <= 256), chunk sizes
-// 16/32/64 (and 128 for K, V <= 64), fp32 or bf16 inputs, both gate kinds and
-// the ungated mode (g == NULL reads as zero). All arithmetic is fp32,
+// Two kernels, for head dims K, V <= 256 and chunk sizes 16/32/64/128, fp32
+// or bf16 inputs, both gate kinds and the ungated mode (g == NULL reads as
+// zero). The chunk kernel streams the head dims through shared memory in tiles
+// of 32 channels, so its footprint depends on C only. All arithmetic is fp32,
 // which is what the fp32-input accuracy bound needs; the bf16 K = V = 128,
 // C = 64 workloads take the tensor-core path instead (gdr_tc.cu).
 //
 //  general_prep_kernel   one CTA per chunk (n, hv, b): L2 norm and scale of q/k,
 //                        gate cumsum G, decayed dots A_kk / A_qk, the unit
-//                        lower-triangular solve for W = M^-1 (exp(G) k) and
-//                        U = M^-1 v, and the per-chunk factors the state pass
-//                        needs ("分块并行计算（Chunkwise）" notes, section
+//                        lower-triangular inverse X = M^-1 (substitution on the
+//                        unit columns), W = X (exp(G) k) and U = X v, and the
+//                        per-chunk factors the state pass needs ("分块并行计算（Chunkwise）" notes, section
 //                        "chunk 内的 cumsum 与下三角解" and listing naive_chunk_kda).
 //  general_state_kernel  one CTA per (V tile, hv, b), serial over chunks: the
 //                        inter-chunk loop r = U - W S, o = (q exp(G)) S + A_qk r,
@@ -87,180 +88,204 @@ struct Args {
   Slabs s;
 };
 
+constexpr int kTk = 32;  // channel tile (keys or values) of the chunk kernel
+
+// Shared memory of the chunk kernel depends on C only: the head dims are
+// streamed in tiles of kTk channels.
 size_t prep_smem_bytes(const Problem& p) {
-  const int KP = p.K + 1, VP = p.V + 1, C = p.C;
-  const int GP = p.gate_mode ? KP : 1;
-  return sizeof(float) * ((size_t)2 * C * KP + (size_t)C * VP + (size_t)C * GP +
-                          (size_t)C * C + 3 * (size_t)C);
+  const int C = p.C;
+  return sizeof(float) * ((size_t)2 * C * C + (size_t)3 * C * (kTk + 1) + (size_t)4 * C);
+}
+
+// Loads channels [c0, c0 + tw) of chunk rows [t0, t0 + C) of a [B, T, heads, D]
+// tensor into t[C][kTk + 1]; rows past T and columns past tw read as zero.
+__device__ __forceinline__ void load_tile(float* t, const void* src, int bf16, const Problem& p,
+                                          int b, int head, int heads, int D, int t0, int c0,
+                                          int tw) {
+  const int C = p.C;
+  for (int idx = threadIdx.x; idx < C * kTk; idx += kThreads) {
+    const int i = idx / kTk, c = idx % kTk, tt = t0 + i;
+    t[i * (kTk + 1) + c] = (tt < p.T && c < tw)
+        ? ld_in(src, (((long)b * p.T + tt) * heads + head) * D + c0 + c, bf16) : 0.f;
+  }
+}
+
+// Per-key gate: channels [c0, c0 + tw) of g for the chunk, cumulated over the
+// chunk rows (G), into t[C][kTk + 1]. g == NULL (ungated) reads as zero.
+__device__ __forceinline__ void load_gate_tile(float* t, const Problem& p, int b, int hv, int t0,
+                                               int c0, int tw) {
+  const int C = p.C;
+  for (int idx = threadIdx.x; idx < C * kTk; idx += kThreads) {
+    const int i = idx / kTk, c = idx % kTk, tt = t0 + i;
+    t[i * (kTk + 1) + c] = (p.g && tt < p.T && c < tw)
+        ? p.g[(((long)b * p.T + tt) * p.HV + hv) * p.K + c0 + c] : 0.f;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < kTk; c += kThreads) {
+    float acc = 0.f;
+    for (int i = 0; i < C; ++i) {
+      acc += t[i * (kTk + 1) + c];
+      t[i * (kTk + 1) + c] = acc;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
   const int n = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-  const int C = p.C, K = p.K, V = p.V;
-  const int KP = K + 1, VP = V + 1;
-  const int KG = p.gate_mode ? K : 1, GP = p.gate_mode ? KP : 1;
+  const int C = p.C, K = p.K, V = p.V, TP = kTk + 1;
   const int h = hv / (p.HV / p.H);
   const int t0 = n * C;
   const int tid = threadIdx.x;
   const long chunk = ((long)b * p.HV + hv) * p.N + n;
 
-  float* qs = sm;             // [C][KP]  scaled normalised q
-  float* ks = qs + C * KP;    // [C][KP]  normalised k, later the W right-hand side / solution
-  float* vs = ks + C * KP;    // [C][VP]  v, later U
-  float* G = vs + C * VP;     // [C][GP]  in-chunk cumsum of g
-  float* L = G + C * GP;      // [C][C]   strictly lower part of M
-  float* bb = L + C * C;      // [C]      beta
-  float* nq = bb + C;         // [C]      scale / ||q||
-  float* nk = nq + C;         // [C]      1 / ||k||
+  float* Aq = sm;              // [C][C] q.k dots, later X = M^-1
+  float* Lm = Aq + C * C;      // [C][C] k.k dots, later the strictly lower part of M
+  float* tq = Lm + C * C;      // [C][TP] q tile, later the W right-hand side
+  float* tk = tq + C * TP;     // [C][TP] k tile, later the v tile
+  float* tg = tk + C * TP;     // [C][TP] per-key gate cumsum of the tile
+  float* Gs = tg + C * TP;     // [C] scalar-gate cumsum
+  float* bb = Gs + C;          // [C] beta
+  float* nq = bb + C;          // [C] sum q^2, then scale / ||q||
+  float* nk = nq + C;          // [C] sum k^2, then 1 / ||k||
 
-  for (int idx = tid; idx < C * K; idx += kThreads) {
-    const int i = idx / K, c = idx % K, t = t0 + i;
-    float qv = 0.f, kv = 0.f;
-    if (t < p.T) {
-      const long off = (((long)b * p.T + t) * p.H + h) * K + c;
-      qv = ld_in(p.q, off, p.in_bf16);
-      kv = ld_in(p.k, off, p.in_bf16);
-    }
-    qs[i * KP + c] = qv;
-    ks[i * KP + c] = kv;
-  }
-  for (int idx = tid; idx < C * V; idx += kThreads) {
-    const int i = idx / V, c = idx % V, t = t0 + i;
-    vs[i * VP + c] = (t < p.T) ? ld_in(p.v, (((long)b * p.T + t) * p.HV + hv) * V + c, p.in_bf16)
-                               : 0.f;
-  }
-  for (int idx = tid; idx < C * KG; idx += kThreads) {
-    const int i = idx / KG, c = idx % KG, t = t0 + i;
-    G[i * GP + c] = (p.g && t < p.T) ? p.g[(((long)b * p.T + t) * p.HV + hv) * KG + c] : 0.f;
-  }
+  for (int idx = tid; idx < C * C; idx += kThreads) Aq[idx] = Lm[idx] = 0.f;
   for (int i = tid; i < C; i += kThreads) {
     const int t = t0 + i;
     // SSD: beta = 1 everywhere (padded rows carry k = v = 0).
     bb[i] = p.ssd ? 1.f : (t < p.T) ? p.beta[((long)b * p.T + t) * p.HV + hv] : 0.f;
+    nq[i] = nk[i] = 0.f;
   }
-  __syncthreads();
-
-  // L2 norms (x / sqrt(sum x^2 + 1e-6)), one warp per row.
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int i = warp; i < C; i += kThreads / 32) {
-    float sq = 0.f, sk = 0.f;
-    for (int c = lane; c < K; c += 32) {
-      sq += qs[i * KP + c] * qs[i * KP + c];
-      sk += ks[i * KP + c] * ks[i * KP + c];
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      sq += __shfl_xor_sync(0xffffffffu, sq, o);
-      sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    if (lane == 0) {
-      nq[i] = p.use_l2 ? p.scale / sqrtf(sq + 1e-6f) : p.scale;
-      nk[i] = p.use_l2 ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
-    }
-  }
-  // Gate cumsum within the chunk, per channel.
-  __syncthreads();
-  for (int c = tid; c < KG; c += kThreads) {
+  if (p.gate_mode == 0 && tid == 0) {
     float acc = 0.f;
     for (int i = 0; i < C; ++i) {
-      acc += G[i * GP + c];
-      G[i * GP + c] = acc;
+      const int t = t0 + i;
+      acc += (p.g && t < p.T) ? p.g[((long)b * p.T + t) * p.HV + hv] : 0.f;
+      Gs[i] = acc;
     }
   }
-  for (int idx = tid; idx < C * K; idx += kThreads) {
-    const int i = idx / K, c = idx % K;
-    qs[i * KP + c] *= nq[i];
-    ks[i * KP + c] *= nk[i];
+
+  // Raw dots and squared norms, accumulated over channel tiles. The per-key
+  // decay sits inside the dot; L2 norms and the scalar decay are applied after.
+  for (int c0 = 0; c0 < K; c0 += kTk) {
+    const int tw = min(kTk, K - c0);
+    __syncthreads();
+    load_tile(tq, p.q, p.in_bf16, p, b, h, p.H, K, t0, c0, tw);
+    load_tile(tk, p.k, p.in_bf16, p, b, h, p.H, K, t0, c0, tw);
+    if (p.gate_mode) load_gate_tile(tg, p, b, hv, t0, c0, tw);
+    __syncthreads();
+    if (tid < 2 * C) {
+      const float* row = (tid < C ? tq : tk) + (tid % C) * TP;
+      float s2 = 0.f;
+      for (int c = 0; c < kTk; ++c) s2 = fmaf(row[c], row[c], s2);
+      (tid < C ? nq : nk)[tid % C] += s2;
+    }
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int i = idx / C, j = idx % C;
+      if (j > i) continue;
+      float dq = 0.f, dk = 0.f;
+      if (p.gate_mode == 0) {
+        for (int c = 0; c < kTk; ++c) {
+          const float kj = tk[j * TP + c];
+          dq = fmaf(tq[i * TP + c], kj, dq);
+          dk = fmaf(tk[i * TP + c], kj, dk);
+        }
+      } else {
+        for (int c = 0; c < kTk; ++c) {
+          const float kj = tk[j * TP + c] * expf(tg[i * TP + c] - tg[j * TP + c]);
+          dq = fmaf(tq[i * TP + c], kj, dq);
+          dk = fmaf(tk[i * TP + c], kj, dk);
+        }
+      }
+      Aq[idx] += dq;
+      Lm[idx] += dk;
+    }
   }
   __syncthreads();
-
-  // Decayed dots. A_kk feeds M = I + tril(A_kk * beta_j, -1); A_qk keeps its
-  // diagonal and carries beta on its columns (listing naive_chunk_kda).
+  for (int i = tid; i < C; i += kThreads) {
+    nq[i] = p.use_l2 ? p.scale / sqrtf(nq[i] + 1e-6f) : p.scale;
+    nk[i] = p.use_l2 ? 1.f / sqrtf(nk[i] + 1e-6f) : 1.f;
+  }
+  __syncthreads();
+  // A_qk (beta on its columns, diagonal kept) -> workspace; M's strictly lower
+  // part L = tril(A_kk beta_j, -1) in place (listing naive_chunk_kda).
   float* AQ = a.s.AQ + chunk * (long)C * C;
   for (int idx = tid; idx < C * C; idx += kThreads) {
     const int i = idx / C, j = idx % C;
-    float akk = 0.f, aqk = 0.f;
-    if (j <= i) {
-      if (p.gate_mode == 0) {
-        float dq = 0.f, dk = 0.f;
-        for (int c = 0; c < K; ++c) {
-          const float kj = ks[j * KP + c];
-          dq = fmaf(qs[i * KP + c], kj, dq);
-          dk = fmaf(ks[i * KP + c], kj, dk);
-        }
-        const float e = expf(G[i] - G[j]);
-        aqk = dq * e;
-        akk = dk * e;
-      } else {
-        for (int c = 0; c < K; ++c) {
-          const float e = expf(G[i * GP + c] - G[j * GP + c]) * ks[j * KP + c];
-          aqk = fmaf(qs[i * KP + c], e, aqk);
-          akk = fmaf(ks[i * KP + c], e, akk);
-        }
-      }
-    }
-    L[idx] = (j < i && !p.ssd) ? akk * bb[j] : 0.f;   // SSD: no erase, M = I
-    AQ[idx] = (j <= i) ? aqk * bb[j] : 0.f;
+    const float e = (p.gate_mode == 0) ? expf(Gs[i] - Gs[j]) : 1.f;
+    const float f = nk[j] * e * bb[j];
+    AQ[idx] = (j <= i) ? Aq[idx] * nq[i] * f : 0.f;
+    Lm[idx] = (j < i && !p.ssd) ? Lm[idx] * nk[i] * f : 0.f;   // SSD: no erase, M = I
   }
-
-  // Per-chunk factors of the state pass.
+  __syncthreads();
+  // X = M^-1 by forward substitution on the unit columns, one column per thread.
+  for (int col = tid; col < C; col += kThreads) {
+    for (int i = 0; i < C; ++i) {
+      float acc = (i == col) ? 1.f : 0.f;
+      for (int m = col; m < i; ++m) acc = fmaf(-Lm[i * C + m], Aq[m * C + col], acc);
+      Aq[i * C + col] = acc;
+    }
+  }
+  // Per-chunk factors of the state pass and W = X (exp(G) k_hat), tile by tile.
+  float* W = a.s.W + chunk * (long)C * K;
   float* QE = a.s.QE + chunk * (long)C * K;
   float* KD = a.s.KD + chunk * (long)C * K;
-  for (int idx = tid; idx < C * K; idx += kThreads) {
-    const int i = idx / K, c = idx % K;
-    const int gc = p.gate_mode ? c : 0;
-    const float gi = G[i * GP + gc], gl = G[(C - 1) * GP + gc];
-    QE[idx] = qs[i * KP + c] * expf(gi);
-    KD[idx] = ks[i * KP + c] * expf(gl - gi) * bb[i];
-  }
-  for (int c = tid; c < KG; c += kThreads) a.s.GM[chunk * K + c] = expf(G[(C - 1) * GP + c]);
-  __syncthreads();
-  // Right-hand side of W: exp(G) * k_hat, in place.
-  for (int idx = tid; idx < C * K; idx += kThreads) {
-    const int i = idx / K, c = idx % K;
-    ks[i * KP + c] *= expf(G[i * GP + (p.gate_mode ? c : 0)]);
-  }
-  __syncthreads();
-
-  // Forward substitution, one right-hand-side column per thread, in place.
-  for (int col = tid; col < K + V; col += kThreads) {
-    float* x = (col < K) ? ks + col : vs + (col - K);
-    const int st = (col < K) ? KP : VP;
-    for (int i = 1; i < C; ++i) {
-      float a0 = x[i * st], a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      const float* Li = L + i * C;
-      int m = 0;
-      for (; m + 3 < i; m += 4) {
-        a0 = fmaf(-Li[m], x[m * st], a0);
-        a1 = fmaf(-Li[m + 1], x[(m + 1) * st], a1);
-        a2 = fmaf(-Li[m + 2], x[(m + 2) * st], a2);
-        a3 = fmaf(-Li[m + 3], x[(m + 3) * st], a3);
+  for (int c0 = 0; c0 < K; c0 += kTk) {
+    const int tw = min(kTk, K - c0);
+    __syncthreads();
+    load_tile(tq, p.q, p.in_bf16, p, b, h, p.H, K, t0, c0, tw);
+    load_tile(tk, p.k, p.in_bf16, p, b, h, p.H, K, t0, c0, tw);
+    if (p.gate_mode) load_gate_tile(tg, p, b, hv, t0, c0, tw);
+    __syncthreads();
+    for (int idx = tid; idx < C * kTk; idx += kThreads) {
+      const int i = idx / kTk, c = idx % kTk;
+      const float gi = p.gate_mode ? tg[i * TP + c] : Gs[i];
+      const float gl = p.gate_mode ? tg[(C - 1) * TP + c] : Gs[C - 1];
+      const float kh = tk[i * TP + c] * nk[i];
+      if (c < tw) {
+        QE[(long)i * K + c0 + c] = tq[i * TP + c] * nq[i] * expf(gi);
+        KD[(long)i * K + c0 + c] = kh * expf(gl - gi) * bb[i];
+        if (i == 0 && (p.gate_mode || c0 + c == 0))
+          a.s.GM[chunk * K + c0 + c] = expf(gl);
       }
-      for (; m < i; ++m) a0 = fmaf(-Li[m], x[m * st], a0);
-      x[i * st] = (a0 + a1) + (a2 + a3);
+      tq[i * TP + c] = kh * expf(gi);   // right-hand side of W
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * tw; idx += kThreads) {
+      const int i = idx / tw, c = idx % tw;
+      float acc = 0.f;
+      for (int m = 0; m <= i; ++m) acc = fmaf(Aq[i * C + m], tq[m * TP + c], acc);
+      W[(long)i * K + c0 + c] = p.ssd ? 0.f : acc;   // SSD: r = U - W S = v
     }
   }
-  __syncthreads();
-  float* W = a.s.W + chunk * (long)C * K;
+  // U = X v, tile by tile.
   float* U = a.s.U + chunk * (long)C * V;
-  for (int idx = tid; idx < C * K; idx += kThreads)
-    W[idx] = p.ssd ? 0.f : ks[(idx / K) * KP + idx % K];   // SSD: r = U - W S = v
-  for (int idx = tid; idx < C * V; idx += kThreads) U[idx] = vs[(idx / V) * VP + idx % V];
+  for (int c0 = 0; c0 < V; c0 += kTk) {
+    const int tw = min(kTk, V - c0);
+    __syncthreads();
+    load_tile(tk, p.v, p.in_bf16, p, b, hv, p.HV, V, t0, c0, tw);
+    __syncthreads();
+    for (int idx = tid; idx < C * tw; idx += kThreads) {
+      const int i = idx / tw, c = idx % tw;
+      float acc = 0.f;
+      for (int m = 0; m <= i; ++m) acc = fmaf(Aq[i * C + m], tk[m * TP + c], acc);
+      U[(long)i * V + c0 + c] = acc;
+    }
+  }
 }
 
+// Shared memory of the state kernel: S and the next S [K][kVt], r [C][kVt],
+// exp(G_last) [K]. The chunk operands are read from the workspace (L2).
 size_t state_smem_bytes(const Problem& p) {
-  const int KP = p.K + 1, C = p.C;
-  return sizeof(float) * ((size_t)p.K * kVt * 2 + (size_t)C * kVt + 3 * (size_t)C * KP +
-                          (size_t)C * C + (size_t)p.K);
+  return sizeof(float) * ((size_t)p.K * kVt * 2 + (size_t)p.C * kVt + (size_t)p.K);
 }
 
 __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
   extern __shared__ float sm[];
   const Problem& p = a.p;
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-  const int C = p.C, K = p.K, V = p.V, KP = K + 1;
-  const int KG = p.gate_mode ? K : 1;
+  const int C = p.C, K = p.K, V = p.V;
   const int v0 = vt * kVt;
   const int vw = min(kVt, V - v0);
   const int tid = threadIdx.x;
@@ -268,11 +293,7 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
   float* S = sm;                  // [K][kVt]
   float* S2 = S + K * kVt;        // [K][kVt] next state
   float* r = S2 + K * kVt;        // [C][kVt]
-  float* Ws = r + C * kVt;        // [C][KP]
-  float* QEs = Ws + C * KP;       // [C][KP]
-  float* KDs = QEs + C * KP;      // [C][KP]
-  float* Aq = KDs + C * KP;       // [C][C]
-  float* gm = Aq + C * C;         // [K]
+  float* gm = r + C * kVt;        // [K]
 
   const long seq = (long)b * p.HV + hv;
   for (int idx = tid; idx < K * kVt; idx += kThreads) {
@@ -288,20 +309,12 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
     const float* U = a.s.U + chunk * (long)C * V;
     const float* AQ = a.s.AQ + chunk * (long)C * C;
     __syncthreads();
-    for (int idx = tid; idx < C * K; idx += kThreads) {
-      const int i = idx / K, c = idx % K;
-      Ws[i * KP + c] = W[idx];
-      QEs[i * KP + c] = QE[idx];
-      KDs[i * KP + c] = KD[idx];
-    }
-    for (int idx = tid; idx < C * C; idx += kThreads) Aq[idx] = AQ[idx];
     for (int c = tid; c < K; c += kThreads) gm[c] = a.s.GM[chunk * K + (p.gate_mode ? c : 0)];
-    __syncthreads();
-    // r = U - W S
+    // r = U - W S (a warp shares its row i: the W loads are broadcasts)
     for (int idx = tid; idx < C * kVt; idx += kThreads) {
       const int i = idx / kVt, j = idx % kVt;
-      float acc = (j < vw) ? U[i * V + v0 + j] : 0.f;
-      for (int c = 0; c < K; ++c) acc = fmaf(-Ws[i * KP + c], S[c * kVt + j], acc);
+      float acc = (j < vw) ? U[(long)i * V + v0 + j] : 0.f;
+      for (int c = 0; c < K; ++c) acc = fmaf(-W[(long)i * K + c], S[c * kVt + j], acc);
       r[idx] = acc;
     }
     __syncthreads();
@@ -311,8 +324,8 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
       const int t = n * C + i;
       if (j >= vw || t >= p.T) continue;
       float acc = 0.f;
-      for (int c = 0; c < K; ++c) acc = fmaf(QEs[i * KP + c], S[c * kVt + j], acc);
-      for (int m = 0; m <= i; ++m) acc = fmaf(Aq[i * C + m], r[m * kVt + j], acc);
+      for (int c = 0; c < K; ++c) acc = fmaf(QE[(long)i * K + c], S[c * kVt + j], acc);
+      for (int m = 0; m <= i; ++m) acc = fmaf(AQ[i * C + m], r[m * kVt + j], acc);
       const long off = (((long)b * p.T + t) * p.HV + hv) * V + v0 + j;
       if (p.out_bf16)
         static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(acc);
@@ -322,14 +335,13 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
     for (int idx = tid; idx < K * kVt; idx += kThreads) {
       const int c = idx / kVt, j = idx % kVt;
       float acc = gm[c] * S[idx];
-      for (int m = 0; m < C; ++m) acc = fmaf(KDs[m * KP + c], r[m * kVt + j], acc);
+      for (int m = 0; m < C; ++m) acc = fmaf(KD[(long)m * K + c], r[m * kVt + j], acc);
       S2[idx] = acc;
     }
     __syncthreads();
     for (int idx = tid; idx < K * kVt; idx += kThreads) S[idx] = S2[idx];
   }
   __syncthreads();
-  (void)KG;
   if (p.sT) {
     for (int idx = tid; idx < K * kVt; idx += kThreads) {
       const int c = idx / kVt, j = idx % kVt;

@@ -92,8 +92,7 @@ typedef struct {
  *                  NULL, with GDR_GATE_NONE
  *   beta           (device) fp32 [B, T, HV]
  *   initial_state  (device) fp32 [B, HV, K, V], or NULL for a zero state
- *   chunk_size     C: 16, 32, 64 (64 is the tensor-core path) or 128 (general path,
- *                  K <= 64 and V <= 64; larger head dims return GDR_ERR_UNSUPPORTED)
+ *   chunk_size     C: 16, 32, 64 (64 is the tensor-core path) or 128 (general path)
  *   scale          multiplies q after the optional L2 norm; finite and > 0
  *                  (the usual choice is 1/sqrt(K))
  *   use_qk_l2norm  nonzero: L2-normalise q and k per token and head first
@@ -104,8 +103,10 @@ typedef struct {
  *   workspace      (device) scratch of at least gdr_chunk_fwd_workspace_size()
  *                  bytes, 256-byte aligned; contents on entry do not matter
  *
- * Supported: K, V in 1..128 with K + V <= 256 on the general path; bf16 inputs
- * with K = V = 128 and C = 64 take the tcgen05 tensor-core path.
+ * Supported: K, V in 1..256 (independently) on the general fp32 path, which
+ * streams the head dims through shared memory; bf16 inputs with K = V = 128 and
+ * C = 64 take the tcgen05 tensor-core path. Larger head dims return
+ * GDR_ERR_UNSUPPORTED.
  * T == 0 writes final_state = initial_state (or zeros) and nothing else.
  * Concurrent calls must use distinct workspaces.
  */

@@ -62,7 +62,8 @@ def test_workspace_size_valid_and_invalid(lib):
     assert gdr.chunk_fwd_workspace_size(dims(), 64, 0) > 256
     assert gdr.chunk_fwd_workspace_size(dims(), 48, 0) == 0          # bad chunk size
     assert gdr.chunk_fwd_workspace_size(dims(HV=3), 64, 0) == 0      # HV % H != 0
-    assert gdr.chunk_fwd_workspace_size(dims(K=256), 64, 0) == 0     # head dim
+    assert gdr.chunk_fwd_workspace_size(dims(K=257), 64, 0) == 0     # head dim
+    assert gdr.chunk_fwd_workspace_size(dims(K=256, V=256), 64, 0) > 0
     assert gdr.chunk_fwd_workspace_size(dims(T=-1), 64, 0) == 0
     assert gdr.chunk_fwd_workspace_size(dims(), 64, 3) == 0          # gate mode
     small = gdr.chunk_fwd_workspace_size(dims(T=64), 64, 0)
@@ -97,7 +98,7 @@ def test_argument_errors_are_synchronous(lib):
         gdr.GDR_ERR_INVALID_ARG
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=48) == gdr.GDR_ERR_UNSUPPORTED
     assert _call(lib, dims(HV=3), q=A, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_INVALID_ARG
-    assert _call(lib, dims(V=200), q=A, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_UNSUPPORTED
+    assert _call(lib, dims(V=300), q=A, k=A, v=A, g=A, beta=A, out=A) == gdr.GDR_ERR_UNSUPPORTED
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, ws=None) == gdr.GDR_ERR_WORKSPACE
     need = gdr.chunk_fwd_workspace_size(d, 64, 0)
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, ws=A, ws_bytes=need - 1) == \
@@ -129,11 +130,12 @@ def test_ungated_mode_and_chunk_size_128_sizes(lib):
     g_bytes = 1 * 256 * 4 * 4
     assert (gdr.chunk_fwd_host_buffer_size(d, 64, gdr.GDR_GATE_SCALAR, False, False) -
             gdr.chunk_fwd_host_buffer_size(d, 64, gdr.GDR_GATE_NONE, False, False)) == g_bytes
-    # C = 128: general path, head dims up to 64 only.
+    # C = 128 and head dims up to 256 run on the general path.
     assert gdr.chunk_fwd_workspace_size(dims(K=64, V=64), 128, 0) > 0
     assert gdr.chunk_fwd_path(dims(K=64, V=64), 128, 1) == 0
-    assert gdr.chunk_fwd_workspace_size(dims(), 128, 0) == 0
-    assert gdr.chunk_fwd_workspace_size(dims(K=64, V=128), 128, 0) == 0
+    assert gdr.chunk_fwd_path(dims(), 128, 0) == 0
+    assert gdr.chunk_fwd_path(dims(K=256, V=64), 64, 1) == 0
+    assert gdr.chunk_fwd_workspace_size(dims(K=64, V=257), 128, 0) == 0
 
 
 def test_gate_array_required_unless_ungated(lib):
@@ -144,7 +146,7 @@ def test_gate_array_required_unless_ungated(lib):
     assert _call(lib, d, q=A, k=A, v=A, g=None, beta=A, out=A, gate=gdr.GDR_GATE_PER_KEY) == \
         gdr.GDR_ERR_INVALID_ARG
     assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, gate=3) == gdr.GDR_ERR_INVALID_ARG
-    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=128) == gdr.GDR_ERR_UNSUPPORTED
+    assert _call(lib, d, q=A, k=A, v=A, g=A, beta=A, out=A, C=96) == gdr.GDR_ERR_UNSUPPORTED
 
 
 def test_recurrent_argument_errors(lib):

@@ -88,8 +88,9 @@ def test_full_workloads_sampled(name):
     check_against_oracle(w, gin.make_inputs(w), sel=FULL_SAMPLES[name])
 
 
-def test_bf16_output_is_fp32_output_rounded():
-    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=257, H=2, HV=2)
+@pytest.mark.parametrize("name", ["gdn_t4096_h12", "kda_gqa_t8192"])
+def test_bf16_output_is_fp32_output_rounded(name):
+    w = gin.shrink(gin.WORKLOADS[name], B=1, T=257, H=1, HV=2)
     x = gin.make_inputs(w)
     o32, S32 = gpu_run(x, w, torch.float32)
     o16, S16 = gpu_run(x, w, torch.bfloat16)
@@ -100,9 +101,18 @@ def test_bf16_output_is_fp32_output_rounded():
 
 
 @pytest.mark.parametrize("T", [1, 5, 63, 64, 65, 129])
-def test_short_and_boundary_lengths(T):
-    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=T, H=1, HV=2)
+@pytest.mark.parametrize("name", ["gdn_long_t65000", "kda_many_b64"])
+def test_short_and_boundary_lengths(name, T):
+    w = gin.shrink(gin.WORKLOADS[name], B=1, T=T, H=1, HV=2, s0_std=0.02)
     check_against_oracle(w, gin.make_inputs(w))
+
+
+def test_per_key_initial_state():
+    """Per-key gate with a carried fp32 state, several chunks, GQA."""
+    w = gin.shrink(gin.WORKLOADS["kda_gqa_t8192"], B=2, T=300, H=1, HV=2, s0_std=0.05)
+    x = gin.make_inputs(w)
+    assert x["s0"] is not None
+    check_against_oracle(w, x)
 
 
 @pytest.mark.parametrize("name", ["gdn_t4096_h12", "kda_many_b64"])
@@ -119,8 +129,9 @@ def test_zero_length_returns_initial_state(name):
     assert np.all(S == 0)
 
 
-def test_final_state_may_alias_initial_state():
-    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=150, H=2, HV=2)
+@pytest.mark.parametrize("name", ["gdn_long_t65000", "kda_many_b64"])
+def test_final_state_may_alias_initial_state(name):
+    w = gin.shrink(gin.WORKLOADS[name], B=1, T=150, H=2, HV=2, s0_std=0.02)
     x = gin.make_inputs(w)
     o_ref, S_ref = gpu_run(x, w)
     dev = torch.device("cuda:0")
@@ -305,6 +316,26 @@ def test_chunk_size_128(name, ov):
     dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V,
                          gdr.GDR_BF16 if w.dtype == torch.bfloat16 else gdr.GDR_F32, gdr.GDR_F32)
     assert gdr.chunk_fwd_path(dims, 128, w.gate_mode) == 0          # general path
+    check_against_oracle(w, gin.make_inputs(w))
+
+
+# Head dims up to 256 and C = 128 with full head dims: the general path streams
+# the head dims through shared memory in 32-channel tiles.
+LARGE_HEADS = [
+    ("gdn_t4096_h12", dict(T=200, H=1, HV=2, K=256, V=256)),
+    ("kda_gqa_t8192", dict(B=1, T=150, H=1, HV=2, K=256, V=128)),
+    ("gdn_t4096_h12", dict(T=300, H=1, HV=2, K=128, V=128, C=128)),
+    ("kda_many_b64", dict(B=2, T=200, H=1, HV=2, K=128, V=256, C=128, s0_std=0.02)),
+    ("gdn_long_t65000", dict(T=170, H=1, HV=1, K=96, V=200, C=32)),
+    ("tiny_fp32", dict(T=100, K=256, V=256, C=32)),
+]
+
+
+@pytest.mark.parametrize("name,ov", LARGE_HEADS)
+def test_large_head_dims(name, ov):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    assert gdr.chunk_fwd_path(gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, 1, 0), w.C,
+                              w.gate_mode) == 0
     check_against_oracle(w, gin.make_inputs(w))
 
 
