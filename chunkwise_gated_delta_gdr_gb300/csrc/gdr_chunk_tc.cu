@@ -106,18 +106,12 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
   uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
 
+  // The input tiles are requested first: the thread that initialised the
+  // barrier issues the loads before the TMEM allocation and the CTA barrier.
   if (tid == 0) {
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     mbar_fence_init();
-  }
-  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-
-  if (tid == 0) {
     mbar_expect_tx(bar_tma, 6 * 8192);
     tma_load4(smem_u32(sm + OFF_K0), &maps.k, 0, h, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_K1), &maps.k, 64, h, t0, b, bar_tma);
@@ -126,9 +120,9 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
     tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_tma);
   }
-  // Gate and beta (plain loads, issued before the TMA wait; zero past the end
-  // and for the ungated mode).
-  float ga = 0.f, gb = 0.f;
+  // Gate and beta (plain loads into registers, in flight during the TMEM
+  // allocation; zero past the end and for the ungated mode).
+  float ga = 0.f, gb = 0.f, bv = 0.f;
   if (warp == 0) {
     const int ta = t0 + 2 * lane;
     if (p.g && ta < p.T) ga = p.g[((size_t)b * p.T + ta) * p.HV + hv];   // g == NULL: ungated
@@ -137,10 +131,16 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   if (tid < C) {
     const int t = t0 + tid;
     // SSD: beta = 1 on real rows.
-    bb[tid] = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
+    bv = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
   }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
   bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tma, 0, kWaitLimit));
   if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
+  if (tid < C) bb[tid] = bv;   // read after the next CTA barrier
 
   // ---- MMA 1: D[0:128, 0:64] = [k; q] k^T -------------------------------------
   if (ok && tid == 0) {
