@@ -15,12 +15,14 @@
 // (the lo lo term this brings in only adds precision).
 //
 // Roles (10 warps):
-//   warps 0-3  the state: thread c holds row c of S (64 fp32 registers) for the
-//              whole sequence; per chunk it publishes S as the hi / lo B operand
-//              (MN-major, 128-byte swizzled rows), forms r = U + D_r from TMEM
-//              and publishes it likewise (lanes 0-15, rows j), then applies
-//              S = gamma S + dS from TMEM.
-//   warps 4-7  read o from TMEM (two buffers) and store it.
+//   warps 0-7  the state: warps w and w + 4 share TMEM lane quadrant w % 4 and
+//              take value columns [32 (w / 4), 32 (w / 4) + 32); thread (c, half)
+//              holds those 32 columns of row c of S in fp32 registers for the
+//              whole sequence. Per chunk they publish S as the hi / lo B operand
+//              (MN-major, 128-byte swizzled rows), store the previous chunk's o
+//              (two TMEM buffers) while the r products run, form r = U + D_r
+//              from TMEM and publish it likewise (lanes 0-15, rows j), then
+//              apply S = gamma S + dS from TMEM.
 //   warp 8     TMA producer. Each operand has its own buffer and is reloaded as
 //              soon as its last reader is done: W (two buffers) after the r
 //              products, QB after QB S, U and gamma (two buffers) after the r
@@ -48,7 +50,7 @@ using namespace ptx;
 
 constexpr int VC = 64;                  // value columns per CTA
 constexpr int THREADS = 320;
-constexpr int SYNC_N = 160;             // state warps + MMA warp on the named barriers
+constexpr int SYNC_N = 288;             // state warps + MMA warp on the named barriers
 constexpr long kWaitLimit = 1L << 24;
 constexpr unsigned int kErrWait = 16u;
 
@@ -97,17 +99,6 @@ __device__ __forceinline__ void publish(uint8_t* hi, uint8_t* lo, int r, int q0,
     *reinterpret_cast<uint4*>(lo + sw_off(r, q)) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
-__device__ __forceinline__ void publish_row(uint8_t* hi, uint8_t* lo, int r, const float* x) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int z = 0; z < 4; ++z) split_pair(x[8 * q + 2 * z], x[8 * q + 2 * z + 1], h[z], l[z]);
-    *reinterpret_cast<uint4*>(hi + sw_off(r, q)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + sw_off(r, q)) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
 __global__ void __launch_bounds__(THREADS, 1)
     state_kda_tc_kernel(const __grid_constant__ Maps maps, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -123,7 +114,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* w_full = bars + 0;      // [2]
   uint64_t* w_empty = bars + 2;     // [2], commit after the r products
   uint64_t* u_full = bars + 4;      // [2]
-  uint64_t* u_empty = bars + 6;     // [2], 4 arrivals (state warps)
+  uint64_t* u_empty = bars + 6;     // [2], 8 arrivals (state warps)
   uint64_t* kb_full = bars + 8;
   uint64_t* kb_empty = bars + 9;    // commit after the dS products
   uint64_t* qb_full = bars + 10;
@@ -133,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* r_done = bars + 14;
   uint64_t* ds_done = bars + 15;
   uint64_t* o_full = bars + 16;     // [2]
-  uint64_t* o_empty = bars + 18;    // [2], 4 arrivals (output warps)
+  uint64_t* o_empty = bars + 18;    // [2], 8 arrivals (state warps)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 20);
 
   if (tid == 0) {
@@ -141,9 +132,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&w_full[i], 1);
       mbar_init(&w_empty[i], 1);
       mbar_init(&u_full[i], 1);
-      mbar_init(&u_empty[i], 4);
+      mbar_init(&u_empty[i], 8);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 4);
+      mbar_init(&o_empty[i], 8);
     }
     mbar_init(kb_full, 1);
     mbar_init(kb_empty, 1);
@@ -162,55 +153,84 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = *tslot;
   bool ok = true;
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ---------------------------------------------------------------- state
-    const int c = tid;                                  // key channel = TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    float S[VC];
+    const int quad = warp & 3, hf = warp >> 2;          // lane quadrant, column half
+    const int c = 32 * quad + lane;                      // key channel = TMEM lane
+    const int j = 16 * quad + (lane & 15);               // D_r / o row held by lanes 0-15
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const int vc = v0 + 32 * hf;                         // first value column of this thread
+    float S[32];
     if (p.s0) {
-      const float4* src = reinterpret_cast<const float4*>(p.s0 + (seq * K + c) * V + v0);
+      const float4* src = reinterpret_cast<const float4*>(p.s0 + (seq * K + c) * V + vc);
 #pragma unroll
-      for (int q = 0; q < VC / 4; ++q) {
+      for (int q = 0; q < 8; ++q) {
         const float4 x = src[q];
         S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < VC; ++i) S[i] = 0.f;
+      for (int i = 0; i < 32; ++i) S[i] = 0.f;
     }
+    // o of chunk m: 32 columns of row j, lanes 0-15.
+    auto store_o = [&](int m) {
+      const int ob = m & 1;
+      ok = ok && mbar_wait(&o_full[ob], (m >> 1) & 1, kWaitLimit);
+      tc_fence_after();
+      float o[32], ol[32];
+      tmem_ld32(tmem + lane_base + T_O + 128 * ob + 32 * hf, o);
+      tmem_ld32(tmem + lane_base + T_O + 128 * ob + 64 + 32 * hf, ol);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[ob]);
+      const int t = m * C + j;
+      if (lane < 16 && t < p.T) {
+        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + vc;
+        if (p.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16(o[8 * q] + ol[8 * q], o[8 * q + 1] + ol[8 * q + 1]),
+                                pack_bf16(o[8 * q + 2] + ol[8 * q + 2], o[8 * q + 3] + ol[8 * q + 3]),
+                                pack_bf16(o[8 * q + 4] + ol[8 * q + 4], o[8 * q + 5] + ol[8 * q + 5]),
+                                pack_bf16(o[8 * q + 6] + ol[8 * q + 6], o[8 * q + 7] + ol[8 * q + 7]));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(o[4 * q] + ol[4 * q], o[4 * q + 1] + ol[4 * q + 1],
+                                 o[4 * q + 2] + ol[4 * q + 2], o[4 * q + 3] + ol[4 * q + 3]);
+        }
+      }
+    };
     for (int n = 0; n < p.N; ++n) {
       const int s = n & 1;
       // S_n -> B operand of the r and QB S products (their previous readers
       // are done: both precede the last dS products in the MMA order).
-      publish_row(sm + S_BASE, sm + S_BASE + 16384, c, S);
+      publish<4>(sm + S_BASE, sm + S_BASE + 16384, c, 4 * hf, S);
       fence_async_shared();
       nb_sync(1, SYNC_N);
-      // r = U + D_r: lanes 0-15 of each warp hold rows j = 16 warp + lane.
+      if (n > 0) store_o(n - 1);                          // overlaps the r products
+      // r = U + D_r: lanes 0-15 of each warp hold rows j = 16 quad + lane.
       ok = ok && mbar_wait(&u_full[s], (n >> 1) & 1, kWaitLimit);
       ok = ok && mbar_wait(r_done, n & 1, kWaitLimit);
       tc_fence_after();
       const float gam = reinterpret_cast<const float*>(sm + GAM_BASE + s * 512)[c];
       {
-        const int j = 16 * warp + (lane & 15);
-        const uint8_t* ub = sm + U_BASE + s * 16384;
+        float r[32], rl[32];
+        tmem_ld32(tmem + lane_base + T_R + 32 * hf, r);
+        tmem_ld32(tmem + lane_base + T_R + 64 + 32 * hf, rl);
+        if (lane < 16) {
+          const uint8_t* ub = sm + U_BASE + s * 16384 + hf * 8192;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {   // value columns 32 h .. 32 h + 31
-          float r[32], rl[32];
-          tmem_ld32(tmem + lane_base + T_R + 32 * h, r);
-          tmem_ld32(tmem + lane_base + T_R + 64 + 32 * h, rl);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] += rl[i];
-          if (lane < 16) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 u = *reinterpret_cast<const float4*>(ub + h * 8192 + sw_off(j, q));
-              r[4 * q] += u.x;
-              r[4 * q + 1] += u.y;
-              r[4 * q + 2] += u.z;
-              r[4 * q + 3] += u.w;
-            }
-            publish<4>(sm + R_BASE, sm + R_BASE + 8192, j, 4 * h, r);
+          for (int q = 0; q < 8; ++q) {
+            const float4 u = *reinterpret_cast<const float4*>(ub + sw_off(j, q));
+            r[4 * q] += rl[4 * q] + u.x;
+            r[4 * q + 1] += rl[4 * q + 1] + u.y;
+            r[4 * q + 2] += rl[4 * q + 2] + u.z;
+            r[4 * q + 3] += rl[4 * q + 3] + u.w;
           }
+          publish<4>(sm + R_BASE, sm + R_BASE + 8192, j, 4 * hf, r);
         }
       }
       fence_async_shared();
@@ -221,59 +241,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       // S_{n+1} = gamma S_n + dS.
       ok = ok && mbar_wait(ds_done, n & 1, kWaitLimit);
       tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
         float d[32], dl[32];
-        tmem_ld32(tmem + lane_base + T_DS + 32 * h, d);
-        tmem_ld32(tmem + lane_base + T_DS + 64 + 32 * h, dl);
+        tmem_ld32(tmem + lane_base + T_DS + 32 * hf, d);
+        tmem_ld32(tmem + lane_base + T_DS + 64 + 32 * hf, dl);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) S[32 * h + i] = fmaf(gam, S[32 * h + i], d[i] + dl[i]);
+        for (int i = 0; i < 32; ++i) S[i] = fmaf(gam, S[i], d[i] + dl[i]);
       }
       tc_fence_before();
     }
+    if (p.N > 0) store_o(p.N - 1);
     if (p.sT) {
-      float4* dst = reinterpret_cast<float4*>(p.sT + (seq * K + c) * V + v0);
+      float4* dst = reinterpret_cast<float4*>(p.sT + (seq * K + c) * V + vc);
 #pragma unroll
-      for (int q = 0; q < VC / 4; ++q)
+      for (int q = 0; q < 8; ++q)
         dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
-    }
-  } else if (warp < 8) {
-    // --------------------------------------------------------------- output
-    const int quad = warp & 3;
-    const int i = 16 * quad + (lane & 15);              // chunk row
-    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-    for (int n = 0; n < p.N; ++n) {
-      const int ob = n & 1;
-      ok = ok && mbar_wait(&o_full[ob], (n >> 1) & 1, kWaitLimit);
-      tc_fence_after();
-      float o[VC];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float ol[32];
-        tmem_ld32(tmem + lane_base + T_O + 128 * ob + 32 * h, o + 32 * h);
-        tmem_ld32(tmem + lane_base + T_O + 128 * ob + 64 + 32 * h, ol);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[32 * h + e] += ol[e];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[ob]);
-      const int t = n * C + i;
-      if (lane < 16 && t < p.T) {
-        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0;
-        if (p.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
-#pragma unroll
-          for (int q = 0; q < VC / 8; ++q)
-            dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
-#pragma unroll
-          for (int q = 0; q < VC / 4; ++q)
-            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
-      }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
