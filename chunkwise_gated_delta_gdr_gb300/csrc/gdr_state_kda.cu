@@ -10,9 +10,9 @@
 // channel (the chunk slab of gdr_fast.cuh). Every product runs on tcgen05
 // (kind::f16, bf16 operands, fp32 accumulators in TMEM) with both operands
 // split into bf16 hi + lo. The B operand is stacked along N as [B_hi | B_lo]
-// (N = 128), so A_hi [B_hi | B_lo] + A_lo [B_hi | B_lo] takes two MMAs per
-// K step; the two column halves of the accumulator are added in the epilogue
-// (the lo lo term this brings in only adds precision).
+// (N = 128): per K step A_hi [B_hi | B_lo] (N = 128) and A_lo B_hi (N = 64,
+// into the first half), i.e. the three terms hi hi + hi lo + lo hi; the two
+// column halves of the accumulator are added in the epilogue.
 //
 // Roles (10 warps):
 //   warps 0-7  the state: warps w and w + 4 share TMEM lane quadrant w % 4 and
@@ -20,9 +20,8 @@
 //              holds those 32 columns of row c of S in fp32 registers for the
 //              whole sequence. Per chunk they publish S as the hi / lo B operand
 //              (MN-major, 128-byte swizzled rows), store the previous chunk's o
-//              (two TMEM buffers) while the r products run, form r = U + D_r
-//              from TMEM and publish it likewise (lanes 0-15, rows j), then
-//              apply S = gamma S + dS from TMEM.
+//              while the r products run, form r = U + D_r from TMEM and publish
+//              it likewise (lanes 0-15, rows j), then apply S = gamma S + dS.
 //   warp 8     TMA producer. Each operand has its own buffer and is reloaded as
 //              soon as its last reader is done: W (two buffers) after the r
 //              products, QB after QB S, U and gamma (two buffers) after the r
@@ -69,8 +68,9 @@ constexpr int SMEM_BYTES = BAR_BASE + 256 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t kUBytes = 16384 + 512;
 
-// TMEM columns (128 each: the B_hi and B_lo halves): D_r, dS, o in two buffers.
-constexpr uint32_t T_R = 0, T_DS = 128, T_O = 256, TMEM_COLS = 512;
+// TMEM columns (128 each: the B_hi and B_lo halves): D_r as two accumulators
+// (even and odd K steps, two independent MMA chains), dS, o.
+constexpr uint32_t T_R = 0, T_R2 = 128, T_DS = 256, T_O = 384, TMEM_COLS = 512;
 
 struct Maps {
   CUtensorMap w2, qb2, kb2, aq2, u;
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* aq_empty = bars + 13;   // commit after A_qk r
   uint64_t* r_done = bars + 14;
   uint64_t* ds_done = bars + 15;
-  uint64_t* o_full = bars + 16;     // [2]
-  uint64_t* o_empty = bars + 18;    // [2], 8 arrivals (state warps)
+  uint64_t* o_full = bars + 16;
+  uint64_t* o_empty = bars + 17;    // 8 arrivals (state warps)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 20);
 
   if (tid == 0) {
@@ -133,8 +133,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&w_empty[i], 1);
       mbar_init(&u_full[i], 1);
       mbar_init(&u_empty[i], 8);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 8);
     }
     mbar_init(kb_full, 1);
     mbar_init(kb_empty, 1);
@@ -142,6 +140,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(qb_empty, 1);
     mbar_init(aq_full, 1);
     mbar_init(aq_empty, 1);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 8);
     mbar_init(r_done, 1);
     mbar_init(ds_done, 1);
     mbar_fence_init();
@@ -174,15 +174,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     // o of chunk m: 32 columns of row j, lanes 0-15.
     auto store_o = [&](int m) {
-      const int ob = m & 1;
-      ok = ok && mbar_wait(&o_full[ob], (m >> 1) & 1, kWaitLimit);
+      ok = ok && mbar_wait(o_full, m & 1, kWaitLimit);
       tc_fence_after();
       float o[32], ol[32];
-      tmem_ld32(tmem + lane_base + T_O + 128 * ob + 32 * hf, o);
-      tmem_ld32(tmem + lane_base + T_O + 128 * ob + 64 + 32 * hf, ol);
+      tmem_ld32(tmem + lane_base + T_O + 32 * hf, o);
+      tmem_ld32(tmem + lane_base + T_O + 64 + 32 * hf, ol);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[ob]);
+      if (lane == 0) mbar_arrive(o_empty);
       const int t = m * C + j;
       if (lane < 16 && t < p.T) {
         const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + vc;
@@ -220,6 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         float r[32], rl[32];
         tmem_ld32(tmem + lane_base + T_R + 32 * hf, r);
         tmem_ld32(tmem + lane_base + T_R + 64 + 32 * hf, rl);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] += rl[i];
+        tmem_ld32(tmem + lane_base + T_R2 + 32 * hf, rl);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] += rl[i];
+        tmem_ld32(tmem + lane_base + T_R2 + 64 + 32 * hf, rl);
         if (lane < 16) {
           const uint8_t* ub = sm + U_BASE + s * 16384 + hf * 8192;
 #pragma unroll
@@ -337,11 +342,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------- MMA issuer
     constexpr uint32_t ID_KMN = idesc_bf16(64, 128, 0, 1);    // A K-major, B MN-major [hi | lo]
+    constexpr uint32_t ID_KMN_H = idesc_bf16(64, 64, 0, 1);   // same, B hi only
     constexpr uint32_t ID_MNMN = idesc_bf16(128, 128, 1, 1);  // both MN-major
+    constexpr uint32_t ID_MNMN_H = idesc_bf16(128, 64, 1, 1);
     const uint32_t sb = smem_u32(sm), rb = smem_u32(sm + R_BASE), sbuf = smem_u32(sm + S_BASE);
     for (int n = 0; n < p.N; ++n) {
-      const int ob = n & 1;
-      const uint32_t d_o = tmem + T_O + 128 * ob;
+      const uint32_t d_o = tmem + T_O;
       const uint32_t wb = sb + W_BASE + (n & 1) * 32768;
       nb_sync(1, SYNC_N);                                          // S_n published
       ok = ok && mbar_wait(&w_full[n & 1], (n >> 1) & 1, kWaitLimit);
@@ -353,8 +359,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t ao = (kk >> 2) * 8192 + (kk & 3) * 32;
             const uint64_t bd = sdesc_sw128_lbo(sbuf + kk * 2048, 16384);
-            umma_bf16(tmem + T_R, sdesc_sw128(wb + ao), bd, ID_KMN, kk > 0);
-            umma_bf16(tmem + T_R, sdesc_sw128(wb + 16384 + ao), bd, ID_KMN, 1);
+            const uint32_t dr = tmem + ((kk & 1) ? T_R2 : T_R);
+            umma_bf16(dr, sdesc_sw128(wb + ao), bd, ID_KMN, kk > 1);
+            umma_bf16(dr, sdesc_sw128(wb + 16384 + ao), bd, ID_KMN_H, 1);
           }
         }
         umma_commit(r_done);
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
       ok = ok && mbar_wait(qb_full, n & 1, kWaitLimit);
-      if (n >= 2) ok = ok && mbar_wait(&o_empty[ob], ((n >> 1) - 1) & 1, kWaitLimit);
+      if (n >= 1) ok = ok && mbar_wait(o_empty, (n - 1) & 1, kWaitLimit);
       tc_fence_after();
       if (lane == 0) {
         if (ok) {
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t ao = (kk >> 2) * 8192 + (kk & 3) * 32;
             const uint64_t bd = sdesc_sw128_lbo(sbuf + kk * 2048, 16384);
             umma_bf16(d_o, sdesc_sw128(sb + QB_BASE + ao), bd, ID_KMN, kk > 0);
-            umma_bf16(d_o, sdesc_sw128(sb + QB_BASE + 16384 + ao), bd, ID_KMN, 1);
+            umma_bf16(d_o, sdesc_sw128(sb + QB_BASE + 16384 + ao), bd, ID_KMN_H, 1);
           }
         }
         umma_commit(qb_empty);
@@ -388,7 +395,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_sw128_lbo(rb + kk * 2048, 8192);
             umma_bf16(tmem + T_DS, sdesc_sw128_lbo(sb + KB_BASE + kk * 2048, 8192), bd, ID_MNMN, kk > 0);
-            umma_bf16(tmem + T_DS, sdesc_sw128_lbo(sb + KB_BASE + 16384 + kk * 2048, 8192), bd, ID_MNMN, 1);
+            umma_bf16(tmem + T_DS, sdesc_sw128_lbo(sb + KB_BASE + 16384 + kk * 2048, 8192), bd, ID_MNMN_H, 1);
           }
         }
         umma_commit(ds_done);
@@ -404,10 +411,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = sdesc_sw128_lbo(rb + kk * 2048, 8192);
             umma_bf16(d_o, sdesc_sw128(sb + AQ_BASE + kk * 32), bd, ID_KMN, 1);
-            umma_bf16(d_o, sdesc_sw128(sb + AQ_BASE + 8192 + kk * 32), bd, ID_KMN, 1);
+            umma_bf16(d_o, sdesc_sw128(sb + AQ_BASE + 8192 + kk * 32), bd, ID_KMN_H, 1);
           }
         }
-        umma_commit(&o_full[ob]);
+        umma_commit(o_full);
         umma_commit(aq_empty);
       }
       __syncwarp();
