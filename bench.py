@@ -97,9 +97,13 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def source_hash():
+def source_hash(files=None):
+    """Hash of the kernel sources (the named files under csrc/, else all of them)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "chunkwise_gated_delta_gdr_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "chunkwise_gated_delta_gdr_gb300", "csrc")
+    paths = ([os.path.join(csrc, f) for f in sorted(files)] if files
+             else sorted(glob.glob(os.path.join(csrc, "*"))))
+    for f in paths:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode() + fh.read())
     return h.hexdigest()[:16]
@@ -107,14 +111,21 @@ def source_hash():
 
 def recorded_traffic(wname):
     """DRAM bytes per step from the committed ncu summary, if it was taken on
-    the kernels as they are now (same source hash); else None."""
+    the kernels as they are now (same hash of the source files the summary
+    names, the files those kernels are built from); else None."""
     path = os.path.join(ROOT, "profiles", f"traffic_{wname}.md")
     try:
         text = open(path).read()
     except OSError:
         return None, None
     mh = re.search(r"source_hash:\s*([0-9a-f]+)", text)
-    if not mh or mh.group(1) != source_hash():
+    ms = re.search(r"^sources:\s*(.+)$", text, re.M)
+    files = ms.group(1).split() if ms else None
+    try:
+        current = source_hash(files)
+    except OSError:
+        return None, None
+    if not mh or mh.group(1) != current:
         return None, None
     per = {}
     for m in re.finditer(r"^kernel\s+(\S+)\s+dram_bytes_per_launch:\s*([0-9.]+)", text, re.M):
