@@ -19,10 +19,11 @@
 // columns in registers while they apply the tokens. (Boxes of 128-byte rows
 // were served several times slower.)
 //
-// Fallback kernel (any V): one CTA per (V tile of 32 columns, hv, b), 16 warps: warp w holds state rows
-// [8 w, 8 w + 8) of the tile's columns (lane = column), so every state access
-// is a coalesced 128-byte row segment; 64 registers per thread keep two CTAs
-// (32 warps) per SM in flight, which the HBM stream needs. Per token the column sums
+// Fallback kernel (any V, K <= 256): one CTA per (V tile of 32 columns, hv, b),
+// 16 warps: warp w holds state rows [R w, R w + R) of the tile's columns
+// (lane = column; R = 8 for K <= 128, 16 for K <= 256), so every state access
+// is a coalesced 128-byte row segment; with R = 8, 64 registers per thread keep
+// two CTAs (32 warps) per SM in flight, which the HBM stream needs. Per token the column sums
 // (S^T k and S^T q over all rows) are combined across the warps through
 // shared memory; everything else is per element.
 #include <math.h>
@@ -37,8 +38,7 @@
 namespace gdr {
 namespace {
 
-constexpr int kWarps = 16, kRows = 128 / kWarps, kThreads = kWarps * 32, kCols = 32;
-static_assert(kWarps * kRows == 128, "rows per CTA must cover K <= 128");
+constexpr int kWarps = 16, kThreads = kWarps * 32, kCols = 32;
 
 struct DecodeArgs {
   const void* q;
@@ -59,8 +59,10 @@ __device__ __forceinline__ float ld_x(const void* p, size_t i, int bf16) {
   return static_cast<const float*>(p)[i];
 }
 
-__global__ void __launch_bounds__(kThreads, 2) recurrent_kernel(DecodeArgs a) {
-  __shared__ float kr[128], qr[128], dec[128];
+// kRows state rows per warp: the CTA covers K <= 16 kRows.
+template <int kRows>
+__global__ void __launch_bounds__(kThreads, 128 / (8 * kRows)) recurrent_kernel(DecodeArgs a) {
+  __shared__ float kr[kWarps * kRows], qr[kWarps * kRows], dec[kWarps * kRows];
   __shared__ float red_u[kWarps][kCols], red_o[kWarps][kCols];
   __shared__ float tok[4];   // |k|^-1, scale |q|^-1, beta, q~ . k^
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
@@ -387,7 +389,7 @@ extern "C" gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void
       (d->out_dtype != GDR_F32 && d->out_dtype != GDR_BF16))
     return GDR_ERR_INVALID_ARG;
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
-  if (d->K > 128) return GDR_ERR_UNSUPPORTED;
+  if (d->K > 256) return GDR_ERR_UNSUPPORTED;
   if (d->HV > 65535 || d->B > 65535) return GDR_ERR_UNSUPPORTED;
   if (d->B == 0 || d->T == 0) return GDR_OK;
   if (!q || !k || !v || !beta || !state || !out || (!g && gate_mode != GDR_GATE_NONE))
@@ -413,7 +415,8 @@ extern "C" gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void
   a.scale = scale;
   a.error_word = nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (d->V % 4 == 0 && d->V <= 128 && (reinterpret_cast<uintptr_t>(state) & 15) == 0) {
+  if (d->K <= 128 && d->V % 4 == 0 && d->V <= 128 &&
+      (reinterpret_cast<uintptr_t>(state) & 15) == 0) {
     // State viewed as [B HV][K][V] fp32; box = one whole head (K rows x V columns).
     CUtensorMap m;
     memset(&m, 0, sizeof m);
@@ -441,6 +444,9 @@ extern "C" gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void
     }
   }
   dim3 grid((d->V + kCols - 1) / kCols, d->HV, d->B);
-  recurrent_kernel<<<grid, kThreads, 0, st>>>(a);
+  if (d->K <= 128)
+    recurrent_kernel<8><<<grid, kThreads, 0, st>>>(a);
+  else
+    recurrent_kernel<16><<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }

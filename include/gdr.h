@@ -227,7 +227,8 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
  *   state    (device) fp32 [B, HV, K, V]: read as the state before token 0 and
  *            overwritten with the state after token T-1 (caller-owned)
  *   out      (device) [B, T, HV, V] out_dtype; must not overlap the inputs
- *   dims     as for gdr_chunk_fwd; K <= 128, any V
+ *   dims     as for gdr_chunk_fwd; K <= 256, any V (K <= 128 with V a multiple
+ *            of 4 up to 128 and a 16-byte aligned state take the pipelined kernel)
  *
  * Errors: invalid arguments return synchronously and enqueue nothing;
  * B == 0 or T == 0 is a no-op. No workspace and no device waits.

@@ -161,7 +161,7 @@ def test_recurrent_argument_errors(lib):
     assert rec(dims(T=1), gate=3) == gdr.GDR_ERR_INVALID_ARG
     assert rec(dims(T=1), scale=0.0) == gdr.GDR_ERR_INVALID_ARG
     assert rec(dims(T=1, HV=3)) == gdr.GDR_ERR_INVALID_ARG
-    assert rec(dims(T=1, K=256)) == gdr.GDR_ERR_UNSUPPORTED
+    assert rec(dims(T=1, K=257)) == gdr.GDR_ERR_UNSUPPORTED
     assert rec(dims(T=0)) == gdr.GDR_OK
     assert rec(dims(B=0, T=1)) == gdr.GDR_OK
 

@@ -53,6 +53,8 @@ CASES = [
     ("tiny_fp32", dict(T=4, K=20, V=40)),                        # ragged rows and columns
     ("tiny_fp32", dict(T=3, K=16, V=30)),                        # V % 4 != 0: fallback kernel
     ("gdn_t4096_h12", dict(B=2, T=2, H=3, HV=6, K=128, V=72)),   # ragged last V tile
+    ("gdn_t4096_h12", dict(T=3, H=1, HV=2, K=256, V=128)),      # K = 256: 16 rows per warp
+    ("kda_many_b64", dict(B=2, T=2, H=1, HV=2, K=200, V=40)),    # per-key, K between 128 and 256
 ]
 
 
