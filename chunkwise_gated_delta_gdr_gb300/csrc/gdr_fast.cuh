@@ -1,11 +1,13 @@
 // gdr_fast.cuh -- shared definitions of the fast path (bf16, K = V = 128, C = 64).
 //
 // The fast path runs two kernels:
-//   1. the chunk-local kernel (tcgen05 + TMA, one CTA per chunk) writes, per
-//      chunk, the operands of the inter-chunk recurrence into a workspace slab;
-//   2. the state kernel (register-resident mma.sync chain, one CTA per
-//      (batch, value head, 16-column V tile)) runs the recurrence over chunks.
-// This header fixes the slab format both kernels agree on.
+//   1. a chunk-local kernel (one CTA per chunk) writes, per chunk, the operands
+//      of the inter-chunk recurrence into a workspace slab: gdr_chunk_tc.cu
+//      (tcgen05, scalar gate) or gdr_chunk_kda.cu (mma.sync, per-key gate);
+//   2. a recurrence kernel runs the chunks in order per (batch, value head,
+//      V tile): gdr_recur.cu (scalar gate; mma.sync chains plus tcgen05 output
+//      CTAs, fallback gdr_state.cu) or gdr_state_kda.cu (per-key gate, tcgen05).
+// This header fixes the slab format both stages agree on.
 #pragma once
 
 #include <cuda_bf16.h>

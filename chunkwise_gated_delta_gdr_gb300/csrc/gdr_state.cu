@@ -49,7 +49,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int c) {
 }
 
 struct Maps {
-  CUtensorMap q, k, w2, aq2, u, qb2, kb2;
+  CUtensorMap q, k, w2, aq2, u;
 };
 
 // ---------------------------------------------------------------------------
