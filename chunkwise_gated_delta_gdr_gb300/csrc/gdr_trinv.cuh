@@ -81,7 +81,7 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
 #pragma unroll
       for (int z = 0; z < 4; ++z) a[z] = fmaf(l, (j0 + z <= m) ? xs[z] : 0.f, a[z]);
     }
-    __syncthreads();   // every thread is past its reads of the level-1 scratch
+    // The level-1 scratch was last read before the barrier that ends level 1.
     *reinterpret_cast<float4*>(T + i * 36 + j0) = make_float4(a[0], a[1], a[2], a[3]);
     __syncthreads();
     float r4[4] = {0.f, 0.f, 0.f, 0.f};
