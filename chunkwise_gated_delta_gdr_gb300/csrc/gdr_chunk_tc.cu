@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, colh = warp >> 2;   // TMEM lane quadrant, column half
   const int idx = (int)slab_index(p, b, hv, n);
+  if (p.zero_flags && idx == 0) {
+    const int nflags = p.B * p.HV * (V / VT);
+    for (int i = threadIdx.x; i < nflags; i += blockDim.x) p.flags[i] = 0u;
+  }
 
   float* L = reinterpret_cast<float*>(sm + OFF_L);
   float* X = reinterpret_cast<float*>(sm + OFF_X);

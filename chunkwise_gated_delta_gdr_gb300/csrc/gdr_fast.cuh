@@ -82,6 +82,10 @@ struct Params {
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;
   int ssd;                  // Mamba2 SSD update: no delta erase (W = 0), beta = 1
+  // Both stages in one call: the chunk kernel zeroes the chains' progress flags
+  // (read only by the recurrence, which runs after it), so the recurrence
+  // launch needs no separate reset.
+  int zero_flags;
   float scale;
   size_t slab_bytes;
 };

@@ -645,8 +645,9 @@ gdr_status launch_recur(const Params& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES) != cudaSuccess)
     return GDR_ERR_CUDA;
-  if (cudaMemsetAsync(p.flags, 0, (size_t)nseq * VTILES * sizeof(unsigned int), stream) !=
-      cudaSuccess)
+  if (!p.zero_flags &&
+      cudaMemsetAsync(p.flags, 0, (size_t)nseq * VTILES * sizeof(unsigned int), stream) !=
+          cudaSuccess)
     return GDR_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_chain + n_out);
