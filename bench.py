@@ -64,6 +64,8 @@ def workload(name):
         return gin.DECODE_WORKLOADS[name]
     if name in gin.SSD_WORKLOADS:
         return gin.SSD_WORKLOADS[name]
+    if name in gin.SEGMENTED_WORKLOADS:
+        return gin.SEGMENTED_WORKLOADS[name]
     return gin.WORKLOADS[name or gin.HEADLINE]
 
 
@@ -73,7 +75,8 @@ def config_of(w, world):
             "in_dtype": "bf16" if str(w.dtype).endswith("bfloat16") else "fp32",
             "out_dtype": "fp32", "use_qk_l2norm": w.use_qk_l2norm,
             "initial_state": w.s0_std is not None, "l2_flush": "512MiB write before each step",
-            "parallelism": f"{world} rank(s), value heads sharded, no collective"}
+            "parallelism": f"{world} rank(s), value heads sharded, no collective",
+            **({"segments": w.segments} if getattr(w, "segments", 1) > 1 else {})}
 
 
 def algorithmic_bytes(w):
@@ -284,8 +287,20 @@ def run_ours(args, rank, local_rank, world):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    segments = getattr(w, "segments", 1)
+    if segments > 1:
+        seg_ws = torch.empty(gdr.chunk_fwd_segmented_workspace_size(dims, w.C, gate, segments),
+                             dtype=torch.uint8, device=dev)
+
     def step():
-        # The call a user makes: both stages in one gdr_chunk_fwd.
+        # The call a user makes: both stages in one gdr_chunk_fwd (or, for a
+        # segmented workload, gdr_chunk_fwd_segmented).
+        if segments > 1:
+            gdr.chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"],
+                                    segments=segments, chunk_size=w.C, scale=w.scale,
+                                    use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
+                                    workspace=seg_ws, out=out, final_state=fin, stream=stream)
+            return
         gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], chunk_size=w.C,
                       scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
                       workspace=ws, out=out, final_state=fin, stream=stream)
@@ -350,15 +365,40 @@ def run_ours(args, rank, local_rank, world):
              for _ in range(E2E_STREAMS)]
     fin_h = [torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32).pin_memory()
              for _ in range(E2E_STREAMS)]
-    hbytes = gdr.chunk_fwd_host_buffer_size(dims, w.C, gate, pin["s0"] is not None, True)
-    hbuf = [torch.empty(hbytes, dtype=torch.uint8, device=dev) for _ in range(E2E_STREAMS)]
     streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
     h2d = sum(t.numel() * t.element_size() for n, t in pin.items() if t is not None)
     d2h = out_h[0].numel() * 4 + fin_h[0].numel() * 4
     e2e_steps = max(4, min(args.steps, 50))
+    if segments > 1:
+        # No host-buffer form of the segmented call: the inputs are copied into
+        # per-stream device tensors, gdr_chunk_fwd_segmented runs, and o and the
+        # final state are copied back, all on that stream.
+        dbuf = [{n: torch.empty_like(t, device=dev) for n, t in pin.items() if t is not None}
+                for _ in range(E2E_STREAMS)]
+        dout = [torch.empty_like(out) for _ in range(E2E_STREAMS)]
+        dfin = [torch.empty_like(fin) for _ in range(E2E_STREAMS)]
+        dws = [torch.empty_like(seg_ws) for _ in range(E2E_STREAMS)]
+        method = f"H2D copies + gdr_chunk_fwd_segmented + D2H copies per step, {E2E_STREAMS} streams alternating"
+    else:
+        hbytes = gdr.chunk_fwd_host_buffer_size(dims, w.C, gate, pin["s0"] is not None, True)
+        hbuf = [torch.empty(hbytes, dtype=torch.uint8, device=dev) for _ in range(E2E_STREAMS)]
+        method = f"gdr_chunk_fwd_host per step, {E2E_STREAMS} streams alternating"
 
     def e2e_step(i):
         j = i % E2E_STREAMS
+        if segments > 1:
+            d = dbuf[j]
+            with torch.cuda.stream(streams[j]):
+                for n, t in d.items():
+                    t.copy_(pin[n], non_blocking=True)
+                gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("s0"),
+                                        segments=segments, chunk_size=w.C, scale=w.scale,
+                                        use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
+                                        workspace=dws[j], out=dout[j], final_state=dfin[j],
+                                        stream=streams[j])
+                out_h[j].copy_(dout[j], non_blocking=True)
+                fin_h[j].copy_(dfin[j], non_blocking=True)
+            return
         gdr.chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"], pin["s0"],
                            out=out_h[j], final_state=fin_h[j], device_buffer=hbuf[j],
                            chunk_size=w.C, scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
@@ -401,18 +441,24 @@ def run_ours(args, rank, local_rank, world):
         "config": config_of(w, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "scope": "one forward call = chunk-local kernel + recurrence kernel",
+                     "scope": ("one gdr_chunk_fwd_segmented call = chunk-local kernel, 4 recurrence "
+                               "launches, identity and combine kernels" if segments > 1 else
+                               "one forward call = chunk-local kernel + recurrence kernel"),
                      "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs",
                      "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
         "kernels": {"chunk_local": {"ms": statistics.mean(prep),
                                     "traffic": (traffic_per or {}).get(ck)},
                     "recurrence": {"ms": statistics.mean(rec),
-                                   "traffic": (traffic_per or {}).get(rk)}},
+                                   "traffic": (traffic_per or {}).get(rk)},
+                    **({"split_of": "the unsegmented forward (gdr_chunk_prepare + "
+                                    "gdr_chunk_recur) on the same inputs"}
+                       if segments > 1 else {})},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "method": f"gdr_chunk_fwd_host per step, {E2E_STREAMS} streams alternating"},
-        "gpu_launches": 2 * args.steps,
+                "method": method},
+        "gpu_launches": (7 if segments > 1 else 2) * args.steps,
+        **({"unsegmented_ms": statistics.mean(prep) + statistics.mean(rec)} if segments > 1 else {}),
         "clocks": clocks,
         "wall_s_timed_loop": t_wall,
     }

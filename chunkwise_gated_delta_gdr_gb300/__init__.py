@@ -32,7 +32,8 @@ EXPORTED = (
     "gdr_chunk_fwd_host",
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
     "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
-    "gdr_ssd_chunk_fwd", "gdr_ssd_chunk_fwd_workspace_size",
+    "gdr_ssd_chunk_fwd", "gdr_ssd_chunk_fwd_workspace_size", "gdr_chunk_fwd_segmented",
+    "gdr_chunk_fwd_segmented_workspace_size",
 )
 # Size of the library-owned scratch used by gdr_chunk_fwd_noalloc (per device).
 GDR_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -93,6 +94,11 @@ def load_library(path: Optional[str] = None):
         lib.gdr_ssd_chunk_fwd.restype = ip
         lib.gdr_ssd_chunk_fwd_workspace_size.argtypes = [dp, ip, ip]
         lib.gdr_ssd_chunk_fwd_workspace_size.restype = sz
+        lib.gdr_chunk_fwd_segmented.argtypes = [vp, vp, vp, vp, vp, vp, ip, fp, ip, ip, ip, vp,
+                                                 vp, dp, vp, sz, vp]
+        lib.gdr_chunk_fwd_segmented.restype = ip
+        lib.gdr_chunk_fwd_segmented_workspace_size.argtypes = [dp, ip, ip, ip]
+        lib.gdr_chunk_fwd_segmented_workspace_size.restype = sz
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ip
         if path is None:
@@ -189,6 +195,45 @@ def chunk_fwd(q, k, v, g, beta, initial_state=None, *, chunk_size: int = 64,
         _stream_handle(stream))
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_fwd")
+    return out, final_state
+
+
+def chunk_fwd_segmented_workspace_size(dims: gdr_dims, chunk_size: int, gate_mode: int,
+                                       segments: int) -> int:
+    return int(load_library().gdr_chunk_fwd_segmented_workspace_size(
+        ctypes.byref(dims), chunk_size, gate_mode, segments))
+
+
+def chunk_fwd_segmented(q, k, v, g, beta, initial_state=None, *, segments: int,
+                        chunk_size: int = 64, scale: Optional[float] = None,
+                        use_qk_l2norm: bool = True, output_final_state: bool = True,
+                        out_dtype=None, out=None, final_state=None, workspace=None, stream=None):
+    """chunk_fwd with each sequence split into ``segments`` parts whose
+    recurrences run at the same time (gdr_chunk_fwd_segmented). Same arguments
+    and results as chunk_fwd."""
+    import torch
+    B, T, H, HV, K, V, gate_mode = _shapes(q, v, g)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    scale = 1.0 / math.sqrt(K) if scale is None else float(scale)
+    dims = make_dims(B, T, H, HV, K, V, _dtype_code(q.dtype), _dtype_code(out_dtype))
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                    ("initial_state", initial_state)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty(B, T, HV, V, dtype=out_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(B, HV, K, V, dtype=torch.float32, device=q.device)
+    ws_bytes = chunk_fwd_segmented_workspace_size(dims, chunk_size, gate_mode, segments)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = load_library().gdr_chunk_fwd_segmented(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), int(chunk_size),
+        ctypes.c_float(scale), int(bool(use_qk_l2norm)), gate_mode, int(segments), _ptr(out),
+        _ptr(final_state), ctypes.byref(dims), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+        _stream_handle(stream))
+    if st != GDR_OK:
+        raise GdrError(st, "gdr_chunk_fwd_segmented")
     return out, final_state
 
 

@@ -147,7 +147,7 @@ gdr_status run(int stage, const void* q, const void* k, const void* v, const flo
                const float* beta, const float* initial_state, int chunk_size, float scale,
                int use_qk_l2norm, int gate_mode, void* out, float* final_state,
                const gdr_dims* dims, void* workspace, size_t workspace_bytes,
-               gdr_stream_t stream, int ssd = 0) {
+               gdr_stream_t stream, int ssd = 0, int zero_u = 0, int recur_mode = 0) {
   gdr_status st = check_dims(dims, chunk_size, gate_mode);
   if (st != GDR_OK) return st;
   if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
@@ -180,12 +180,15 @@ gdr_status run(int stage, const void* q, const void* k, const void* v, const flo
   Problem p = make_problem(q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm,
                            gate_mode, out, final_state, dims);
   p.ssd = ssd;
+  p.zero_u = zero_u;
+  p.recur_mode = recur_mode;
   auto* hdr = static_cast<WorkspaceHeader*>(workspace);
   if ((stage & 1) &&
       cudaMemsetAsync(&hdr->error_word, 0, sizeof(unsigned int), s) != cudaSuccess)
     return GDR_ERR_CUDA;
   void* body = static_cast<char*>(workspace) + sizeof(WorkspaceHeader);
   if (tc_supported(p)) return launch_tc(p, body, &hdr->error_word, s, stage);
+  if (recur_mode == 2) return GDR_OK;   // the general path writes outputs with the states
   return launch_general(p, body, s, stage);
 }
 
@@ -294,6 +297,115 @@ gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace) {
   if (cudaMemcpy(&word, &hdr->error_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
     return GDR_ERR_CUDA;
   return word ? GDR_ERR_TIMEOUT : GDR_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Segmented scan (gdr_segment.cu has the plan).
+namespace {
+
+struct SegLayout {
+  size_t inner, bst, ast, sin, oscr, total;
+};
+
+// The sequences viewed as B P sequences of T / P tokens.
+gdr_dims segment_dims(const gdr_dims* d, int P) {
+  gdr_dims d2 = *d;
+  d2.B = d->B * P;
+  d2.T = d->T / P;
+  return d2;
+}
+
+SegLayout seg_layout(const gdr_dims* d2, int chunk_size, int gate_mode) {
+  SegLayout L;
+  const size_t st = (size_t)d2->B * d2->HV * d2->K * d2->V * sizeof(float);
+  const size_t oo = (size_t)d2->B * d2->T * d2->HV * d2->V * elem_out(d2);
+  size_t off = 0;
+  L.inner = gdr_chunk_fwd_workspace_size(d2, chunk_size, gate_mode);
+  off = align_up(L.inner);
+  L.bst = off; off += align_up(st);
+  L.ast = off; off += align_up(st);
+  L.sin = off; off += align_up(st);
+  L.oscr = off; off += align_up(oo);
+  L.total = off;
+  return L;
+}
+
+gdr_status segment_check(const gdr_dims* d, int chunk_size, int gate_mode, int segments) {
+  const gdr_status st = check_dims(d, chunk_size, gate_mode);
+  if (st != GDR_OK) return st;
+  if (segments < 1) return GDR_ERR_INVALID_ARG;
+  if (segments == 1) return GDR_OK;
+  if (d->K != d->V) return GDR_ERR_UNSUPPORTED;               // A_p is a K x K state
+  if (d->T % (segments * chunk_size) != 0) return GDR_ERR_UNSUPPORTED;
+  const gdr_dims d2 = segment_dims(d, segments);
+  return check_dims(&d2, chunk_size, gate_mode);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdr_chunk_fwd_segmented_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode,
+                                              int segments) {
+  if (segment_check(dims, chunk_size, gate_mode, segments) != GDR_OK) return 0;
+  if (segments == 1) return gdr_chunk_fwd_workspace_size(dims, chunk_size, gate_mode);
+  const gdr_dims d2 = segment_dims(dims, segments);
+  return seg_layout(&d2, chunk_size, gate_mode).total;
+}
+
+gdr_status gdr_chunk_fwd_segmented(const void* q, const void* k, const void* v, const float* g,
+                                   const float* beta, const float* initial_state,
+                                   int chunk_size, float scale, int use_qk_l2norm, int gate_mode,
+                                   int segments, void* out, float* final_state,
+                                   const gdr_dims* dims, void* workspace,
+                                   size_t workspace_bytes, gdr_stream_t stream) {
+  gdr_status st = segment_check(dims, chunk_size, gate_mode, segments);
+  if (st != GDR_OK) return st;
+  if (segments == 1 || dims->B == 0 || dims->T == 0)
+    return gdr_chunk_fwd(q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm,
+                         gate_mode, out, final_state, dims, workspace, workspace_bytes, stream);
+  if (!(isfinite(scale) && scale > 0.f)) return GDR_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || (!g && gate_mode != GDR_GATE_NONE) || !beta)
+    return GDR_ERR_INVALID_ARG;
+  const gdr_dims d2 = segment_dims(dims, segments);
+  const SegLayout L = seg_layout(&d2, chunk_size, gate_mode);
+  if (!workspace || workspace_bytes < L.total) return GDR_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return GDR_ERR_ALIGNMENT;
+  if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+    return GDR_ERR_ALIGNMENT;
+  char* base = static_cast<char*>(workspace);
+  float* Bst = reinterpret_cast<float*>(base + L.bst);
+  float* Ast = reinterpret_cast<float*>(base + L.ast);
+  float* Sin = reinterpret_cast<float*>(base + L.sin);
+  void* oscr = base + L.oscr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // 1. chunk-local kernel on the B P segments
+  st = run(1, q, k, v, g, beta, nullptr, chunk_size, scale, use_qk_l2norm, gate_mode, nullptr,
+           nullptr, &d2, workspace, L.inner, stream);
+  if (st != GDR_OK) return st;
+  // 2. B_p: each segment from a zero state (states only where outputs are separate)
+  st = run(2, q, k, nullptr, nullptr, nullptr, nullptr, chunk_size, scale, use_qk_l2norm,
+           gate_mode, oscr, Bst, &d2, workspace, L.inner, stream, 0, 0, 1);
+  if (st != GDR_OK) return st;
+  // 3. A_p: each segment from the identity, U read as zero (final state in place)
+  st = launch_segment_identity(Ast, (long)d2.B * d2.HV, d2.K, s);
+  if (st != GDR_OK) return st;
+  st = run(2, q, k, nullptr, nullptr, nullptr, Ast, chunk_size, scale, use_qk_l2norm, gate_mode,
+           oscr, Ast, &d2, workspace, L.inner, stream, 0, 1, 1);
+  if (st != GDR_OK) return st;
+  // 4. segment initial states and the final state
+  st = launch_segment_combine(Ast, Bst, initial_state, Sin, final_state, dims->B, segments,
+                              dims->HV, dims->K, s);
+  if (st != GDR_OK) return st;
+  // 5. each segment from its true initial state: the states, then the outputs on
+  // every SM (one pass where a kernel writes both)
+  st = run(2, q, k, nullptr, nullptr, nullptr, Sin, chunk_size, scale, use_qk_l2norm, gate_mode,
+           out, nullptr, &d2, workspace, L.inner, stream, 0, 0, 1);
+  if (st != GDR_OK) return st;
+  return run(2, q, k, nullptr, nullptr, nullptr, Sin, chunk_size, scale, use_qk_l2norm,
+             gate_mode, out, nullptr, &d2, workspace, L.inner, stream, 0, 0, 2);
 }
 
 }  // extern "C"

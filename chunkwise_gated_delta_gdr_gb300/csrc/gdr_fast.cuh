@@ -86,6 +86,8 @@ struct Params {
   // (read only by the recurrence, which runs after it), so the recurrence
   // launch needs no separate reset.
   int zero_flags;
+  int zero_u;               // recurrence reads U as zero (the chunk map's linear part)
+  int recur_mode;           // 0 chains + outputs; 1 chains only; 2 outputs only (gdr_internal.cuh)
   float scale;
   size_t slab_bytes;
 };

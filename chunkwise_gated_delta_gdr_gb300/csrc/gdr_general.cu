@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
     // r = U - W S (a warp shares its row i: the W loads are broadcasts)
     for (int idx = tid; idx < C * kVt; idx += kThreads) {
       const int i = idx / kVt, j = idx % kVt;
-      float acc = (j < vw) ? U[(long)i * V + v0 + j] : 0.f;
+      float acc = (j < vw && !p.zero_u) ? U[(long)i * V + v0 + j] : 0.f;
       for (int c = 0; c < K; ++c) acc = fmaf(-W[(long)i * K + c], S[c * kVt + j], acc);
       r[idx] = acc;
     }

@@ -25,6 +25,11 @@ struct Problem {
   int in_bf16, out_bf16, gate_mode, use_l2;
   float scale;
   int ssd = 0;           // Mamba2 SSD update: no delta erase, no beta (general path only)
+  int zero_u = 0;        // recurrence reads U as zero: S <- (gamma - KB^T W) S, the linear
+                         // part of the chunk map (segmented scan)
+  int recur_mode = 0;    // 0: states and outputs; 1: states only where the outputs are a
+                         // separate pass (the fused recurrence), else both; 2: that
+                         // separate output pass after a mode-1 launch (else nothing)
 };
 
 // Workspace header: first 256 bytes of every workspace.
@@ -48,5 +53,11 @@ bool tc_supported(const Problem& p);
 size_t tc_workspace_bytes(const Problem& p);
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
                      cudaStream_t stream, int stage);
+
+// Segmented scan helpers (gdr_segment.cu): n identity K x K states; the serial
+// combine S_{p+1} = A_p S_p + B_p over the P segments of each (b, hv).
+gdr_status launch_segment_identity(float* A, long n, int K, cudaStream_t stream);
+gdr_status launch_segment_combine(const float* A, const float* Bst, const float* s0, float* Sin,
+                                  float* sT, int B, int P, int HV, int K, cudaStream_t stream);
 
 }  // namespace gdr

@@ -295,10 +295,11 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
 #pragma unroll
       for (int jt = 0; jt < 2; ++jt) {
         const int j = jw + 8 * jt + 2 * t4;
-        Rhh[jt][0] = su[j * VT + g];
-        Rhh[jt][1] = su[(j + 1) * VT + g];
-        Rhh[jt][2] = su[j * VT + g + 8];
-        Rhh[jt][3] = su[(j + 1) * VT + g + 8];
+        const float uf = p.zero_u ? 0.f : 1.f;
+        Rhh[jt][0] = uf * su[j * VT + g];
+        Rhh[jt][1] = uf * su[(j + 1) * VT + g];
+        Rhh[jt][2] = uf * su[j * VT + g + 8];
+        Rhh[jt][3] = uf * su[(j + 1) * VT + g + 8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = 0.f;
       }
@@ -613,13 +614,24 @@ DeviceInfo device_info() {
 gdr_status launch_recur(const Params& p, cudaStream_t stream) {
   if (!p.xchg || !p.flags || p.gate_mode != 0) return GDR_ERR_UNSUPPORTED;
   const int nseq = p.B * p.HV;
-  const int n_chain = nseq * VTILES;
   const long long items = 2LL * nseq * p.N;
-  // The outputs need at least an eighth as many SMs as the chains (and 8).
   const DeviceInfo dev = device_info();
-  const int spare = dev.sms - n_chain;
-  if (!dev.coop || spare < 8 || spare * 8 < n_chain) return GDR_ERR_UNSUPPORTED;
-  const int n_out = (int)(items < spare ? items : spare);
+  int n_chain = nseq * VTILES, n_out = 0;
+  bool coop = false;
+  if (p.recur_mode == 1) {
+    // Chains only: they wait on nothing, so any number may run, in waves.
+  } else if (p.recur_mode == 2) {
+    // Outputs only, on every SM: the flags of the previous chains-only launch
+    // are final, so no output CTA waits for long.
+    n_chain = 0;
+    n_out = (int)(items < dev.sms ? items : dev.sms);
+  } else {
+    // The outputs need at least an eighth as many SMs as the chains (and 8).
+    const int spare = dev.sms - n_chain;
+    if (!dev.coop || spare < 8 || spare * 8 < n_chain) return GDR_ERR_UNSUPPORTED;
+    n_out = (int)(items < spare ? items : spare);
+    coop = true;
+  }
 
   Maps m;
   memset(&m, 0, sizeof m);
@@ -645,7 +657,7 @@ gdr_status launch_recur(const Params& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES) != cudaSuccess)
     return GDR_ERR_CUDA;
-  if (!p.zero_flags &&
+  if (!p.zero_flags && p.recur_mode != 2 &&
       cudaMemsetAsync(p.flags, 0, (size_t)nseq * VTILES * sizeof(unsigned int), stream) !=
           cudaSuccess)
     return GDR_ERR_CUDA;
@@ -658,7 +670,7 @@ gdr_status launch_recur(const Params& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = coop ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, recur_kernel, m, p, n_chain, n_out);
   if (e == cudaSuccess) return GDR_OK;
   if (e == cudaErrorCooperativeLaunchTooLarge) {

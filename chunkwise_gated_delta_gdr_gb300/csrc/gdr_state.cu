@@ -217,10 +217,11 @@ __global__ void __launch_bounds__(ws::THREADS) state_ws_kernel(const __grid_cons
 #pragma unroll
       for (int jt = 0; jt < 2; ++jt) {
         const int j = jw + 8 * jt + 2 * t4;
-        Rhh[jt][0] = su[j * VT + g];
-        Rhh[jt][1] = su[(j + 1) * VT + g];
-        Rhh[jt][2] = su[j * VT + g + 8];
-        Rhh[jt][3] = su[(j + 1) * VT + g + 8];
+        const float uf = p.zero_u ? 0.f : 1.f;
+        Rhh[jt][0] = uf * su[j * VT + g];
+        Rhh[jt][1] = uf * su[(j + 1) * VT + g];
+        Rhh[jt][2] = uf * su[j * VT + g + 8];
+        Rhh[jt][3] = uf * su[(j + 1) * VT + g + 8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = 0.f;
       }
@@ -503,11 +504,13 @@ gdr_status launch_ws(const Params& p, cudaStream_t stream) {
 }  // namespace
 
 gdr_status launch_state(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode) return launch_state_kda_tc(p, stream);
+  // Kernels that write the outputs with the states have no separate output pass.
+  if (p.gate_mode) return p.recur_mode == 2 ? GDR_OK : launch_state_kda_tc(p, stream);
   // Scalar gate: the fused chain + output launch when the chains leave SMs
   // for the outputs, else chain and outputs in the same CTAs.
   const gdr_status st = launch_recur(p, stream);
-  return st == GDR_ERR_UNSUPPORTED ? launch_ws(p, stream) : st;
+  if (st != GDR_ERR_UNSUPPORTED) return st;
+  return p.recur_mode == 2 ? GDR_OK : launch_ws(p, stream);
 }
 
 }  // namespace fast

@@ -227,13 +227,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tmem + lane_base + T_R2 + 64 + 32 * hf, rl);
         if (lane < 16) {
           const uint8_t* ub = sm + U_BASE + s * 16384 + hf * 8192;
+          const float uf = p.zero_u ? 0.f : 1.f;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 u = *reinterpret_cast<const float4*>(ub + sw_off(j, q));
-            r[4 * q] += rl[4 * q] + u.x;
-            r[4 * q + 1] += rl[4 * q + 1] + u.y;
-            r[4 * q + 2] += rl[4 * q + 2] + u.z;
-            r[4 * q + 3] += rl[4 * q + 3] + u.w;
+            r[4 * q] += rl[4 * q] + uf * u.x;
+            r[4 * q + 1] += rl[4 * q + 1] + uf * u.y;
+            r[4 * q + 2] += rl[4 * q + 2] + uf * u.z;
+            r[4 * q + 3] += rl[4 * q + 3] + uf * u.w;
           }
           publish<4>(sm + R_BASE, sm + R_BASE + 8192, j, 4 * hf, r);
         }

@@ -61,6 +61,8 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.gate_mode = p.gate_mode;
   f.use_l2 = p.use_l2;
   f.ssd = p.ssd;
+  f.zero_u = p.zero_u;
+  f.recur_mode = p.recur_mode;
   f.zero_flags = (stage == 3 && f.flags) ? 1 : 0;
   f.scale = p.scale;
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);

@@ -51,6 +51,7 @@ class Workload:
     seed: int
     use_qk_l2norm: bool = True
     description: str = ""
+    segments: int = 1           # > 1: the forward runs as a segmented scan of this many parts
 
     @property
     def scale(self) -> float:
@@ -91,6 +92,15 @@ DECODE_WORKLOADS = {
         "decode_b64_h16", B=64, T=1, H=16, HV=16, K=128, V=128, C=64, dtype=torch.bfloat16,
         gate_mode=0, g_mean=0.0, g_std=1.0, s0_std=0.02, seed=5,
         description="decode step: 64 sequences x 16 heads, one token each, fp32 state in place"),
+}
+
+# Few, long sequences: the case the segmented scan of the chunk recurrence serves
+# (16 state chains for 152 SMs unsegmented).
+SEGMENTED_WORKLOADS = {
+    "gdn_h2_t65536": Workload(
+        "gdn_h2_t65536", B=1, T=65536, H=2, HV=2, K=128, V=128, C=64, dtype=torch.bfloat16,
+        gate_mode=0, g_mean=1.0, g_std=1.0, s0_std=0.02, seed=7, segments=8,
+        description="scalar-gate forward, 2 heads x 65536 tokens, carried state, 8 segments"),
 }
 
 # The Mamba2 SSD recurrence on the headline shape (beta is drawn but not used).

@@ -254,6 +254,35 @@ gdr_status gdr_ssd_chunk_fwd(const void* q, const void* k, const void* v, const 
                              gdr_stream_t stream);
 size_t gdr_ssd_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, int gate_mode);
 
+/*
+ * Segmented (parallel) scan of the same forward pass. Over a chunk the state
+ * map of the chunk form is affine in S ("DeltaNet chunk kernel optimization",
+ * cross-chunk state passing as a keyed scan of affine maps), so each sequence
+ * is split into `segments` equal parts that run their recurrences at the same
+ * time: each part's map S -> A_p S + B_p is computed (A_p from the identity
+ * with the values' contribution dropped, B_p from a zero state), the maps are
+ * chained serially to give every part its initial state, and the parts are
+ * run once more from those states to write the outputs. The serial chain is
+ * T / segments chunks long instead of T, at about three times the recurrence
+ * work: it pays for few, long sequences (few chains for many SMs).
+ *
+ * Arguments as for gdr_chunk_fwd, plus
+ *   segments   P >= 1 (1: exactly gdr_chunk_fwd). P > 1 needs K == V and T a
+ *              multiple of P * chunk_size (else GDR_ERR_UNSUPPORTED), and the
+ *              B P sequences of T / P tokens must be a supported problem.
+ *   workspace  gdr_chunk_fwd_segmented_workspace_size() bytes (0: unsupported).
+ * Results equal gdr_chunk_fwd's up to rounding; errors as for gdr_chunk_fwd
+ * (gdr_stream_status reads this workspace).
+ */
+gdr_status gdr_chunk_fwd_segmented(const void* q, const void* k, const void* v, const float* g,
+                                   const float* beta, const float* initial_state,
+                                   int chunk_size, float scale, int use_qk_l2norm, int gate_mode,
+                                   int segments, void* out, float* final_state,
+                                   const gdr_dims* dims, void* workspace,
+                                   size_t workspace_bytes, gdr_stream_t stream);
+size_t gdr_chunk_fwd_segmented_workspace_size(const gdr_dims* dims, int chunk_size,
+                                              int gate_mode, int segments);
+
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status s);
 

@@ -175,3 +175,26 @@ def test_ssd_workspace_and_arguments(lib):
     st = lib.gdr_ssd_chunk_fwd(P(A), P(A), P(A), None, None, 64, ctypes.c_float(0.1), 1, 0, P(A),
                                None, ctypes.byref(d), P(A), ctypes.c_size_t(1 << 40), None)
     assert st == gdr.GDR_ERR_INVALID_ARG                    # g required for a gated mode
+
+
+def test_segmented_sizes_and_arguments(lib):
+    d = dims(T=4096)
+    plain = gdr.chunk_fwd_workspace_size(d, 64, 0)
+    assert gdr.chunk_fwd_segmented_workspace_size(d, 64, 0, 1) == plain
+    seg = gdr.chunk_fwd_segmented_workspace_size(d, 64, 0, 4)
+    assert seg > plain                                                     # + states + o scratch
+    assert gdr.chunk_fwd_segmented_workspace_size(d, 64, 0, 0) == 0        # segments >= 1
+    assert gdr.chunk_fwd_segmented_workspace_size(dims(T=4000), 64, 0, 4) == 0   # T % (P C)
+    assert gdr.chunk_fwd_segmented_workspace_size(dims(T=4096, V=64), 64, 0, 4) == 0  # K != V
+    P = ctypes.c_void_p
+    A = 1 << 20
+    def seg(dd, segments, q=A, ws=None, nbytes=0):
+        return lib.gdr_chunk_fwd_segmented(P(q) if q else None, P(A), P(A), P(A), P(A), None, 64,
+                                           ctypes.c_float(0.1), 1, 0, segments, P(A), None,
+                                           ctypes.byref(dd), P(ws) if ws else None,
+                                           ctypes.c_size_t(nbytes), None)
+    assert seg(d, 0) == gdr.GDR_ERR_INVALID_ARG
+    assert seg(dims(T=4000), 4) == gdr.GDR_ERR_UNSUPPORTED
+    assert seg(dims(T=4096, V=64), 4) == gdr.GDR_ERR_UNSUPPORTED
+    assert seg(d, 4, q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert seg(d, 4) == gdr.GDR_ERR_WORKSPACE                               # nothing launched

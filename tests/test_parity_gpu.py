@@ -408,3 +408,47 @@ def test_fused_recurrence_reuses_its_flags():
         torch.cuda.synchronize()
         assert gdr.stream_status(None, ws) == gdr.GDR_OK
         assert relerr(o.cpu().numpy(), ro) <= 2e-3 and relerr(S.cpu().numpy(), rS) <= 2e-3
+
+
+# ---- segmented scan (gdr_chunk_fwd_segmented) ---------------------------------------
+SEGMENTED = [
+    ("gdn_t4096_h12", dict(T=1024, H=2, HV=2, s0_std=0.02), 4),        # tensor-core path
+    ("gdn_long_t65000", dict(T=2048, H=1, HV=2), 8),                   # carried state, long
+    ("kda_gqa_t8192", dict(B=2, T=512, H=1, HV=2), 4),                 # per-key gate
+    ("kda_many_b64", dict(B=1, T=256, H=1, HV=1, s0_std=0.02), 2),     # strong per-key decay
+    ("tiny_fp32", dict(T=128), 2),                                     # fp32 general path
+    ("gdn_t4096_h12", dict(T=512, H=1, HV=1, K=64, V=64, C=32), 4),    # general path, C = 32
+]
+
+
+@pytest.mark.parametrize("name,ov,segments", SEGMENTED)
+def test_segmented_matches_oracle(name, ov, segments):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], d["s0"],
+                                   segments=segments, chunk_size=w.C, scale=w.scale,
+                                   use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale,
+                              use_qk_l2norm=w.use_qk_l2norm)
+    o, S = o.cpu().numpy(), S.cpu().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    tol = tol_for(w)
+    assert relerr(o, ro) <= tol and relerr(S, rS) <= tol
+    # and close to the unsegmented call
+    po, pS = gpu_run(x, w)
+    assert relerr(o, po) <= tol and relerr(S, pS) <= tol
+
+
+def test_segmented_one_segment_is_chunk_fwd():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=300, H=2, HV=2)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], None, segments=1,
+                                   chunk_size=w.C, scale=w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    po, pS = gpu_run(x, w)
+    assert np.array_equal(o.cpu().numpy(), po) and np.array_equal(S.cpu().numpy(), pS)
