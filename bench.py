@@ -448,9 +448,9 @@ def run_ours(args, rank, local_rank, world):
                      "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
         "kernels": {"chunk_local": {"ms": statistics.mean(prep),
-                                    "traffic": (traffic_per or {}).get(ck)},
+                                    "traffic": None if segments > 1 else (traffic_per or {}).get(ck)},
                     "recurrence": {"ms": statistics.mean(rec),
-                                   "traffic": (traffic_per or {}).get(rk)},
+                                   "traffic": None if segments > 1 else (traffic_per or {}).get(rk)},
                     **({"split_of": "the unsegmented forward (gdr_chunk_prepare + "
                                     "gdr_chunk_recur) on the same inputs"}
                        if segments > 1 else {})},
