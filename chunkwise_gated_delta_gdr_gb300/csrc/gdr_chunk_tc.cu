@@ -37,6 +37,7 @@ constexpr int THREADS = 256;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr long kWaitLimit = 1L << 24;   // bounded spin: ~tens of ms, then error word
 constexpr unsigned int kErrTmaWait = 1u, kErrMmaWait = 2u;
+constexpr float kSplitSpan = 80.f;      // |G_i - G_m| bound of the split decays
 
 // Shared-memory map (bytes from a 1024-aligned base).
 constexpr int OFF_K0 = 0;          // k cols 0-63   (8 KB, 128-byte swizzle, from TMA)
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
+  int* split_ok = reinterpret_cast<int*>(tslot + 1);   // decay factorisation allowed
   uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
 
   // The input tiles are requested first: the thread that initialised the
@@ -189,10 +191,29 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
       if (lane >= o) s += y;
     }
     const float excl = s - (ga + gb);
-    G[2 * lane] = excl + ga;
-    G[2 * lane + 1] = excl + ga + gb;
+    const float g0 = excl + ga, g1 = excl + ga + gb;
+    G[2 * lane] = g0;
+    G[2 * lane + 1] = g1;
+    // The decays exp(G_i - G_j) may be split at the middle row m = C/2 - 1 as
+    // exp(G_i - G_m) exp(G_m - G_j) while every |G_i - G_m| <= 80: both factors
+    // then stay inside the fp32 range (NaN gates fail the test).
+    const float gm = __shfl_sync(0xffffffffu, g1, C / 4 - 1);
+    float dev = fmaxf(fabsf(g0 - gm), fabsf(g1 - gm));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, o));
+    if (lane == 0) *split_ok = dev <= kSplitSpan ? 1 : 0;
   }
   __syncthreads();
+  // Split decays: column factor |k_j|^-1 beta_j exp(G_m - G_j) once per column
+  // (in the column-factor array, free until the row factors below); the row and
+  // column factors are multiplied before the dot, so the intermediate is the
+  // size of exp(G_i - G_j).
+  const bool split = *split_ok != 0;
+  const float Gm = G[C / 2 - 1];
+  if (split) {
+    if (tid < C) cfac[tid] = nk[tid] * bb[tid] * __expf(Gm - G[tid]);
+    __syncthreads();
+  }
 
   // ---- epilogue 1: A_kk -> L (fp32, smem), A_qk -> swizzled bf16 hi/lo boxes ----
   // Warp w: TMEM lanes of quadrant w % 4 (rows of [k; q]), columns
@@ -200,7 +221,45 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 0, kWaitLimit));
   if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
   tc_fence_after();
-  if (ok) {
+  if (ok && split) {
+    const int r = 32 * quad + lane, rr = r & 63;
+    const bool is_q = r >= 64;
+    const float rowe = (is_q ? p.scale * nq[rr] : nk[rr]) * __expf(G[rr] - Gm);
+    float v[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * colh, v);
+    const int jb = 32 * colh;
+    if (!is_q) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 cf = *reinterpret_cast<const float4*>(cfac + jb + e);
+        const float cs[4] = {cf.x, cf.y, cf.z, cf.w};
+        float a4[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z)
+          a4[z] = (jb + e + z < rr && !p.ssd) ? v[e + z] * (rowe * cs[z]) : 0.f;
+        *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+      }
+    } else {
+      uint8_t* aqs = sm + OFF_AQS;
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        const float4 c0 = *reinterpret_cast<const float4*>(cfac + jb + e);
+        const float4 c1 = *reinterpret_cast<const float4*>(cfac + jb + e + 4);
+        const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int f = 0; f < 8; f += 2) {
+          const float a0 = (jb + e + f <= rr) ? v[e + f] * (rowe * cs[f]) : 0.f;
+          const float a1 = (jb + e + f + 1 <= rr) ? v[e + f + 1] * (rowe * cs[f + 1]) : 0.f;
+          split_pair(a0, a1, hi[f / 2], lo[f / 2]);
+        }
+        const int c = (jb + e) >> 3;
+        *reinterpret_cast<uint4*>(aqs + box_off(rr, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(aqs + 8192 + box_off(rr, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+  } else if (ok) {
+    // Decays too far apart to split: exp(G_i - G_j) element by element.
     const int r = 32 * quad + lane, rr = r & 63;
     const bool is_q = r >= 64;
     const float Gi = G[rr];

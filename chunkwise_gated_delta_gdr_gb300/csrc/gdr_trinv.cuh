@@ -8,10 +8,12 @@
 //            x_i = delta_ij - sum_{m<i} L_im x_m (one column per thread);
 //   level 1: X_10 = -X_11 L_10 X_00 and X_32 = -X_33 L_32 X_22;
 //   level 2: X[32:64, 0:32] = -X[32:64, 32:64] L[32:64, 0:32] X[0:32, 0:32].
-// Only the strictly lower entries of L are read. Blocks of X above the diagonal
-// are never written; the diagonal blocks come out with exact zeros above their
-// diagonal. All 256 threads of the CTA call it; it synchronises the CTA between
-// levels but not after the last writes (the caller does).
+// Only the strictly lower entries of L are read. Inside the two 32x32 diagonal
+// blocks everything above the diagonal is written as exact zeros (the 16x16
+// diagonal blocks' upper triangles and the blocks X_01, X_23), so the level-2
+// products need no masks; X[0:32, 32:64] is never written. All 256 threads of
+// the CTA call it; it synchronises the CTA between levels but not after the
+// last writes (the caller does).
 #pragma once
 
 namespace gdr {
@@ -29,11 +31,17 @@ __device__ __forceinline__ void inverse_level0(const float* L, float (&xd)[16], 
     xd[i] = acc;
   }
 }
+// Threads 0-63 store their column; those of diagonal blocks 0 and 2 also zero
+// the same column of the block to the right (X_01, X_23).
 template <int LDX>
 __device__ __forceinline__ void inverse_level0_store(float* X, const float (&xd)[16], int tid) {
   const int o = (tid >> 4) * 16, col = tid & 15;
+  const bool zero_right = ((tid >> 4) & 1) == 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) X[(o + i) * LDX + o + col] = xd[i];
+  for (int i = 0; i < 16; ++i) {
+    X[(o + i) * LDX + o + col] = xd[i];
+    if (zero_right) X[(o + i) * LDX + o + 16 + col] = 0.f;
+  }
 }
 
 // Levels 1 and 2, once the diagonal blocks of X are in place and visible.
@@ -68,8 +76,9 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
     }
   }
   __syncthreads();
-  // Level 2: each thread one row segment of 4 columns. Entries above the
-  // diagonal of X are read as zero through the masks.
+  // Level 2: each thread one row segment of 4 columns. The zeros above the
+  // diagonal of X[0:32, 0:32] and X[32:64, 32:64] are stored, so the products
+  // run over the full 32 x 32 blocks.
   {
     const int i = tid >> 3, j0 = (tid & 7) * 4;
     float a[4] = {0.f, 0.f, 0.f, 0.f};
@@ -77,9 +86,8 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
     for (int m = 0; m < 32; ++m) {
       const float l = L[(32 + i) * LDL + m];
       const float4 x0 = *reinterpret_cast<const float4*>(X + m * LDX + j0);
-      const float xs[4] = {x0.x, x0.y, x0.z, x0.w};
-#pragma unroll
-      for (int z = 0; z < 4; ++z) a[z] = fmaf(l, (j0 + z <= m) ? xs[z] : 0.f, a[z]);
+      a[0] = fmaf(l, x0.x, a[0]); a[1] = fmaf(l, x0.y, a[1]);
+      a[2] = fmaf(l, x0.z, a[2]); a[3] = fmaf(l, x0.w, a[3]);
     }
     // The level-1 scratch was last read before the barrier that ends level 1.
     *reinterpret_cast<float4*>(T + i * 36 + j0) = make_float4(a[0], a[1], a[2], a[3]);
@@ -87,7 +95,7 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
     float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {
-      const float xv = (m <= i) ? X[(32 + i) * LDX + 32 + m] : 0.f;
+      const float xv = X[(32 + i) * LDX + 32 + m];
       const float4 t4 = *reinterpret_cast<const float4*>(T + m * 36 + j0);
       const float ts[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll

@@ -169,6 +169,28 @@ def test_positive_small_gate():
     check_against_oracle(w, x)
 
 
+# Scalar-gate recipes for the tensor-core chunk kernel: a chunk whose gate
+# cumsum strays more than 80 from its middle row's takes the decays element by
+# element, the others as a row factor times a column factor; these cover both
+# forms, and both within one sequence.
+SCALAR_GATES = {
+    "steep": lambda shape, gen: torch.full(shape, -4.0),            # spans ~250: element form
+    "moderate": lambda shape, gen: torch.full(shape, -1.2),         # |G_i - G_m| <= 39: split form
+    "mixed_spans": lambda shape, gen: -torch.randn(shape, generator=gen).abs() * 3.0,
+    "alternating_chunks": lambda shape, gen: torch.where(
+        (torch.arange(shape[1]) // 64) % 2 == 0, torch.tensor(-4.0), torch.tensor(-0.05)
+    ).view(1, -1, 1).expand(shape).clone(),
+}
+
+
+@pytest.mark.parametrize("recipe", list(SCALAR_GATES))
+def test_scalar_gate_ranges(recipe):
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=264, H=2, HV=2, s0_std=0.02)
+    x = gin.make_inputs(w)
+    x["g"] = SCALAR_GATES[recipe](tuple(x["g"].shape), torch.Generator().manual_seed(22)).float()
+    check_against_oracle(w, x)
+
+
 # Per-key gate recipes for the factorised decayed dots: a 16-row block whose
 # gate span exceeds the factor limit is computed element by element, so these
 # cover both branches and their mix within one chunk.
