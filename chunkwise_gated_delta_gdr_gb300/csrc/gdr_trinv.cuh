@@ -16,6 +16,8 @@
 // last writes (the caller does).
 #pragma once
 
+#include "gdr_ptx.cuh"
+
 namespace gdr {
 namespace fast {
 
@@ -105,7 +107,90 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
   }
 }
 
-// L: [64][LDL] fp32; X: [64][LDX] fp32; T: scratch [32][36] fp32.
+// D += A B for one 16x8 tile on the tensor cores, A a 16x16 block of the fp32
+// matrix A (row stride lda) at (ar, ac), B a 16x8 block of the fp32 matrix B
+// (row stride ldb) at (bk, bn): both split into bf16 hi + lo, three products
+// (hi hi, lo hi, hi lo; the lo lo term and the lo parts' own rounding leave a
+// relative error near 2^-16). Fragment layouts of mma.m16n8k16: lane (g, t) =
+// (lane / 4, lane % 4) holds A rows g, g + 8 at columns 2t, 2t + 1, 2t + 8,
+// 2t + 9, and B rows 2t, 2t + 1, 2t + 8, 2t + 9 at column g.
+__device__ __forceinline__ void mma16x8_split(float (&d)[4], const float* A, int lda, int ar,
+                                              int ac, const float* B, int ldb, int bk, int bn,
+                                              int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* a0 = A + (ar + g) * lda + ac + 2 * t;
+  const float2 x0 = *reinterpret_cast<const float2*>(a0);
+  const float2 x1 = *reinterpret_cast<const float2*>(a0 + 8 * lda);
+  const float2 x2 = *reinterpret_cast<const float2*>(a0 + 8);
+  const float2 x3 = *reinterpret_cast<const float2*>(a0 + 8 * lda + 8);
+  uint32_t ah[4], al[4];
+  ptx::split_pair(x0.x, x0.y, ah[0], al[0]);
+  ptx::split_pair(x1.x, x1.y, ah[1], al[1]);
+  ptx::split_pair(x2.x, x2.y, ah[2], al[2]);
+  ptx::split_pair(x3.x, x3.y, ah[3], al[3]);
+  const float* b0 = B + (bk + 2 * t) * ldb + bn + g;
+  uint32_t bh0, bl0, bh1, bl1;
+  ptx::split_pair(b0[0], b0[ldb], bh0, bl0);
+  ptx::split_pair(b0[8 * ldb], b0[9 * ldb], bh1, bl1);
+  ptx::mma_bf16_16816(d, ah, bh0, bh1);
+  ptx::mma_bf16_16816(d, al, bh0, bh1);
+  ptx::mma_bf16_16816(d, ah, bl0, bl1);
+}
+
+// Stores s * D of a 16x8 tile at (r0, c0) of the fp32 matrix M (row stride ld).
+__device__ __forceinline__ void store16x8(float* M, int ld, int r0, int c0, const float (&d)[4],
+                                          float s, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float* m = M + (r0 + g) * ld + c0 + 2 * t;
+  *reinterpret_cast<float2*>(m) = make_float2(s * d[0], s * d[1]);
+  *reinterpret_cast<float2*>(m + 8 * ld) = make_float2(s * d[2], s * d[3]);
+}
+
+// Levels 1 and 2 as split-bf16 mma.sync products (same blocks and order as
+// inverse_levels12): level 1 on warps 0-3 (block pair w / 2, 8-column tile
+// w % 2), level 2 on all 8 warps (16-row tile w / 4, 8-column tile w % 4).
+// The scratch T holds the 16x16 level-1 products in rows 0-31, columns 0-15,
+// then the 32x32 level-2 product.
+template <int LDL, int LDX>
+__device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, float* T, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  constexpr int LDT = 36;
+  {
+    const int which = warp >> 1, nt = warp & 1;
+    const int I = 16 * (2 * which + 1), J = I - 16;
+    if (warp < 4) {                                   // T_w = L[I, J] X[J, J]
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16x8_split(d, L, LDL, I, J, X, LDX, J, J + 8 * nt, lane);
+      store16x8(T, LDT, 16 * which, 8 * nt, d, 1.f, lane);
+    }
+    __syncthreads();
+    if (warp < 4) {                                   // X[I, J] = -X[I, I] T_w
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16x8_split(d, X, LDX, I, I, T, LDT, 16 * which, 8 * nt, lane);
+      store16x8(X, LDX, I, J + 8 * nt, d, -1.f, lane);
+    }
+  }
+  __syncthreads();
+  const int mt = warp >> 2, nt = warp & 3;
+  {                                                   // T = L[32:64, 0:32] X[0:32, 0:32]
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8_split(d, L, LDL, 32 + 16 * mt, 0, X, LDX, 0, 8 * nt, lane);
+    mma16x8_split(d, L, LDL, 32 + 16 * mt, 16, X, LDX, 16, 8 * nt, lane);
+    store16x8(T, LDT, 16 * mt, 8 * nt, d, 1.f, lane);
+  }
+  __syncthreads();
+  {                                                   // X[32:64, 0:32] = -X[32:64, 32:64] T
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8_split(d, X, LDX, 32 + 16 * mt, 32, T, LDT, 0, 8 * nt, lane);
+    mma16x8_split(d, X, LDX, 32 + 16 * mt, 48, T, LDT, 16, 8 * nt, lane);
+    store16x8(X, LDX, 32 + 16 * mt, 8 * nt, d, -1.f, lane);
+  }
+}
+
+// L: [64][LDL] fp32; X: [64][LDX] fp32; T: scratch [32][36] fp32. Levels 1
+// and 2 on the tensor cores (inverse_levels12_mma): X then carries a relative
+// error near 2^-16, the size of the residual the callers' own hi/lo split of X
+// leaves.
 template <int LDL, int LDX>
 __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, float* T, int tid) {
   if (tid < 64) {
@@ -114,7 +199,7 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, f
     inverse_level0_store<LDX>(X, xd, tid);
   }
   __syncthreads();
-  inverse_levels12<LDL, LDX>(L, X, T, tid);
+  inverse_levels12_mma<LDL, LDX>(L, X, T, tid);
 }
 
 }  // namespace fast
