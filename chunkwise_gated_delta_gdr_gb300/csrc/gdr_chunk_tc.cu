@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
     // SSD: beta = 1 on real rows.
     bv = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
   }
-  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  if (warp == 1) tmem_alloc(tslot, TMEM_COLS);   // warp 0 is issuing the loads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -303,8 +303,10 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
 
-  // A_qk hi / lo out by TMA; the per-row factors of the state pass.
-  if (tid == 0) {
+  // A_qk hi / lo out by TMA and the per-row factors of the state pass, on
+  // warps 2-7 while warps 0-1 run level 0 of the inverse.
+  constexpr int kRowTid = 64;          // first thread of the row-factor warps
+  if (tid == kRowTid) {
     tma_store3(&maps.aq2, smem_u32(sm + OFF_AQS), 0, 0, idx);
     tma_store3(&maps.aq2, smem_u32(sm + OFF_AQS) + 8192, 0, C, idx);
     bulk_commit();
@@ -312,17 +314,18 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   {
     float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
     const float gl = G[C - 1];
-    if (tid < C) {
-      vec[tid] = p.scale * nq[tid] * __expf(G[tid]);
-      vec[C + tid] = bb[tid] * nk[tid] * __expf(gl - G[tid]);
-      cfac[tid] = __expf(G[tid]) * nk[tid];   // column factor of X' = X diag(exp(G) |k|^-1)
+    const int e = tid - kRowTid;
+    if (e >= 0 && e < C) {
+      vec[e] = p.scale * nq[e] * __expf(G[e]);
+      vec[C + e] = bb[e] * nk[e] * __expf(gl - G[e]);
+      cfac[e] = __expf(G[e]) * nk[e];   // column factor of X' = X diag(exp(G) |k|^-1)
     }
-    if (tid < K) vec[2 * C + tid] = __expf(gl);
+    if (e >= 0 && e < K) vec[2 * C + e] = __expf(gl);
   }
 
   // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
   unit_lower_inverse64<LDL, LDX>(L, X, T, tid);
-  if (tid == 0) bulk_wait_read<0>();   // the A_qk staging is read before XU overwrites it
+  if (tid == kRowTid) bulk_wait_read<0>();   // the A_qk staging is read before XU overwrites it
   __syncthreads();   // X complete; L and the A_qk staging are dead from here on
 
   // ---- A operands XW = [X' hi/lo], XU = [X hi/lo] (rows interleaved, see stacked_row)
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
     bulk_commit();
     bulk_wait_read<0>();                  // staging read before the CTA's smem is released
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
