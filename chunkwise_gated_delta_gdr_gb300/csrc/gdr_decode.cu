@@ -14,10 +14,11 @@
 // Main kernel (V <= 128 and a multiple of 4, state 16-byte aligned): one
 // persistent CTA per SM walks the heads. A producer warp streams each head's
 // whole state (K x V fp32, one TMA box of up to 512-byte rows) through a
-// three-stage shared-memory ring and stores the finished state back by TMA, so
-// about 190 KB per SM are in flight; 16 compute warps each hold 8 rows x 4
-// columns in registers while they apply the tokens. (Boxes of 128-byte rows
-// were served several times slower.)
+// three-stage shared-memory ring, so about 190 KB per SM are in flight; 16
+// compute warps each take 8 rows x 4 columns into registers, release the stage
+// at once (the producer refills it while they apply the tokens) and write the
+// finished state back with coalesced 128-byte stores from registers. (Boxes of
+// 128-byte rows were served several times slower.)
 //
 // Fallback kernel (any V, K <= 256): one CTA per (V tile of 32 columns, hv, b),
 // 16 warps: warp w holds state rows [R w, R w + R) of the tile's columns
@@ -207,32 +208,27 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
 
   if (warp == CW) {
     // ---------------------------------------------------------------- producer
+    // Stage s takes plane i once the compute warps hold plane i - STAGES in
+    // registers (completion i / STAGES - 1 of done[s]).
     if (lane == 0) {
       const uint32_t tbytes = (uint32_t)K * V * 4;
-      for (int i = 0; i < my + STAGES && ok; ++i) {
+      for (int i = 0; i < my && ok; ++i) {
         const int s = i % STAGES;
-        if (i >= STAGES) {
-          // Plane i - STAGES is finished in stage s: store it, then reuse the stage.
-          ok = mbar_wait(&done[s], ((i / STAGES) - 1) & 1, kWaitLimit);
-          if (!ok) break;
-          tma_store3(&smap, smem_u32(sm + s * TILE), 0, 0, blockIdx.x + (i - STAGES) * gridDim.x);
-          bulk_commit();
-          bulk_wait_read<0>();
-        }
-        if (i < my) {
-          mbar_expect_tx(&full[s], tbytes);
-          tma_load3(smem_u32(sm + s * TILE), &smap, 0, 0, blockIdx.x + i * gridDim.x, &full[s]);
-        }
+        if (i >= STAGES) ok = mbar_wait(&done[s], ((i / STAGES) - 1) & 1, kWaitLimit);
+        if (!ok) break;
+        mbar_expect_tx(&full[s], tbytes);
+        tma_load3(smem_u32(sm + s * TILE), &smap, 0, 0, blockIdx.x + i * gridDim.x, &full[s]);
       }
-      bulk_wait<0>();
     }
   } else {
     // ------------------------------------------------------------ compute warps
     // Warp w holds rows [8 w, 8 w + 8) of columns lane + 32 m (m < 4).
+    // Per token two CTA barriers: C (column partials written) and D (the
+    // delta-rule write per column written, and the next token's inputs staged).
+    // Every warp forms the token's norms itself from the staged k and q.
     // Threads 0-127 load a token's inputs (channel / column tid) into registers
-    // one head ahead: the next head's first token while this head finishes.
-    // (Staging them in the producer warp, or two heads ahead in registers,
-    // measured slower.)
+    // one token ahead (across heads too) and stage them between C and D: every
+    // read of the staged inputs of a token happens before its barrier C.
     const int r0 = warp * ROWS;
     struct Tok {
       float k, q, g, v, beta;
@@ -251,14 +247,25 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
       if (tid < V) x.v = ld_x(a.v, (bt * a.HV + hv) * V + tid, a.in_bf16);
       if (tid == 0) x.beta = a.beta[bt * a.HV + hv];
     };
+    auto stage_tok = [&](const Tok& x) {
+      if (tid < 128) {
+        kr[tid] = x.k;
+        qr[tid] = x.q;
+        dec[tid] = tid < K ? expf(x.g) : 0.f;
+        if (tid == 0) tok[0] = x.beta;
+      }
+    };
     Tok nx;
-    if (my > 0) load_tok(blockIdx.x, 0, nx);
+    if (my > 0) {
+      load_tok(blockIdx.x, 0, nx);
+      stage_tok(nx);
+    }
+    nb_sync(1, CW * 32);                               // the first token is staged
     for (int i = 0; i < my; ++i) {
       const int s = i % STAGES;
       const int plane = blockIdx.x + i * gridDim.x;
       const int b = plane / a.HV, hv = plane % a.HV;
       const float* tile = reinterpret_cast<const float*>(sm + s * TILE);   // [K][V] fp32
-      float* tilew = reinterpret_cast<float*>(sm + s * TILE);
       ok = ok && mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit);
       float S[ROWS][CPL];
 #pragma unroll
@@ -268,41 +275,35 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
           const int c = lane + 32 * m;
           S[r][m] = (r0 + r < K && c < V) ? tile[(r0 + r) * V + c] : 0.f;
         }
+      // The head is in registers: stage s may be refilled.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&done[s]);
       for (int tk = 0; tk < a.T; ++tk) {
         const size_t bt = (size_t)b * a.T + tk;
-        Tok x = nx;
-        if (tk > 0) load_tok(plane, tk, x);
-        if (tid < 128) {
-          kr[tid] = x.k;
-          qr[tid] = x.q;
-          dec[tid] = tid < K ? expf(x.g) : 0.f;
-          if (tid == 0) tok[2] = x.beta;
-        }
-        nb_sync(1, CW * 32);
-        if (warp == 0) {
-          float sk = 0.f, sq = 0.f, sqk = 0.f;
+        const Tok x = nx;                              // this token (staged)
+        const bool more = tk + 1 < a.T || i + 1 < my;
+        if (tk + 1 < a.T)
+          load_tok(plane, tk + 1, nx);
+        else if (i + 1 < my)
+          load_tok(plane + gridDim.x, 0, nx);
+        // Norms of the staged k and q (zero past K), every warp for itself.
+        float sk = 0.f, sq = 0.f, sqk = 0.f;
 #pragma unroll
-          for (int c = lane; c < 128; c += 32) {
-            sk = fmaf(kr[c], kr[c], sk);
-            sq = fmaf(qr[c], qr[c], sq);
-            sqk = fmaf(qr[c], kr[c], sqk);
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
-          }
-          if (lane == 0) {
-            const float nk = a.use_l2 ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
-            const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
-            tok[0] = nk;
-            tok[1] = nq;
-            tok[3] = nq * nk * sqk;
-          }
+        for (int c = lane; c < 128; c += 32) {
+          const float kc = kr[c], qc = qr[c];
+          sk = fmaf(kc, kc, sk);
+          sq = fmaf(qc, qc, sq);
+          sqk = fmaf(qc, kc, sqk);
         }
-        nb_sync(1, CW * 32);
-        const float nk = tok[0], nq = tok[1], beta = tok[2], qk = tok[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          sk += __shfl_xor_sync(0xffffffffu, sk, o);
+          sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
+        }
+        const float nk = a.use_l2 ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
+        const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
+        const float qk = nq * nk * sqk, beta = tok[0];
         // Decay, then this warp's share of k^T (D S) and q^T (D S) per column.
         const float4 kk0 = *reinterpret_cast<const float4*>(kr + r0);
         const float4 kk1 = *reinterpret_cast<const float4*>(kr + r0 + 4);
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
           }
           red[warp][lane + 32 * m] = make_float2(pu, po);
         }
-        nb_sync(1, CW * 32);
+        nb_sync(1, CW * 32);                           // C: partials written
         if (tid < 128) {
           // Column tid: sum the warps' partials, form the write and the output.
           float u = 0.f, oq = 0.f;
@@ -344,27 +345,25 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
             else
               static_cast<float*>(a.out)[off] = o;
           }
+          if (more) stage_tok(nx);                     // the next token's inputs
         }
-        nb_sync(1, CW * 32);
+        nb_sync(1, CW * 32);                           // D: writes and next inputs visible
 #pragma unroll
         for (int m = 0; m < CPL; ++m) {
           const float wk = wcol[lane + 32 * m];
 #pragma unroll
           for (int r = 0; r < ROWS; ++r) S[r][m] = fmaf(kv[r], wk, S[r][m]);
         }
-        nb_sync(1, CW * 32);   // kr / qr / dec / red / wcol are rewritten by the next token
       }
+      // Row r0 + r of the head: each warp store is one 128-byte segment.
+      float* dst = a.state + (size_t)plane * K * V;
 #pragma unroll
       for (int r = 0; r < ROWS; ++r)
 #pragma unroll
         for (int m = 0; m < CPL; ++m) {
           const int c = lane + 32 * m;
-          if (r0 + r < K && c < V) tilew[(r0 + r) * V + c] = S[r][m];
+          if (r0 + r < K && c < V) dst[(size_t)(r0 + r) * V + c] = S[r][m];
         }
-      fence_async_shared();                            // the TMA store reads the tile
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&done[s]);
-      if (i + 1 < my) load_tok(plane + gridDim.x, 0, nx);
     }
   }
   if (!ok && a.error_word) atomicOr(a.error_word, 16u);
