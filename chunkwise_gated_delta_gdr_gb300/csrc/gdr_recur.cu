@@ -69,6 +69,7 @@ constexpr unsigned int kErrChainWait = 4u, kErrOutputWait = 8u;
 // chunks copied since its previous release.
 namespace ch {
 constexpr int CW = 4;
+static_assert(K / 32 == CW && C / 16 == CW, "one channel pair and one j-step of 16 per chain warp");
 // Operand stage (three-deep ring): -W hi, -W lo and the chunk's k rows
 // ([64][128] bf16, two 128-byte swizzled 8 KB boxes each), the U tile [64][16]
 // fp32 and VEC (qscale, kscale, gamma).
@@ -211,13 +212,13 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         const int u = lane + 32 * i, pl = u >> 7, row = (u >> 3) & 15, c = u & 7;
         val[i] = *reinterpret_cast<const uint4*>(xr + pl * 2048 + row * 128 + ((c ^ (row & 7)) << 4));
       }
+      nb_arrive(8 + s, SYNC);                          // buffer s read: it may be overwritten
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int u = lane + 32 * i, pl = u >> 7, row = (u >> 3) & 15, c = u & 7;
         *reinterpret_cast<uint4*>(blk + Xchg::R_HI + pl * (Xchg::R_LO - Xchg::R_HI) +
                                   (size_t)(v0 + row) * (C * 2) + c * 16) = val[i];
       }
-      nb_arrive(8 + s, SYNC);                          // buffer s may be overwritten
       __syncwarp();                                    // orders the lanes' stores before:
       if (lane == 0) st_release_cta_shared(done, (unsigned int)(n + 1));
     }
@@ -274,22 +275,22 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       uint8_t* xrh = sm + XR + s * XR_BUF;             // r^T hi; lo at + 2048
       if (n >= NXB) nb_sync(8 + s, SYNC);              // chunk n - NXB copied out of buffer s
       // S^T hi / lo by stmatrix: matrix i of call q is channel tile 2 q + i / 2,
-      // value rows 8 (i % 2) .. + 8.
+      // value rows 8 (i % 2) .. + 8. The registers stored are also this warp's
+      // A fragments of its own two k-steps (channels cw + 16 q ...) of the r
+      // products, which therefore run before the barrier.
+      uint32_t oah[2][4], oal[2][4];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        uint32_t hi[4], lo[4];
-        split_pair(S[2 * q][0], S[2 * q][1], hi[0], lo[0]);
-        split_pair(S[2 * q][2], S[2 * q][3], hi[1], lo[1]);
-        split_pair(S[2 * q + 1][0], S[2 * q + 1][1], hi[2], lo[2]);
-        split_pair(S[2 * q + 1][2], S[2 * q + 1][3], hi[3], lo[3]);
+        split_pair(S[2 * q][0], S[2 * q][1], oah[q][0], oal[q][0]);
+        split_pair(S[2 * q][2], S[2 * q][3], oah[q][1], oal[q][1]);
+        split_pair(S[2 * q + 1][0], S[2 * q + 1][1], oah[q][2], oal[q][2]);
+        split_pair(S[2 * q + 1][2], S[2 * q + 1][3], oah[q][3], oal[q][3]);
         const int mi = lane >> 3;
         const uint32_t a = smem_u32(xsh) + tile16_off(8 * (mi & 1) + (lane & 7), cw + 16 * q + 8 * (mi >> 1));
-        stsm_x4(a, hi[0], hi[1], hi[2], hi[3]);
-        stsm_x4(a + 4096, lo[0], lo[1], lo[2], lo[3]);
+        stsm_x4(a, oah[q][0], oah[q][1], oah[q][2], oah[q][3]);
+        stsm_x4(a + 4096, oal[q][0], oal[q][1], oal[q][2], oal[q][3]);
       }
       ok = ok && mbar_wait(&full[st], (n / NST) & 1, kWaitLimit);
-      nb_sync(1, CW * 32);                             // S^T complete
-      nb_arrive(2 + s, SYNC);
       // r^T = U^T + S^T (-W)^T, j in [jw, jw + 16)
       float Rhh[2][4], Rlh[2][4], Rhl[2][4];
 #pragma unroll
@@ -304,8 +305,27 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         for (int e = 0; e < 4; ++e) Rlh[jt][e] = Rhl[jt][e] = 0.f;
       }
       if (!p.ssd) {                                    // SSD: r = U
+        // This warp's own channels (k-steps 2 warp, 2 warp + 1) from registers.
 #pragma unroll
-        for (int ks2 = 0; ks2 < K / 16; ks2 += 2) {
+        for (int jt = 0; jt < 2; ++jt) {
+          uint32_t wh[4], wl[4];
+          ldsm_x4(wh, tile_addr(w_hi, jw + 8 * jt + brow, cw + bcol));
+          ldsm_x4(wl, tile_addr(w_lo, jw + 8 * jt + brow, cw + bcol));
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            mma_bf16_16816(Rhh[jt], oah[h2], wh[2 * h2], wh[2 * h2 + 1]);
+            mma_bf16_16816(Rlh[jt], oal[h2], wh[2 * h2], wh[2 * h2 + 1]);
+            mma_bf16_16816(Rhl[jt], oah[h2], wl[2 * h2], wl[2 * h2 + 1]);
+          }
+        }
+      }
+      nb_sync(1, CW * 32);                             // S^T complete
+      nb_arrive(2 + s, SYNC);
+      if (!p.ssd) {
+        // The other warps' channels, from the published S^T.
+#pragma unroll
+        for (int kp = 1; kp < CW; ++kp) {
+          const int ks2 = 2 * ((warp + kp) & (CW - 1));
           uint32_t ah[2][4], al[2][4];
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
@@ -326,6 +346,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
           }
         }
       }
+      float Dl[4][4];
       {
         // r^T and rho^T = (kscale r)^T hi / lo by stmatrix: matrix i is j tile
         // i / 2, value rows 8 (i % 2) .. + 8.
@@ -349,23 +370,33 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         const uint32_t b = smem_u32(xp_hi + row * LDA + col);
         stsm_x4(b, ph[0], ph[1], ph[2], ph[3]);
         stsm_x4(b + 16 * LDA * 2, pl[0], pl[1], pl[2], pl[3]);
+        // S^T = gamma S^T + rho^T k, c in [cw, cw + 32); the scalar gate's decay
+        // gamma is the same on every channel. ph / pl are also this warp's A
+        // fragments of its own k-step (j in [jw, jw + 16)), taken before the barrier.
+        const float gm = gam[0];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            S[nt][e] *= gm;
+            Dl[nt][e] = 0.f;
+          }
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          uint32_t kh[4];
+          ldsm_x4_t(kh, tile_addr(k_t, jw + arow, kcol + 16 * np));
+          mma_bf16_16816(S[2 * np], ph, kh[0], kh[1]);
+          mma_bf16_16816(S[2 * np + 1], ph, kh[2], kh[3]);
+          mma_bf16_16816(Dl[2 * np], pl, kh[0], kh[1]);
+          mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
+        }
       }
       nb_sync(1, CW * 32);                             // r^T, rho^T complete
       nb_arrive(5 + s, SYNC);
-      // S^T = gamma S^T + rho^T k, c in [cw, cw + 32); the scalar gate's decay
-      // gamma is the same on every channel.
-      const float gm = gam[0];
+      // The other warps' j-steps, from the published rho^T.
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S[nt][e] *= gm;
-      float Dl[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) Dl[nt][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk) {
+      for (int kp = 1; kp < CW; ++kp) {
+        const int kk = (warp + kp) & (CW - 1);
         uint32_t ph[4], pl[4];
         ldsm_x4(ph, smem_u32(xp_hi + arow * LDA + 16 * kk + acol));
         ldsm_x4(pl, smem_u32(xp_lo + arow * LDA + 16 * kk + acol));
