@@ -54,7 +54,7 @@ namespace {
 using namespace ptx;
 
 constexpr int VTILES = V / VT;          // chains per sequence
-constexpr int THREADS = 224;            // 7 warps in either role
+constexpr int THREADS = 256;            // 8 warps in either role
 constexpr int LDA = C + 8;              // bf16 row stride of the rho^T tile (144 B)
 constexpr long kWaitLimit = 1L << 24;   // mbarrier polls before a wait gives up
 constexpr long kFlagLimit = 1L << 24;   // flag polls (64 ns apart) before a wait gives up
@@ -66,7 +66,8 @@ constexpr unsigned int kErrChainWait = 4u, kErrOutputWait = 8u;
 // unit is busy with them; the published tiles leave through plain stores of
 // warp 5). Warp 6 raises the chain's flag: a GPU-scope release costs about as
 // much as a chunk step, so it runs apart from the copies and covers all
-// chunks copied since its previous release.
+// chunks copied since its previous release. Warp 7 (gate) confirms each
+// chunk's operand stage ahead of the chain warps.
 namespace ch {
 constexpr int CW = 4;
 static_assert(K / 32 == CW && C / 16 == CW, "one channel pair and one j-step of 16 per chain warp");
@@ -85,14 +86,17 @@ constexpr int XS = NST * STAGE, XR = XS + NXB * XS_BUF, XP = XR + NXB * XR_BUF, 
 constexpr int DONE = BAR + 2 * NST * 8;     // chunks copied out (u32)
 constexpr int BYTES = DONE + 16;
 constexpr int SYNC = CW * 32 + 32;         // chain warps + copy warp
-// Named barriers: 1 chain warps; 2 + s S^T of buffer s published; 5 + s r^T
-// of buffer s published; 8 + s buffer s copied out (s < NXB).
+// Named barriers: 1 chain warps (S^T complete); 11 chain warps + gate warp
+// (r^T complete, and the next chunk's operands are in their stage); 2 + s S^T
+// of buffer s published; 5 + s r^T of buffer s published; 8 + s buffer s
+// copied out (s < NXB).
+constexpr int GATE_SYNC = CW * 32 + 32;     // chain warps + gate warp
 }  // namespace ch
 
 // ----------------------------------------------------------------- output role
 // Warp 0 issues the TMA loads, warp 1 the MMAs (and owns the TMEM), warps 2-5
 // run the epilogue (warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)),
-// warp 6 has no work.
+// warps 6 and 7 have no work.
 namespace ou {
 // Operand stage (double-buffered), 128-byte swizzled K-major tiles: q [64 i]
 // [128 k] (two boxes), A_qk hi / lo [64 i][64 j], S^T hi / lo [64 v][128 k]
@@ -245,6 +249,18 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         }
       }
     }
+  } else if (warp == CW + 3) {
+    // ------------------------------------------------------------------- gate
+    // Joins the chain warps' r^T barrier of step n once chunk n + 1's operands
+    // are in their stage: the chain warps then start step n + 1 without
+    // testing the stage's barrier themselves (the test costs about as much as
+    // a barrier). It joins every generation, also after a wait gave up.
+    for (int n = 0; n < p.N; ++n) {
+      if (n + 1 < p.N && lane == 0)
+        ok = ok && mbar_wait(&full[(n + 1) % NST], ((n + 1) / NST) & 1, kWaitLimit);
+      __syncwarp();
+      nb_sync(11, GATE_SYNC);
+    }
   } else {
     // ------------------------------------------------------------ chain warps
     const int jw = 16 * warp, cw = 32 * warp;          // r^T j-tiles, state channels
@@ -290,7 +306,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         stsm_x4(a, oah[q][0], oah[q][1], oah[q][2], oah[q][3]);
         stsm_x4(a + 4096, oal[q][0], oal[q][1], oal[q][2], oal[q][3]);
       }
-      ok = ok && mbar_wait(&full[st], (n / NST) & 1, kWaitLimit);
+      if (n == 0) ok = ok && mbar_wait(&full[st], 0, kWaitLimit);   // later chunks: the gate warp
       // r^T = U^T + S^T (-W)^T, j in [jw, jw + 16)
       float Rhh[2][4], Rlh[2][4], Rhl[2][4];
 #pragma unroll
@@ -391,7 +407,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
           mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
         }
       }
-      nb_sync(1, CW * 32);                             // r^T, rho^T complete
+      nb_sync(11, GATE_SYNC);                          // r^T, rho^T complete; chunk n + 1 in place
       nb_arrive(5 + s, SYNC);
       // The other warps' j-steps, from the published rho^T.
 #pragma unroll
