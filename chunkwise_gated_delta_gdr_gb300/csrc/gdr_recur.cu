@@ -77,19 +77,21 @@ static_assert(K / 32 == CW && C / 16 == CW, "one channel pair and one j-step of 
 constexpr int W_HI = 0, W_LO = 16384, KT = 32768, U = 49152, VEC = 53248, STAGE = 55296;
 constexpr uint32_t TX = 32768 + 16384 + 4096 + 1024;
 constexpr int NST = 3;
-// Published tiles (three buffers), 128-byte swizzled: S^T hi, lo as two
+// Published tiles (NXB buffers), 128-byte swizzled: S^T hi, lo as two
 // [16 v][64 k] boxes each; r^T hi, lo as one [16 v][64 j] box each. rho^T
 // (chain-internal) is a padded [2][16][LDA] bf16 tile.
 constexpr int XS_BUF = 2 * 2 * 2048, XR_BUF = 2 * 2048, XP_BYTES = 2 * 16 * LDA * 2;
-constexpr int NXB = 3;                     // published-tile buffers
+constexpr int NXB = 4;                     // published-tile buffers
 constexpr int XS = NST * STAGE, XR = XS + NXB * XS_BUF, XP = XR + NXB * XR_BUF, BAR = XP + XP_BYTES;
 constexpr int DONE = BAR + 2 * NST * 8;     // chunks copied out (u32)
 constexpr int BYTES = DONE + 16;
 constexpr int SYNC = CW * 32 + 32;         // chain warps + copy warp
-// Named barriers: 1 chain warps (S^T complete); 11 chain warps + gate warp
-// (r^T complete, and the next chunk's operands are in their stage); 2 + s S^T
-// of buffer s published; 5 + s r^T of buffer s published; 8 + s buffer s
-// copied out (s < NXB).
+// Named barriers: 1 chain warps (S^T complete); BAR_R chain warps + gate warp
+// (r^T complete, and the next chunk's operands are in their stage); BAR_XS + s
+// S^T of buffer s published; BAR_XR + s r^T of buffer s published; BAR_CP + s
+// buffer s copied out (s < NXB).
+constexpr int BAR_XS = 2, BAR_XR = BAR_XS + NXB, BAR_CP = BAR_XR + NXB, BAR_R = BAR_CP + NXB;
+static_assert(BAR_R < 16, "named barrier ids");
 constexpr int GATE_SYNC = CW * 32 + 32;     // chain warps + gate warp
 }  // namespace ch
 
@@ -194,7 +196,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
     for (int n = 0; n < p.N; ++n) {
       const int s = n % NXB;
       uint8_t* blk = p.xchg + (size_t)(chunk0 + n) * Xchg::BYTES;
-      nb_sync(2 + s, SYNC);
+      nb_sync(BAR_XS + s, SYNC);
       const uint8_t* xs = sm + XS + s * XS_BUF;
       uint4 val[16];
 #pragma unroll
@@ -209,14 +211,14 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         *reinterpret_cast<uint4*>(blk + Xchg::S_HI + pl * (Xchg::S_LO - Xchg::S_HI) +
                                   (size_t)(v0 + row) * (K * 2) + c * 16) = val[i];
       }
-      nb_sync(5 + s, SYNC);
+      nb_sync(BAR_XR + s, SYNC);
       const uint8_t* xr = sm + XR + s * XR_BUF;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {                    // 2 planes x 16 rows x 8 chunks
         const int u = lane + 32 * i, pl = u >> 7, row = (u >> 3) & 15, c = u & 7;
         val[i] = *reinterpret_cast<const uint4*>(xr + pl * 2048 + row * 128 + ((c ^ (row & 7)) << 4));
       }
-      nb_arrive(8 + s, SYNC);                          // buffer s read: it may be overwritten
+      nb_arrive(BAR_CP + s, SYNC);                          // buffer s read: it may be overwritten
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int u = lane + 32 * i, pl = u >> 7, row = (u >> 3) & 15, c = u & 7;
@@ -259,7 +261,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       if (n + 1 < p.N && lane == 0)
         ok = ok && mbar_wait(&full[(n + 1) % NST], ((n + 1) / NST) & 1, kWaitLimit);
       __syncwarp();
-      nb_sync(11, GATE_SYNC);
+      nb_sync(BAR_R, GATE_SYNC);
     }
   } else {
     // ------------------------------------------------------------ chain warps
@@ -289,7 +291,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       const float* gam = ks + C;
       uint8_t* xsh = sm + XS + s * XS_BUF;             // S^T hi; lo at + 4096
       uint8_t* xrh = sm + XR + s * XR_BUF;             // r^T hi; lo at + 2048
-      if (n >= NXB) nb_sync(8 + s, SYNC);              // chunk n - NXB copied out of buffer s
+      if (n >= NXB) nb_sync(BAR_CP + s, SYNC);              // chunk n - NXB copied out of buffer s
       // S^T hi / lo by stmatrix: matrix i of call q is channel tile 2 q + i / 2,
       // value rows 8 (i % 2) .. + 8. The registers stored are also this warp's
       // A fragments of its own two k-steps (channels cw + 16 q ...) of the r
@@ -336,7 +338,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
         }
       }
       nb_sync(1, CW * 32);                             // S^T complete
-      nb_arrive(2 + s, SYNC);
+      nb_arrive(BAR_XS + s, SYNC);
       if (!p.ssd) {
         // The other warps' channels, from the published S^T.
 #pragma unroll
@@ -407,8 +409,8 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
           mma_bf16_16816(Dl[2 * np + 1], pl, kh[2], kh[3]);
         }
       }
-      nb_sync(11, GATE_SYNC);                          // r^T, rho^T complete; chunk n + 1 in place
-      nb_arrive(5 + s, SYNC);
+      nb_sync(BAR_R, GATE_SYNC);                       // r^T, rho^T complete; chunk n + 1 in place
+      nb_arrive(BAR_XR + s, SYNC);
       // The other warps' j-steps, from the published rho^T.
 #pragma unroll
       for (int kp = 1; kp < CW; ++kp) {
@@ -434,7 +436,7 @@ __device__ __forceinline__ void chain_role(const Maps& maps, const Params& p, ui
       if (lane == 0) mbar_arrive(&empty[st]);          // this warp is done with stage st
     }
     // Balance the copy-out barrier generations of the last NXB chunks.
-    for (int n = (p.N >= NXB ? p.N - NXB : 0); n < p.N; ++n) nb_sync(8 + n % NXB, SYNC);
+    for (int n = (p.N >= NXB ? p.N - NXB : 0); n < p.N; ++n) nb_sync(BAR_CP + n % NXB, SYNC);
     if (p.sT) {
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
