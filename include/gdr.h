@@ -271,6 +271,7 @@ size_t gdr_ssd_chunk_fwd_workspace_size(const gdr_dims* dims, int chunk_size, in
  *              multiple of P * chunk_size (else GDR_ERR_UNSUPPORTED), and the
  *              B P sequences of T / P tokens must be a supported problem.
  *   workspace  gdr_chunk_fwd_segmented_workspace_size() bytes (0: unsupported).
+ *   final_state may alias initial_state, as for gdr_chunk_fwd.
  * Results equal gdr_chunk_fwd's up to rounding; errors as for gdr_chunk_fwd
  * (gdr_stream_status reads this workspace).
  */

@@ -474,3 +474,57 @@ def test_segmented_one_segment_is_chunk_fwd():
     torch.cuda.synchronize()
     po, pS = gpu_run(x, w)
     assert np.array_equal(o.cpu().numpy(), po) and np.array_equal(S.cpu().numpy(), pS)
+
+
+def test_segmented_aliased_state_bf16_output():
+    """final_state aliasing initial_state and bf16 output (two batches, GQA): the
+    bf16 output is the fp32 output rounded, the state the same bits."""
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], B=2, T=512, H=1, HV=2, s0_std=0.02)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o32, S32 = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], d["s0"],
+                                       segments=4, chunk_size=w.C, scale=w.scale,
+                                       out_dtype=torch.float32)
+    state = d["s0"].clone()
+    o16, S16 = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], state,
+                                       segments=4, chunk_size=w.C, scale=w.scale,
+                                       out_dtype=torch.bfloat16, final_state=state)
+    torch.cuda.synchronize()
+    assert S16.data_ptr() == state.data_ptr()
+    ref = o32.to(torch.bfloat16).float().cpu().numpy()
+    assert np.all(np.abs(o16.float().cpu().numpy() - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
+    assert np.array_equal(state.cpu().numpy(), S32.cpu().numpy())
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale)
+    tol = tol_for(w)
+    assert relerr(o32.cpu().numpy(), ro) <= tol and relerr(state.cpu().numpy(), rS) <= tol
+
+
+def test_segmented_more_chains_than_sms():
+    """64 segments x 2 value heads x 8 column tiles = 1024 chains: the states-only
+    launches of the recurrence run in waves; the outputs-only launch covers every SM."""
+    w = gin.shrink(gin.WORKLOADS["gdn_long_t65000"], T=4096, H=1, HV=2)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], d["s0"],
+                                   segments=64, chunk_size=w.C, scale=w.scale,
+                                   out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], scale=w.scale)
+    tol = tol_for(w)
+    assert relerr(o.cpu().numpy(), ro) <= tol and relerr(S.cpu().numpy(), rS) <= tol
+
+
+def test_segmented_ungated():
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], T=512, H=2, HV=2, s0_std=0.02)
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], None, d["beta"], d["s0"], segments=4,
+                                   chunk_size=w.C, scale=w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    g0 = torch.zeros(w.B, w.T, w.HV, dtype=torch.float32)
+    ro, rS = oracle.recurrent(x["q"], x["k"], x["v"], g0, x["beta"], x["s0"], scale=w.scale)
+    tol = tol_for(w)
+    assert relerr(o.cpu().numpy(), ro) <= tol and relerr(S.cpu().numpy(), rS) <= tol
