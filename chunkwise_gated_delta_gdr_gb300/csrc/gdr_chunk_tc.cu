@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
   int* split_ok = reinterpret_cast<int*>(tslot + 1);   // decay factorisation allowed
+  uint64_t* bar_v = bar_tma + 3;                       // v tiles (read by MMA 3 only)
   uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
 
   // The input tiles are requested first: the thread that initialised the
@@ -117,14 +118,18 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   if (tid == 0) {
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_v, 1);
     mbar_fence_init();
-    mbar_expect_tx(bar_tma, 6 * 8192);
+    // k and q first (MMA 1 and the norms wait for them); v on its own barrier,
+    // waited for only by the MMA that reads it.
+    mbar_expect_tx(bar_tma, 4 * 8192);
     tma_load4(smem_u32(sm + OFF_K0), &maps.k, 0, h, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_K1), &maps.k, 64, h, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_Q0), &maps.q, 0, h, t0, b, bar_tma);
     tma_load4(smem_u32(sm + OFF_Q1), &maps.q, 64, h, t0, b, bar_tma);
-    tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_tma);
-    tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_tma);
+    mbar_expect_tx(bar_v, 2 * 8192);
+    tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_v);
+    tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_v);
   }
   // Gate and beta (plain loads into registers, in flight during the TMEM
   // allocation; zero past the end and for the ungated mode).
@@ -360,6 +365,10 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
   __syncthreads();
 
   // ---- MMA 2/3: D_W = XW k (TMEM cols 0-127), D_U = XU v (cols 128-255) ----------
+  if (ok && tid == 0) {
+    ok = mbar_wait(bar_v, 0, kWaitLimit);            // the v tiles (normally long arrived)
+    if (!ok) atomicOr(p.error_word, kErrTmaWait);
+  }
   if (ok && tid == 0) {
     tc_fence_after();
     constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
