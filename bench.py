@@ -1,13 +1,16 @@
 #!/usr/bin/env python3
 """Throughput benchmark of the chunkwise gated delta rule forward pass.
 
-One step = one full forward pass (chunk-local kernel + state recurrence) over
-the headline workload: B=1, T=4096, H=HV=12 heads, K=V=128, C=64, bf16 q/k/v,
-fp32 gate and beta, q/k L2-normalised in the kernel, fp32 output and fp32
-final state. Inputs are seeded synthetic tensors already resident in HBM; the
-L2 cache is flushed (a 512 MiB write) before every timed step.
+One step = one full forward pass (gdr_chunk_fwd: the chunk-local stage and the
+state recurrence) over the headline workload: B=1, T=4096, H=HV=12 heads,
+K=V=128, C=64, bf16 q/k/v, fp32 gate and beta, q/k L2-normalised in the kernel,
+output in the input dtype (bf16, as the optimisation script returns it) and an
+fp32 final state. The same forward with fp32 output is timed beside it. Inputs
+are seeded synthetic tensors already resident in HBM; the L2 cache is flushed
+(a 512 MiB write) before every timed step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--out-dtype bf16|fp32]
 
 With N > 1 (launched by torch.distributed.run) every rank runs the same
 workload on its own GPU as a shard of 12 value heads of a 12N-head layer
@@ -50,6 +53,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
+    ap.add_argument("--out-dtype", choices=["bf16", "fp32"], default="bf16",
+                    help="dtype of o in the timed forward (the other is timed beside it)")
     return ap.parse_args()
 
 
@@ -69,23 +74,25 @@ def workload(name):
     return gin.WORKLOADS[name or gin.HEADLINE]
 
 
-def config_of(w, world):
+def config_of(w, world, out_dtype="bf16"):
     return {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "HV": w.HV, "K": w.K, "V": w.V,
             "C": w.C, "gate": "scalar" if w.gate_mode == 0 else "per-key",
             "in_dtype": "bf16" if str(w.dtype).endswith("bfloat16") else "fp32",
-            "out_dtype": "fp32", "use_qk_l2norm": w.use_qk_l2norm,
+            "out_dtype": out_dtype, "use_qk_l2norm": w.use_qk_l2norm,
             "initial_state": w.s0_std is not None, "l2_flush": "512MiB write before each step",
             "parallelism": f"{world} rank(s), value heads sharded, no collective",
             **({"segments": w.segments} if getattr(w, "segments", 1) > 1 else {})}
 
 
-def algorithmic_bytes(w):
+def algorithmic_bytes(w, out_bytes=4):
+    """Compulsory HBM bytes of one forward: q, k (H heads), v, g, beta, o in its
+    dtype, the fp32 final state and the fp32 initial state when there is one."""
     BT = w.B * w.T
     qk = 2 * BT * w.H * w.K * 2
     v = BT * w.HV * w.V * 2
     g = BT * w.HV * (w.K if w.gate_mode else 1) * 4
     beta = BT * w.HV * 4
-    o = BT * w.HV * w.V * 4
+    o = BT * w.HV * w.V * out_bytes
     state = w.B * w.HV * w.K * w.V * 4
     return qk + v + g + beta + o + state + (state if w.s0_std is not None else 0)
 
@@ -232,50 +239,74 @@ def warm_l2_ms(step, stream, n):
 
 
 def run_reference(args, rank, world):
-    """The float64 oracle, as it stands, timed on the host cores. Each step is a
-    bounded sample of the workload: the first `ts` tokens of one (batch, head)
-    sequence, with `ts` sized so that the whole warm-up + timed run stays near
-    90 s of CPU time; the throughput is scaled to the full workload (the
-    recurrence costs the same per token and per sequence)."""
+    """The float64 oracle, as it stands, timed on the host cores: OpenMP over
+    all B x HV sequences of the workload, as many threads as cpu_baseline uses.
+    A step is the whole workload when warm-up + timed steps fit about 90 s,
+    else the first `ts` tokens of every sequence (all heads), sized to that
+    budget; ms_per_step is the measured wall time of the step that ran, and
+    the tokens/s are the tokens it processed over that time (the recurrence
+    costs the same per token, so the rate is the full workload's)."""
     if rank != 0:
         return 0
     import oracle
     from chunkwise_gated_delta_gdr_gb300 import inputs as gin
     w = workload(args.workload)
     x = gin.make_inputs(w)
+    ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    nseq = w.B * w.HV
+    threads = max(1, min(ncpu, nseq))
     cut = lambda ts: {n: (t[:, :ts].contiguous() if (t is not None and n != "s0") else t)
                       for n, t in x.items()}
-    # Calibrate: seconds per token of one sequence on one core.
-    cal = cut(min(w.T, 256))
+
+    def step(xs):
+        oracle.recurrent(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], xs["s0"],
+                         scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, nthreads=threads)
+
+    # Calibrate on a short prefix of every sequence, then size the step.
+    cal_ts = min(w.T, 256)
     t0 = time.perf_counter()
-    oracle.recurrent(cal["q"], cal["k"], cal["v"], cal["g"], cal["beta"], cal["s0"], scale=w.scale,
-                     use_qk_l2norm=w.use_qk_l2norm, sel=[0], nthreads=1)
-    per_token = (time.perf_counter() - t0) / min(w.T, 256)
+    step(cut(cal_ts))
+    per_token = (time.perf_counter() - t0) / cal_ts
     budget = 90.0 / max(1, args.warmup + args.steps)
     ts = int(max(32, min(w.T, budget / per_token)))
-    xs = cut(ts)
+    xs = x if ts == w.T else cut(ts)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.recurrent(xs["q"], xs["k"], xs["v"], xs["g"], xs["beta"], xs["s0"], scale=w.scale,
-                         use_qk_l2norm=w.use_qk_l2norm, sel=[0], nthreads=1)
+        step(xs)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    per_step = statistics.mean(times) * (w.T / ts) * (w.B * w.HV)   # seconds for the workload
-    value = w.B * w.T / per_step
-    sample = (f"first {ts} tokens of 1 of {w.B * w.HV} (batch, head) sequences per step, float64 "
-              f"token recurrence on 1 core, scaled to the full workload ({w.B}x{w.T} tokens x "
-              f"{w.HV} heads)")
+    per_step = statistics.mean(times)
+    value = w.B * ts / per_step
+    sample = ("whole workload" if ts == w.T else f"first {ts} of {w.T} tokens") + \
+        (f" of all {nseq} (batch, head) sequences per step ({w.B}x{ts} tokens x {w.HV} heads), "
+         f"float64 token recurrence, OpenMP over the sequences, {threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w, 1),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "data": "synthetic", "config": config_of(w, 1, "f64"),
+            "full_workload_ms": per_step * 1e3 * (w.T / ts),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def timed(fn, stream, n, flush):
+    """CUDA-event times (ms) of n calls of fn, each after an L2 flush that lies
+    outside its events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
 
 
 def run_ours(args, rank, local_rank, world):
@@ -296,71 +327,78 @@ def run_ours(args, rank, local_rank, world):
     x_cpu = gin.make_inputs(wr)
     x = {n: (t.to(dev) if t is not None else None) for n, t in x_cpu.items()}
     gate = w.gate_mode
-    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
-    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims, w.C, gate), dtype=torch.uint8, device=dev)
-    out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32, device=dev)
+    DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
+    CODE = {"bf16": gdr.GDR_BF16, "fp32": gdr.GDR_F32}
+    main_dt = args.out_dtype
+    other_dt = "fp32" if main_dt == "bf16" else "bf16"
+    dims = {k_: gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, CODE[k_])
+            for k_ in DT}
+    path = gdr.chunk_fwd_path(dims[main_dt], w.C, gate)
+    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims[main_dt], w.C, gate), dtype=torch.uint8,
+                     device=dev)
+    outs = {k_: torch.empty(w.B, w.T, w.HV, w.V, dtype=DT[k_], device=dev) for k_ in DT}
     fin = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     segments = getattr(w, "segments", 1)
     if segments > 1:
-        seg_ws = torch.empty(gdr.chunk_fwd_segmented_workspace_size(dims, w.C, gate, segments),
+        seg_ws = torch.empty(gdr.chunk_fwd_segmented_workspace_size(dims[main_dt], w.C, gate,
+                                                                    segments),
                              dtype=torch.uint8, device=dev)
 
-    def step():
-        # The call a user makes: both stages in one gdr_chunk_fwd (or, for a
-        # segmented workload, gdr_chunk_fwd_segmented).
+    def step(dt=main_dt):
+        # The call a user makes: gdr_chunk_fwd (or, for a segmented workload,
+        # gdr_chunk_fwd_segmented).
         if segments > 1:
             gdr.chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"],
                                     segments=segments, chunk_size=w.C, scale=w.scale,
-                                    use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
-                                    workspace=seg_ws, out=out, final_state=fin, stream=stream)
+                                    use_qk_l2norm=w.use_qk_l2norm, out_dtype=DT[dt],
+                                    workspace=seg_ws, out=outs[dt], final_state=fin,
+                                    stream=stream)
             return
         gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"], chunk_size=w.C,
-                      scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
-                      workspace=ws, out=out, final_state=fin, stream=stream)
+                      scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=DT[dt],
+                      workspace=ws, out=outs[dt], final_state=fin, stream=stream)
 
     def split_step(mid):
-        # The same forward as two calls, to time each kernel on the launching stream.
+        # The two-launch form of the same forward (gdr_chunk_prepare +
+        # gdr_chunk_recur), to time the chunk-local and recurrence kernels apart.
         gdr.chunk_prepare(x["q"], x["k"], x["v"], x["g"], x["beta"], workspace=ws,
                           chunk_size=w.C, scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
-                          out_dtype=torch.float32, stream=stream)
+                          out_dtype=DT[main_dt], stream=stream)
         mid.record(stream)
-        gdr.chunk_recur(x["q"], x["k"], x["s0"], workspace=ws, out=out, final_state=fin, HV=w.HV,
-                        V=w.V, gate_mode=gate, chunk_size=w.C, scale=w.scale,
-                        use_qk_l2norm=w.use_qk_l2norm, stream=stream)
+        gdr.chunk_recur(x["q"], x["k"], x["s0"], workspace=ws, out=outs[main_dt],
+                        final_state=fin, HV=w.HV, V=w.V, gate_mode=gate, chunk_size=w.C,
+                        scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
         step()
+        step(other_dt)
     torch.cuda.synchronize()
-    assert torch.isfinite(out).all() and torch.isfinite(fin).all()
+    assert torch.isfinite(outs[main_dt].float()).all() and torch.isfinite(fin).all()
+    assert gdr.stream_status(stream, seg_ws if segments > 1 else ws) == gdr.GDR_OK
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     time.sleep(0.2)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for a, b in evs:
-        flush.zero_()
-        a.record(stream)
-        step()
-        b.record(stream)
-    torch.cuda.synchronize()
+    tot = timed(step, stream, args.steps, flush)
     if pg:
         pg.barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
-    tot = [a.elapsed_time(b) for a, b in evs]
     ms = shard.step_time_across_ranks(statistics.mean(tot), pg)
 
-    # Per-kernel times (outside the timed region): the split form, same flushes.
-    n_split = max(4, min(args.steps, 200))
-    sevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n_split)]
+    # Outside the timed region: the same forward with the other output dtype,
+    # the two-launch form split per kernel, and the warm-L2 figure.
+    n_side = max(4, min(args.steps, 200))
+    other = timed(lambda: step(other_dt), stream, n_side, flush)
+    ms_other = shard.step_time_across_ranks(statistics.mean(other), pg)
+    sevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(n_side)]
     for a, m, b in sevs:
         flush.zero_()
         a.record(stream)
@@ -369,7 +407,7 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
     prep = [a.elapsed_time(m) for a, m, b in sevs]
     rec = [m.elapsed_time(b) for a, m, b in sevs]
-    warm_ms = warm_l2_ms(step, stream, n_split)
+    warm_ms = warm_l2_ms(step, stream, n_side)
 
     # End to end through the C ABI with host buffers: pinned inputs copied in,
     # o and the final state copied out, every step. Consecutive steps are
@@ -378,13 +416,13 @@ def run_ours(args, rank, local_rank, world):
     # overlap another step's kernels, as a caller streaming batches would run.
     pin = {n: (t.pin_memory() if t is not None else None) for n, t in x_cpu.items()}
     E2E_STREAMS = 2
-    out_h = [torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32).pin_memory()
+    out_h = [torch.empty(w.B, w.T, w.HV, w.V, dtype=DT[main_dt]).pin_memory()
              for _ in range(E2E_STREAMS)]
     fin_h = [torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32).pin_memory()
              for _ in range(E2E_STREAMS)]
     streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS)]
     h2d = sum(t.numel() * t.element_size() for n, t in pin.items() if t is not None)
-    d2h = out_h[0].numel() * 4 + fin_h[0].numel() * 4
+    d2h = out_h[0].numel() * out_h[0].element_size() + fin_h[0].numel() * 4
     e2e_steps = max(4, min(args.steps, 50))
     if segments > 1:
         # No host-buffer form of the segmented call: the inputs are copied into
@@ -392,12 +430,13 @@ def run_ours(args, rank, local_rank, world):
         # final state are copied back, all on that stream.
         dbuf = [{n: torch.empty_like(t, device=dev) for n, t in pin.items() if t is not None}
                 for _ in range(E2E_STREAMS)]
-        dout = [torch.empty_like(out) for _ in range(E2E_STREAMS)]
+        dout = [torch.empty_like(outs[main_dt]) for _ in range(E2E_STREAMS)]
         dfin = [torch.empty_like(fin) for _ in range(E2E_STREAMS)]
         dws = [torch.empty_like(seg_ws) for _ in range(E2E_STREAMS)]
         method = f"H2D copies + gdr_chunk_fwd_segmented + D2H copies per step, {E2E_STREAMS} streams alternating"
     else:
-        hbytes = gdr.chunk_fwd_host_buffer_size(dims, w.C, gate, pin["s0"] is not None, True)
+        hbytes = gdr.chunk_fwd_host_buffer_size(dims[main_dt], w.C, gate, pin["s0"] is not None,
+                                                True)
         hbuf = [torch.empty(hbytes, dtype=torch.uint8, device=dev) for _ in range(E2E_STREAMS)]
         method = f"gdr_chunk_fwd_host per step, {E2E_STREAMS} streams alternating"
 
@@ -410,7 +449,7 @@ def run_ours(args, rank, local_rank, world):
                     t.copy_(pin[n], non_blocking=True)
                 gdr.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("s0"),
                                         segments=segments, chunk_size=w.C, scale=w.scale,
-                                        use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32,
+                                        use_qk_l2norm=w.use_qk_l2norm, out_dtype=DT[main_dt],
                                         workspace=dws[j], out=dout[j], final_state=dfin[j],
                                         stream=streams[j])
                 out_h[j].copy_(dout[j], non_blocking=True)
@@ -443,39 +482,57 @@ def run_ours(args, rank, local_rank, world):
             pg.destroy_process_group()
         return 0
     hbm, tflops, peak_kind = load_peaks()
-    bytes_alg = algorithmic_bytes(w)
+    obytes = {"bf16": 2, "fp32": 4}
+    bytes_alg = algorithmic_bytes(w, obytes[main_dt])
+    bytes_other = algorithmic_bytes(w, obytes[other_dt])
     flops_alg = FLOP_PER_TOKEN_HEAD * w.B * w.T * w.HV
     achieved = bytes_alg / (ms * 1e-3) / 1e9
     traffic, traffic_per = recorded_traffic(w.name)
-    # Kernel names in the ncu summaries: tcgen05 chunk kernel + fused recurrence
-    # (scalar gate), mma.sync chunk kernel + tcgen05 state kernel (per-key gate).
-    ck, rk = ("chunk_kda_kernel", "state_kda_tc_kernel") if w.gate_mode else ("chunk_tc_kernel", "recur_kernel")
+    # Kernels: the one-launch forward (fused_kernel) or the chunk-local kernel
+    # and the recurrence kernel (chunk_tc_kernel + chain_kernel, scalar gate;
+    # chunk_kda_kernel + state_kda_tc_kernel, per-key gate).
+    ck, rk = ("chunk_kda_kernel", "state_kda_tc_kernel") if gate else ("chunk_tc_kernel", "chain_kernel")
+    one_launch = path == 2 and segments == 1
+    if one_launch:
+        kernel_scope = "fused_kernel: one cooperative launch of the whole forward (chains and chunk producers)"
+        launches = 1
+        step_traffic = (traffic_per or {}).get("fused_kernel")
+    elif segments > 1:
+        kernel_scope = ("one gdr_chunk_fwd_segmented call: chunk-local kernel, 3 recurrence "
+                        "launches, identity and combine kernels")
+        launches = 6
+        step_traffic = None
+    else:
+        kernel_scope = f"one forward call: {ck} + {rk}"
+        launches = 2
+        step_traffic = traffic
     tokens = world * w.B * w.T
     line = {
         "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, world),
+        "config": config_of(w, world, main_dt),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
-                     "scope": ("one gdr_chunk_fwd_segmented call = chunk-local kernel, 4 recurrence "
-                               "launches, identity and combine kernels" if segments > 1 else
-                               "one forward call = chunk-local kernel + recurrence kernel"),
+                     "frac": achieved / hbm, "traffic": step_traffic, "scope": kernel_scope,
                      "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs",
                      "tensor_tflops": flops_alg / (ms * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops_alg / (ms * 1e-3) / 1e12 / tflops},
-        "kernels": {"chunk_local": {"ms": statistics.mean(prep),
-                                    "traffic": None if segments > 1 else (traffic_per or {}).get(ck)},
-                    "recurrence": {"ms": statistics.mean(rec),
-                                   "traffic": None if segments > 1 else (traffic_per or {}).get(rk)},
-                    **({"split_of": "the unsegmented forward (gdr_chunk_prepare + "
-                                    "gdr_chunk_recur) on the same inputs"}
-                       if segments > 1 else {})},
+        f"{other_dt}_output": {"ms_per_step": ms_other, "value": tokens / (ms_other * 1e-3),
+                               "algorithmic_bytes_per_step": bytes_other,
+                               "roofline_frac": bytes_other / (ms_other * 1e-3) / 1e9 / hbm,
+                               "steps": n_side},
+        "two_launch_form": {"chunk_local": {"kernel": ck, "ms": statistics.mean(prep),
+                                            "traffic": (traffic_per or {}).get(ck)},
+                            "recurrence": {"kernel": rk, "ms": statistics.mean(rec),
+                                           "traffic": (traffic_per or {}).get(rk)},
+                            **({"split_of": "the unsegmented forward (gdr_chunk_prepare + "
+                                            "gdr_chunk_recur) on the same inputs"}
+                               if segments > 1 else {})},
+        "path": path,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": method},
-        "gpu_launches": (7 if segments > 1 else 2) * args.steps,
-        **({"unsegmented_ms": statistics.mean(prep) + statistics.mean(rec)} if segments > 1 else {}),
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "wall_s_timed_loop": t_wall,
         "median_ms": statistics.median(tot),

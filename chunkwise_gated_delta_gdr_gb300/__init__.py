@@ -33,7 +33,8 @@ EXPORTED = (
     "gdr_chunk_fwd_host_buffer_size", "gdr_stream_status", "gdr_status_string",
     "gdr_chunk_fwd_path", "gdr_version", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
     "gdr_ssd_chunk_fwd", "gdr_ssd_chunk_fwd_workspace_size", "gdr_chunk_fwd_segmented",
-    "gdr_chunk_fwd_segmented_workspace_size",
+    "gdr_chunk_fwd_segmented_workspace_size", "gdr_noalloc_stream_status",
+    "gdr_set_flag_wait_limit",
 )
 # Size of the library-owned scratch used by gdr_chunk_fwd_noalloc (per device).
 GDR_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -101,6 +102,10 @@ def load_library(path: Optional[str] = None):
         lib.gdr_chunk_fwd_segmented_workspace_size.restype = sz
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = ip
+        lib.gdr_noalloc_stream_status.argtypes = [vp]
+        lib.gdr_noalloc_stream_status.restype = ip
+        lib.gdr_set_flag_wait_limit.argtypes = [ctypes.c_int64]
+        lib.gdr_set_flag_wait_limit.restype = ctypes.c_int64
         if path is None:
             _lib = lib
         return lib
@@ -370,6 +375,19 @@ def chunk_fwd_host(q, k, v, g, beta, initial_state=None, *, out, final_state=Non
     if st != GDR_OK:
         raise GdrError(st, "gdr_chunk_fwd_host")
     return out, final_state
+
+
+def set_flag_wait_limit(polls: int) -> int:
+    """gdr_set_flag_wait_limit: bound (polls, about 64 ns apart) of the
+    one-launch forward's waits on chunk flags for later calls; polls < 0 leaves
+    it unchanged. Returns the previous bound."""
+    return int(load_library().gdr_set_flag_wait_limit(int(polls)))
+
+
+def noalloc_stream_status(stream=None) -> int:
+    """gdr_noalloc_stream_status: synchronise the stream and report the last
+    gdr_chunk_fwd_noalloc call's device-side status on the current device."""
+    return int(load_library().gdr_noalloc_stream_status(_stream_handle(stream)))
 
 
 def stream_status(stream=None, workspace=None) -> int:

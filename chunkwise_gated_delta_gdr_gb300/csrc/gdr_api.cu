@@ -134,7 +134,8 @@ int gdr_chunk_fwd_path(const gdr_dims* dims, int chunk_size, int gate_mode, gdr_
   if (st != GDR_OK) return -1;
   Problem p = make_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, chunk_size,
                            1.f, 0, gate_mode, nullptr, nullptr, dims);
-  return tc_supported(p) ? 1 : 0;
+  if (!tc_supported(p)) return 0;
+  return tc_one_launch(p) ? 2 : 1;
 }
 
 }  // extern "C"
@@ -286,6 +287,8 @@ gdr_status gdr_chunk_fwd_host(const void* q, const void* k, const void* v, const
     return GDR_ERR_CUDA;
   return GDR_OK;
 }
+
+int64_t gdr_set_flag_wait_limit(int64_t polls) { return set_wait_limit(polls); }
 
 gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

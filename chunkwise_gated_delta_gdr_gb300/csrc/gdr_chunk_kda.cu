@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
   float* X = reinterpret_cast<float*>(sm + OFF_X);
   if (tid < 64) inverse_level0_store<LDL>(X, xd, tid);
   __syncthreads();
-  inverse_levels12_mma<LDL, LDL>(L, X, reinterpret_cast<float*>(sm + OFF_T), tid);
+  inverse_levels12_mma<LDL, LDL>(L, X, reinterpret_cast<float*>(sm + OFF_T), tid, 0);
   cp_async_wait<0>();   // v
   __syncthreads();   // L is dead: the X hi / lo boxes take its place
 

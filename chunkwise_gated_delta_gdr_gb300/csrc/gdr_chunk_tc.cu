@@ -1,6 +1,6 @@
-// gdr_chunk_tc.cu -- chunk-local kernel of the fast path on tcgen05 tensor cores.
+// gdr_chunk_tc.cu -- chunk-local stage of the fast path on tcgen05 tensor cores.
 //
-// One CTA (8 warps) per chunk (n, hv, b), scalar gate, bf16 inputs, C = 64,
+// One group of 8 warps per chunk (n, hv, b), scalar gate, bf16 inputs, C = 64,
 // K = V = 128. It computes, for one chunk of the "分块并行计算（Chunkwise）"
 // notes (section "chunk 内的 cumsum 与下三角解"):
 //   G     = cumsum(g)                                 (in-chunk gate cumsum)
@@ -19,433 +19,56 @@
 // the last chunk); accumulators live in TMEM; A_qk, -W and U are staged as
 // 128-byte swizzled tiles and leave by TMA stores. Each per-thread phase is
 // spread over the 8 warps (two per TMEM lane quadrant, one per column half).
-#include <cuda.h>
-#include <cuda_bf16.h>
-
-#include "gdr_fast.cuh"
-#include "gdr_ptx.cuh"
-#include "gdr_tmap.cuh"
-#include "gdr_trinv.cuh"
+//
+// The work of one chunk is the device function produce_chunk. It runs in the
+// chunk kernel below (one CTA per chunk, two CTAs per SM) and, for the
+// one-launch forward, in the worker CTAs of gdr_chain.cu (two groups of 8
+// warps per CTA, each taking chunks in chunk order and raising a flag per
+// chunk once its slab is in global memory).
+#include "gdr_chunk_tc.cuh"
 
 namespace gdr {
 namespace fast {
-namespace {
+namespace chunk {
 
-using namespace ptx;
-
-constexpr int THREADS = 256;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr long kWaitLimit = 1L << 24;   // bounded spin: ~tens of ms, then error word
-constexpr unsigned int kErrTmaWait = 1u, kErrMmaWait = 2u;
-constexpr float kSplitSpan = 80.f;      // |G_i - G_m| bound of the split decays
-
-// Shared-memory map (bytes from a 1024-aligned base).
-constexpr int OFF_K0 = 0;          // k cols 0-63   (8 KB, 128-byte swizzle, from TMA)
-constexpr int OFF_Q0 = 8192;       // q cols 0-63
-constexpr int OFF_K1 = 16384;      // k cols 64-127
-constexpr int OFF_Q1 = 24576;      // q cols 64-127
-constexpr int OFF_V0 = 32768;      // v cols 0-63
-constexpr int OFF_V1 = 40960;      // v cols 64-127
-constexpr int LDL = 68;            // fp32 row stride of L (272 B: float4 rows, conflict-free)
-constexpr int OFF_L = 49152;       // L [64][LDL] fp32; later XW (16 KB)
-constexpr int OFF_AQS = 66560;     // A_qk hi / lo staging, two swizzled [64][64] bf16 boxes
-constexpr int OFF_XU = 65536;      // XU (16 KB), written once L and the A_qk staging are dead
-constexpr int LDX = 68;            // fp32 row stride of X
-constexpr int OFF_X = 84992;       // X = (I + L)^-1 [64][LDX] fp32
-constexpr int OFF_T = 8192;        // block-product scratch [32][36] fp32 (in the dead q tile)
-constexpr int OFF_SMALL = 102400;  // G, nq, nk, beta, column factor (5 x 64 fp32)
-constexpr int OFF_BAR = 103680;    // mbarriers + TMEM slot
-constexpr int SMEM_BYTES = OFF_BAR + 64 + 1024;  // + alignment slack
-// Epilogue-2 staging (after the W / U MMAs, over the dead operand tiles):
-// -W hi / lo as [plane][column half] swizzled [64][64] bf16 boxes; U as four
-// swizzled [64][32] fp32 boxes.
-constexpr int OFF_WS = 0;
-constexpr int OFF_US = 32768;
-static_assert(OFF_AQS % 1024 == 0 && OFF_AQS + 16384 <= OFF_X, "A_qk staging placement");
-static_assert(OFF_XU + 16384 <= OFF_X && OFF_US + 32768 <= OFF_X, "staging overlaps X");
-static_assert(OFF_X + 64 * LDX * 4 <= OFF_SMALL, "X overlaps");
-static_assert(OFF_T + 32 * 36 * 4 <= OFF_K1, "scratch overlaps the k tile");
-
-// Rows of the stacked A operands [X_hi; X_lo] of the W / U MMAs are
-// interleaved in blocks of 16 so that the hi and lo products of output row i
-// land in the same warp's TMEM lanes (lanes 32 w + t and 32 w + 16 + t):
-//   row i, hi part -> A row 32 (i / 16) + (i % 16); lo part -> that + 16.
-__host__ __device__ constexpr int stacked_row(int i, int lo) { return 32 * (i >> 4) + (i & 15) + 16 * lo; }
-
-// Byte offset of 16-byte chunk c of row r in a swizzled box of 128-byte rows.
-__device__ __forceinline__ uint32_t box_off(int r, int c) {
-  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+// Encodes the tensor maps of the chunk-local stage.
+bool make_maps(Maps* m, const Params& p) {
+  const size_t nch = (size_t)p.B * p.HV * p.N;
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  return tmap_bthd(&m->q, p.q, p.B, p.T, p.H) && tmap_bthd(&m->k, p.k, p.B, p.T, p.H) &&
+         tmap_bthd(&m->v, p.v, p.B, p.T, p.HV) &&
+         tmap_blocks(&m->aq2, p.slabs + Slab::AQ2, BF, 2, C, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
+         tmap_blocks(&m->w2, p.slabs + Slab::W2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
+         tmap_blocks(&m->u, p.slabs + Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, nch,
+                     p.slab_bytes, 32, 64, SW);
 }
 
-struct Maps {
-  CUtensorMap q, k, v;          // [B, T, heads, 128] bf16 inputs
-  CUtensorMap aq2, w2, u;       // slab arrays (stores)
-};
+}  // namespace chunk
 
-__global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_constant__ Maps maps,
-                                                              Params p) {
+namespace {
+
+__global__ void __launch_bounds__(chunk::THREADS, 2) chunk_tc_kernel(
+    const __grid_constant__ chunk::Maps maps, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  const int n = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-  const int h = hv / (p.HV / p.H);
-  const int t0 = n * C;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, colh = warp >> 2;   // TMEM lane quadrant, column half
-  const int idx = (int)slab_index(p, b, hv, n);
-  if (p.zero_flags && idx == 0) {
-    const int nflags = p.B * p.HV * (V / VT);
-    for (int i = threadIdx.x; i < nflags; i += blockDim.x) p.flags[i] = 0u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bars, 1);       // tiles k, q
+    ptx::mbar_init(bars + 1, 1);   // MMAs
+    ptx::mbar_init(bars + 3, 1);   // tiles v
+    ptx::mbar_fence_init();
   }
-
-  float* L = reinterpret_cast<float*>(sm + OFF_L);
-  float* X = reinterpret_cast<float*>(sm + OFF_X);
-  float* T = reinterpret_cast<float*>(sm + OFF_T);
-  float* G = reinterpret_cast<float*>(sm + OFF_SMALL);
-  float* nq = G + C;
-  float* nk = nq + C;
-  float* bb = nk + C;
-  float* cfac = bb + C;
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_mma = bar_tma + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
-  int* split_ok = reinterpret_cast<int*>(tslot + 1);   // decay factorisation allowed
-  uint64_t* bar_v = bar_tma + 3;                       // v tiles (read by MMA 3 only)
-  uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
-
-  // The input tiles are requested first: the thread that initialised the
-  // barrier issues the loads before the TMEM allocation and the CTA barrier.
-  if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
-    mbar_init(bar_v, 1);
-    mbar_fence_init();
-    // k and q first (MMA 1 and the norms wait for them); v on its own barrier,
-    // waited for only by the MMA that reads it.
-    mbar_expect_tx(bar_tma, 4 * 8192);
-    tma_load4(smem_u32(sm + OFF_K0), &maps.k, 0, h, t0, b, bar_tma);
-    tma_load4(smem_u32(sm + OFF_K1), &maps.k, 64, h, t0, b, bar_tma);
-    tma_load4(smem_u32(sm + OFF_Q0), &maps.q, 0, h, t0, b, bar_tma);
-    tma_load4(smem_u32(sm + OFF_Q1), &maps.q, 64, h, t0, b, bar_tma);
-    mbar_expect_tx(bar_v, 2 * 8192);
-    tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_v);
-    tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_v);
-  }
-  // Gate and beta (plain loads into registers, in flight during the TMEM
-  // allocation; zero past the end and for the ungated mode).
-  float ga = 0.f, gb = 0.f, bv = 0.f;
-  if (warp == 0) {
-    const int ta = t0 + 2 * lane;
-    if (p.g && ta < p.T) ga = p.g[((size_t)b * p.T + ta) * p.HV + hv];   // g == NULL: ungated
-    if (p.g && ta + 1 < p.T) gb = p.g[((size_t)b * p.T + ta + 1) * p.HV + hv];
-  }
-  if (tid < C) {
-    const int t = t0 + tid;
-    // SSD: beta = 1 on real rows.
-    bv = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
-  }
-  if (warp == 1) tmem_alloc(tslot, TMEM_COLS);   // warp 0 is issuing the loads
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tma, 0, kWaitLimit));
-  if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
-  if (tid < C) bb[tid] = bv;   // read after the next CTA barrier
-
-  // ---- MMA 1: D[0:128, 0:64] = [k; q] k^T -------------------------------------
-  if (ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t id = idesc_bf16(128, 64, 0, 0);
-    const uint32_t base = smem_u32(sm + OFF_K0);
-#pragma unroll
-    for (int s = 0; s < K / 16; ++s) {
-      const uint32_t a = base + (s >> 2) * 16384 + (s & 3) * 32;
-      umma_bf16(tmem, sdesc_sw128(a), sdesc_sw128(a), id, s > 0);
-    }
-    umma_commit(bar_mma);
-  }
-  // Row norms while the MMA runs: thread pair (2 r, 2 r + 1) sums the squares
-  // of row r of [k; q] (r < 64: k, else q), one 64-column tile each.
-  {
-    const int r = tid >> 1, part = tid & 1, rr = r & 63;
-    const uint8_t* tp = sm + (r < 64 ? OFF_K0 : OFF_Q0) + part * 16384;
-    float ss = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      const uint4 u = *reinterpret_cast<const uint4*>(tp + swz128((uint32_t)(rr * 128 + ch * 16)));
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-        ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-      }
-    }
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    const float inv = p.use_l2 ? 1.f / sqrtf(ss + 1e-6f) : 1.f;
-    if (part == 0) {
-      if (r < 64) nk[rr] = inv; else nq[rr] = inv;
-    }
-  }
-  if (warp == 0) {
-    // Inclusive scan of the chunk's 64 gate values, two per lane.
-    float s = ga + gb;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    const float excl = s - (ga + gb);
-    const float g0 = excl + ga, g1 = excl + ga + gb;
-    G[2 * lane] = g0;
-    G[2 * lane + 1] = g1;
-    // The decays exp(G_i - G_j) may be split at the middle row m = C/2 - 1 as
-    // exp(G_i - G_m) exp(G_m - G_j) while every |G_i - G_m| <= 80: both factors
-    // then stay inside the fp32 range (NaN gates fail the test).
-    const float gm = __shfl_sync(0xffffffffu, g1, C / 4 - 1);
-    float dev = fmaxf(fabsf(g0 - gm), fabsf(g1 - gm));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, o));
-    if (lane == 0) *split_ok = dev <= kSplitSpan ? 1 : 0;
-  }
-  __syncthreads();
-  // Split decays: column factor |k_j|^-1 beta_j exp(G_m - G_j) once per column
-  // (in the column-factor array, free until the row factors below); the row and
-  // column factors are multiplied before the dot, so the intermediate is the
-  // size of exp(G_i - G_j).
-  const bool split = *split_ok != 0;
-  const float Gm = G[C / 2 - 1];
-  if (split) {
-    if (tid < C) cfac[tid] = nk[tid] * bb[tid] * __expf(Gm - G[tid]);
-    __syncthreads();
-  }
-
-  // ---- epilogue 1: A_kk -> L (fp32, smem), A_qk -> swizzled bf16 hi/lo boxes ----
-  // Warp w: TMEM lanes of quadrant w % 4 (rows of [k; q]), columns
-  // [32 (w / 4), 32 (w / 4) + 32).
-  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 0, kWaitLimit));
-  if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
-  tc_fence_after();
-  if (ok && split) {
-    const int r = 32 * quad + lane, rr = r & 63;
-    const bool is_q = r >= 64;
-    const float rowe = (is_q ? p.scale * nq[rr] : nk[rr]) * __expf(G[rr] - Gm);
-    float v[32];
-    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * colh, v);
-    const int jb = 32 * colh;
-    if (!is_q) {
-#pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 cf = *reinterpret_cast<const float4*>(cfac + jb + e);
-        const float cs[4] = {cf.x, cf.y, cf.z, cf.w};
-        float a4[4];
-#pragma unroll
-        for (int z = 0; z < 4; ++z)
-          a4[z] = (jb + e + z < rr && !p.ssd) ? v[e + z] * (rowe * cs[z]) : 0.f;
-        *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-      }
-    } else {
-      uint8_t* aqs = sm + OFF_AQS;
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        const float4 c0 = *reinterpret_cast<const float4*>(cfac + jb + e);
-        const float4 c1 = *reinterpret_cast<const float4*>(cfac + jb + e + 4);
-        const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int f = 0; f < 8; f += 2) {
-          const float a0 = (jb + e + f <= rr) ? v[e + f] * (rowe * cs[f]) : 0.f;
-          const float a1 = (jb + e + f + 1 <= rr) ? v[e + f + 1] * (rowe * cs[f + 1]) : 0.f;
-          split_pair(a0, a1, hi[f / 2], lo[f / 2]);
-        }
-        const int c = (jb + e) >> 3;
-        *reinterpret_cast<uint4*>(aqs + box_off(rr, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(aqs + 8192 + box_off(rr, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-  } else if (ok) {
-    // Decays too far apart to split: exp(G_i - G_j) element by element.
-    const int r = 32 * quad + lane, rr = r & 63;
-    const bool is_q = r >= 64;
-    const float Gi = G[rr];
-    const float rowf = is_q ? p.scale * nq[rr] : nk[rr];
-    float v[32];
-    tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * colh, v);
-    const int jb = 32 * colh;
-    if (!is_q) {
-#pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        float a4[4];
-#pragma unroll
-        for (int z = 0; z < 4; ++z) {
-          const int j = jb + e + z;
-          a4[z] = (j < rr && !p.ssd) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
-        }
-        *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-      }
-    } else {
-      uint8_t* aqs = sm + OFF_AQS;
-#pragma unroll
-      for (int e = 0; e < 32; e += 8) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int f = 0; f < 8; f += 2) {
-          float a2[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const int j = jb + e + f + z;
-            a2[z] = (j <= rr) ? v[e + f + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
-          }
-          split_pair(a2[0], a2[1], hi[f / 2], lo[f / 2]);
-        }
-        const int c = (jb + e) >> 3;
-        *reinterpret_cast<uint4*>(aqs + box_off(rr, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(aqs + 8192 + box_off(rr, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
-  }
-  fence_async_shared();
-  tc_fence_before();
-  __syncthreads();
-
-  // A_qk hi / lo out by TMA and the per-row factors of the state pass, on
-  // warps 2-7 while warps 0-1 run level 0 of the inverse.
-  constexpr int kRowTid = 64;          // first thread of the row-factor warps
-  if (tid == kRowTid) {
-    tma_store3(&maps.aq2, smem_u32(sm + OFF_AQS), 0, 0, idx);
-    tma_store3(&maps.aq2, smem_u32(sm + OFF_AQS) + 8192, 0, C, idx);
-    bulk_commit();
-  }
-  {
-    float* vec = reinterpret_cast<float*>(slab + Slab::VEC);
-    const float gl = G[C - 1];
-    const int e = tid - kRowTid;
-    if (e >= 0 && e < C) {
-      vec[e] = p.scale * nq[e] * __expf(G[e]);
-      vec[C + e] = bb[e] * nk[e] * __expf(gl - G[e]);
-      cfac[e] = __expf(G[e]) * nk[e];   // column factor of X' = X diag(exp(G) |k|^-1)
-    }
-    if (e >= 0 && e < K) vec[2 * C + e] = __expf(gl);
-  }
-
-  // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
-  unit_lower_inverse64<LDL, LDX>(L, X, T, tid);
-  if (tid == kRowTid) bulk_wait_read<0>();   // the A_qk staging is read before XU overwrites it
-  __syncthreads();   // X complete; L and the A_qk staging are dead from here on
-
-  // ---- A operands XW = [X' hi/lo], XU = [X hi/lo] (rows interleaved, see stacked_row)
-  // Each thread: one row i, 8 consecutive columns, 2 items.
-  {
-    uint8_t* xw = sm + OFF_L;
-    uint8_t* xu = sm + OFF_XU;
-#pragma unroll
-    for (int it = tid; it < C * 8; it += THREADS) {
-      const int i = it >> 3, c8 = (it & 7) * 8;
-      const float4 x0 = *reinterpret_cast<const float4*>(X + i * LDX + c8);
-      const float4 x1 = *reinterpret_cast<const float4*>(X + i * LDX + c8 + 4);
-      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      uint32_t whi[4], wlo[4], uhi[4], ulo[4];
-#pragma unroll
-      for (int z = 0; z < 8; z += 2) {
-        const float u0 = (c8 + z <= i) ? xs[z] : 0.f;
-        const float u1 = (c8 + z + 1 <= i) ? xs[z + 1] : 0.f;
-        split_pair(u0 * cfac[c8 + z], u1 * cfac[c8 + z + 1], whi[z / 2], wlo[z / 2]);
-        split_pair(u0, u1, uhi[z / 2], ulo[z / 2]);
-      }
-      const uint32_t o_hi = swz128((uint32_t)(stacked_row(i, 0) * 128 + c8 * 2));
-      const uint32_t o_lo = swz128((uint32_t)(stacked_row(i, 1) * 128 + c8 * 2));
-      *reinterpret_cast<uint4*>(xw + o_hi) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-      *reinterpret_cast<uint4*>(xw + o_lo) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-      *reinterpret_cast<uint4*>(xu + o_hi) = make_uint4(uhi[0], uhi[1], uhi[2], uhi[3]);
-      *reinterpret_cast<uint4*>(xu + o_lo) = make_uint4(ulo[0], ulo[1], ulo[2], ulo[3]);
-    }
-  }
-  fence_async_shared();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- MMA 2/3: D_W = XW k (TMEM cols 0-127), D_U = XU v (cols 128-255) ----------
-  if (ok && tid == 0) {
-    ok = mbar_wait(bar_v, 0, kWaitLimit);            // the v tiles (normally long arrived)
-    if (!ok) atomicOr(p.error_word, kErrTmaWait);
-  }
-  if (ok && tid == 0) {
-    tc_fence_after();
-    constexpr uint32_t id = idesc_bf16(128, 128, 0, 1);
-    const uint32_t xw = smem_u32(sm + OFF_L), xu = smem_u32(sm + OFF_XU);
-    const uint32_t kb = smem_u32(sm + OFF_K0), vb = smem_u32(sm + OFF_V0);
-#pragma unroll
-    for (int s = 0; s < C / 16; ++s) {
-      umma_bf16(tmem, sdesc_sw128(xw + s * 32), sdesc_sw128_lbo(kb + s * 2048, 16384), id, s > 0);
-      umma_bf16(tmem + 128, sdesc_sw128(xu + s * 32), sdesc_sw128_lbo(vb + s * 2048, 8192), id,
-                s > 0);
-    }
-    umma_commit(bar_mma);
-  }
-  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 1, kWaitLimit));
-  if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
-  tc_fence_after();
-
-  // ---- epilogue 2: W = hi + lo rows, U likewise; -W hi/lo and U staged --------
-  // Lane t < 16 of quadrant q holds the hi product of row r = 16 q + t, lane
-  // t + 16 the lo product of the same row: one shuffle per value sums them,
-  // after which lane t keeps columns [0,16) and lane t + 16 columns [16,32) of
-  // each 32-column block. Warps 0-3 take the W blocks, warps 4-7 the U blocks.
-  if (ok) {
-    const int r = 16 * quad + (lane & 15);
-    const int half = lane >> 4;
-    const bool is_u = colh == 1;
-    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      float v[32];
-      tmem_ld32(tmem + lane_base + (is_u ? 128 : 0) + cc * 32, v);
-      float s[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float send = half ? v[e] : v[16 + e];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-        s[e] = (half ? v[16 + e] : v[e]) + recv;
-      }
-      const int c0 = cc * 32 + half * 16;   // first column of this lane's 16
-      if (!is_u) {
-        uint32_t hi[8], lo[8];
-        // SSD keeps no erase term: W = 0 (then X = I and U = v).
-        const float ws = p.ssd ? 0.f : -1.f;
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) split_pair(ws * s[e], ws * s[e + 1], hi[e / 2], lo[e / 2]);
-        const int bx = c0 >> 6, c = (c0 & 63) >> 3;
-        uint8_t* wh = sm + OFF_WS + bx * 8192;
-        uint8_t* wl = wh + 16384;
-        *reinterpret_cast<uint4*>(wh + box_off(r, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(wh + box_off(r, c + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        *reinterpret_cast<uint4*>(wl + box_off(r, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(wl + box_off(r, c + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-      } else {
-        uint8_t* ub = sm + OFF_US + cc * 8192;   // box cc: columns [32 cc, 32 cc + 32)
-        const int c = (c0 & 31) >> 2;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(ub + box_off(r, c + e / 4)) =
-              make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
-      }
-    }
-  }
-  fence_async_shared();
-  tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t ws = smem_u32(sm + OFF_WS), us = smem_u32(sm + OFF_US);
-    for (int pl = 0; pl < 2; ++pl)
-      for (int bx = 0; bx < 2; ++bx)
-        tma_store3(&maps.w2, ws + pl * 16384 + bx * 8192, 64 * bx, C * pl, idx);
-    for (int bx = 0; bx < 4; ++bx) tma_store3(&maps.u, us + bx * 8192, 32 * bx, 0, idx);
-    bulk_commit();
-    bulk_wait_read<0>();                  // staging read before the CTA's smem is released
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+  // (the first barrier inside produce_chunk orders the initialisation before
+  // any wait; only thread 0 uses the barriers before it)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  chunk::produce_chunk(maps, p, sm, threadIdx.x, 1, blockIdx.x, blockIdx.y, blockIdx.z, 0, 0,
+                       tslot, nullptr);
+  if (threadIdx.x == 0) ptx::bulk_wait_read<0>();   // staging read before the smem is released
+  if ((threadIdx.x >> 5) == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(*tslot, chunk::TMEM_COLS);
   }
 }
 
@@ -453,22 +76,13 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_tc_kernel(const __grid_const
 
 gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream) {
   if (p.gate_mode != 0) return launch_chunk_kda(p, stream);
-  Maps m;
-  const size_t nch = (size_t)p.B * p.HV * p.N;
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!tmap_bthd(&m.q, p.q, p.B, p.T, p.H) || !tmap_bthd(&m.k, p.k, p.B, p.T, p.H) ||
-      !tmap_bthd(&m.v, p.v, p.B, p.T, p.HV) ||
-      !tmap_blocks(&m.aq2, p.slabs + Slab::AQ2, BF, 2, C, 2 * C, nch, p.slab_bytes, 64, 64, SW) ||
-      !tmap_blocks(&m.w2, p.slabs + Slab::W2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 64, SW) ||
-      !tmap_blocks(&m.u, p.slabs + Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, nch,
-                   p.slab_bytes, 32, 64, SW))
-    return GDR_ERR_CUDA;
+  chunk::Maps m;
+  if (!chunk::make_maps(&m, p)) return GDR_ERR_CUDA;
   if (cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES) != cudaSuccess)
+                           chunk::SMEM_BYTES) != cudaSuccess)
     return GDR_ERR_CUDA;
   dim3 grid(p.N, p.HV, p.B);
-  chunk_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(m, p);
+  chunk_tc_kernel<<<grid, chunk::THREADS, chunk::SMEM_BYTES, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

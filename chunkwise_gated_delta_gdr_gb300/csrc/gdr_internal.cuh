@@ -47,12 +47,18 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 size_t general_workspace_bytes(const Problem& p);
 gdr_status launch_general(const Problem& p, void* ws_body, cudaStream_t stream, int stage);
 
-// Fast path (bf16, K = V = 128, C = 64): tcgen05 chunk-local kernel and
-// mma.sync state recurrence.
+// Fast path (bf16, K = V = 128, C = 64): chunk-local stage and state
+// recurrence on tcgen05 (the per-key gate's chunk-local stage on mma.sync).
 bool tc_supported(const Problem& p);
 size_t tc_workspace_bytes(const Problem& p);
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
                      cudaStream_t stream, int stage);
+// Whether gdr_chunk_fwd takes the one-launch form of the fast path (scalar
+// gate) for this problem on the current device.
+bool tc_one_launch(const Problem& p);
+// Bound (polls) of the one-launch forward's waits on chunk flags, for calls
+// enqueued from now on (polls < 0: unchanged); returns the previous bound.
+long long set_wait_limit(long long polls);
 
 // Segmented scan helpers (gdr_segment.cu): n identity K x K states; the serial
 // combine S_{p+1} = A_p S_p + B_p over the P segments of each (b, hv).

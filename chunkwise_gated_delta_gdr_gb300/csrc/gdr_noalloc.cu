@@ -6,8 +6,8 @@
 // sits inside a region where cudaMalloc is forbidden (it synchronises the
 // device and is not allowed while another stream is being captured). For them
 // this file owns a fixed scratch buffer in device global memory, declared as a
-// file-scope __device__ array, and gdr_chunk_fwd_noalloc runs the usual two
-// kernels on it. Nothing here calls cudaMalloc, cudaFree or any allocating
+// file-scope __device__ array, and gdr_chunk_fwd_noalloc runs the usual
+// forward pass on it. Nothing here calls cudaMalloc, cudaFree or any allocating
 // library routine.
 //
 // The array exists once per device that loads this library and stays
@@ -24,24 +24,34 @@ static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte alignme
 
 // The scratch buffer itself. Host code must not use this name as an address:
 // on the host it denotes a stand-in object, so the device address is looked up
-// once per device with cudaGetSymbolAddress and cached below.
+// with cudaGetSymbolAddress (below) and cached per device.
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 256;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device (first use on a device
-// resolves it with that device current).
-gdr_status scratch_address(void** out) {
+// Device address of g_scratch on the current device. Outside stream capture
+// it is looked up again on every call (cheap), so a cudaDeviceReset, after
+// which the module and the array may come back at another address, leaves no
+// stale pointer behind; while `stream` is being captured the address cached by
+// an earlier call on this device is used.
+gdr_status scratch_address(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDR_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDR_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cs = cudaStreamCaptureStatusActive;     // unknown: do not touch the module
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (cs == cudaStreamCaptureStatusNone || !g_scratch_ptr[dev]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr)
+    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) {
+      (void)cudaGetLastError();
       return GDR_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = ptr;
   }
   *out = g_scratch_ptr[dev];
@@ -62,7 +72,7 @@ extern "C" gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const 
   if (need > gdr::kScratchBytes) return GDR_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
-    const gdr_status st = gdr::scratch_address(&scratch);
+    const gdr_status st = gdr::scratch_address(reinterpret_cast<cudaStream_t>(stream), &scratch);
     if (st != GDR_OK) return st;
   }
   // need == 0 means the sizes are invalid or unsupported: gdr_chunk_fwd then
@@ -70,4 +80,14 @@ extern "C" gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const 
   return gdr_chunk_fwd(q, k, v, g, beta, initial_state, chunk_size, scale, use_qk_l2norm,
                        gate_mode, out, final_state, dims, scratch, scratch ? gdr::kScratchBytes : 0,
                        stream);
+}
+
+// The scratch array starts with the workspace header, whose error word the
+// kernels set when a bounded wait gives up: read it the way gdr_stream_status
+// reads a caller's workspace.
+extern "C" gdr_status gdr_noalloc_stream_status(gdr_stream_t stream) {
+  void* scratch = nullptr;
+  const gdr_status st = gdr::scratch_address(reinterpret_cast<cudaStream_t>(stream), &scratch);
+  if (st != GDR_OK) return st;
+  return gdr_stream_status(stream, scratch);
 }

@@ -1,4 +1,6 @@
 // gdr_tc.cu -- dispatch of the fast path (bf16 inputs, K = V = 128, C = 64).
+#include <atomic>
+
 #include "gdr_fast.cuh"
 
 namespace gdr {
@@ -10,10 +12,15 @@ bool tc_supported(const Problem& p) {
 
 namespace {
 
-// Workspace body of the fast path: the chunk slabs, then (scalar gate) the
-// exchange blocks of the state chain and its per-chain progress flags.
+// Polls of a chain's wait on a chunk flag (one-launch forward), about 64 ns
+// apart: 2^24 is about a second.
+constexpr long long kDefaultWaitLimit = 1LL << 24;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+
+// Workspace body of the fast path: the chunk slabs, then (scalar gate) one
+// ready flag per chunk for the one-launch forward.
 struct TcLayout {
-  size_t xchg = 0, flags = 0, total = 0;
+  size_t flags = 0, total = 0;
 };
 
 TcLayout tc_layout(const Problem& p) {
@@ -21,12 +28,9 @@ TcLayout tc_layout(const Problem& p) {
   TcLayout L;
   size_t off = nch * fast::Slab::bytes(p.gate_mode);
   if (p.gate_mode == 0) {
-    off = align_up(off, 1024);
-    L.xchg = off;
-    off += nch * fast::Xchg::BYTES;
     off = align_up(off, 256);
     L.flags = off;
-    off += (size_t)p.B * p.HV * (fast::V / fast::VT) * sizeof(unsigned int);
+    off += nch * sizeof(unsigned int);
   }
   L.total = off;
   return L;
@@ -34,7 +38,15 @@ TcLayout tc_layout(const Problem& p) {
 
 }  // namespace
 
+long long set_wait_limit(long long polls) {
+  return polls < 0 ? g_wait_limit.load() : g_wait_limit.exchange(polls);
+}
+
 size_t tc_workspace_bytes(const Problem& p) { return tc_layout(p).total; }
+
+bool tc_one_launch(const Problem& p) {
+  return tc_supported(p) && p.gate_mode == 0 && fast::fused_fits(p.B, p.HV);
+}
 
 gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
                      cudaStream_t stream, int stage) {
@@ -49,7 +61,6 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.sT = p.sT;
   f.slabs = static_cast<uint8_t*>(ws_body);
   const TcLayout L = tc_layout(p);
-  f.xchg = p.gate_mode == 0 ? f.slabs + L.xchg : nullptr;
   f.flags = p.gate_mode == 0 ? reinterpret_cast<unsigned int*>(f.slabs + L.flags) : nullptr;
   f.error_word = error_word;
   f.B = p.B;
@@ -63,14 +74,25 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.ssd = p.ssd;
   f.zero_u = p.zero_u;
   f.recur_mode = p.recur_mode;
-  f.zero_flags = (stage == 3 && f.flags) ? 1 : 0;
   f.scale = p.scale;
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
+  f.wait_limit = (long)g_wait_limit.load();
+  // Both stages in one call, scalar gate: one cooperative launch when the
+  // chains leave enough SMs to the producers.
+  if (stage == 3 && p.gate_mode == 0 && p.recur_mode == 0) {
+    const gdr_status st = fast::launch_fused(f, stream);
+    if (st != GDR_ERR_UNSUPPORTED) return st;
+  }
   if (stage & 1) {
     gdr_status st = fast::launch_chunk_tc(f, stream);
     if (st != GDR_OK) return st;
   }
-  if (stage & 2) return fast::launch_state(f, stream);
+  if (stage & 2) {
+    // Both recurrence kernels write the outputs with the states: there is no
+    // separate output pass (recur_mode 2).
+    if (p.recur_mode == 2) return GDR_OK;
+    return p.gate_mode ? fast::launch_state_kda_tc(f, stream) : fast::launch_chain(f, stream);
+  }
   return GDR_OK;
 }
 

@@ -13,13 +13,18 @@
 // diagonal blocks' upper triangles and the blocks X_01, X_23), so the level-2
 // products need no masks; X[0:32, 32:64] is never written. All 256 threads of
 // the CTA call it; it synchronises the CTA between levels but not after the
-// last writes (the caller does).
+// last writes (the caller does). The 256 threads meet on named barrier bar_id
+// (a whole 256-thread CTA may pass 0, the barrier of __syncthreads).
 #pragma once
 
 #include "gdr_ptx.cuh"
 
 namespace gdr {
 namespace fast {
+
+__device__ __forceinline__ void trinv_sync(int bar_id) {
+  asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+}
 
 // Level 0 for threads 0-63: column (tid & 15) of diagonal block tid >> 4, in registers.
 template <int LDL>
@@ -48,7 +53,8 @@ __device__ __forceinline__ void inverse_level0_store(float* X, const float (&xd)
 
 // Levels 1 and 2, once the diagonal blocks of X are in place and visible.
 template <int LDL, int LDX>
-__device__ __forceinline__ void inverse_levels12(const float* L, float* X, float* T, int tid) {
+__device__ __forceinline__ void inverse_levels12(const float* L, float* X, float* T, int tid,
+                                                 int bar_id) {
   // Level 1: threads 0-127, each one row segment of 4 columns.
   {
     const int which = (tid >> 6) & 1, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
@@ -64,7 +70,7 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
       }
       *reinterpret_cast<float4*>(T + (which * 16 + i) * 36 + j0) = acc;
     }
-    __syncthreads();
+    trinv_sync(bar_id);
     if (tid < 128) {
       float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -77,7 +83,7 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
       *reinterpret_cast<float4*>(X + (I + i) * LDX + J + j0) = make_float4(-r4.x, -r4.y, -r4.z, -r4.w);
     }
   }
-  __syncthreads();
+  trinv_sync(bar_id);
   // Level 2: each thread one row segment of 4 columns. The zeros above the
   // diagonal of X[0:32, 0:32] and X[32:64, 32:64] are stored, so the products
   // run over the full 32 x 32 blocks.
@@ -93,7 +99,7 @@ __device__ __forceinline__ void inverse_levels12(const float* L, float* X, float
     }
     // The level-1 scratch was last read before the barrier that ends level 1.
     *reinterpret_cast<float4*>(T + i * 36 + j0) = make_float4(a[0], a[1], a[2], a[3]);
-    __syncthreads();
+    trinv_sync(bar_id);
     float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {
@@ -152,7 +158,8 @@ __device__ __forceinline__ void store16x8(float* M, int ld, int r0, int c0, cons
 // The scratch T holds the 16x16 level-1 products in rows 0-31, columns 0-15,
 // then the 32x32 level-2 product.
 template <int LDL, int LDX>
-__device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, float* T, int tid) {
+__device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, float* T, int tid,
+                                                     int bar_id) {
   const int warp = tid >> 5, lane = tid & 31;
   constexpr int LDT = 36;
   {
@@ -163,14 +170,14 @@ __device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, f
       mma16x8_split(d, L, LDL, I, J, X, LDX, J, J + 8 * nt, lane);
       store16x8(T, LDT, 16 * which, 8 * nt, d, 1.f, lane);
     }
-    __syncthreads();
+    trinv_sync(bar_id);
     if (warp < 4) {                                   // X[I, J] = -X[I, I] T_w
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       mma16x8_split(d, X, LDX, I, I, T, LDT, 16 * which, 8 * nt, lane);
       store16x8(X, LDX, I, J + 8 * nt, d, -1.f, lane);
     }
   }
-  __syncthreads();
+  trinv_sync(bar_id);
   const int mt = warp >> 2, nt = warp & 3;
   {                                                   // T = L[32:64, 0:32] X[0:32, 0:32]
     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -178,7 +185,7 @@ __device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, f
     mma16x8_split(d, L, LDL, 32 + 16 * mt, 16, X, LDX, 16, 8 * nt, lane);
     store16x8(T, LDT, 16 * mt, 8 * nt, d, 1.f, lane);
   }
-  __syncthreads();
+  trinv_sync(bar_id);
   {                                                   // X[32:64, 0:32] = -X[32:64, 32:64] T
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     mma16x8_split(d, X, LDX, 32 + 16 * mt, 32, T, LDT, 0, 8 * nt, lane);
@@ -192,14 +199,15 @@ __device__ __forceinline__ void inverse_levels12_mma(const float* L, float* X, f
 // error near 2^-16, the size of the residual the callers' own hi/lo split of X
 // leaves.
 template <int LDL, int LDX>
-__device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, float* T, int tid) {
+__device__ __forceinline__ void unit_lower_inverse64(const float* L, float* X, float* T, int tid,
+                                                     int bar_id) {
   if (tid < 64) {
     float xd[16];
     inverse_level0<LDL>(L, xd, tid);
     inverse_level0_store<LDX>(X, xd, tid);
   }
-  __syncthreads();
-  inverse_levels12_mma<LDL, LDX>(L, X, T, tid);
+  trinv_sync(bar_id);
+  inverse_levels12_mma<LDL, LDX>(L, X, T, tid, bar_id);
 }
 
 }  // namespace fast

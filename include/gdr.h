@@ -177,6 +177,25 @@ size_t gdr_chunk_fwd_host_buffer_size(const gdr_dims* dims, int chunk_size, int 
 gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace);
 
 /*
+ * gdr_set_flag_wait_limit -- bound of the device waits of the one-launch forward.
+ *
+ * With the scalar gate on the tensor-core path, gdr_chunk_fwd runs both stages
+ * in one cooperative launch when the problem has few enough chains: worker
+ * CTAs produce each chunk's operands and raise a flag for it, chain CTAs of
+ * the same launch wait for the flag before they read the chunk. A chain polls
+ * a flag at most `polls` times, about 64 ns apart. If the flag is still down,
+ * it records GDR_ERR_TIMEOUT in the workspace error word (gdr_stream_status
+ * reports it) and runs to its end on whatever the workspace holds: the call
+ * then finishes with wrong outputs instead of hanging. The default, 2^24
+ * polls (about a second), is far beyond any real wait.
+ *
+ *   polls   >= 0: the new bound, for calls enqueued from now on (all devices,
+ *           all threads); < 0: leave the bound as it is.
+ * Returns the bound in force before the call.
+ */
+int64_t gdr_set_flag_wait_limit(int64_t polls);
+
+/*
  * gdr_chunk_fwd_noalloc -- gdr_chunk_fwd without a caller workspace.
  *
  * There is no counterpart of this entry point in the method's sources; it
@@ -193,15 +212,20 @@ gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace);
  * Arguments, layouts and errors are those of gdr_chunk_fwd, minus the
  * workspace. Sizes whose gdr_chunk_fwd_workspace_size() exceeds
  * GDR_NOALLOC_SCRATCH_BYTES are rejected with GDR_ERR_WORKSPACE before
- * anything is enqueued (64 MiB fits, for example, B=1, T=4096, 12 value heads,
- * K=V=128, C=64).
+ * anything is enqueued. 64 MiB fits, for example, B=1, T=4096, 12 value heads,
+ * K=V=128, C=64, scalar gate, bf16 inputs (a workspace of about 63.7 MB); the
+ * same call with 16 value heads (about 85 MB) does not.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
- * capture. All calls on a device share the one array, which keeps whatever
- * the last call left in it (each call rewrites everything it reads, and clears
- * the error word itself). Calls that can overlap on the GPU (different streams
- * without ordering) race on the array and must not be issued.
+ * capture. Later calls outside capture look the address up again, so a
+ * cudaDeviceReset leaves no stale address behind; calls on a stream being
+ * captured use the cached one. All calls on a device share the one array,
+ * which keeps whatever the last call left in it (each call rewrites everything
+ * it reads, and clears the error word itself). Calls that can overlap on the
+ * GPU (different streams without ordering) race on the array and must not be
+ * issued. A device-side timeout of such a call is reported by
+ * gdr_noalloc_stream_status, not by gdr_stream_status.
  */
 #define GDR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
@@ -209,6 +233,17 @@ gdr_status gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  const float* beta, const float* initial_state, int chunk_size,
                                  float scale, int use_qk_l2norm, int gate_mode, void* out,
                                  float* final_state, const gdr_dims* dims, gdr_stream_t stream);
+
+/*
+ * gdr_noalloc_stream_status -- gdr_stream_status for gdr_chunk_fwd_noalloc.
+ * The library-owned array holds the error word of the last no-alloc call on
+ * the current device; this synchronises `stream` and reports it:
+ * GDR_ERR_CUDA if the stream reports an error, GDR_ERR_TIMEOUT if a device
+ * wait of that call gave up, else GDR_OK. No counterpart in the method's
+ * sources; it completes gdr_chunk_fwd_noalloc, whose callers hold no
+ * workspace to pass to gdr_stream_status.
+ */
+gdr_status gdr_noalloc_stream_status(gdr_stream_t stream);
 
 /*
  * gdr_recurrent_fwd -- the token-by-token (recurrent) form, for decoding.
@@ -287,9 +322,12 @@ size_t gdr_chunk_fwd_segmented_workspace_size(const gdr_dims* dims, int chunk_si
 /* Static, human-readable name of a status code. */
 const char* gdr_status_string(gdr_status s);
 
-/* Which kernel path gdr_chunk_fwd takes for these arguments:
- * 0 = general fp32 CUDA-core path, 1 = tcgen05 tensor-core path,
- * -1 = arguments rejected (the status is written to *status if non-NULL). */
+/* Which kernel path gdr_chunk_fwd takes for these arguments on the current
+ * device: 0 = general fp32 CUDA-core path, 1 = tcgen05 tensor-core path in two
+ * launches (chunk-local kernel, then the recurrence), 2 = tensor-core path in
+ * one cooperative launch (scalar gate, few enough sequences for the device's
+ * SMs: chains and chunk producers side by side), -1 = arguments rejected (the
+ * status is written to *status if non-NULL). */
 int gdr_chunk_fwd_path(const gdr_dims* dims, int chunk_size, int gate_mode, gdr_status* status);
 
 /* Library version, (major << 16) | (minor << 8) | patch. */
