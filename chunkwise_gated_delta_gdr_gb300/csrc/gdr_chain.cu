@@ -1,52 +1,76 @@
 // gdr_chain.cu -- inter-chunk recurrence of the fast path for the scalar gate
-// (Gated DeltaNet) on tcgen05 tensor cores, and the one-launch forward.
+// (Gated DeltaNet) on tcgen05 tensor cores, its output pass, and the
+// one-launch forward.
 //
 // Per chunk n the inter-chunk loop of the "分块并行计算（Chunkwise）" notes
-// (section "chunk 间递推") reads
+// (section "chunk 间递推") reads, with S_n the state at the start of chunk n,
 //     r_n     = U_n - W_n S_n
 //     o_n     = (q exp(G)) S_n + A_qk r_n
-//     S_{n+1} = exp(G_last) S_n + (exp(G_last - G) k)^T (beta r_n)
-// Only the S update is serial. One chain CTA per (batch, value head, 32 value
-// columns v0 .. v0 + 31) keeps its 128 x 32 slice of S in fp32 registers (one
-// key channel per thread) for the whole sequence and forms the chunk outputs
-// of its columns as it goes. Per chunk, on tcgen05 (kind::f16, fp32
-// accumulators in TMEM):
-//     D_r  = [-W_hi; -W_lo] [S_hi | S_lo]      M = 128 (stacked rows), N = 64, K = 128
-//     r    = U + (the four quarters of D_r),   rho = kscale r        (fp32, registers)
-//     D_S  = k^T [rho_hi | rho_lo]             M = 128, N = 64, K = 64 (k raw bf16)
-//     S    = gamma S + (the two halves of D_S)
-//     D_qs = q [S_hi | S_lo]                   M = 64,  N = 64, K = 128 (q raw bf16)
-//     D_ar = [A_hi; A_lo] [r_hi | r_lo]        M = 128 (stacked rows), N = 64, K = 64
-//     o    = qscale (D_qs halves) + (the four quarters of D_ar)
-// Every operand holding fp32 values enters as a bf16 hi + lo pair: hi hi,
-// hi lo and lo hi products (the lo lo products come along and are kept). q and
-// k are exact in bf16 and carry their L2 norms, scale and decays as fp32 row
-// factors (qscale, kscale), which is why their products need no lo part.
+//     S_{n+1} = gamma_n S_n + k_n^T rho_n,     rho_n = kscale_n r_n
+// (gamma_n = exp(G_last) of chunk n, kscale the row factors of
+// (exp(G_last - G) k)^T beta). The serial dependence is r_n -> S_{n+1} ->
+// r_{n+1}. Substituting S_n in r_n:
+//     W_n S_n = gamma_{n-1} W_n S_{n-1} + T_n rho_{n-1},   T_n = W_n k_{n-1}^T (C x C)
+// so with T_n formed in the chunk-local stage,
+//     r_n = U_n + gamma_{n-1} (-W_n) S_{n-1} + (-T_n) rho_{n-1}
+// and the only product between rho_{n-1} and r_n is (-T_n) rho_{n-1} (K = C),
+// while (-W_n) S_{n-1} and the state update run one chunk ahead.
 //
-// Roles of a chain CTA (10 warps):
-//   warps 0-3  the state: thread (w, lane) holds channel c = 32 w + lane (TMEM
-//              lane c of D_S). They form r from D_r (lanes 0-15 hold the hi
-//              rows j = 16 w + lane, lanes 16-31 the lo rows of the same j),
-//              publish r and rho as MN-major B operands, then S from D_S, and
-//              publish S (bf16 hi | lo per row, 128-byte swizzled).
-//   warps 4-7  the outputs: o rows i = 16 (w - 4) + lane % 16, 16 columns per
-//              lane, stored straight to global memory (rows past T skipped).
-//   warp 8     TMA producer: -W (stacked), k, q, A_qk (stacked), the U tile
-//              and VEC of chunk n into one of two operand stages.
-//   warp 9     MMA issuer and TMEM owner, per chunk in the order D_r, D_qs,
-//              D_S, D_ar: the output products run while the state warps work
-//              on r and on S and never sit in front of D_r or D_S.
-// TMEM: D_r 64 columns, D_S 64, two output accumulator pairs (D_qs, D_ar) of
-// 128 so that one chunk's outputs are read while the next chunk's are formed.
+// Chain role: one CTA per (sequence, 32 value columns). Its operands arrive as
+// the byte images the chunk-local stage stored (one bulk copy per array: on
+// GB300 an SM takes in about 120 bytes per cycle this way against about 43 by
+// tensor-map loads of 128-byte swizzled boxes). Per chunk, on tcgen05
+// (kind::f16, fp32 accumulators in TMEM, every fp32-valued operand as a bf16
+// hi + lo pair):
+//     D_ws(n) = [-W_hi; -W_lo] [S_{n-1,hi} | S_{n-1,lo}]   M = 128 (stacked), N = 64, K = 128
+//     D_t(n)  = [-T_hi; -T_lo] [rho_{n-1,hi} | rho_{n-1,lo}] M = 128 (stacked), N = 64, K = 64
+//     D_S(n)  = k_{n-1}^T [rho_{n-1,hi} | rho_{n-1,lo}]      M = 128 (k raw bf16), N = 64, K = 64
+// (for n = 0: D_ws(0) = (-W_0) S_0 with gamma := 1 and no D_t).
+// Each product is issued as soon as its last input is published, by a thread
+// released through a named barrier: an mbarrier hand-off costs several hundred
+// cycles per product on this serial path, and the tensor pipe itself needs
+// only about 1.2k cycles per chunk for the sixteen MMAs.
+// Roles (16 warps):
+//   warps 0-7  the state: thread (w, lane) holds channel c = 32 (w % 4) + lane
+//              of S (TMEM lane c of D_S), value columns [16 h, 16 h + 16) with
+//              h = w / 4, for the whole sequence: S_n = gamma_{n-1} S_{n-1} +
+//              D_S(n), published as the bf16 [hi 32 | lo 32] rows of an
+//              MN-major B operand.
+//   warps 8-11 r: lanes 0-15 of quadrant q hold the hi rows j = 16 q + lane of
+//              D_ws and D_t, lanes 16-31 the lo rows of the same j; they form
+//              r_n and rho_n and publish both as tiles of the same format (rho
+//              for the products, r for the output pass).
+//   warp 12    TMA producer (three rings of two slots: {-W}, {-T, U, VEC}, {k}).
+//   warp 14    issues D_S(n + 1) and D_t(n + 1) once the r warps have published
+//              rho_n; warp 15 issues D_ws(n + 1) once the state warps have
+//              published S_n. Each is released by a named barrier that the
+//              producing warps arrive on without waiting.
+//   warp 13    TMEM owner and exporter: once S_n and r_n are published it copies both tiles
+//              to the exchange block (bulk copies, one group per chunk),
+//              announces them read out (the tiles are double buffered), and
+//              in the one-launch forward counts the chunk as exported a few
+//              chunks later, when the copies have long been written. A
+//              release or proxy fence waits for all of its thread's memory
+//              operations in flight, the TMA producer's loads included, so
+//              none runs on the warps of the recurrence itself.
+// The S_n and r_n tiles of every chunk leave by bulk copies (a plain store of a
+// row-per-thread tile would touch 32 lines per instruction and hold up the
+// SM's memory pipe) as the exchange block of gdr_fast.cuh; the output pass
+// then forms
+//     o_n = qscale (q S_n) + A_qk r_n
+// per (chunk, sequence, 64 value columns) on tcgen05.
 //
 // One-launch forward (launch_fused): one cooperative launch of one CTA per SM.
-// The first CTAs take the chain role; the others are workers, two groups of 8
-// warps each, that run the chunk-local stage (gdr_chunk_tc.cuh) over the
-// chunks in chunk order and raise each chunk's flag once its slab is in
-// global memory. A chain's TMA warp waits for chunk n's flag before loading
-// it. Workers never wait on chains and all CTAs are co-resident, so the waits
-// end; every wait is bounded all the same and records a code in the workspace
-// error word when it gives up, after which the CTA runs to its end.
+// The first CTAs are the chains; the other CTAs are workers, two groups of 8
+// warps each, that first run the chunk-local stage (gdr_chunk_tc.cuh) over the
+// chunks in chunk order, raising each chunk's flag once its slab is in global
+// memory, and then form the outputs of the chunks in chunk order. A chain's
+// TMA warp waits for chunk n's flag before loading it; the chain counts each
+// export of chunk n once it is in global memory, and a worker forms the
+// outputs of chunk n once the count is complete. Workers wait on chains only
+// after their last slab, and all CTAs are co-resident, so the waits end; every
+// wait is bounded all the same and records a code in the workspace error word
+// when it gives up, after which the CTA runs to its end.
 #include <string.h>
 
 #include <cuda.h>
@@ -63,44 +87,92 @@ using namespace ptx;
 
 constexpr int VC = 32;                  // value columns per chain CTA
 constexpr int VTILES = V / VC;          // chain CTAs per sequence
-constexpr int CHAIN_THREADS = 320;
+constexpr int CHAIN_THREADS = 512;
 constexpr int FUSED_THREADS = 512;      // worker CTA: two chunk groups of 256
 constexpr long kWaitLimit = 1L << 24;   // mbarrier polls before a wait gives up
-constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u;
+constexpr long kTmaIdleLimit = 1L << 24;  // TMA event-loop rounds (64 ns sleeps) likewise
+// A release or a proxy fence waits for all memory operations of its thread in
+// flight (bulk copies included), some microseconds here: the exporter counts a
+// chunk's exports only when it has no copies in flight, and the TMA producer
+// acquires up to kFlagWindow slab flags at once.
+constexpr int kFlagWindow = 8;
+constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u, kErrXchgWait = 32u;
 
-// Shared memory of a chain CTA (bytes from a 1024-aligned base). Operand stage:
-constexpr int ST_W = 0;          // -W stacked [128][128] bf16: two [128][64] boxes
-constexpr int ST_K = 32768;      // k [64 j][128 c] bf16: two [64][64] boxes
-constexpr int ST_Q = 49152;      // q [64 i][128 c] bf16: two [64][64] boxes
-constexpr int ST_AQ = 65536;     // A_qk stacked [128][64] bf16
-constexpr int ST_U = 81920;      // U [64 j][32 v] fp32, 128-byte swizzled
-constexpr int ST_VEC = 90112;    // qscale[64], kscale[64], gamma[128] fp32
-constexpr int STAGE = 91136;
-constexpr uint32_t STAGE_TX = 32768 + 16384 + 16384 + 16384 + 8192 + 1024;
-constexpr int NST = 2;
-constexpr int S_TILE = NST * STAGE;      // S [128 c][S_hi 32 | S_lo 32] bf16, swizzled rows
-constexpr int R_TILE = S_TILE + 16384;   // r [64 j][r_hi 32 | r_lo 32]
-constexpr int P_TILE = R_TILE + 8192;    // rho [64 j][rho_hi 32 | rho_lo 32]
-constexpr int BARS = P_TILE + 8192;
-constexpr int CHAIN_SMEM = BARS + 256 + 1024;
-static_assert(STAGE % 1024 == 0 && S_TILE % 1024 == 0 && R_TILE % 1024 == 0 &&
-                  P_TILE % 1024 == 0,
+// Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
+// of two slots, each slot released as soon as its last reader is done:
+// Ring W slot (chunk n): -W stacked [128][128] bf16 (two [128][64] boxes); free
+// once D_ws(n) is complete, so chunk n + 2 streams in a step before it is used.
+constexpr int W_SLOT = 32768;
+constexpr uint32_t W_TX = 32768;
+// Ring A slot (chunk n): -T stacked [128][64] bf16, U [64 j][32 v] fp32
+// (128-byte swizzled), VEC.
+constexpr int A_T = 0, A_U = 16384, A_VEC = 24576, A_SLOT = 25600;
+constexpr uint32_t A_TX = 16384 + 8192 + 1024;
+// Ring B slot (chunk n): k [64 j][128 c] bf16 (two [64][64] boxes).
+constexpr int KB_SLOT = 16384;
+constexpr uint32_t B_TX = 16384;
+constexpr int OFF_W = 0;
+constexpr int OFF_A = OFF_W + 2 * W_SLOT;
+constexpr int OFF_B = OFF_A + 2 * A_SLOT;
+constexpr int OFF_S = OFF_B + 2 * KB_SLOT;     // S tiles [128 c][hi 32 | lo 32] bf16, x 2
+constexpr int OFF_P = OFF_S + 2 * 16384;      // rho tiles [64 j][hi 32 | lo 32], x 2
+constexpr int OFF_R = OFF_P + 2 * 8192;       // r tiles, the same format, x 2
+constexpr int OFF_BARS = OFF_R + 2 * 8192;
+constexpr int CHAIN_SMEM = OFF_BARS + 256 + 1024;
+static_assert(A_SLOT % 1024 == 0 && OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && OFF_S % 1024 == 0 &&
+                  OFF_P % 1024 == 0 && OFF_R % 1024 == 0 && A_T % 1024 == 0 && A_U % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
 static_assert(CHAIN_SMEM <= 232448, "chain shared memory");
 constexpr int FUSED_SMEM =
     (CHAIN_SMEM > 2 * chunk::GROUP_BYTES + 1024) ? CHAIN_SMEM : 2 * chunk::GROUP_BYTES + 1024;
 static_assert(FUSED_SMEM <= 232448, "one-launch shared memory");
 
-// TMEM columns.
-constexpr uint32_t T_R = 0, T_S = 64, T_O = 128;   // output pair b: D_qs at T_O + 128 b, D_ar + 64
-constexpr uint32_t TMEM_COLS = 512;
+// TMEM columns of a chain CTA: D_ws (two buffers), D_t, D_S (two buffers).
+constexpr uint32_t T_WS = 0, T_T = 128, T_S = 192, CHAIN_TMEM = 512;
+
+// Barriers of a chain CTA (index into a uint64_t array at OFF_BARS).
+enum : int {
+  B_FULLA = 0,    // [2] ring A slot loaded (local arrive + transaction bytes)
+  B_EMPTYA = 2,   // [2] ring A slot free: 4 r warps (after D_t of the chunk completed)
+                  //     + 8 S warps
+  B_FULLB = 4,    // [2] ring B slot loaded
+  B_EMPTYB = 6,   // [2] ring B slot free: 8 S warps (after the D_S that read it)
+  B_ES = 8,       // [2] S_n published, barrier n % 2 (8 state warps; for the exporter)
+  B_WS = 10,      // [2] D_ws complete (commit), buffer n % 2
+  B_T = 12,       // D_t complete (commit)
+  B_DS = 13,      // [2] D_S complete (commit), buffer (n - 1) % 2 for D_S(n)
+  B_RP = 15,      // [2] r_n tile published, barrier n % 2 (4 r warps)
+  B_XR = 17,      // [2] exports of chunk n (S and r tiles) read out, barrier n % 2 (exporter)
+  B_FULLW = 19,   // [2] ring W slot loaded
+  B_EMPTYW = 21,  // [2] ring W slot free: 4 r warps (after D_ws of the chunk completed)
+  B_SLOT = 23     // TMEM slot (u32)
+};
+// A waiter tests an mbarrier phase by parity, so a barrier must never run two
+// phases ahead of one of its waiters. The S, r and export barriers could (S_{n+1}
+// may be published before chunk n is exported, and chunk n - 1 exported before
+// the MMA thread checks chunk n - 2), so each has one barrier per chunk parity:
+// barrier n % 2 completes phase n / 2 for chunk n, and its next phase (chunk
+// n + 2) depends on the waiter having passed chunk n.
+constexpr int kEmptyA = 4 + 8;
+constexpr int kEmptyB = 8;
+constexpr int kEmptyW = 4;
 
 __device__ __forceinline__ void nb_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// Arrives on named barrier id (n threads in all) without waiting for it.
+__device__ __forceinline__ void nb_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Byte offset of 16-byte chunk q of row r in 128-byte swizzled rows.
 __device__ __forceinline__ uint32_t sw_off(int r, int q) {
   return (uint32_t)(r * 128 + ((q ^ (r & 7)) << 4));
+}
+// Bounded wait by polling (no suspension of the thread between polls).
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, long limit) {
+  for (long i = 0; i <= limit; ++i)
+    if (mbar_test(bar, parity)) return true;
+  return false;
 }
 // A bounded wait of a whole warp; false for every lane once any lane gave up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, bool ok) {
@@ -118,293 +190,432 @@ __device__ __forceinline__ void publish16(uint8_t* tile, int r, int q0, const fl
   *reinterpret_cast<uint4*>(tile + sw_off(r, q0 + 4)) = make_uint4(l[0], l[1], l[2], l[3]);
   *reinterpret_cast<uint4*>(tile + sw_off(r, q0 + 5)) = make_uint4(l[4], l[5], l[6], l[7]);
 }
+// Sums the hi and lo rows of a stacked accumulator: lane t < 16 holds the hi
+// row, lane t + 16 the lo row of the same output row; in each, columns
+// [0, 32) come from the B hi part and [32, 64) from the B lo part. Returns the
+// 16 columns [16 half, 16 half + 16) this lane keeps.
+__device__ __forceinline__ void stacked_sum(const float* d, int half, float* out) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float col_a = d[i] + d[32 + i];          // column i
+    const float col_b = d[16 + i] + d[48 + i];     // column 16 + i
+    const float send = half ? col_a : col_b;       // what the partner lane keeps
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    out[i] = (half ? col_b : col_a) + recv;
+  }
+}
 
 // ============================================================================ chain
-// seq = b * HV + hv, value columns [32 vt, 32 vt + 32). wait_flags: chunk n's
-// slab is produced in the same launch (wait for its flag before loading it).
-__device__ __forceinline__ void chain_role(const chunk::Maps& maps, const Params& p, uint8_t* sm,
-                                           int seq, int vt, bool wait_flags) {
-  const int b = seq / p.HV, hv = seq % p.HV, h = hv / (p.HV / p.H);
+// seq = b * HV + hv, value columns [32 vt, 32 vt + 32). wait_flags: chunk
+// n's slab is produced in the same launch (wait for its flag before loading it).
+__device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq, int vt,
+                                           bool wait_flags) {
   const int v0 = vt * VC;
+  const int N = p.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk0 = seq * p.N;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + BARS);
-  uint64_t* full = bars;           // [NST] operand stage loaded
-  uint64_t* empty = bars + 2;      // [NST] stage free: MMA commit + 4 output warps (VEC read)
-  uint64_t* s_ready = bars + 4;    // S tile published (4 state warps)
-  uint64_t* rho_ready = bars + 5;  // r and rho tiles published (4 state warps)
-  uint64_t* r_done = bars + 6;     // D_r complete (commit)
-  uint64_t* ds_done = bars + 7;    // D_S complete (commit)
-  uint64_t* o_full = bars + 8;     // [2] output pair complete (commit)
-  uint64_t* o_empty = bars + 10;   // [2] output pair read (4 output warps)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 12);
+  const int chunk0 = seq * N;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_SLOT);
 
   if (tid == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 5);
-    }
-    mbar_init(s_ready, 4);
-    mbar_init(rho_ready, 4);
-    mbar_init(r_done, 1);
-    mbar_init(ds_done, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 4);
+      mbar_init(&bars[B_FULLA + i], 1);
+      mbar_init(&bars[B_EMPTYA + i], kEmptyA);
+      mbar_init(&bars[B_FULLW + i], 1);
+      mbar_init(&bars[B_EMPTYW + i], kEmptyW);
+      mbar_init(&bars[B_FULLB + i], 1);
+      mbar_init(&bars[B_EMPTYB + i], kEmptyB);
+      mbar_init(&bars[B_WS + i], 1);
+      mbar_init(&bars[B_DS + i], 1);
+      mbar_init(&bars[B_ES + i], 8);
+      mbar_init(&bars[B_RP + i], 4);
+      mbar_init(&bars[B_XR + i], 1);
     }
+    mbar_init(&bars[B_T], 1);
     mbar_fence_init();
   }
-  if (warp == 9) tmem_alloc(tslot, TMEM_COLS);
+  if (warp == 13) tmem_alloc(tslot, CHAIN_TMEM);
   tc_fence_before();
   nb_sync(1, CHAIN_THREADS);
   tc_fence_after();
   const uint32_t tmem = *tslot;
   bool ok = true;
+  uint8_t* xbase = p.xchg + (size_t)chunk0 * Xchg::BYTES;
+  const uint32_t sb = smem_u32(sm);
+  constexpr uint32_t ID_KMN = idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major
+  constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, 1, 1);  // A = k^T read MN-major
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ---------------------------------------------------------------- state
-    const int c = 32 * warp + lane;                      // key channel = TMEM lane
-    const uint32_t lb = (uint32_t)(32 * warp) << 16;
-    const int half = lane >> 4;
-    const int j = 16 * warp + (lane & 15);               // r row of this lane's D_r lane
-    uint8_t* stile = sm + S_TILE;
-    float S[32];
+    // After publishing S_n the eight warps arrive on named barrier 2, which
+    // releases the D_ws issuer (warp 15).
+    const int qd = warp & 3, h = warp >> 2;
+    const int c = 32 * qd + lane;                        // key channel = TMEM lane
+    const uint32_t lb = (uint32_t)(32 * qd) << 16;
+    float S[16];
     if (p.s0) {
-      const float4* src = reinterpret_cast<const float4*>(p.s0 + ((size_t)seq * K + c) * V + v0);
+      const float4* src =
+          reinterpret_cast<const float4*>(p.s0 + ((size_t)seq * K + c) * V + v0 + 16 * h);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const float4 x = src[q];
         S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) S[i] = 0.f;
+      for (int i = 0; i < 16; ++i) S[i] = 0.f;
     }
-    publish16(stile, c, 0, S);
-    publish16(stile, c, 2, S + 16);
-    fence_async_shared();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(s_ready);
-    for (int n = 0; n < p.N; ++n) {
-      const uint8_t* stg = sm + (n % NST) * STAGE;
-      // r = U + D_r; rho = kscale r.
-      ok = warp_wait(r_done, n & 1, ok);
-      tc_fence_after();
-      float gam;
-      {
-        float d[64];
-        tmem_ld64(tmem + lb + T_R, d);
-        // Lanes 0-15: hi row j (cols 0-31 W_hi S_hi, 32-63 W_hi S_lo); lanes
-        // 16-31: lo row j. Lane t keeps columns [16 half, 16 half + 16).
-        float r[16];
+    float gam = 1.f;
+    for (int n = 0; n <= N; ++n) {
+      if (n > 0) {
+        // S_n = gamma_{n-1} S_{n-1} + D_S(n) (hi and lo columns of B), from
+        // D_S buffer (n - 1) % 2.
+        const int bs = (n - 1) & 1;
+        ok = warp_wait(&bars[B_DS + bs], ((n - 1) >> 1) & 1, ok);
+        if (lane == 0) mbar_arrive(&bars[B_EMPTYB + bs]);   // k_{n-1} read
+        tc_fence_after();
+        float d[32];
+        const uint32_t ts = tmem + lb + T_S + 64 * bs;
+        tmem_ld16x2(ts + 16 * h, ts + 32 + 16 * h, d);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float col_a = d[i] + d[32 + i];          // column i
-          const float col_b = d[16 + i] + d[48 + i];     // column 16 + i
-          const float send = half ? col_a : col_b;       // what the partner lane keeps
-          const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-          r[i] = (half ? col_b : col_a) + recv;
-        }
-        const float* vec = reinterpret_cast<const float*>(stg + ST_VEC);
-        const float ks = vec[C + j];
-        gam = vec[2 * C + c];
-        if (!p.zero_u) {
-          const uint8_t* ub = stg + ST_U;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 u = *reinterpret_cast<const float4*>(ub + sw_off(j, 4 * half + q));
-            r[4 * q] += u.x; r[4 * q + 1] += u.y; r[4 * q + 2] += u.z; r[4 * q + 3] += u.w;
-          }
-        }
-        publish16(sm + R_TILE, j, 2 * half, r);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] *= ks;
-        publish16(sm + P_TILE, j, 2 * half, r);
+        for (int i = 0; i < 16; ++i) S[i] = fmaf(gam, S[i], d[i] + d[16 + i]);
+        tc_fence_before();
       }
+      if (n == N) break;
+      // S tile n % 2 held S_{n-2}: D_ws(n - 1) has read it (its completion) and
+      // so has its export.
+      if (n >= 2) {
+        ok = warp_wait(&bars[B_WS + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ok);
+        ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
+      }
+      uint8_t* st = sm + OFF_S + (n & 1) * 16384;
+      publish16(st, c, 2 * h, S);
       fence_async_shared();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(rho_ready);
-      // S = gamma S + D_S.
-      ok = warp_wait(ds_done, n & 1, ok);
-      tc_fence_after();
-      {
-        float d[64];
-        tmem_ld64(tmem + lb + T_S, d);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) S[i] = fmaf(gam, S[i], d[i] + d[32 + i]);
-      }
+      if (lane == 0) mbar_arrive(&bars[B_ES + (n & 1)]);   // for the exporter
       tc_fence_before();
-      if (n + 1 < p.N) {
-        publish16(stile, c, 0, S);
-        publish16(stile, c, 2, S + 16);
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_ready);
-      }
+      nb_arrive(2, 288);
+      // gamma_n for S_{n+1}; then this warp is done with ring A slot n % 2.
+      ok = warp_wait(&bars[B_FULLA + (n & 1)], (n >> 1) & 1, ok);
+      gam = reinterpret_cast<const float*>(sm + OFF_A + (n & 1) * A_SLOT + A_VEC)[2 * C];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_EMPTYA + (n & 1)]);
     }
     if (p.sT) {
-      float4* dst = reinterpret_cast<float4*>(p.sT + ((size_t)seq * K + c) * V + v0);
+      float4* dst = reinterpret_cast<float4*>(p.sT + ((size_t)seq * K + c) * V + v0 + 16 * h);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < 4; ++q)
         dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
-  } else if (warp < 8) {
-    // -------------------------------------------------------------- outputs
-    const int qd = warp - 4;
+  } else if (warp < 12) {
+    // -------------------------------------------------------------------- r
+    // After publishing rho_n the four warps arrive on named barrier 3, which
+    // releases the D_S / D_t issuer (warp 14).
+    const int qd = warp - 8;
     const uint32_t lb = (uint32_t)(32 * qd) << 16;
     const int half = lane >> 4;
-    const int i = 16 * qd + (lane & 15);                 // chunk row
-    for (int n = 0; n < p.N; ++n) {
-      const int ob = n & 1, st = n % NST;
-      ok = warp_wait(&o_full[ob], (n >> 1) & 1, ok);
+    const int j = 16 * qd + (lane & 15);                 // r row of this lane
+    float gam_prev = 1.f;
+    for (int n = 0; n < N; ++n) {
+      const int sa = n & 1;
+      const uint8_t* slot = sm + OFF_A + sa * A_SLOT;
+      ok = warp_wait(&bars[B_WS + sa], (n >> 1) & 1, ok);
+      if (lane == 0) mbar_arrive(&bars[B_EMPTYW + sa]);   // D_ws(n) done: W_n read
+      ok = warp_wait(&bars[B_FULLA + sa], (n >> 1) & 1, ok);
       tc_fence_after();
-      const float qs = reinterpret_cast<const float*>(sm + st * STAGE + ST_VEC)[i];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);            // this warp is done with the stage
-      float x[32];
+      float r[16];
       {
         float d[64];
-        tmem_ld64(tmem + lb + T_O + 128 * ob, d);        // D_qs: lanes 0-15
+        tmem_ld64(tmem + lb + T_WS + 64 * sa, d);
+        stacked_sum(d, half, r);
+      }
+      const float* vec = reinterpret_cast<const float*>(slot + A_VEC);
+      const float ks = vec[C + j];
+      const float gam_n = vec[2 * C];
+      const float uf = p.zero_u ? 0.f : 1.f;
+      const uint8_t* ub = slot + A_U;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = half ? 0.f : qs * (d[e] + d[32 + e]);
-        tmem_ld64(tmem + lb + T_O + 128 * ob + 64, d);   // D_ar: hi rows 0-15, lo rows 16-31
+      for (int q = 0; q < 4; ++q) {
+        const float4 u = *reinterpret_cast<const float4*>(ub + sw_off(j, 4 * half + q));
+        r[4 * q] = fmaf(gam_prev, r[4 * q], uf * u.x);
+        r[4 * q + 1] = fmaf(gam_prev, r[4 * q + 1], uf * u.y);
+        r[4 * q + 2] = fmaf(gam_prev, r[4 * q + 2], uf * u.z);
+        r[4 * q + 3] = fmaf(gam_prev, r[4 * q + 3], uf * u.w);
+      }
+      if (n > 0) {
+        ok = warp_wait(&bars[B_T], (n - 1) & 1, ok);
+        tc_fence_after();
+        float d[64], t[16];
+        tmem_ld64(tmem + lb + T_T, d);
+        stacked_sum(d, half, t);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] += d[e] + d[32 + e];
+        for (int i = 0; i < 16; ++i) r[i] += t[i];
       }
       tc_fence_before();
+      // rho into tile n % 2: rho_{n-2} there was read by D_S(n - 1) and
+      // D_t(n - 1), issued by the same thread before D_t(n), whose completion
+      // this step waited for.
+      float rho[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) rho[i] = r[i] * ks;
+      publish16(sm + OFF_P + sa * 8192, j, 2 * half, rho);
+      fence_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[ob]);
-      float o[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float send = half ? x[e] : x[16 + e];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-        o[e] = (half ? x[16 + e] : x[e]) + recv;
-      }
-      const int t = n * C + i;
-      if (t < p.T) {
-        const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0 + 16 * half;
-        if (p.out_bf16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                                pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&bars[B_EMPTYA + sa]);   // U, VEC read; D_t(n) (T_n) done
+      tc_fence_before();
+      nb_arrive(3, 160);
+      // r into its tile n % 2 once the export of r_{n-2} from it is read out.
+      if (n >= 2) ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
+      publish16(sm + OFF_R + sa * 8192, j, 2 * half, r);
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_RP + (n & 1)]);
+      gam_prev = gam_n;
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
+    // Ring W takes chunk nw once its slot is free (chunk nw - 2 done), rings A
+    // and B likewise; one bulk copy per array.
     if (lane == 0) {
       const uint32_t sb = smem_u32(sm);
+      int nw = 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
       bool flags_ok = wait_flags;
-      for (int n = 0; n < p.N; ++n) {
-        const int st = n % NST, idx = chunk0 + n;
-        if (n >= NST) ok = ok && mbar_wait(&empty[st], ((n / NST) - 1) & 1, kWaitLimit);
-        if (!ok) break;
-        if (flags_ok) {
-          // The chunk's slab is written by a worker of this launch. A wait that
-          // gives up records the error and stops waiting: the chain then runs
-          // to its end on whatever the workspace holds (in bounds), so no
-          // other wait of the launch has to run out as well.
-          const unsigned int* fl = p.flags + idx;
-          long polls = 0;
-          while (ld_acquire_gpu(fl) == 0u) {
-            if (++polls > p.wait_limit) {
-              flags_ok = false;
-              atomicOr(p.error_word, kErrFlagWait);
-              break;
-            }
-            __nanosleep(64);
+      long idle = 0, flag_polls = 0;
+      while ((nw < N || na < N || nb < N) && ok) {
+        bool progress = false, polled = false;
+        const int lead = nw > na ? (nw > nb ? nw : nb) : (na > nb ? na : nb);
+        if (flags_ok && nflag < N && nflag < lead + 2) {
+          polled = true;
+          // The next flags (chunk slabs are written by workers of this
+          // launch): every consecutive one already set, then one acquire.
+          int m = nflag;
+          const int lim = nflag + kFlagWindow < N ? nflag + kFlagWindow : N;
+          while (m < lim && ld_relaxed_gpu(p.flags + chunk0 + m) != 0u) ++m;
+          if (m > nflag) {
+            fence_acq_rel_gpu();                         // acquire the slabs' writes
+            fence_async_global();                        // ... for the bulk reads
+            nflag = m;
+            flag_polls = 0;
+            progress = true;
+          } else if (++flag_polls > p.wait_limit) {
+            // Give up waiting: record it, then run to the end on whatever the
+            // workspace holds (in bounds), so that no other wait runs out too.
+            flags_ok = false;
+            nflag = N;
+            atomicOr(p.error_word, kErrFlagWait);
           }
-          fence_async_global();                          // slab (generic acquire) -> TMA reads
         }
-        const uint32_t stg = sb + st * STAGE;
-        mbar_expect_tx(&full[st], STAGE_TX);
-        tma_load3(stg + ST_W, &maps.w2, 0, 0, idx, &full[st]);
-        tma_load3(stg + ST_W + 16384, &maps.w2, 64, 0, idx, &full[st]);
-        tma_load4(stg + ST_K, &maps.k, 0, h, n * C, b, &full[st]);
-        tma_load4(stg + ST_K + 8192, &maps.k, 64, h, n * C, b, &full[st]);
-        tma_load4(stg + ST_Q, &maps.q, 0, h, n * C, b, &full[st]);
-        tma_load4(stg + ST_Q + 8192, &maps.q, 64, h, n * C, b, &full[st]);
-        tma_load3(stg + ST_AQ, &maps.aq2, 0, 0, idx, &full[st]);
-        tma_load3(stg + ST_U, &maps.u, v0, 0, idx, &full[st]);
-        bulk_load(stg + ST_VEC, p.slabs + (size_t)idx * p.slab_bytes + Slab::VEC, 1024, &full[st]);
+        if (nw < N && nw < nflag &&
+            (nw < 2 || mbar_test(&bars[B_EMPTYW + (nw & 1)], ((nw >> 1) - 1) & 1))) {
+          uint64_t* fb = &bars[B_FULLW + (nw & 1)];
+          mbar_expect_tx(fb, W_TX);
+          bulk_load(sb + OFF_W + (nw & 1) * W_SLOT, p.slabs + (size_t)(chunk0 + nw) * p.slab_bytes + Slab::W2,
+                    32768, fb);
+          ++nw;
+          progress = true;
+        }
+        if (na < N && na < nflag &&
+            (na < 2 || mbar_test(&bars[B_EMPTYA + (na & 1)], ((na >> 1) - 1) & 1))) {
+          const uint8_t* slab = p.slabs + (size_t)(chunk0 + na) * p.slab_bytes;
+          uint64_t* fb = &bars[B_FULLA + (na & 1)];
+          const uint32_t slot = sb + OFF_A + (na & 1) * A_SLOT;
+          mbar_expect_tx(fb, A_TX);
+          bulk_load(slot + A_T, slab + Slab::T2, 16384, fb);   // (first chunk: not used)
+          bulk_load(slot + A_U, slab + Slab::U + vt * 8192, 8192, fb);
+          bulk_load(slot + A_VEC, slab + Slab::VEC, 1024, fb);
+          ++na;
+          progress = true;
+        }
+        if (nb < N && nb < nflag &&
+            (nb < 2 || mbar_test(&bars[B_EMPTYB + (nb & 1)], ((nb >> 1) - 1) & 1))) {
+          uint64_t* fb = &bars[B_FULLB + (nb & 1)];
+          const uint32_t slot = sb + OFF_B + (nb & 1) * KB_SLOT;
+          mbar_expect_tx(fb, B_TX);
+          bulk_load(slot, p.slabs + (size_t)(chunk0 + nb) * p.slab_bytes + Slab::K2, 16384, fb);
+          ++nb;
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+        } else {
+          // (a flag wait has its own bound, p.wait_limit polls)
+          if (!polled && ++idle > kTmaIdleLimit) ok = false;
+          __nanosleep(64);
+        }
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- MMA issuer
+    __syncwarp();
+  } else if (warp == 14) {
+    // ------------------------------------------------------- D_S / D_t issuer
+    // Once rho_n is published (named barrier 3): D_S(n + 1) = k_n^T rho_n into
+    // D_S buffer n % 2 (read for S_{n-1}, which D_ws(n), complete before rho_n,
+    // consumed), then D_t(n + 1) = (-T_{n+1}) rho_n (the last round: D_S(N)
+    // alone, for the final state).
+    for (int n = 0; n < N; ++n) {
+      nb_sync(3, 160);
+      if (lane == 0 && ok) {
+        const int sa = n & 1;
+        ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
+        if (ok) {
+          tc_fence_after();
+          const uint32_t kb = sb + OFF_B + sa * KB_SLOT;
+          const uint32_t pt = sb + OFF_P + sa * 8192;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + T_S + 64 * sa, sdesc_sw128_lbo(kb + kk * 2048, 8192),
+                      sdesc_sw128_lbo(pt + kk * 2048, 8192), ID_MNMN, kk > 0);
+          umma_commit(&bars[B_DS + sa]);
+        }
+        if (ok && n + 1 < N) {
+          const int m = n + 1;
+          ok = mbar_spin(&bars[B_FULLA + (m & 1)], (m >> 1) & 1, kWaitLimit);   // T_{n+1}
+          if (ok) {
+            const uint32_t ta = sb + OFF_A + (m & 1) * A_SLOT + A_T;
+            const uint32_t pt = sb + OFF_P + sa * 8192;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + T_T, sdesc_sw128(ta + kk * 32), sdesc_sw128_lbo(pt + kk * 2048, 8192),
+                        ID_KMN, kk > 0);
+            umma_commit(&bars[B_T]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == 15) {
+    // ------------------------------------------------------------ D_ws issuer
+    // Once S_n is published (named barrier 2): D_ws(n + 1) = (-W_{n+1}) S_n
+    // into buffer (n + 1) % 2 (after S_0 also D_ws(0) = (-W_0) S_0).
+    auto issue_ws = [&](int m) {
+      ok = mbar_spin(&bars[B_FULLW + (m & 1)], (m >> 1) & 1, kWaitLimit);
+      if (!ok) return;
+      const uint32_t wa = sb + OFF_W + (m & 1) * W_SLOT;
+      const uint32_t st = sb + OFF_S + ((m > 0 ? m - 1 : 0) & 1) * 16384;
+      const uint32_t d = tmem + T_WS + 64 * (m & 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_bf16(d, sdesc_sw128(wa + (kk >> 2) * 16384 + (kk & 3) * 32),
+                  sdesc_sw128_lbo(st + kk * 2048, 8192), ID_KMN, kk > 0);
+      umma_commit(&bars[B_WS + (m & 1)]);
+    };
+    for (int n = 0; n < N; ++n) {
+      nb_sync(2, 288);
+      if (lane == 0 && ok) {
+        tc_fence_after();
+        if (n == 0) issue_ws(0);
+        if (ok && n + 1 < N) issue_ws(n + 1);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 13) {
+    // ---------------------------------------------------------------- exporter
     if (lane == 0) {
-      constexpr uint32_t ID_R = idesc_bf16(128, 64, 0, 1);    // A K-major, B MN-major
-      constexpr uint32_t ID_QS = idesc_bf16(64, 64, 0, 1);
-      constexpr uint32_t ID_S = idesc_bf16(128, 64, 1, 1);    // A = k^T read MN-major
-      const uint32_t sb = smem_u32(sm);
-      const uint32_t stile = sb + S_TILE, rtile = sb + R_TILE, ptile = sb + P_TILE;
-      for (int n = 0; n < p.N; ++n) {
-        const int st = n % NST, ob = n & 1;
-        const uint32_t stg = sb + st * STAGE;
-        const uint32_t d_qs = tmem + T_O + 128 * ob, d_ar = d_qs + 64;
-        ok = ok && mbar_wait(&full[st], (n / NST) & 1, kWaitLimit);
-        ok = ok && mbar_wait(s_ready, n & 1, kWaitLimit);
-        tc_fence_after();
-        if (ok) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(tmem + T_R, sdesc_sw128(stg + ST_W + (kk >> 2) * 16384 + (kk & 3) * 32),
-                      sdesc_sw128_lbo(stile + kk * 2048, 8192), ID_R, kk > 0);
+      int nx = 0;
+      for (; nx < N && ok; ++nx) {
+        ok = mbar_wait(&bars[B_ES + (nx & 1)], (nx >> 1) & 1, kWaitLimit) &&
+             mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
+        if (!ok) break;
+        // The previous chunk's copies (issued a chunk ago) written: count them
+        // now, while nothing of this thread is in flight, so that the release
+        // does not wait for copies.
+        if (p.xflags && nx > 0) {
+          bulk_wait<0>();
+          fence_async_global();
+          red_release_add_gpu(p.xflags + chunk0 + nx - 1, 1u);
         }
-        umma_commit(r_done);
-        if (n >= 2) ok = ok && mbar_wait(&o_empty[ob], ((n >> 1) - 1) & 1, kWaitLimit);
-        tc_fence_after();
-        if (ok) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16(d_qs, sdesc_sw128(stg + ST_Q + (kk >> 2) * 8192 + (kk & 3) * 32),
-                      sdesc_sw128_lbo(stile + kk * 2048, 8192), ID_QS, kk > 0);
-        }
-        ok = ok && mbar_wait(rho_ready, n & 1, kWaitLimit);
-        tc_fence_after();
-        if (ok) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + T_S, sdesc_sw128_lbo(stg + ST_K + kk * 2048, 8192),
-                      sdesc_sw128_lbo(ptile + kk * 2048, 8192), ID_S, kk > 0);
-        }
-        umma_commit(ds_done);
-        if (ok) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d_ar, sdesc_sw128(stg + ST_AQ + kk * 32),
-                      sdesc_sw128_lbo(rtile + kk * 2048, 8192), ID_R, kk > 0);
-        }
-        umma_commit(&o_full[ob]);
-        umma_commit(&empty[st]);
+        // Both tiles of chunk nx out as one bulk group; once read out they may
+        // be rewritten.
+        uint8_t* xb = xbase + (size_t)nx * Xchg::BYTES;
+        bulk_store(xb + Xchg::S + vt * Xchg::S_TILE, sb + OFF_S + (nx & 1) * 16384, 16384);
+        bulk_store(xb + Xchg::R + vt * Xchg::R_TILE, sb + OFF_R + (nx & 1) * 8192, 8192);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&bars[B_XR + (nx & 1)]);
+      }
+      bulk_wait<0>();
+      if (p.xflags && nx > 0) {
+        fence_async_global();
+        red_release_add_gpu(p.xflags + chunk0 + nx - 1, 1u);
       }
     }
     __syncwarp();
   }
   if (!ok) atomicOr(p.error_word, kErrChainWait);
+
   tc_fence_before();
   nb_sync(1, CHAIN_THREADS);
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, CHAIN_TMEM);
   }
 }
 
-__global__ void __launch_bounds__(CHAIN_THREADS, 1)
-    chain_kernel(const __grid_constant__ chunk::Maps maps, Params p) {
+__global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  chain_role(maps, p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, false);
+  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, false);
 }
+
+// Output products of one (sequence, chunk n, 64 value columns vh): o = qscale
+// (q S_n) + A_qk r_n from the exchange block of chunk n (the S and r tiles of
+// value tiles 2 vh, 2 vh + 1) and the slab (A_qk, qscale), with raw q by TMA.
+//   D_qs = q [S_a | S_b]            M = 64,  N = 128 (two tiles of [hi 32 | lo 32]), K = 128
+//   D_ar = [A_hi; A_lo] [R_a | R_b] M = 128 (stacked), N = 128, K = 64
+// Shared-memory map (from a 1024-aligned base) and TMEM use of both forms that
+// compute them: the output kernel and a worker group of the one-launch forward.
+namespace out {
+constexpr int THREADS = 128;
+constexpr int Q = 0, AQ = 16384, S = 32768, R = 65536, QS = 81920, BAR = 82176;
+constexpr int SMEM = BAR + 64 + 1024;
+constexpr uint32_t TX = 16384 + 16384 + 32768 + 16384 + 256;
+constexpr uint32_t TMEM_COLS = 256;
+static_assert(QS + 256 <= chunk::OFF_SMALL, "output tiles inside a worker group region");
+
+// Loads of an output item (one thread), completing on `bar`.
+__device__ __forceinline__ void issue_loads(const CUtensorMap* qmap, const Params& p, uint32_t sb,
+                                            int seq, int n, int vh, uint64_t* bar) {
+  const int b = seq / p.HV, hv = seq % p.HV, h = hv / (p.HV / p.H);
+  const size_t idx = (size_t)seq * p.N + n;
+  const uint8_t* xb = p.xchg + idx * Xchg::BYTES;
+  mbar_expect_tx(bar, TX);
+  tma_load4(sb + Q, qmap, 0, h, n * C, b, bar);
+  tma_load4(sb + Q + 8192, qmap, 64, h, n * C, b, bar);
+  bulk_load(sb + AQ, p.slabs + idx * p.slab_bytes + Slab::AQ2, 16384, bar);
+  bulk_load(sb + S, xb + Xchg::S + 2 * vh * Xchg::S_TILE, 2 * Xchg::S_TILE, bar);
+  bulk_load(sb + R, xb + Xchg::R + 2 * vh * Xchg::R_TILE, 2 * Xchg::R_TILE, bar);
+  bulk_load(sb + QS, p.slabs + idx * p.slab_bytes + Slab::VEC, 256, bar);
+}
+// The two products (one thread), accumulators at TMEM columns 0-127 and 128-255.
+__device__ __forceinline__ void issue_mmas(uint32_t tmem, uint32_t sb) {
+  constexpr uint32_t ID_QS = idesc_bf16(64, 128, 0, 1);
+  constexpr uint32_t ID_AR = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(tmem, sdesc_sw128(sb + Q + (kk >> 2) * 8192 + (kk & 3) * 32),
+              sdesc_sw128_lbo(sb + S + kk * 2048, 16384), ID_QS, kk > 0);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    umma_bf16(tmem + 128, sdesc_sw128(sb + AQ + kk * 32),
+              sdesc_sw128_lbo(sb + R + kk * 2048, 8192), ID_AR, kk > 0);
+}
+// Writes 16 outputs of row t (value columns v0 .. v0 + 15) of head hv.
+__device__ __forceinline__ void store16(const Params& p, int b, int t, int hv, int v0, const float* o) {
+  const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0;
+  if (p.out_bf16) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                          pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+}
+}  // namespace out
 
 // =========================================================================== worker
 // Two groups of 8 warps run the chunk-local stage over chunk items in chunk
@@ -415,16 +626,10 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
   const int tid = threadIdx.x, warp = tid >> 5;
   const int grp = warp >> 3, gtid = tid & 255;
   uint8_t* sm = sm_base + grp * chunk::GROUP_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
   // The CTA's TMEM allocation (both groups' 256 columns) is recorded in the
   // TMEM slot of group 0, which produce_chunk leaves alone when given its columns.
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm_base + chunk::OFF_BAR) + 4;
-  if (gtid == 0) {
-    mbar_init(bars, 1);       // tiles k, q
-    mbar_init(bars + 1, 1);   // MMAs
-    mbar_init(bars + 3, 1);   // tiles v
-    mbar_fence_init();
-  }
+  if (gtid == 0) chunk::init_group_bars(sm);
   if (warp == 0) tmem_alloc(tslot, 2 * chunk::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -447,6 +652,75 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
     fence_async_global();
     st_release_gpu(pending, 1u);
   }
+  // Output items (chunk n, sequence, 64 value columns vh) in chunk order, each
+  // once the chains have counted all exports of its chunk. The MMA barrier
+  // completed two phases per production item, so its next phase has parity 0.
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
+  uint64_t* bar_mma = bar_tma + 1;
+  const uint32_t sb = smem_u32(sm);
+  const int lane = tid & 31, gw = gtid >> 5;
+  uint32_t mph = 0;
+  for (long it = G; it < items * 2; it += NG) {
+    const int n = (int)(it / (2 * nseq)), rem = (int)(it % (2 * nseq));
+    const int seq = rem >> 1, vh = rem & 1;
+    const int b = seq / p.HV, hv = seq % p.HV;
+    if (gtid == 0) {
+      bulk_wait_read<0>();     // the last production item's stores have read their staging
+      const unsigned int* xf = p.xflags + (size_t)seq * p.N + n;
+      long polls = 0;
+      while (ld_acquire_gpu(xf) < kXchgParts) {
+        if (++polls > p.wait_limit) {
+          atomicOr(p.error_word, kErrXchgWait);
+          break;
+        }
+        __nanosleep(64);
+      }
+      fence_async_global();     // exports (generic acquire) -> bulk reads
+      out::issue_loads(&maps.q, p, sb, seq, n, vh, bar_tma);
+      bool ok = mbar_wait(bar_tma, ph, kWaitLimit);
+      if (ok) {
+        tc_fence_after();
+        out::issue_mmas(tmem, sb);
+      } else {
+        atomicOr(p.error_word, kErrOutWait);
+      }
+      umma_commit(bar_mma);
+    }
+    ph ^= 1u;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, mph, kWaitLimit));
+    mph ^= 1u;
+    tc_fence_after();
+    // Warp gw: TMEM lane quadrant gw % 4, value tile u = gw / 4. Lanes 0-15 hold
+    // row i = 16 (gw % 4) + lane of D_qs and the hi rows of D_ar, lanes 16-31
+    // the lo rows of D_ar; the pair's sums are added by one shuffle, after
+    // which lane half keeps 16 of the tile's 32 columns.
+    const int qd = gw & 3, u = gw >> 2, half = lane >> 4;
+    const int i = 16 * qd + (lane & 15);
+    const uint32_t lb = (uint32_t)(32 * qd) << 16;
+    const float qs = reinterpret_cast<const float*>(sm + out::QS)[i];
+    float x[32];
+    {
+      float d[64];
+      tmem_ld64(tmem + lb + 64 * u, d);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = half ? 0.f : qs * (d[e] + d[32 + e]);
+      tmem_ld64(tmem + lb + 128 + 64 * u, d);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] += d[e] + d[32 + e];
+    }
+    float o[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float send = half ? x[e] : x[16 + e];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      o[e] = (half ? x[16 + e] : x[e]) + recv;
+    }
+    const int t = n * C + i;
+    if (ok && t < p.T) out::store16(p, b, t, hv, 64 * vh + 32 * u + 16 * half, o);
+    if (!ok && lane == 0) atomicOr(p.error_word, kErrOutWait);
+    tc_fence_before();
+    chunk::group_sync(1 + grp);   // smem and TMEM free for the next item
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -462,9 +736,101 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   const int cta = blockIdx.x;
   if (cta < n_chain) {
-    if (threadIdx.x < CHAIN_THREADS) chain_role(maps, p, sm, cta / VTILES, cta % VTILES, true);
+    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, true);
   } else {
     worker_role(maps, p, sm, cta - n_chain, n_workers);
+  }
+}
+
+// =========================================================================== outputs
+// The output pass after a finished recurrence: one CTA per (sequence, 64 value
+// columns vh, chunk n), the products of namespace out.
+struct OutMaps {
+  CUtensorMap q;
+};
+
+__global__ void __launch_bounds__(out::THREADS, 2)
+    output_kernel(const __grid_constant__ OutMaps maps, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const int vh = blockIdx.x & 1, seq = blockIdx.x >> 1, n = blockIdx.y;
+  const int b = seq / p.HV, hv = seq % p.HV;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + out::BAR);
+  uint64_t* mma_bar = bar + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init(mma_bar, 1);
+    mbar_fence_init();
+    out::issue_loads(&maps.q, p, smem_u32(sm), seq, n, vh, bar);
+  }
+  if (warp == 1) tmem_alloc(tslot, out::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  bool ok = true;
+  if (tid == 0) {
+    ok = mbar_wait(bar, 0, kWaitLimit);
+    if (ok) {
+      tc_fence_after();
+      out::issue_mmas(tmem, smem_u32(sm));
+    }
+    umma_commit(mma_bar);
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  ok = __all_sync(0xffffffffu, mbar_wait(mma_bar, 0, kWaitLimit)) && ok;
+  tc_fence_after();
+  // Warp w: rows i = 16 w + lane % 16 (lanes 0-15: D_qs rows and the hi rows of
+  // D_ar; lanes 16-31: the lo rows of D_ar). Column 64 u + x of either
+  // accumulator is tile u, part x / 32 (hi, lo), value column 32 u + x % 32 of
+  // this CTA's 64; lane half keeps tile u = half.
+  const int half = lane >> 4;
+  const int i = 16 * warp + (lane & 15);
+  const uint32_t lb = (uint32_t)(32 * warp) << 16;
+  const float qs = reinterpret_cast<const float*>(sm + out::QS)[i];
+  float x[2][32];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    float d[64];
+    tmem_ld64(tmem + lb + 64 * u, d);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[u][e] = half ? 0.f : qs * (d[e] + d[32 + e]);
+    tmem_ld64(tmem + lb + 128 + 64 * u, d);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[u][e] += d[e] + d[32 + e];
+  }
+  float o[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float send = half ? x[0][e] : x[1][e];       // the partner keeps tile 1 - half
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    o[e] = (half ? x[1][e] : x[0][e]) + recv;
+  }
+  const int t = n * C + i;
+  if (ok && t < p.T) {
+    const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + 64 * vh + 32 * half;
+    if (p.out_bf16) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                            pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+    } else {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    }
+  }
+  if (!ok && tid == 0) atomicOr(p.error_word, kErrOutWait);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, out::TMEM_COLS);
   }
 }
 
@@ -473,71 +839,77 @@ struct DeviceInfo {
   bool coop = false;
 };
 
-DeviceInfo device_info() {
+DeviceInfo& device_info() {
   static DeviceInfo cache[64];
   static bool known[64] = {};
+  static DeviceInfo none;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DeviceInfo{};
-  if (dev < 64 && known[dev]) return cache[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    none = DeviceInfo{};
+    return none;
+  }
+  if (known[dev]) return cache[dev];
   DeviceInfo d;
   int coop = 0;
   cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   d.coop = coop != 0;
-  if (dev < 64) {
-    cache[dev] = d;
-    known[dev] = true;
-  }
-  return d;
-}
-
-// Maps of the chain role: q, k inputs and the slab arrays (v is not read).
-bool chain_maps(chunk::Maps* m, const Params& p) {
-  memset(m, 0, sizeof *m);
-  const size_t nch = (size_t)p.B * p.HV * p.N;
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  return tmap_bthd(&m->q, p.q, p.B, p.T, p.H) && tmap_bthd(&m->k, p.k, p.B, p.T, p.H) &&
-         tmap_blocks(&m->aq2, p.slabs + Slab::AQ2, BF, 2, C, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
-         tmap_blocks(&m->w2, p.slabs + Slab::W2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
-         tmap_blocks(&m->u, p.slabs + Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, nch,
-                     p.slab_bytes, 32, 64, SW);
+  cache[dev] = d;
+  known[dev] = true;
+  return cache[dev];
 }
 
 }  // namespace
 
 gdr_status launch_chain(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode != 0) return GDR_ERR_UNSUPPORTED;
-  chunk::Maps m;
-  if (!chain_maps(&m, p)) return GDR_ERR_CUDA;
+  if (p.gate_mode != 0 || !p.xchg) return GDR_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            CHAIN_SMEM) != cudaSuccess)
     return GDR_ERR_CUDA;
+  Params q = p;
+  q.xflags = nullptr;       // the output pass is a separate launch: nothing counts exports
   dim3 grid(p.HV * VTILES, p.B);
-  chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM, stream>>>(m, p);
+  chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM, stream>>>(q);
+  return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status launch_outputs(const Params& p, cudaStream_t stream) {
+  if (p.gate_mode != 0 || !p.xchg) return GDR_ERR_UNSUPPORTED;
+  if (p.N > 65535) return GDR_ERR_UNSUPPORTED;
+  OutMaps m;
+  if (!tmap_bthd(&m.q, p.q, p.B, p.T, p.H)) return GDR_ERR_CUDA;
+  if (cudaFuncSetAttribute(output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           out::SMEM) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  dim3 grid(2 * p.B * p.HV, p.N);
+  output_kernel<<<grid, out::THREADS, out::SMEM, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 bool fused_fits(int B, int HV) {
-  const DeviceInfo dev = device_info();
+  const DeviceInfo& dev = device_info();
   const long long n_chain = (long long)B * HV * VTILES;
   // The workers must produce chunks about as fast as the chains consume them:
   // at least as many worker CTAs as chain CTAs.
-  return dev.coop && n_chain * 2 <= dev.sms;
+  return dev.coop && dev.sms > 0 && n_chain * 2 <= dev.sms;
 }
 
 gdr_status launch_fused(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode != 0 || !p.flags || !fused_fits(p.B, p.HV)) return GDR_ERR_UNSUPPORTED;
-  const DeviceInfo dev = device_info();
-  const long long n_chain = (long long)p.B * p.HV * VTILES;
-  const int n_workers = dev.sms - (int)n_chain;
+  if (p.gate_mode != 0 || !p.flags || !p.xflags || !p.xchg || !fused_fits(p.B, p.HV))
+    return GDR_ERR_UNSUPPORTED;
+  const DeviceInfo& dev = device_info();
+  const int n_chain = p.B * p.HV * VTILES;
+  const int n_workers = dev.sms - n_chain;
   chunk::Maps m;
   if (!chunk::make_maps(&m, p)) return GDR_ERR_CUDA;
   if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FUSED_SMEM) != cudaSuccess)
     return GDR_ERR_CUDA;
+  // Slab flags and export counts (adjacent in the workspace) start at zero.
   const size_t nch = (size_t)p.B * p.HV * p.N;
-  if (cudaMemsetAsync(p.flags, 0, nch * sizeof(unsigned int), stream) != cudaSuccess)
+  if (p.xflags != p.flags + nch) return GDR_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(p.flags, 0, 2 * nch * sizeof(unsigned int), stream) != cudaSuccess)
     return GDR_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dev.sms);
@@ -549,13 +921,12 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, m, p, (int)n_chain, n_workers);
-  if (e == cudaSuccess) return GDR_OK;
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, m, p, n_chain, n_workers);
+  if (e != cudaSuccess) {
     (void)cudaGetLastError();
-    return GDR_ERR_UNSUPPORTED;
+    return e == cudaErrorCooperativeLaunchTooLarge ? GDR_ERR_UNSUPPORTED : GDR_ERR_CUDA;
   }
-  return GDR_ERR_CUDA;
+  return GDR_OK;
 }
 
 }  // namespace fast

@@ -16,8 +16,10 @@
 //                                                      and the raw bf16 k / v tile as B
 // and writes the slab of gdr_fast.cuh. q, k and v arrive by TMA (128-byte
 // swizzle, zero fill past the end of the sequence, which is the zero padding of
-// the last chunk); accumulators live in TMEM; A_qk, -W and U are staged as
-// 128-byte swizzled tiles and leave by TMA stores. Each per-thread phase is
+// the last chunk); accumulators live in TMEM; A_qk, -W, U, -T and the key
+// tile are staged as 128-byte swizzled tiles whose byte images leave by bulk
+// copies (the recurrence loads them back the same way, which restores the
+// swizzled layout without a tensor map). Each per-thread phase is
 // spread over the 8 warps (two per TMEM lane quadrant, one per column half).
 //
 // The work of one chunk is the device function produce_chunk. It runs in the
@@ -33,15 +35,8 @@ namespace chunk {
 
 // Encodes the tensor maps of the chunk-local stage.
 bool make_maps(Maps* m, const Params& p) {
-  const size_t nch = (size_t)p.B * p.HV * p.N;
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   return tmap_bthd(&m->q, p.q, p.B, p.T, p.H) && tmap_bthd(&m->k, p.k, p.B, p.T, p.H) &&
-         tmap_bthd(&m->v, p.v, p.B, p.T, p.HV) &&
-         tmap_blocks(&m->aq2, p.slabs + Slab::AQ2, BF, 2, C, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
-         tmap_blocks(&m->w2, p.slabs + Slab::W2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 128, SW) &&
-         tmap_blocks(&m->u, p.slabs + Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, nch,
-                     p.slab_bytes, 32, 64, SW);
+         tmap_bthd(&m->v, p.v, p.B, p.T, p.HV);
 }
 
 }  // namespace chunk
@@ -54,12 +49,7 @@ __global__ void __launch_bounds__(chunk::THREADS, 2) chunk_tc_kernel(
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(bars, 1);       // tiles k, q
-    ptx::mbar_init(bars + 1, 1);   // MMAs
-    ptx::mbar_init(bars + 3, 1);   // tiles v
-    ptx::mbar_fence_init();
-  }
+  if (threadIdx.x == 0) chunk::init_group_bars(sm);
   // (the first barrier inside produce_chunk orders the initialisation before
   // any wait; only thread 0 uses the barriers before it)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);

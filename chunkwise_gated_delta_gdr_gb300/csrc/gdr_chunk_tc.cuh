@@ -38,6 +38,8 @@ constexpr int OFF_XU = 65536;      // XU (16 KB), written once L and the A_qk st
 constexpr int LDX = 68;            // fp32 row stride of X
 constexpr int OFF_X = 84992;       // X = (I + L)^-1 [64][LDX] fp32
 constexpr int OFF_T = 8192;        // block-product scratch [32][36] fp32 (in the dead q tile)
+constexpr int OFF_KP = 86016;      // previous chunk's k tile (16 KB), in the dead X region;
+                                   // later the -T hi / lo staging box
 constexpr int OFF_SMALL = 102400;  // G, nq, nk, beta, column factor (5 x 64 fp32)
 constexpr int OFF_BAR = 103680;    // mbarriers + TMEM slot
 constexpr int GROUP_BYTES = 104448;            // one group's region (1 KB multiple)
@@ -52,11 +54,28 @@ static_assert(OFF_XU + 16384 <= OFF_X && OFF_US + 32768 <= OFF_X, "staging overl
 static_assert(OFF_X + 64 * LDX * 4 <= OFF_SMALL, "X overlaps");
 static_assert(OFF_T + 32 * 36 * 4 <= OFF_K1, "scratch overlaps the k tile");
 static_assert(OFF_BAR + 64 <= GROUP_BYTES, "group region");
+static_assert(OFF_KP % 1024 == 0 && OFF_KP >= OFF_X && OFF_KP + 16384 <= OFF_SMALL,
+              "previous k tile inside the dead X region");
+// mbarriers at OFF_BAR (the caller initialises them, count 1 each): +0 k and q
+// tiles, +8 MMAs, +16 TMEM slot and split flag (not a barrier), +24 v tiles,
+// +32 previous chunk's k tile, +40 the T product.
+constexpr int kNumBars = 6;
 
 struct Maps {
   CUtensorMap q, k, v;          // [B, T, heads, 128] bf16 inputs
-  CUtensorMap aq2, w2, u;       // slab arrays (stores)
 };
+
+// Initialises the mbarriers of a group region (one thread, then an
+// mbarrier-init fence; the group barrier that follows orders it before use).
+__device__ __forceinline__ void init_group_bars(uint8_t* sm) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  mbar_init(bars + 0, 1);
+  mbar_init(bars + 1, 1);
+  mbar_init(bars + 3, 1);
+  mbar_init(bars + 4, 1);
+  mbar_init(bars + 5, 1);
+  mbar_fence_init();
+}
 
 // Encodes the tensor maps of the chunk-local stage (false: the driver refused).
 bool make_maps(Maps* m, const Params& p);
@@ -99,6 +118,8 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tma + 2);
   int* split_ok = reinterpret_cast<int*>(tslot + 1);   // decay factorisation allowed
   uint64_t* bar_v = bar_tma + 3;                       // v tiles (read by MMA 3 only)
+  uint64_t* bar_kp = bar_tma + 4;                      // previous chunk's k tile
+  uint64_t* bar_t = bar_tma + 5;                       // T product
   uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
 
   // The input tiles are requested first: before the TMEM allocation and the
@@ -146,6 +167,13 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tma, ph, kWaitLimit));
   if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
   if (tid < C) bb[tid] = bv;   // read after the next group barrier
+  // The key tile's image (the recurrence's A operand k^T) goes to the slab as
+  // it is; it must be read out before epilogue 2 overwrites the tile.
+  if (tid == 0) {
+    bulk_store(slab + Slab::K2, smem_u32(sm + OFF_K0), 8192);
+    bulk_store(slab + Slab::K2 + 8192, smem_u32(sm + OFF_K1), 8192);
+    bulk_commit();
+  }
 
   // ---- MMA 1: D[0:128, 0:64] = [k; q] k^T -------------------------------------
   if (ok && tid == 0) {
@@ -307,7 +335,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   // warps 2-7 while warps 0-1 run level 0 of the inverse.
   constexpr int kRowTid = 64;          // first thread of the row-factor warps
   if (tid == kRowTid) {
-    tma_store3(&maps.aq2, smem_u32(sm + OFF_AQS), 0, 0, idx);
+    bulk_store(slab + Slab::AQ2, smem_u32(sm + OFF_AQS), 16384);
     bulk_commit();
   }
   {
@@ -359,8 +387,22 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   fence_async_shared();
   tc_fence_before();
   group_sync(bar_id);
+  // X is dead: the previous chunk's keys (for T) go where it was. The first
+  // chunk of a sequence has none; its barriers complete a phase all the same,
+  // so that a group's barrier phases stay one per chunk.
+  if (tid == 0) {
+    if (n > 0) {
+      mbar_expect_tx(bar_kp, 2 * 8192);
+      tma_load4(smem_u32(sm + OFF_KP), &maps.k, 0, h, t0 - C, b, bar_kp);
+      tma_load4(smem_u32(sm + OFF_KP + 8192), &maps.k, 64, h, t0 - C, b, bar_kp);
+    } else {
+      mbar_arrive(bar_kp);
+      mbar_arrive(bar_t);
+    }
+  }
 
   // ---- MMA 2/3: D_W = XW k (TMEM cols 0-127), D_U = XU v (cols 128-255) ----------
+  if (tid == 0) bulk_wait_read<0>();                 // key image read out (epilogue 2 reuses the tile)
   if (ok && tid == 0) {
     ok = mbar_wait(bar_v, ph, kWaitLimit);           // the v tiles (normally long arrived)
     if (!ok) atomicOr(p.error_word, kErrTmaWait);
@@ -433,10 +475,65 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   tc_fence_before();
   group_sync(bar_id);
   if (tid == 0) {
-    const uint32_t ws = smem_u32(sm + OFF_WS), us = smem_u32(sm + OFF_US);
-    for (int bx = 0; bx < 2; ++bx) tma_store3(&maps.w2, ws + bx * 16384, 64 * bx, 0, idx);
-    for (int bx = 0; bx < 4; ++bx) tma_store3(&maps.u, us + bx * 8192, 32 * bx, 0, idx);
+    bulk_store(slab + Slab::W2, smem_u32(sm + OFF_WS), 32768);
+    bulk_store(slab + Slab::U, smem_u32(sm + OFF_US), 32768);
     bulk_commit();
+  }
+
+  // ---- T = W k_prev^T for the recurrence's look-ahead (not for the first chunk) ----
+  // A = the -W hi / lo staging (stacked rows, K-major, two 64-column boxes),
+  // B = the previous chunk's raw key tile (K-major: rows j, channels
+  // contiguous): D_T [128 stacked rows][64 j] in TMEM columns 0-63, whose hi
+  // and lo rows are added like W's. -T leaves as one stacked [128][64] box
+  // staged over the (then dead) key tile.
+  if (n > 0) {
+    if (ok && tid == 0) {
+      ok = mbar_wait(bar_kp, ph, kWaitLimit);
+      if (!ok) atomicOr(p.error_word, kErrTmaWait);
+    }
+    if (ok && tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t id = idesc_bf16(128, 64, 0, 0);
+      const uint32_t ws = smem_u32(sm + OFF_WS), kp = smem_u32(sm + OFF_KP);
+#pragma unroll
+      for (int s = 0; s < K / 16; ++s)
+        umma_bf16(tmem, sdesc_sw128(ws + (s >> 2) * 16384 + (s & 3) * 32),
+                  sdesc_sw128(kp + (s >> 2) * 8192 + (s & 3) * 32), id, s > 0);
+      umma_commit(bar_t);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_t, ph, kWaitLimit));
+    if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
+    tc_fence_after();
+    if (ok) {
+      const int r = 16 * quad + (lane & 15);
+      const int half = lane >> 4;
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * colh, v);
+      float t[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float send = half ? v[e] : v[16 + e];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        t[e] = (half ? v[16 + e] : v[e]) + recv;     // (-W) k_prev^T: already -T
+      }
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) split_pair(t[e], t[e + 1], hi[e / 2], lo[e / 2]);
+      const int c = (32 * colh + 16 * half) >> 3;
+      uint8_t* tb = sm + OFF_KP;
+      const int rh = stacked_row(r, 0), rl = stacked_row(r, 1);
+      *reinterpret_cast<uint4*>(tb + box_off(rh, c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(tb + box_off(rh, c + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      *reinterpret_cast<uint4*>(tb + box_off(rl, c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(tb + box_off(rl, c + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    }
+    fence_async_shared();
+    tc_fence_before();
+    group_sync(bar_id);
+    if (tid == 0) {
+      bulk_store(slab + Slab::T2, smem_u32(sm + OFF_KP), 16384);
+      bulk_commit();
+    }
   }
   return ok;
 }

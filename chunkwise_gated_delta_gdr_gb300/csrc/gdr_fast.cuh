@@ -1,17 +1,21 @@
 // gdr_fast.cuh -- shared definitions of the fast path (bf16, K = V = 128, C = 64).
 //
-// The fast path has two stages:
+// The fast path has three stages:
 //   1. a chunk-local stage (one chunk per CTA or per worker group) writes, per
 //      chunk, the operands of the inter-chunk recurrence into a workspace slab:
 //      gdr_chunk_tc.cu (tcgen05, scalar gate) or gdr_chunk_kda.cu (mma.sync,
 //      per-key gate);
 //   2. a recurrence stage runs the chunks in order per (batch, value head,
-//      V tile) and writes the outputs: gdr_chain.cu (scalar gate, tcgen05) or
-//      gdr_state_kda.cu (per-key gate, tcgen05).
-// For the scalar gate gdr_chain.cu can also run both stages in one cooperative
-// launch: worker CTAs produce the slabs in chunk order and raise one flag per
-// chunk, chain CTAs consume them as they appear.
-// This header fixes the slab format both stages agree on.
+//      V tile): gdr_chain.cu (scalar gate, tcgen05, the state and r of every
+//      chunk exported to an exchange area) or gdr_state_kda.cu (per-key gate,
+//      tcgen05, outputs written with the states);
+//   3. scalar gate: an output pass forms o from the exchange (gdr_chain.cu).
+// For the scalar gate, all three can also run in one cooperative launch:
+// worker CTAs produce the slabs in chunk order and raise one flag per chunk,
+// chain CTAs consume them as they appear and count their exports per chunk,
+// and the workers then form the outputs of each chunk once its exports are
+// complete.
+// This header fixes the slab and exchange formats the stages agree on.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,34 +39,60 @@ __host__ __device__ constexpr int stacked_row(int i, int lo) { return 32 * (i >>
 
 // Slab of one chunk (b, hv, n), chunk index ((b * HV + hv) * N + n). All
 // offsets in bytes from the slab start; every array is 16-byte aligned.
-//   W2   [2C][K] bf16  hi / lo of -W, W = M^-1 (exp(G) k_hat). Scalar gate:
-//                      the two parts stacked by stacked_row; per-key gate: hi
-//                      rows 0 .. C-1, then lo rows.
-//   AQ2  [2C][C] bf16  hi / lo of A_qk (beta on its columns, zero above the
-//                      diagonal), arranged like W2.
-//   U    [C][V]    fp32  U = M^-1 v
-//   VEC  qscale[C], kscale[C], gamma[K] fp32
-//        scalar gate: qscale_i = scale |q_i|^-1 exp(G_i), kscale_j = beta_j |k_j|^-1
-//        exp(G_last - G_j), gamma = exp(G_last) on every channel;
-//        per-key gate: qscale = kscale = 1, gamma_c = exp(G_last,c)
-//   QB2  [2][C][K] bf16  per-key gate only: hi / lo of scale q_hat exp(G)
-//   KB2  [2][C][K] bf16  per-key gate only: hi / lo of beta k_hat exp(G_last - G)
-// For the scalar gate the recurrence reads raw q and k from the inputs (exact
-// in bf16) and applies qscale / kscale as fp32 row factors.
+// Scalar gate: every array except VEC is the byte image of a 128-byte swizzled
+// shared-memory tile (the chunk-local stage stores its staging tiles with bulk
+// copies; a bulk copy into a 1024-aligned tile restores the layout):
+//   W2   -W hi / lo stacked by stacked_row: two [2C][64] bf16 boxes (channel halves)
+//   AQ2  A_qk hi / lo (beta on its columns, zero above the diagonal), stacked: [2C][C] bf16
+//   U    U = M^-1 v: four [C][32] fp32 boxes, box t = value columns 32 t .. 32 t + 31
+//   VEC  qscale[C], kscale[C], gamma[K] fp32 (plain)
+//   T2   -T hi / lo stacked, T = W k_prev^T with k_prev the raw keys of the
+//        previous chunk of the sequence (not written for the first chunk): [2C][C] bf16
+//   K2   the chunk's raw keys: two [C][64] bf16 boxes (channel halves)
+// with qscale_i = scale |q_i|^-1 exp(G_i), kscale_j = beta_j |k_j|^-1
+// exp(G_last - G_j), gamma = exp(G_last) on every channel; the recurrence
+// applies them as fp32 row factors to the exact bf16 q and k.
+// Per-key gate (plain row-major arrays, read by TMA tensor loads):
+//   W2   [2][C][K] bf16  hi / lo of -W, W = M^-1 (exp(G) k_hat)
+//   AQ2  [2][C][C] bf16  hi / lo of A_qk
+//   U    [C][V]    fp32
+//   VEC  qscale = kscale = 1, gamma_c = exp(G_last,c)
+//   QB2  [2][C][K] bf16  hi / lo of scale q_hat exp(G)
+//   KB2  [2][C][K] bf16  hi / lo of beta k_hat exp(G_last - G)
 struct Slab {
   static constexpr size_t W2 = 0;
   static constexpr size_t AQ2 = W2 + 2ull * C * K * 2;
   static constexpr size_t U = AQ2 + 2ull * C * C * 2;
   static constexpr size_t VEC = U + (size_t)C * V * 4;
-  static constexpr size_t QB2 = VEC + (size_t)(2 * C + K) * 4;
+  static constexpr size_t T2 = VEC + (size_t)(2 * C + K) * 4;
+  static constexpr size_t K2 = T2 + 2ull * C * C * 2;
+  static constexpr size_t QB2 = T2;
   static constexpr size_t KB2 = QB2 + 2ull * C * K * 2;
-  static constexpr size_t SCALAR_BYTES = QB2;
+  static constexpr size_t SCALAR_BYTES = K2 + (size_t)C * K * 2;
   static constexpr size_t PERKEY_BYTES = KB2 + 2ull * C * K * 2;
   static constexpr size_t bytes(int gate_mode) { return gate_mode ? PERKEY_BYTES : SCALAR_BYTES; }
 };
 static_assert(Slab::AQ2 % 16 == 0 && Slab::U % 16 == 0 && Slab::VEC % 16 == 0 &&
-                  Slab::QB2 % 16 == 0 && Slab::KB2 % 16 == 0,
+                  Slab::T2 % 16 == 0 && Slab::K2 % 16 == 0 && Slab::QB2 % 16 == 0 &&
+                  Slab::KB2 % 16 == 0 && Slab::SCALAR_BYTES % 16 == 0,
               "slab arrays must stay 16-byte aligned");
+
+// Exchange block of one chunk (scalar gate): what the chain CTAs of the
+// sequence export for the output pass, as the byte images of their shared
+// tiles (128-byte swizzled rows, the layout the output products read):
+//   S  [4 tiles][128 c][S_hi 32 | S_lo 32] bf16   the state at the chunk start,
+//                                                 tile t = value columns 32 t ..
+//   R  [4 tiles][64 j][r_hi 32 | r_lo 32] bf16    r = U - W S, same columns
+// Exports of one chunk a one-launch forward counts before its outputs are
+// formed: one per chain CTA (its S and r tiles).
+constexpr unsigned int kXchgParts = 4;
+struct Xchg {
+  static constexpr size_t S_TILE = 128ull * 64 * 2;
+  static constexpr size_t R_TILE = 64ull * 64 * 2;
+  static constexpr size_t S = 0;
+  static constexpr size_t R = S + 4 * S_TILE;
+  static constexpr size_t BYTES = R + 4 * R_TILE;
+};
 
 // Everything both stages of the fast path need.
 struct Params {
@@ -75,8 +105,11 @@ struct Params {
   void* out;                // [B, T, HV, V]
   float* sT;                // [B, HV, K, V] or null
   uint8_t* slabs;           // N * B * HV slabs
+  uint8_t* xchg;            // N * B * HV exchange blocks (scalar gate), else null
   unsigned int* flags;      // one per chunk (slab index): nonzero once its slab is written
                             // (one-launch forward of the scalar gate), else null
+  unsigned int* xflags;     // one per chunk: count of its exports (S and r tiles) written,
+                            // kXchgParts when complete (one-launch forward), else null
   unsigned int* error_word;
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;
@@ -97,6 +130,8 @@ inline __host__ __device__ size_t slab_index(const Params& p, int b, int hv, int
 // Launchers.
 // Scalar gate: recurrence after a finished chunk-local stage (gdr_chain.cu).
 gdr_status launch_chain(const Params& p, cudaStream_t stream);
+// Scalar gate: the output pass over the exchange of a finished recurrence.
+gdr_status launch_outputs(const Params& p, cudaStream_t stream);
 // Scalar gate: both stages in one cooperative launch (gdr_chain.cu); declines
 // with GDR_ERR_UNSUPPORTED (nothing enqueued) when it does not pay.
 gdr_status launch_fused(const Params& p, cudaStream_t stream);

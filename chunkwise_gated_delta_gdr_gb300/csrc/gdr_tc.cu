@@ -7,7 +7,9 @@ namespace gdr {
 
 bool tc_supported(const Problem& p) {
   // SSD with the per-key gate stays on the general path.
-  return !(p.ssd && p.gate_mode) && p.in_bf16 && p.K == fast::K && p.V == fast::V && p.C == fast::C;
+  // (the scalar gate's output pass puts the chunk index in gridDim.y)
+  return !(p.ssd && p.gate_mode) && p.in_bf16 && p.K == fast::K && p.V == fast::V &&
+         p.C == fast::C && (p.gate_mode != 0 || p.N <= 65535);
 }
 
 namespace {
@@ -17,10 +19,11 @@ namespace {
 constexpr long long kDefaultWaitLimit = 1LL << 24;
 std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 
-// Workspace body of the fast path: the chunk slabs, then (scalar gate) one
-// ready flag per chunk for the one-launch forward.
+// Workspace body of the fast path: the chunk slabs, then (scalar gate) the
+// exchange blocks the recurrence writes for the output pass, and one ready
+// flag and one export count per chunk for the one-launch forward.
 struct TcLayout {
-  size_t flags = 0, total = 0;
+  size_t xchg = 0, flags = 0, total = 0;
 };
 
 TcLayout tc_layout(const Problem& p) {
@@ -28,9 +31,12 @@ TcLayout tc_layout(const Problem& p) {
   TcLayout L;
   size_t off = nch * fast::Slab::bytes(p.gate_mode);
   if (p.gate_mode == 0) {
+    off = align_up(off, 1024);
+    L.xchg = off;
+    off += nch * fast::Xchg::BYTES;
     off = align_up(off, 256);
     L.flags = off;
-    off += nch * sizeof(unsigned int);
+    off += 2 * nch * sizeof(unsigned int);   // slab ready flags, then export counts
   }
   L.total = off;
   return L;
@@ -61,7 +67,9 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.sT = p.sT;
   f.slabs = static_cast<uint8_t*>(ws_body);
   const TcLayout L = tc_layout(p);
+  f.xchg = p.gate_mode == 0 ? f.slabs + L.xchg : nullptr;
   f.flags = p.gate_mode == 0 ? reinterpret_cast<unsigned int*>(f.slabs + L.flags) : nullptr;
+  f.xflags = f.flags ? f.flags + (size_t)p.B * p.HV * p.N : nullptr;
   f.error_word = error_word;
   f.B = p.B;
   f.T = p.T;
@@ -78,7 +86,7 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
   f.wait_limit = (long)g_wait_limit.load();
   // Both stages in one call, scalar gate: one cooperative launch when the
-  // chains leave enough SMs to the producers.
+  // chains leave enough SMs to the producers (it enqueues the output pass too).
   if (stage == 3 && p.gate_mode == 0 && p.recur_mode == 0) {
     const gdr_status st = fast::launch_fused(f, stream);
     if (st != GDR_ERR_UNSUPPORTED) return st;
@@ -88,10 +96,15 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
     if (st != GDR_OK) return st;
   }
   if (stage & 2) {
-    // Both recurrence kernels write the outputs with the states: there is no
-    // separate output pass (recur_mode 2).
-    if (p.recur_mode == 2) return GDR_OK;
-    return p.gate_mode ? fast::launch_state_kda_tc(f, stream) : fast::launch_chain(f, stream);
+    // The per-key recurrence writes the outputs with the states (no separate
+    // output pass, recur_mode 2 is nothing); the scalar-gate chain leaves them
+    // to the output pass (recur_mode 1: the states alone).
+    if (p.gate_mode) return p.recur_mode == 2 ? GDR_OK : fast::launch_state_kda_tc(f, stream);
+    if (p.recur_mode != 2) {
+      const gdr_status st = fast::launch_chain(f, stream);
+      if (st != GDR_OK || p.recur_mode == 1) return st;
+    }
+    return fast::launch_outputs(f, stream);
   }
   return GDR_OK;
 }

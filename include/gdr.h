@@ -212,9 +212,10 @@ int64_t gdr_set_flag_wait_limit(int64_t polls);
  * Arguments, layouts and errors are those of gdr_chunk_fwd, minus the
  * workspace. Sizes whose gdr_chunk_fwd_workspace_size() exceeds
  * GDR_NOALLOC_SCRATCH_BYTES are rejected with GDR_ERR_WORKSPACE before
- * anything is enqueued. 64 MiB fits, for example, B=1, T=4096, 12 value heads,
- * K=V=128, C=64, scalar gate, bf16 inputs (a workspace of about 63.7 MB); the
- * same call with 16 value heads (about 85 MB) does not.
+ * anything is enqueued. 64 MiB fits, for example, B=1, T=4096, 4 value heads,
+ * K=V=128, C=64, scalar gate, bf16 inputs (a workspace of about 54.8 MB); the
+ * same call with 5 value heads (about 68.5 MB) does not. (The scalar-gate fast
+ * path needs about 214 KB per chunk of 64 tokens and value head.)
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream

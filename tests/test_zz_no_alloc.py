@@ -71,13 +71,18 @@ def test_noalloc_alternating_paths():
 
 
 def test_noalloc_documented_size():
-    """The example the header gives as fitting the scratch: B=1, T=4096, 12
-    value heads, K=V=128, C=64, scalar gate, bf16 inputs."""
-    w = gin.WORKLOADS["gdn_t4096_h12"]
+    """The examples the header gives: B=1, T=4096, 4 value heads, K=V=128,
+    C=64, scalar gate, bf16 inputs fits the scratch (and runs); 5 value heads
+    does not."""
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], H=4, HV=4)
+    assert (w.B, w.T, w.HV, w.K, w.V, w.C) == (1, 4096, 4, 128, 128, 64)
     dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
-    assert (w.B, w.T, w.HV, w.K, w.V, w.C) == (1, 4096, 12, 128, 128, 64)
-    assert gdr.chunk_fwd_workspace_size(dims, w.C, w.gate_mode) <= gdr.GDR_NOALLOC_SCRATCH_BYTES
-    _compare("gdn_t4096_h12", dict(), 0)
+    size = gdr.chunk_fwd_workspace_size(dims, w.C, w.gate_mode)
+    assert size <= gdr.GDR_NOALLOC_SCRATCH_BYTES and abs(size / 1e6 - 54.8) < 0.05
+    dims5 = gdr.make_dims(w.B, w.T, 5, 5, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    size5 = gdr.chunk_fwd_workspace_size(dims5, w.C, w.gate_mode)
+    assert size5 > gdr.GDR_NOALLOC_SCRATCH_BYTES and abs(size5 / 1e6 - 68.5) < 0.05
+    _compare("gdn_t4096_h12", dict(H=4, HV=4), 0)
 
 
 def test_noalloc_reports_a_device_timeout():
