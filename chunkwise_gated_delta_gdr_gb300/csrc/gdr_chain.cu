@@ -62,15 +62,17 @@
 //
 // One-launch forward (launch_fused): one cooperative launch of one CTA per SM.
 // The first CTAs are the chains; the other CTAs are workers, two groups of 8
-// warps each, that first run the chunk-local stage (gdr_chunk_tc.cuh) over the
+// warps each, that run the chunk-local stage (gdr_chunk_tc.cuh) over the
 // chunks in chunk order, raising each chunk's flag once its slab is in global
-// memory, and then form the outputs of the chunks in chunk order. A chain's
-// TMA warp waits for chunk n's flag before loading it; the chain counts each
-// export of chunk n once it is in global memory, and a worker forms the
-// outputs of chunk n once the count is complete. Workers wait on chains only
-// after their last slab, and all CTAs are co-resident, so the waits end; every
-// wait is bounded all the same and records a code in the workspace error word
-// when it gives up, after which the CTA runs to its end.
+// memory. A chain's TMA warp waits for chunk n's flag before loading it.
+// Workers never wait on chains and all CTAs are co-resident, so the waits end;
+// every wait is bounded all the same and records a code in the workspace
+// error word when it gives up, after which the CTA runs to its end. The output
+// pass follows as a second launch: a GPU-scope acquire or release by any
+// thread of a chain CTA waits until every memory operation in flight on its
+// SM (the ring loads included) has completed, a microsecond or more, so the
+// chains signal nothing per chunk; they acquire the workers' slab flags as
+// rarely as they can (every flag already set at once).
 #include <string.h>
 
 #include <cuda.h>
@@ -91,12 +93,9 @@ constexpr int CHAIN_THREADS = 512;
 constexpr int FUSED_THREADS = 512;      // worker CTA: two chunk groups of 256
 constexpr long kWaitLimit = 1L << 24;   // mbarrier polls before a wait gives up
 constexpr long kTmaIdleLimit = 1L << 24;  // TMA event-loop rounds (64 ns sleeps) likewise
-// A release or a proxy fence waits for all memory operations of its thread in
-// flight (bulk copies included), some microseconds here: the exporter counts a
-// chunk's exports only when it has no copies in flight, and the TMA producer
-// acquires up to kFlagWindow slab flags at once.
-constexpr int kFlagWindow = 8;
-constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u, kErrXchgWait = 32u;
+// Slab flags the TMA producer reads at once (one acquire for all of those set).
+constexpr int kFlagWindow = 32;
+constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u;
 
 // Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
 // of two slots, each slot released as soon as its last reader is done:
@@ -387,10 +386,16 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         if (flags_ok && nflag < N && nflag < lead + 2) {
           polled = true;
           // The next flags (chunk slabs are written by workers of this
-          // launch): every consecutive one already set, then one acquire.
+          // launch): kFlagWindow of them read at once, then one acquire for
+          // the run of those already set.
+          unsigned int f[kFlagWindow];
+#pragma unroll
+          for (int z = 0; z < kFlagWindow; ++z)
+            f[z] = nflag + z < N ? ld_relaxed_gpu(p.flags + chunk0 + nflag + z) : 0u;
           int m = nflag;
-          const int lim = nflag + kFlagWindow < N ? nflag + kFlagWindow : N;
-          while (m < lim && ld_relaxed_gpu(p.flags + chunk0 + m) != 0u) ++m;
+#pragma unroll
+          for (int z = 0; z < kFlagWindow; ++z)
+            if (m == nflag + z && f[z] != 0u) ++m;
           if (m > nflag) {
             fence_acq_rel_gpu();                         // acquire the slabs' writes
             fence_async_global();                        // ... for the bulk reads
@@ -510,19 +515,10 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   } else if (warp == 13) {
     // ---------------------------------------------------------------- exporter
     if (lane == 0) {
-      int nx = 0;
-      for (; nx < N && ok; ++nx) {
+      for (int nx = 0; nx < N && ok; ++nx) {
         ok = mbar_wait(&bars[B_ES + (nx & 1)], (nx >> 1) & 1, kWaitLimit) &&
              mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
         if (!ok) break;
-        // The previous chunk's copies (issued a chunk ago) written: count them
-        // now, while nothing of this thread is in flight, so that the release
-        // does not wait for copies.
-        if (p.xflags && nx > 0) {
-          bulk_wait<0>();
-          fence_async_global();
-          red_release_add_gpu(p.xflags + chunk0 + nx - 1, 1u);
-        }
         // Both tiles of chunk nx out as one bulk group; once read out they may
         // be rewritten.
         uint8_t* xb = xbase + (size_t)nx * Xchg::BYTES;
@@ -533,10 +529,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         mbar_arrive(&bars[B_XR + (nx & 1)]);
       }
       bulk_wait<0>();
-      if (p.xflags && nx > 0) {
-        fence_async_global();
-        red_release_add_gpu(p.xflags + chunk0 + nx - 1, 1u);
-      }
     }
     __syncwarp();
   }
@@ -562,15 +554,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
 // value tiles 2 vh, 2 vh + 1) and the slab (A_qk, qscale), with raw q by TMA.
 //   D_qs = q [S_a | S_b]            M = 64,  N = 128 (two tiles of [hi 32 | lo 32]), K = 128
 //   D_ar = [A_hi; A_lo] [R_a | R_b] M = 128 (stacked), N = 128, K = 64
-// Shared-memory map (from a 1024-aligned base) and TMEM use of both forms that
-// compute them: the output kernel and a worker group of the one-launch forward.
+// Shared-memory map (from a 1024-aligned base) and TMEM use of the output kernel.
 namespace out {
 constexpr int THREADS = 128;
 constexpr int Q = 0, AQ = 16384, S = 32768, R = 65536, QS = 81920, BAR = 82176;
 constexpr int SMEM = BAR + 64 + 1024;
 constexpr uint32_t TX = 16384 + 16384 + 32768 + 16384 + 256;
 constexpr uint32_t TMEM_COLS = 256;
-static_assert(QS + 256 <= chunk::OFF_SMALL, "output tiles inside a worker group region");
 
 // Loads of an output item (one thread), completing on `bar`.
 __device__ __forceinline__ void issue_loads(const CUtensorMap* qmap, const Params& p, uint32_t sb,
@@ -598,22 +588,6 @@ __device__ __forceinline__ void issue_mmas(uint32_t tmem, uint32_t sb) {
   for (int kk = 0; kk < 4; ++kk)
     umma_bf16(tmem + 128, sdesc_sw128(sb + AQ + kk * 32),
               sdesc_sw128_lbo(sb + R + kk * 2048, 8192), ID_AR, kk > 0);
-}
-// Writes 16 outputs of row t (value columns v0 .. v0 + 15) of head hv.
-__device__ __forceinline__ void store16(const Params& p, int b, int t, int hv, int v0, const float* o) {
-  const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0;
-  if (p.out_bf16) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-      dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
-                          pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
-  } else {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-  }
 }
 }  // namespace out
 
@@ -651,75 +625,6 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
     bulk_wait<0>();
     fence_async_global();
     st_release_gpu(pending, 1u);
-  }
-  // Output items (chunk n, sequence, 64 value columns vh) in chunk order, each
-  // once the chains have counted all exports of its chunk. The MMA barrier
-  // completed two phases per production item, so its next phase has parity 0.
-  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
-  uint64_t* bar_mma = bar_tma + 1;
-  const uint32_t sb = smem_u32(sm);
-  const int lane = tid & 31, gw = gtid >> 5;
-  uint32_t mph = 0;
-  for (long it = G; it < items * 2; it += NG) {
-    const int n = (int)(it / (2 * nseq)), rem = (int)(it % (2 * nseq));
-    const int seq = rem >> 1, vh = rem & 1;
-    const int b = seq / p.HV, hv = seq % p.HV;
-    if (gtid == 0) {
-      bulk_wait_read<0>();     // the last production item's stores have read their staging
-      const unsigned int* xf = p.xflags + (size_t)seq * p.N + n;
-      long polls = 0;
-      while (ld_acquire_gpu(xf) < kXchgParts) {
-        if (++polls > p.wait_limit) {
-          atomicOr(p.error_word, kErrXchgWait);
-          break;
-        }
-        __nanosleep(64);
-      }
-      fence_async_global();     // exports (generic acquire) -> bulk reads
-      out::issue_loads(&maps.q, p, sb, seq, n, vh, bar_tma);
-      bool ok = mbar_wait(bar_tma, ph, kWaitLimit);
-      if (ok) {
-        tc_fence_after();
-        out::issue_mmas(tmem, sb);
-      } else {
-        atomicOr(p.error_word, kErrOutWait);
-      }
-      umma_commit(bar_mma);
-    }
-    ph ^= 1u;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, mph, kWaitLimit));
-    mph ^= 1u;
-    tc_fence_after();
-    // Warp gw: TMEM lane quadrant gw % 4, value tile u = gw / 4. Lanes 0-15 hold
-    // row i = 16 (gw % 4) + lane of D_qs and the hi rows of D_ar, lanes 16-31
-    // the lo rows of D_ar; the pair's sums are added by one shuffle, after
-    // which lane half keeps 16 of the tile's 32 columns.
-    const int qd = gw & 3, u = gw >> 2, half = lane >> 4;
-    const int i = 16 * qd + (lane & 15);
-    const uint32_t lb = (uint32_t)(32 * qd) << 16;
-    const float qs = reinterpret_cast<const float*>(sm + out::QS)[i];
-    float x[32];
-    {
-      float d[64];
-      tmem_ld64(tmem + lb + 64 * u, d);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = half ? 0.f : qs * (d[e] + d[32 + e]);
-      tmem_ld64(tmem + lb + 128 + 64 * u, d);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] += d[e] + d[32 + e];
-    }
-    float o[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float send = half ? x[e] : x[16 + e];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-      o[e] = (half ? x[16 + e] : x[e]) + recv;
-    }
-    const int t = n * C + i;
-    if (ok && t < p.T) out::store16(p, b, t, hv, 64 * vh + 32 * u + 16 * half, o);
-    if (!ok && lane == 0) atomicOr(p.error_word, kErrOutWait);
-    tc_fence_before();
-    chunk::group_sync(1 + grp);   // smem and TMEM free for the next item
   }
   tc_fence_before();
   __syncthreads();
@@ -867,10 +772,8 @@ gdr_status launch_chain(const Params& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            CHAIN_SMEM) != cudaSuccess)
     return GDR_ERR_CUDA;
-  Params q = p;
-  q.xflags = nullptr;       // the output pass is a separate launch: nothing counts exports
   dim3 grid(p.HV * VTILES, p.B);
-  chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM, stream>>>(q);
+  chain_kernel<<<grid, CHAIN_THREADS, CHAIN_SMEM, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
@@ -896,8 +799,7 @@ bool fused_fits(int B, int HV) {
 }
 
 gdr_status launch_fused(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode != 0 || !p.flags || !p.xflags || !p.xchg || !fused_fits(p.B, p.HV))
-    return GDR_ERR_UNSUPPORTED;
+  if (p.gate_mode != 0 || !p.flags || !p.xchg || !fused_fits(p.B, p.HV)) return GDR_ERR_UNSUPPORTED;
   const DeviceInfo& dev = device_info();
   const int n_chain = p.B * p.HV * VTILES;
   const int n_workers = dev.sms - n_chain;
@@ -906,10 +808,8 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FUSED_SMEM) != cudaSuccess)
     return GDR_ERR_CUDA;
-  // Slab flags and export counts (adjacent in the workspace) start at zero.
   const size_t nch = (size_t)p.B * p.HV * p.N;
-  if (p.xflags != p.flags + nch) return GDR_ERR_UNSUPPORTED;
-  if (cudaMemsetAsync(p.flags, 0, 2 * nch * sizeof(unsigned int), stream) != cudaSuccess)
+  if (cudaMemsetAsync(p.flags, 0, nch * sizeof(unsigned int), stream) != cudaSuccess)
     return GDR_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dev.sms);
@@ -926,7 +826,7 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
     (void)cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? GDR_ERR_UNSUPPORTED : GDR_ERR_CUDA;
   }
-  return GDR_OK;
+  return launch_outputs(p, stream);
 }
 
 }  // namespace fast

@@ -10,11 +10,9 @@
 //      chunk exported to an exchange area) or gdr_state_kda.cu (per-key gate,
 //      tcgen05, outputs written with the states);
 //   3. scalar gate: an output pass forms o from the exchange (gdr_chain.cu).
-// For the scalar gate, all three can also run in one cooperative launch:
+// For the scalar gate, stages 1 and 2 can also run in one cooperative launch:
 // worker CTAs produce the slabs in chunk order and raise one flag per chunk,
-// chain CTAs consume them as they appear and count their exports per chunk,
-// and the workers then form the outputs of each chunk once its exports are
-// complete.
+// chain CTAs consume them as they appear; the output pass follows.
 // This header fixes the slab and exchange formats the stages agree on.
 #pragma once
 
@@ -83,9 +81,6 @@ static_assert(Slab::AQ2 % 16 == 0 && Slab::U % 16 == 0 && Slab::VEC % 16 == 0 &&
 //   S  [4 tiles][128 c][S_hi 32 | S_lo 32] bf16   the state at the chunk start,
 //                                                 tile t = value columns 32 t ..
 //   R  [4 tiles][64 j][r_hi 32 | r_lo 32] bf16    r = U - W S, same columns
-// Exports of one chunk a one-launch forward counts before its outputs are
-// formed: one per chain CTA (its S and r tiles).
-constexpr unsigned int kXchgParts = 4;
 struct Xchg {
   static constexpr size_t S_TILE = 128ull * 64 * 2;
   static constexpr size_t R_TILE = 64ull * 64 * 2;
@@ -108,8 +103,6 @@ struct Params {
   uint8_t* xchg;            // N * B * HV exchange blocks (scalar gate), else null
   unsigned int* flags;      // one per chunk (slab index): nonzero once its slab is written
                             // (one-launch forward of the scalar gate), else null
-  unsigned int* xflags;     // one per chunk: count of its exports (S and r tiles) written,
-                            // kXchgParts when complete (one-launch forward), else null
   unsigned int* error_word;
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;

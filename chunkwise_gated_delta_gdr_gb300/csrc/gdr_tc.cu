@@ -20,8 +20,8 @@ constexpr long long kDefaultWaitLimit = 1LL << 24;
 std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 
 // Workspace body of the fast path: the chunk slabs, then (scalar gate) the
-// exchange blocks the recurrence writes for the output pass, and one ready
-// flag and one export count per chunk for the one-launch forward.
+// exchange blocks the recurrence writes for the output pass and one ready flag
+// per chunk for the one-launch forward.
 struct TcLayout {
   size_t xchg = 0, flags = 0, total = 0;
 };
@@ -36,7 +36,7 @@ TcLayout tc_layout(const Problem& p) {
     off += nch * fast::Xchg::BYTES;
     off = align_up(off, 256);
     L.flags = off;
-    off += 2 * nch * sizeof(unsigned int);   // slab ready flags, then export counts
+    off += nch * sizeof(unsigned int);
   }
   L.total = off;
   return L;
@@ -69,7 +69,6 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   const TcLayout L = tc_layout(p);
   f.xchg = p.gate_mode == 0 ? f.slabs + L.xchg : nullptr;
   f.flags = p.gate_mode == 0 ? reinterpret_cast<unsigned int*>(f.slabs + L.flags) : nullptr;
-  f.xflags = f.flags ? f.flags + (size_t)p.B * p.HV * p.N : nullptr;
   f.error_word = error_word;
   f.B = p.B;
   f.T = p.T;
