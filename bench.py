@@ -488,16 +488,17 @@ def run_ours(args, rank, local_rank, world):
     flops_alg = FLOP_PER_TOKEN_HEAD * w.B * w.T * w.HV
     achieved = bytes_alg / (ms * 1e-3) / 1e9
     traffic, traffic_per = recorded_traffic(w.name)
-    # Kernels: the one-launch forward (fused_kernel: chains and chunk
-    # producers) and its output pass (output_kernel), or the chunk-local kernel
-    # and the recurrence (chunk_tc_kernel, chain_kernel + output_kernel for the
-    # scalar gate; chunk_kda_kernel, state_kda_tc_kernel for the per-key gate).
-    ck, rk = ("chunk_kda_kernel", "state_kda_tc_kernel") if gate else ("chunk_tc_kernel", "chain_kernel")
+    # Kernels: the one-launch forward (fused_kernel: chunk producers, chains
+    # and output items), or the chunk-local kernel and the recurrence
+    # (chunk_tc_kernel, chain_kernel + output_kernel for the scalar gate;
+    # chunk_kda_kernel, state_kda_tc_kernel for the per-key gate).
+    ck, rk = (("chunk_kda_kernel", "state_kda_tc_kernel") if gate
+              else ("chunk_tc_kernel", "chain_kernel+output_kernel"))
     one_launch = path == 2 and segments == 1
     if one_launch:
-        kernel_scope = ("fused_kernel (one cooperative launch: chains and chunk producers) + "
-                        "output_kernel")
-        launches = 2
+        kernel_scope = ("fused_kernel (one cooperative launch: chunk producers, chains and "
+                        "output items) after a memset of the chunk flags")
+        launches = 1
         step_traffic = traffic
     elif segments > 1:
         kernel_scope = ("one gdr_chunk_fwd_segmented call: chunk-local kernel, 3 recurrence "
@@ -505,7 +506,7 @@ def run_ours(args, rank, local_rank, world):
         launches = 7 if not gate else 6
         step_traffic = None
     else:
-        kernel_scope = f"one forward call: {ck} + {rk}" + ("" if gate else " + output_kernel")
+        kernel_scope = f"one forward call: {ck} + {rk}"
         launches = 2 if gate else 3
         step_traffic = traffic
     tokens = world * w.B * w.T

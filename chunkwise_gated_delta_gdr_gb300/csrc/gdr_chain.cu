@@ -46,13 +46,10 @@
 //              published S_n. Each is released by a named barrier that the
 //              producing warps arrive on without waiting.
 //   warp 13    TMEM owner and exporter: once S_n and r_n are published it copies both tiles
-//              to the exchange block (bulk copies, one group per chunk),
-//              announces them read out (the tiles are double buffered), and
-//              in the one-launch forward counts the chunk as exported a few
-//              chunks later, when the copies have long been written. A
-//              release or proxy fence waits for all of its thread's memory
-//              operations in flight, the TMA producer's loads included, so
-//              none runs on the warps of the recurrence itself.
+//              to the exchange block (bulk copies, one group per chunk) and
+//              announces them read out (the tiles are double buffered). In
+//              the one-launch forward it also marks the chunks exported so
+//              far, every kMarkEvery chunks and a little behind the copies.
 // The S_n and r_n tiles of every chunk leave by bulk copies (a plain store of a
 // row-per-thread tile would touch 32 lines per instruction and hold up the
 // SM's memory pipe) as the exchange block of gdr_fast.cuh; the output pass
@@ -64,15 +61,19 @@
 // The first CTAs are the chains; the other CTAs are workers, two groups of 8
 // warps each, that run the chunk-local stage (gdr_chunk_tc.cuh) over the
 // chunks in chunk order, raising each chunk's flag once its slab is in global
-// memory. A chain's TMA warp waits for chunk n's flag before loading it.
-// Workers never wait on chains and all CTAs are co-resident, so the waits end;
-// every wait is bounded all the same and records a code in the workspace
-// error word when it gives up, after which the CTA runs to its end. The output
-// pass follows as a second launch: a GPU-scope acquire or release by any
-// thread of a chain CTA waits until every memory operation in flight on its
-// SM (the ring loads included) has completed, a microsecond or more, so the
-// chains signal nothing per chunk; they acquire the workers' slab flags as
-// rarely as they can (every flag already set at once).
+// memory. A chain's TMA warp waits for chunk n's flag before loading it. Each
+// worker group then takes output items (chunk n, sequence, 64 value columns)
+// in chunk order from a counter, and forms o_n once the chains of both value
+// tiles have marked chunk n exported; a chain CTA joins them once its chain
+// is done. A GPU-scope acquire or release by any thread of a chain CTA waits
+// until every memory operation in flight on its SM (the ring loads included)
+// has completed, a microsecond or more, so the chains acquire the slab flags
+// as rarely as they can (every flag already set at once) and mark their
+// exports only every kMarkEvery chunks. Workers wait on chains only after
+// their last slab, chains never wait on output items, and all CTAs are
+// co-resident, so the waits end; every wait is bounded all the same and
+// records a code in the workspace error word when it gives up, after which
+// the CTA runs to its end.
 #include <string.h>
 
 #include <cuda.h>
@@ -95,7 +96,15 @@ constexpr long kWaitLimit = 1L << 24;   // mbarrier polls before a wait gives up
 constexpr long kTmaIdleLimit = 1L << 24;  // TMA event-loop rounds (64 ns sleeps) likewise
 // Slab flags the TMA producer reads at once (one acquire for all of those set).
 constexpr int kFlagWindow = 32;
-constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u;
+constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u, kErrXchgWait = 32u;
+// One-launch forward: a chain announces its exports every kMarkEvery chunks
+// (every kMarkTail in the last kMarkEvery, which the outputs wait for after
+// the chains end), kMarkLag bulk groups behind the newest one (by then long
+// written), so that the release, which waits for every memory operation in
+// flight on the SM, rarely holds up the exporter.
+constexpr int kMarkEvery = 16;
+constexpr int kMarkTail = 4;
+constexpr int kMarkLag = 2;
 
 // Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
 // of two slots, each slot released as soon as its last reader is done:
@@ -204,11 +213,159 @@ __device__ __forceinline__ void stacked_sum(const float* d, int half, float* out
   }
 }
 
+// Output products of one (sequence, chunk n, 64 value columns vh): o = qscale
+// (q S_n) + A_qk r_n from the exchange block of chunk n (the S and r tiles of
+// value tiles 2 vh, 2 vh + 1) and the slab (A_qk, qscale), with raw q by TMA.
+//   D_qs = q [S_a | S_b]            M = 64,  N = 128 (two tiles of [hi 32 | lo 32]), K = 128
+//   D_ar = [A_hi; A_lo] [R_a | R_b] M = 128 (stacked), N = 128, K = 64
+// Shared-memory map (from a 1024-aligned base) and TMEM use of both forms that
+// compute them: the output kernel and a group of 8 warps of the one-launch forward.
+namespace out {
+constexpr int THREADS = 128;
+constexpr int Q = 0, AQ = 16384, S = 32768, R = 65536, QS = 81920, BAR = 82176;
+constexpr int SMEM = BAR + 64 + 1024;
+constexpr uint32_t TX = 16384 + 16384 + 32768 + 16384 + 256;
+constexpr uint32_t TMEM_COLS = 256;
+static_assert(QS + 256 <= chunk::OFF_SMALL, "output tiles inside a worker group region");
+
+// Loads of an output item (one thread), completing on `bar`.
+__device__ __forceinline__ void issue_loads(const CUtensorMap* qmap, const Params& p, uint32_t sb,
+                                            int seq, int n, int vh, uint64_t* bar) {
+  const int b = seq / p.HV, hv = seq % p.HV, h = hv / (p.HV / p.H);
+  const size_t idx = (size_t)seq * p.N + n;
+  const uint8_t* xb = p.xchg + idx * Xchg::BYTES;
+  mbar_expect_tx(bar, TX);
+  tma_load4(sb + Q, qmap, 0, h, n * C, b, bar);
+  tma_load4(sb + Q + 8192, qmap, 64, h, n * C, b, bar);
+  // (the exchange tiles are read once, the slab's A_qk and qscale by both
+  // value halves)
+  const uint64_t pol = l2_evict_first();
+  bulk_load(sb + AQ, p.slabs + idx * p.slab_bytes + Slab::AQ2, 16384, bar);
+  bulk_load_hint(sb + S, xb + Xchg::S + 2 * vh * Xchg::S_TILE, 2 * Xchg::S_TILE, bar, pol);
+  bulk_load_hint(sb + R, xb + Xchg::R + 2 * vh * Xchg::R_TILE, 2 * Xchg::R_TILE, bar, pol);
+  bulk_load(sb + QS, p.slabs + idx * p.slab_bytes + Slab::VEC, 256, bar);
+}
+// The two products (one thread), accumulators at TMEM columns 0-127 and 128-255.
+__device__ __forceinline__ void issue_mmas(uint32_t tmem, uint32_t sb) {
+  constexpr uint32_t ID_QS = idesc_bf16(64, 128, 0, 1);
+  constexpr uint32_t ID_AR = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(tmem, sdesc_sw128(sb + Q + (kk >> 2) * 8192 + (kk & 3) * 32),
+              sdesc_sw128_lbo(sb + S + kk * 2048, 16384), ID_QS, kk > 0);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    umma_bf16(tmem + 128, sdesc_sw128(sb + AQ + kk * 32),
+              sdesc_sw128_lbo(sb + R + kk * 2048, 8192), ID_AR, kk > 0);
+}
+// Writes 16 outputs of row t (value columns v0 .. v0 + 15) of head hv.
+__device__ __forceinline__ void store16(const Params& p, int b, int t, int hv, int v0, const float* o) {
+  const size_t off = (((size_t)b * p.T + t) * p.HV + hv) * V + v0;
+  if (p.out_bf16) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      dst[q] = make_uint4(pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                          pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + off);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+  }
+}
+}  // namespace out
+
+// Output items of the one-launch forward, run by a group of 8 warps (threads
+// gtid = 0 .. 255, named barrier bar_id) in a worker group region gsm with
+// 256 TMEM columns at tmem, its TMA and MMA barriers (chunk layout) next in
+// phases ph and mph. Items (chunk n, sequence, 64 value columns vh) are
+// claimed in that order from the counter after the export marks; an item
+// waits until both of its value tiles have marked chunk n exported.
+__device__ __forceinline__ void output_items(const CUtensorMap* qmap, const Params& p, uint8_t* gsm,
+                                             int gtid, int bar_id, uint32_t tmem, uint32_t ph,
+                                             uint32_t mph) {
+  const int nseq = p.B * p.HV;
+  const long items = 2L * nseq * p.N;
+  unsigned int* counter = p.xmark + (size_t)nseq * VTILES;
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(gsm + chunk::OFF_BAR);
+  uint64_t* bar_mma = bar_tma + 1;
+  int* claim = reinterpret_cast<int*>(bar_tma + 2) + 1;   // the chunk stage's split flag word
+  const uint32_t sb = smem_u32(gsm);
+  const int lane = gtid & 31, gw = gtid >> 5;
+  for (;;) {
+    if (gtid == 0) *claim = (int)atomicAdd(counter, 1u);
+    chunk::group_sync(bar_id);
+    const long it = *claim;
+    if (it >= items) break;
+    const int n = (int)(it / (2 * nseq)), rem = (int)(it % (2 * nseq));
+    const int seq = rem >> 1, vh = rem & 1;
+    const int b = seq / p.HV, hv = seq % p.HV;
+    if (gtid == 0) {
+      const unsigned int* xm = p.xmark + (size_t)seq * VTILES + 2 * vh;
+      long polls = 0;
+      while (ld_acquire_gpu(xm) <= (unsigned int)n || ld_acquire_gpu(xm + 1) <= (unsigned int)n) {
+        if (++polls > p.wait_limit) {
+          atomicOr(p.error_word, kErrXchgWait);
+          break;
+        }
+        __nanosleep(64);
+      }
+      fence_async_global();     // the exports (generic acquire) -> bulk reads
+      out::issue_loads(qmap, p, sb, seq, n, vh, bar_tma);
+      const bool ok = mbar_wait(bar_tma, ph, kWaitLimit);
+      if (ok) {
+        tc_fence_after();
+        out::issue_mmas(tmem, sb);
+      } else {
+        atomicOr(p.error_word, kErrOutWait);
+      }
+      umma_commit(bar_mma);
+    }
+    ph ^= 1u;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, mph, kWaitLimit));
+    mph ^= 1u;
+    tc_fence_after();
+    // Warp gw: TMEM lane quadrant gw % 4, value tile u = gw / 4. Lanes 0-15 hold
+    // row i = 16 (gw % 4) + lane of D_qs and the hi rows of D_ar, lanes 16-31
+    // the lo rows of D_ar; one shuffle adds the pair, after which lane half
+    // keeps 16 of the tile's 32 columns.
+    const int qd = gw & 3, u = gw >> 2, half = lane >> 4;
+    const int i = 16 * qd + (lane & 15);
+    const uint32_t lb = (uint32_t)(32 * qd) << 16;
+    const float qs = reinterpret_cast<const float*>(gsm + out::QS)[i];
+    float x[32];
+    {
+      float d[64];
+      tmem_ld64(tmem + lb + 64 * u, d);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = half ? 0.f : qs * (d[e] + d[32 + e]);
+      tmem_ld64(tmem + lb + 128 + 64 * u, d);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] += d[e] + d[32 + e];
+    }
+    float o[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float send = half ? x[e] : x[16 + e];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      o[e] = (half ? x[16 + e] : x[e]) + recv;
+    }
+    const int t = n * C + i;
+    if (ok && t < p.T) out::store16(p, b, t, hv, 64 * vh + 32 * u + 16 * half, o);
+    if (!ok && lane == 0) atomicOr(p.error_word, kErrOutWait);
+    tc_fence_before();
+    chunk::group_sync(bar_id);   // shared memory, TMEM and the claim free for the next item
+  }
+}
+
 // ============================================================================ chain
 // seq = b * HV + hv, value columns [32 vt, 32 vt + 32). wait_flags: chunk
-// n's slab is produced in the same launch (wait for its flag before loading it).
+// n's slab is produced in the same launch (wait for its flag before loading
+// it), and the exports are marked for the output items, which the CTA joins
+// (with q by qmap) once its chain is done.
 __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq, int vt,
-                                           bool wait_flags) {
+                                           bool wait_flags, const CUtensorMap* qmap) {
   const int v0 = vt * VC;
   const int N = p.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -378,6 +535,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     if (lane == 0) {
       const uint32_t sb = smem_u32(sm);
       int nw = 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
+      // This CTA's U columns are read once; -W, -T and k by the four V-tile
+      // CTAs of the sequence.
+      const uint64_t pol_last_read = l2_evict_first();
       bool flags_ok = wait_flags;
       long idle = 0, flag_polls = 0;
       while ((nw < N || na < N || nb < N) && ok) {
@@ -426,7 +586,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
           const uint32_t slot = sb + OFF_A + (na & 1) * A_SLOT;
           mbar_expect_tx(fb, A_TX);
           bulk_load(slot + A_T, slab + Slab::T2, 16384, fb);   // (first chunk: not used)
-          bulk_load(slot + A_U, slab + Slab::U + vt * 8192, 8192, fb);
+          bulk_load_hint(slot + A_U, slab + Slab::U + vt * 8192, 8192, fb, pol_last_read);
           bulk_load(slot + A_VEC, slab + Slab::VEC, 1024, fb);
           ++na;
           progress = true;
@@ -455,7 +615,8 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // Once rho_n is published (named barrier 3): D_S(n + 1) = k_n^T rho_n into
     // D_S buffer n % 2 (read for S_{n-1}, which D_ws(n), complete before rho_n,
     // consumed), then D_t(n + 1) = (-T_{n+1}) rho_n (the last round: D_S(N)
-    // alone, for the final state).
+    // alone, for the final state). (D_t first measured slower: S_{n+1}, and
+    // with it D_ws(n + 2), comes later.)
     for (int n = 0; n < N; ++n) {
       nb_sync(3, 160);
       if (lane == 0 && ok) {
@@ -515,6 +676,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   } else if (warp == 13) {
     // ---------------------------------------------------------------- exporter
     if (lane == 0) {
+      // The output pass reads the exchange next: keep it in L2.
+      const uint64_t pol_keep = l2_evict_last();
+      unsigned int* mark = wait_flags ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
       for (int nx = 0; nx < N && ok; ++nx) {
         ok = mbar_wait(&bars[B_ES + (nx & 1)], (nx >> 1) & 1, kWaitLimit) &&
              mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
@@ -522,13 +686,28 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         // Both tiles of chunk nx out as one bulk group; once read out they may
         // be rewritten.
         uint8_t* xb = xbase + (size_t)nx * Xchg::BYTES;
-        bulk_store(xb + Xchg::S + vt * Xchg::S_TILE, sb + OFF_S + (nx & 1) * 16384, 16384);
-        bulk_store(xb + Xchg::R + vt * Xchg::R_TILE, sb + OFF_R + (nx & 1) * 8192, 8192);
+        bulk_store_hint(xb + Xchg::S + vt * Xchg::S_TILE, sb + OFF_S + (nx & 1) * 16384, 16384, pol_keep);
+        bulk_store_hint(xb + Xchg::R + vt * Xchg::R_TILE, sb + OFF_R + (nx & 1) * 8192, 8192, pol_keep);
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(&bars[B_XR + (nx & 1)]);
+        // Chunks 0 .. done - 1 are in global memory once all but the newest
+        // kMarkLag groups are.
+        const int done = nx + 1 - kMarkLag;
+        if (mark && done > 0 && nx + 1 < N &&
+            (done % kMarkEvery == 0 || (done >= N - kMarkEvery && done % kMarkTail == 0))) {
+          bulk_wait<kMarkLag>();
+          fence_async_global();
+          st_release_gpu(mark, (unsigned int)done);
+        }
       }
       bulk_wait<0>();
+      // All chunks, also after a wait gave up (recorded): the output items
+      // never wait for exports that will not come.
+      if (mark) {
+        fence_async_global();
+        st_release_gpu(mark, (unsigned int)N);
+      }
     }
     __syncwarp();
   }
@@ -536,6 +715,19 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
 
   tc_fence_before();
   nb_sync(1, CHAIN_THREADS);
+  if (qmap) {
+    // One-launch forward: the CTA joins the output work as two groups of 8
+    // warps in the worker group layout, each with 256 of the chain's TMEM
+    // columns (the chain's tiles and rings are dead).
+    tc_fence_after();
+    const int grp = warp >> 3;
+    uint8_t* gsm = sm + grp * chunk::GROUP_BYTES;
+    if ((tid & 255) == 0) chunk::init_group_bars(gsm);
+    output_items(qmap, p, gsm, tid & 255, 1 + grp, tmem + 256 * grp, 0u, 0u);
+    // (barrier 0: group 0 may still be on named barrier 1 with 256 threads)
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, CHAIN_TMEM);
@@ -546,55 +738,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, false);
+  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, false, nullptr);
 }
 
-// Output products of one (sequence, chunk n, 64 value columns vh): o = qscale
-// (q S_n) + A_qk r_n from the exchange block of chunk n (the S and r tiles of
-// value tiles 2 vh, 2 vh + 1) and the slab (A_qk, qscale), with raw q by TMA.
-//   D_qs = q [S_a | S_b]            M = 64,  N = 128 (two tiles of [hi 32 | lo 32]), K = 128
-//   D_ar = [A_hi; A_lo] [R_a | R_b] M = 128 (stacked), N = 128, K = 64
-// Shared-memory map (from a 1024-aligned base) and TMEM use of the output kernel.
-namespace out {
-constexpr int THREADS = 128;
-constexpr int Q = 0, AQ = 16384, S = 32768, R = 65536, QS = 81920, BAR = 82176;
-constexpr int SMEM = BAR + 64 + 1024;
-constexpr uint32_t TX = 16384 + 16384 + 32768 + 16384 + 256;
-constexpr uint32_t TMEM_COLS = 256;
-
-// Loads of an output item (one thread), completing on `bar`.
-__device__ __forceinline__ void issue_loads(const CUtensorMap* qmap, const Params& p, uint32_t sb,
-                                            int seq, int n, int vh, uint64_t* bar) {
-  const int b = seq / p.HV, hv = seq % p.HV, h = hv / (p.HV / p.H);
-  const size_t idx = (size_t)seq * p.N + n;
-  const uint8_t* xb = p.xchg + idx * Xchg::BYTES;
-  mbar_expect_tx(bar, TX);
-  tma_load4(sb + Q, qmap, 0, h, n * C, b, bar);
-  tma_load4(sb + Q + 8192, qmap, 64, h, n * C, b, bar);
-  bulk_load(sb + AQ, p.slabs + idx * p.slab_bytes + Slab::AQ2, 16384, bar);
-  bulk_load(sb + S, xb + Xchg::S + 2 * vh * Xchg::S_TILE, 2 * Xchg::S_TILE, bar);
-  bulk_load(sb + R, xb + Xchg::R + 2 * vh * Xchg::R_TILE, 2 * Xchg::R_TILE, bar);
-  bulk_load(sb + QS, p.slabs + idx * p.slab_bytes + Slab::VEC, 256, bar);
-}
-// The two products (one thread), accumulators at TMEM columns 0-127 and 128-255.
-__device__ __forceinline__ void issue_mmas(uint32_t tmem, uint32_t sb) {
-  constexpr uint32_t ID_QS = idesc_bf16(64, 128, 0, 1);
-  constexpr uint32_t ID_AR = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    umma_bf16(tmem, sdesc_sw128(sb + Q + (kk >> 2) * 8192 + (kk & 3) * 32),
-              sdesc_sw128_lbo(sb + S + kk * 2048, 16384), ID_QS, kk > 0);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    umma_bf16(tmem + 128, sdesc_sw128(sb + AQ + kk * 32),
-              sdesc_sw128_lbo(sb + R + kk * 2048, 8192), ID_AR, kk > 0);
-}
-}  // namespace out
 
 // =========================================================================== worker
 // Two groups of 8 warps run the chunk-local stage over chunk items in chunk
 // order (item it: chunk it / (B HV) of sequence it % (B HV)); group G of
-// NG takes items G, G + NG, ...
+// NG takes items G, G + NG, ... Then each group takes output items.
 __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Params& p,
                                             uint8_t* sm_base, int worker, int n_workers) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -619,6 +770,16 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
     const int b = seq / p.HV, hv = seq % p.HV;
     chunk::produce_chunk(maps, p, sm, gtid, 1 + grp, n, hv, b, ph, tmem, nullptr, pending);
     pending = p.flags + slab_index(p, b, hv, n);
+    if (it < NG) {
+      // The first wave (the chunks the chains start on): published at once
+      // rather than at the start of the next item.
+      if (gtid == 0) {
+        bulk_wait<0>();
+        fence_async_global();
+        st_release_gpu(pending, 1u);
+      }
+      pending = nullptr;
+    }
     ph ^= 1u;
   }
   if (gtid == 0 && pending) {
@@ -626,6 +787,9 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
     fence_async_global();
     st_release_gpu(pending, 1u);
   }
+  // Then the output items. The chunk stage's MMA barrier completed two phases
+  // per item, so its next phase has parity 0; its TMA barrier one (ph).
+  output_items(&maps.q, p, sm, gtid, 1 + grp, tmem, ph, 0u);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -641,7 +805,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   const int cta = blockIdx.x;
   if (cta < n_chain) {
-    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, true);
+    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, true, &maps.q);
   } else {
     worker_role(maps, p, sm, cta - n_chain, n_workers);
   }
@@ -808,8 +972,10 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FUSED_SMEM) != cudaSuccess)
     return GDR_ERR_CUDA;
-  const size_t nch = (size_t)p.B * p.HV * p.N;
-  if (cudaMemsetAsync(p.flags, 0, nch * sizeof(unsigned int), stream) != cudaSuccess)
+  // Slab flags, export marks and the output item counter start at zero.
+  const size_t words = (size_t)p.B * p.HV * (p.N + VTILES) + 1;
+  if (!p.xmark || p.xmark != p.flags + (size_t)p.B * p.HV * p.N) return GDR_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(p.flags, 0, words * sizeof(unsigned int), stream) != cudaSuccess)
     return GDR_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dev.sms);
@@ -826,7 +992,7 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
     (void)cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? GDR_ERR_UNSUPPORTED : GDR_ERR_CUDA;
   }
-  return launch_outputs(p, stream);
+  return GDR_OK;
 }
 
 }  // namespace fast

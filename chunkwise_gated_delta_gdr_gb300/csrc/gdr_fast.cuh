@@ -10,9 +10,11 @@
 //      chunk exported to an exchange area) or gdr_state_kda.cu (per-key gate,
 //      tcgen05, outputs written with the states);
 //   3. scalar gate: an output pass forms o from the exchange (gdr_chain.cu).
-// For the scalar gate, stages 1 and 2 can also run in one cooperative launch:
+// For the scalar gate, all three can also run in one cooperative launch:
 // worker CTAs produce the slabs in chunk order and raise one flag per chunk,
-// chain CTAs consume them as they appear; the output pass follows.
+// chain CTAs consume them as they appear and mark their exports every few
+// chunks, and the workers (and each chain CTA once its chain is done) form the
+// outputs of the chunks already marked.
 // This header fixes the slab and exchange formats the stages agree on.
 #pragma once
 
@@ -103,6 +105,9 @@ struct Params {
   uint8_t* xchg;            // N * B * HV exchange blocks (scalar gate), else null
   unsigned int* flags;      // one per chunk (slab index): nonzero once its slab is written
                             // (one-launch forward of the scalar gate), else null
+  unsigned int* xmark;      // after the flags: per (sequence, 32 value columns) the number of
+                            // chunks whose exports are in global memory, then the counter of
+                            // claimed output items (one-launch forward), else null
   unsigned int* error_word;
   int B, T, H, HV, N;
   int out_bf16, gate_mode, use_l2;
@@ -125,8 +130,8 @@ inline __host__ __device__ size_t slab_index(const Params& p, int b, int hv, int
 gdr_status launch_chain(const Params& p, cudaStream_t stream);
 // Scalar gate: the output pass over the exchange of a finished recurrence.
 gdr_status launch_outputs(const Params& p, cudaStream_t stream);
-// Scalar gate: both stages in one cooperative launch (gdr_chain.cu); declines
-// with GDR_ERR_UNSUPPORTED (nothing enqueued) when it does not pay.
+// Scalar gate: the whole forward in one cooperative launch (gdr_chain.cu);
+// declines with GDR_ERR_UNSUPPORTED (nothing enqueued) when it does not pay.
 gdr_status launch_fused(const Params& p, cudaStream_t stream);
 // Whether launch_fused runs for B x HV sequences on the current device.
 bool fused_fits(int B, int HV);

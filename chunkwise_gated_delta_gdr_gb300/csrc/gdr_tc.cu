@@ -20,8 +20,9 @@ constexpr long long kDefaultWaitLimit = 1LL << 24;
 std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 
 // Workspace body of the fast path: the chunk slabs, then (scalar gate) the
-// exchange blocks the recurrence writes for the output pass and one ready flag
-// per chunk for the one-launch forward.
+// exchange blocks the recurrence writes for the output pass and, for the
+// one-launch forward, one ready flag per chunk, one export mark per (sequence,
+// 32 value columns) and an output item counter.
 struct TcLayout {
   size_t xchg = 0, flags = 0, total = 0;
 };
@@ -36,7 +37,7 @@ TcLayout tc_layout(const Problem& p) {
     off += nch * fast::Xchg::BYTES;
     off = align_up(off, 256);
     L.flags = off;
-    off += nch * sizeof(unsigned int);
+    off += (nch + (size_t)p.B * p.HV * (fast::V / 32) + 1) * sizeof(unsigned int);
   }
   L.total = off;
   return L;
@@ -69,6 +70,7 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   const TcLayout L = tc_layout(p);
   f.xchg = p.gate_mode == 0 ? f.slabs + L.xchg : nullptr;
   f.flags = p.gate_mode == 0 ? reinterpret_cast<unsigned int*>(f.slabs + L.flags) : nullptr;
+  f.xmark = f.flags ? f.flags + (size_t)p.B * p.HV * p.N : nullptr;
   f.error_word = error_word;
   f.B = p.B;
   f.T = p.T;
@@ -85,7 +87,7 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
   f.slab_bytes = fast::Slab::bytes(p.gate_mode);
   f.wait_limit = (long)g_wait_limit.load();
   // Both stages in one call, scalar gate: one cooperative launch when the
-  // chains leave enough SMs to the producers (it enqueues the output pass too).
+  // chains leave enough SMs to the producers.
   if (stage == 3 && p.gate_mode == 0 && p.recur_mode == 0) {
     const gdr_status st = fast::launch_fused(f, stream);
     if (st != GDR_ERR_UNSUPPORTED) return st;
