@@ -334,8 +334,9 @@ def run_ours(args, rank, local_rank, world):
     dims = {k_: gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, CODE[k_])
             for k_ in DT}
     path = gdr.chunk_fwd_path(dims[main_dt], w.C, gate)
-    ws = torch.empty(gdr.chunk_fwd_workspace_size(dims[main_dt], w.C, gate), dtype=torch.uint8,
-                     device=dev)
+    # (one workspace serves both output dtypes: sized for the larger)
+    ws = torch.empty(max(gdr.chunk_fwd_workspace_size(dims[k_], w.C, gate) for k_ in DT),
+                     dtype=torch.uint8, device=dev)
     outs = {k_: torch.empty(w.B, w.T, w.HV, w.V, dtype=DT[k_], device=dev) for k_ in DT}
     fin = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -343,8 +344,8 @@ def run_ours(args, rank, local_rank, world):
 
     segments = getattr(w, "segments", 1)
     if segments > 1:
-        seg_ws = torch.empty(gdr.chunk_fwd_segmented_workspace_size(dims[main_dt], w.C, gate,
-                                                                    segments),
+        seg_ws = torch.empty(max(gdr.chunk_fwd_segmented_workspace_size(dims[k_], w.C, gate,
+                                                                        segments) for k_ in DT),
                              dtype=torch.uint8, device=dev)
 
     def step(dt=main_dt):

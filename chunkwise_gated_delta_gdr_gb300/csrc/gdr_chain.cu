@@ -43,8 +43,8 @@
 //   warp 12    TMA producer (three rings of two slots: {-W}, {-T, U, VEC}, {k}).
 //   warp 14    issues D_S(n + 1) and D_t(n + 1) once the r warps have published
 //              rho_n; warp 15 issues D_ws(n + 1) once the state warps have
-//              published S_n. Each is released by a named barrier that the
-//              producing warps arrive on without waiting.
+//              published S_n. Each is released by a named barrier (the r
+//              warps arrive on theirs without waiting, the state warps sync).
 //   warp 13    TMEM owner and exporter: once S_n and r_n are published it copies both tiles
 //              to the exchange block (bulk copies, one group per chunk) and
 //              announces them read out (the tiles are double buffered). In
@@ -98,12 +98,14 @@ constexpr long kTmaIdleLimit = 1L << 24;  // TMA event-loop rounds (64 ns sleeps
 constexpr int kFlagWindow = 32;
 constexpr unsigned int kErrChainWait = 4u, kErrFlagWait = 8u, kErrOutWait = 16u, kErrXchgWait = 32u;
 // One-launch forward: a chain announces its exports every kMarkEvery chunks
-// (every kMarkTail in the last kMarkEvery, which the outputs wait for after
-// the chains end), kMarkLag bulk groups behind the newest one (by then long
-// written), so that the release, which waits for every memory operation in
-// flight on the SM, rarely holds up the exporter.
+// and every kMarkTail chunks in the last kMarkEvery (whose outputs wait for
+// the chains to end), kMarkLag bulk groups behind the newest export (by then
+// long written). Each release waits for every memory operation in flight on
+// the SM and can hold up the exporter for about a chain step, so the marks
+// are few. (Every 32 chunks measured slower: the workers then wait longer.)
 constexpr int kMarkEvery = 16;
 constexpr int kMarkTail = 4;
+constexpr int kMarkTailSpan = kMarkEvery;
 constexpr int kMarkLag = 2;
 
 // Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
@@ -397,13 +399,17 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   const uint32_t tmem = *tslot;
   bool ok = true;
   uint8_t* xbase = p.xchg + (size_t)chunk0 * Xchg::BYTES;
+  // Mamba2 SSD: W = 0, so D_ws and D_t vanish and r_n = U_n does not depend on
+  // the state; the W ring, both products and their waits are skipped, and
+  // only the state update stays serial.
+  const bool no_w = p.ssd != 0;
   const uint32_t sb = smem_u32(sm);
   constexpr uint32_t ID_KMN = idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major
   constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, 1, 1);  // A = k^T read MN-major
 
   if (warp < 8) {
     // ---------------------------------------------------------------- state
-    // After publishing S_n the eight warps arrive on named barrier 2, which
+    // After publishing S_n the eight warps meet on named barrier 2, which
     // releases the D_ws issuer (warp 15).
     const int qd = warp & 3, h = warp >> 2;
     const int c = 32 * qd + lane;                        // key channel = TMEM lane
@@ -441,7 +447,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       // S tile n % 2 held S_{n-2}: D_ws(n - 1) has read it (its completion) and
       // so has its export.
       if (n >= 2) {
-        ok = warp_wait(&bars[B_WS + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ok);
+        if (!no_w) ok = warp_wait(&bars[B_WS + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ok);
         ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
       }
       uint8_t* st = sm + OFF_S + (n & 1) * 16384;
@@ -450,7 +456,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_ES + (n & 1)]);   // for the exporter
       tc_fence_before();
-      nb_arrive(2, 288);
+      // (a sync, not an arrive: a state warp that ran a step ahead could
+      // otherwise complete the phase of a slower one and release D_ws early)
+      nb_sync(2, 288);
       // gamma_n for S_{n+1}; then this warp is done with ring A slot n % 2.
       ok = warp_wait(&bars[B_FULLA + (n & 1)], (n >> 1) & 1, ok);
       gam = reinterpret_cast<const float*>(sm + OFF_A + (n & 1) * A_SLOT + A_VEC)[2 * C];
@@ -475,15 +483,20 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     for (int n = 0; n < N; ++n) {
       const int sa = n & 1;
       const uint8_t* slot = sm + OFF_A + sa * A_SLOT;
-      ok = warp_wait(&bars[B_WS + sa], (n >> 1) & 1, ok);
-      if (lane == 0) mbar_arrive(&bars[B_EMPTYW + sa]);   // D_ws(n) done: W_n read
+      if (!no_w) {
+        ok = warp_wait(&bars[B_WS + sa], (n >> 1) & 1, ok);
+        if (lane == 0) mbar_arrive(&bars[B_EMPTYW + sa]);   // D_ws(n) done: W_n read
+      }
       ok = warp_wait(&bars[B_FULLA + sa], (n >> 1) & 1, ok);
       tc_fence_after();
       float r[16];
-      {
+      if (!no_w) {
         float d[64];
         tmem_ld64(tmem + lb + T_WS + 64 * sa, d);
         stacked_sum(d, half, r);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0.f;
       }
       const float* vec = reinterpret_cast<const float*>(slot + A_VEC);
       const float ks = vec[C + j];
@@ -498,7 +511,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         r[4 * q + 2] = fmaf(gam_prev, r[4 * q + 2], uf * u.z);
         r[4 * q + 3] = fmaf(gam_prev, r[4 * q + 3], uf * u.w);
       }
-      if (n > 0) {
+      if (n > 0 && !no_w) {
         ok = warp_wait(&bars[B_T], (n - 1) & 1, ok);
         tc_fence_after();
         float d[64], t[16];
@@ -507,6 +520,8 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] += t[i];
       }
+      // (no D_t to wait for: D_S(n - 1), the last reader of rho tile n % 2)
+      if (no_w && n >= 2) ok = warp_wait(&bars[B_DS + sa], ((n - 2) >> 1) & 1, ok);
       tc_fence_before();
       // rho into tile n % 2: rho_{n-2} there was read by D_S(n - 1) and
       // D_t(n - 1), issued by the same thread before D_t(n), whose completion
@@ -519,7 +534,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_EMPTYA + sa]);   // U, VEC read; D_t(n) (T_n) done
       tc_fence_before();
-      nb_arrive(3, 160);
+      // An arrive: r_{n+1} needs D_t(n + 1), issued only after this phase, so
+      // no r warp can reach the next phase early. Under SSD (no D_t) a sync.
+      if (no_w) nb_sync(3, 160); else nb_arrive(3, 160);
       // r into its tile n % 2 once the export of r_{n-2} from it is read out.
       if (n >= 2) ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
       publish16(sm + OFF_R + sa * 8192, j, 2 * half, r);
@@ -534,7 +551,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // and B likewise; one bulk copy per array.
     if (lane == 0) {
       const uint32_t sb = smem_u32(sm);
-      int nw = 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
+      int nw = no_w ? N : 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
       // This CTA's U columns are read once; -W, -T and k by the four V-tile
       // CTAs of the sequence.
       const uint64_t pol_last_read = l2_evict_first();
@@ -621,7 +638,11 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       nb_sync(3, 160);
       if (lane == 0 && ok) {
         const int sa = n & 1;
-        ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
+        // (SSD: rho_n does not wait for the state, so D_S buffer n % 2 is
+        // free only once the state warps have read D_S(n - 1) for S_{n-1})
+        if (no_w && n >= 2)
+          ok = mbar_spin(&bars[B_ES + ((n - 1) & 1)], ((n - 1) >> 1) & 1, kWaitLimit);
+        if (ok) ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
         if (ok) {
           tc_fence_after();
           const uint32_t kb = sb + OFF_B + sa * KB_SLOT;
@@ -632,7 +653,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
                       sdesc_sw128_lbo(pt + kk * 2048, 8192), ID_MNMN, kk > 0);
           umma_commit(&bars[B_DS + sa]);
         }
-        if (ok && n + 1 < N) {
+        if (ok && n + 1 < N && !no_w) {
           const int m = n + 1;
           ok = mbar_spin(&bars[B_FULLA + (m & 1)], (m >> 1) & 1, kWaitLimit);   // T_{n+1}
           if (ok) {
@@ -666,7 +687,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     };
     for (int n = 0; n < N; ++n) {
       nb_sync(2, 288);
-      if (lane == 0 && ok) {
+      if (lane == 0 && ok && !no_w) {
         tc_fence_after();
         if (n == 0) issue_ws(0);
         if (ok && n + 1 < N) issue_ws(n + 1);
@@ -695,7 +716,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         // kMarkLag groups are.
         const int done = nx + 1 - kMarkLag;
         if (mark && done > 0 && nx + 1 < N &&
-            (done % kMarkEvery == 0 || (done >= N - kMarkEvery && done % kMarkTail == 0))) {
+            (done % kMarkEvery == 0 || (done >= N - kMarkTailSpan && done % kMarkTail == 0))) {
           bulk_wait<kMarkLag>();
           fence_async_global();
           st_release_gpu(mark, (unsigned int)done);

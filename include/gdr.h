@@ -279,7 +279,9 @@ gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void* v, const 
  *   S <- diag(exp(g_t)) S + k_t v_t^T,   o_t = S^T (scale q_t)
  * i.e. the gated recurrence without the delta erase and without beta. It
  * runs on the same chunk machinery with the triangular solve dropped
- * (M = I, W = 0, U = v) on the general fp32 path. Arguments as for
+ * (M = I, W = 0, U = v): for bf16 inputs with K = V = 128, C = 64 and the
+ * scalar gate on the tensor-core path (chunk-local kernel, state chain and
+ * output kernel), otherwise on the general fp32 path. Arguments as for
  * gdr_chunk_fwd, minus beta; the workspace must hold
  * gdr_ssd_chunk_fwd_workspace_size() bytes.
  */
