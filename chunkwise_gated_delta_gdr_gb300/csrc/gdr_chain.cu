@@ -115,23 +115,30 @@ constexpr int kMarkLag = 2;
 constexpr int W_SLOT = 32768;
 constexpr uint32_t W_TX = 32768;
 // Ring A slot (chunk n): -T stacked [128][64] bf16, U [64 j][32 v] fp32
-// (128-byte swizzled), VEC.
-constexpr int A_T = 0, A_U = 16384, A_VEC = 24576, A_SLOT = 25600;
-constexpr uint32_t A_TX = 16384 + 8192 + 1024;
+// (128-byte swizzled); beside it, outside the 1 KB-aligned slots, the chunk's
+// kscale[64] and gamma (the VEC entries from kscale on, 512 bytes).
+constexpr int A_T = 0, A_U = 16384, A_SLOT = 24576;
+constexpr int VEC_OFF = C * 4, VEC_BYTES = 512;   // slab VEC bytes the chain reads (kscale, gamma)
+constexpr uint32_t A_TX = 16384 + 8192 + VEC_BYTES;
 // Ring B slot (chunk n): k [64 j][128 c] bf16 (two [64][64] boxes).
 constexpr int KB_SLOT = 16384;
 constexpr uint32_t B_TX = 16384;
+// S tiles: three, so that S_n overwrites S_{n-3}, whose readers (D_ws(n - 2)
+// and its export) are long done, and the state warps wait for neither.
+constexpr int S_TILES = 3;
 constexpr int OFF_W = 0;
 constexpr int OFF_A = OFF_W + 2 * W_SLOT;
 constexpr int OFF_B = OFF_A + 2 * A_SLOT;
-constexpr int OFF_S = OFF_B + 2 * KB_SLOT;     // S tiles [128 c][hi 32 | lo 32] bf16, x 2
-constexpr int OFF_P = OFF_S + 2 * 16384;      // rho tiles [64 j][hi 32 | lo 32], x 2
-constexpr int OFF_R = OFF_P + 2 * 8192;       // r tiles, the same format, x 2
-constexpr int OFF_BARS = OFF_R + 2 * 8192;
+constexpr int OFF_S = OFF_B + 2 * KB_SLOT;          // S tiles [128 c][hi 32 | lo 32] bf16
+constexpr int OFF_P = OFF_S + S_TILES * 16384;     // rho tiles [64 j][hi 32 | lo 32], x 2
+constexpr int OFF_R = OFF_P + 2 * 8192;            // r tiles, the same format, x 2
+constexpr int OFF_V = OFF_R + 2 * 8192;            // ring A's VEC part, x 2
+constexpr int OFF_BARS = OFF_V + 2 * VEC_BYTES;
 constexpr int CHAIN_SMEM = OFF_BARS + 256 + 1024;
 static_assert(A_SLOT % 1024 == 0 && OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && OFF_S % 1024 == 0 &&
                   OFF_P % 1024 == 0 && OFF_R % 1024 == 0 && A_T % 1024 == 0 && A_U % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
+static_assert(Slab::VEC % 16 == 0 && VEC_OFF % 16 == 0, "bulk copy alignment");
 static_assert(CHAIN_SMEM <= 232448, "chain shared memory");
 constexpr int FUSED_SMEM =
     (CHAIN_SMEM > 2 * chunk::GROUP_BYTES + 1024) ? CHAIN_SMEM : 2 * chunk::GROUP_BYTES + 1024;
@@ -147,22 +154,24 @@ enum : int {
                   //     + 8 S warps
   B_FULLB = 4,    // [2] ring B slot loaded
   B_EMPTYB = 6,   // [2] ring B slot free: 8 S warps (after the D_S that read it)
-  B_ES = 8,       // [2] S_n published, barrier n % 2 (8 state warps; for the exporter)
-  B_WS = 10,      // [2] D_ws complete (commit), buffer n % 2
-  B_T = 12,       // D_t complete (commit)
-  B_DS = 13,      // [2] D_S complete (commit), buffer (n - 1) % 2 for D_S(n)
-  B_RP = 15,      // [2] r_n tile published, barrier n % 2 (4 r warps)
-  B_XR = 17,      // [2] exports of chunk n (S and r tiles) read out, barrier n % 2 (exporter)
-  B_FULLW = 19,   // [2] ring W slot loaded
-  B_EMPTYW = 21,  // [2] ring W slot free: 4 r warps (after D_ws of the chunk completed)
-  B_SLOT = 23     // TMEM slot (u32)
+  B_WS = 8,       // [2] D_ws complete (commit), buffer n % 2
+  B_T = 10,       // D_t complete (commit)
+  B_DS = 11,      // [2] D_S complete (commit), buffer (n - 1) % 2 for D_S(n)
+  B_FULLW = 13,   // [2] ring W slot loaded
+  B_EMPTYW = 15,  // [2] ring W slot free: 4 r warps (after D_ws of the chunk completed)
+  B_RP = 17,      // [2] r_n tile published, barrier n % 2 (4 r warps)
+  B_ES = 19,      // [3] S_n published, barrier n % 3 (8 state warps; for the exporter)
+  B_XR = 22,      // [3] exports of chunk n (S and r tiles) read out, barrier n % 3 (exporter)
+  B_SLOT = 25     // TMEM slot (u32)
 };
 // A waiter tests an mbarrier phase by parity, so a barrier must never run two
 // phases ahead of one of its waiters. The S, r and export barriers could (S_{n+1}
 // may be published before chunk n is exported, and chunk n - 1 exported before
-// the MMA thread checks chunk n - 2), so each has one barrier per chunk parity:
-// barrier n % 2 completes phase n / 2 for chunk n, and its next phase (chunk
-// n + 2) depends on the waiter having passed chunk n.
+// the MMA thread checks chunk n - 2), so each has one barrier per tile: barrier
+// n % T completes phase n / T for chunk n (T = S_TILES for S and the exports,
+// 2 for r), and its next phase (chunk n + T) depends on the waiter having
+// passed chunk n.
+__device__ __forceinline__ uint32_t tile_parity(int n, int tiles) { return (uint32_t)(n / tiles) & 1u; }
 constexpr int kEmptyA = 4 + 8;
 constexpr int kEmptyB = 8;
 constexpr int kEmptyW = 4;
@@ -385,8 +394,10 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       mbar_init(&bars[B_EMPTYB + i], kEmptyB);
       mbar_init(&bars[B_WS + i], 1);
       mbar_init(&bars[B_DS + i], 1);
-      mbar_init(&bars[B_ES + i], 8);
       mbar_init(&bars[B_RP + i], 4);
+    }
+    for (int i = 0; i < S_TILES; ++i) {
+      mbar_init(&bars[B_ES + i], 8);
       mbar_init(&bars[B_XR + i], 1);
     }
     mbar_init(&bars[B_T], 1);
@@ -444,24 +455,23 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         tc_fence_before();
       }
       if (n == N) break;
-      // S tile n % 2 held S_{n-2}: D_ws(n - 1) has read it (its completion) and
-      // so has its export.
-      if (n >= 2) {
-        if (!no_w) ok = warp_wait(&bars[B_WS + ((n - 1) & 1)], ((n - 1) >> 1) & 1, ok);
-        ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
-      }
-      uint8_t* st = sm + OFF_S + (n & 1) * 16384;
+      // S tile n % 3 held S_{n-3}: D_ws(n - 2) read it, and completed before
+      // D_ws(n - 1), whose completion the r warps saw before rho_{n-1}, the
+      // operand of D_S(n); its export is checked.
+      if (n >= S_TILES)
+        ok = warp_wait(&bars[B_XR + n % S_TILES], tile_parity(n - S_TILES, S_TILES), ok);
+      uint8_t* st = sm + OFF_S + (n % S_TILES) * 16384;
       publish16(st, c, 2 * h, S);
       fence_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_ES + (n & 1)]);   // for the exporter
+      if (lane == 0) mbar_arrive(&bars[B_ES + n % S_TILES]);   // for the exporter
       tc_fence_before();
       // (a sync, not an arrive: a state warp that ran a step ahead could
       // otherwise complete the phase of a slower one and release D_ws early)
       nb_sync(2, 288);
       // gamma_n for S_{n+1}; then this warp is done with ring A slot n % 2.
       ok = warp_wait(&bars[B_FULLA + (n & 1)], (n >> 1) & 1, ok);
-      gam = reinterpret_cast<const float*>(sm + OFF_A + (n & 1) * A_SLOT + A_VEC)[2 * C];
+      gam = reinterpret_cast<const float*>(sm + OFF_V + (n & 1) * VEC_BYTES)[C];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_EMPTYA + (n & 1)]);
     }
@@ -498,9 +508,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = 0.f;
       }
-      const float* vec = reinterpret_cast<const float*>(slot + A_VEC);
-      const float ks = vec[C + j];
-      const float gam_n = vec[2 * C];
+      const float* vec = reinterpret_cast<const float*>(sm + OFF_V + sa * VEC_BYTES);
+      const float ks = vec[j];
+      const float gam_n = vec[C];
       const float uf = p.zero_u ? 0.f : 1.f;
       const uint8_t* ub = slot + A_U;
 #pragma unroll
@@ -538,7 +548,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       // no r warp can reach the next phase early. Under SSD (no D_t) a sync.
       if (no_w) nb_sync(3, 160); else nb_arrive(3, 160);
       // r into its tile n % 2 once the export of r_{n-2} from it is read out.
-      if (n >= 2) ok = warp_wait(&bars[B_XR + (n & 1)], ((n - 2) >> 1) & 1, ok);
+      if (n >= 2) ok = warp_wait(&bars[B_XR + (n - 2) % S_TILES], tile_parity(n - 2, S_TILES), ok);
       publish16(sm + OFF_R + sa * 8192, j, 2 * half, r);
       fence_async_shared();
       __syncwarp();
@@ -604,7 +614,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
           mbar_expect_tx(fb, A_TX);
           bulk_load(slot + A_T, slab + Slab::T2, 16384, fb);   // (first chunk: not used)
           bulk_load_hint(slot + A_U, slab + Slab::U + vt * 8192, 8192, fb, pol_last_read);
-          bulk_load(slot + A_VEC, slab + Slab::VEC, 1024, fb);
+          bulk_load(sb + OFF_V + (na & 1) * VEC_BYTES, slab + Slab::VEC + VEC_OFF, VEC_BYTES, fb);
           ++na;
           progress = true;
         }
@@ -641,7 +651,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         // (SSD: rho_n does not wait for the state, so D_S buffer n % 2 is
         // free only once the state warps have read D_S(n - 1) for S_{n-1})
         if (no_w && n >= 2)
-          ok = mbar_spin(&bars[B_ES + ((n - 1) & 1)], ((n - 1) >> 1) & 1, kWaitLimit);
+          ok = mbar_spin(&bars[B_ES + (n - 1) % S_TILES], tile_parity(n - 1, S_TILES), kWaitLimit);
         if (ok) ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
         if (ok) {
           tc_fence_after();
@@ -677,7 +687,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       ok = mbar_spin(&bars[B_FULLW + (m & 1)], (m >> 1) & 1, kWaitLimit);
       if (!ok) return;
       const uint32_t wa = sb + OFF_W + (m & 1) * W_SLOT;
-      const uint32_t st = sb + OFF_S + ((m > 0 ? m - 1 : 0) & 1) * 16384;
+      const uint32_t st = sb + OFF_S + ((m > 0 ? m - 1 : 0) % S_TILES) * 16384;
       const uint32_t d = tmem + T_WS + 64 * (m & 1);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -701,17 +711,18 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       const uint64_t pol_keep = l2_evict_last();
       unsigned int* mark = wait_flags ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
       for (int nx = 0; nx < N && ok; ++nx) {
-        ok = mbar_wait(&bars[B_ES + (nx & 1)], (nx >> 1) & 1, kWaitLimit) &&
+        ok = mbar_wait(&bars[B_ES + nx % S_TILES], tile_parity(nx, S_TILES), kWaitLimit) &&
              mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
         if (!ok) break;
         // Both tiles of chunk nx out as one bulk group; once read out they may
         // be rewritten.
         uint8_t* xb = xbase + (size_t)nx * Xchg::BYTES;
-        bulk_store_hint(xb + Xchg::S + vt * Xchg::S_TILE, sb + OFF_S + (nx & 1) * 16384, 16384, pol_keep);
+        bulk_store_hint(xb + Xchg::S + vt * Xchg::S_TILE, sb + OFF_S + (nx % S_TILES) * 16384, 16384,
+                        pol_keep);
         bulk_store_hint(xb + Xchg::R + vt * Xchg::R_TILE, sb + OFF_R + (nx & 1) * 8192, 8192, pol_keep);
         bulk_commit();
         bulk_wait_read<0>();
-        mbar_arrive(&bars[B_XR + (nx & 1)]);
+        mbar_arrive(&bars[B_XR + nx % S_TILES]);
         // Chunks 0 .. done - 1 are in global memory once all but the newest
         // kMarkLag groups are.
         const int done = nx + 1 - kMarkLag;
