@@ -107,6 +107,7 @@ constexpr int kMarkEvery = 16;
 constexpr int kMarkTail = 4;
 constexpr int kMarkTailSpan = kMarkEvery;
 constexpr int kMarkLag = 2;
+constexpr int kProduceBar = 4;   // named barrier of a chain CTA's chunk production (warps 0-7)
 
 // Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
 // of two slots, each slot released as soon as its last reader is done:
@@ -371,12 +372,14 @@ __device__ __forceinline__ void output_items(const CUtensorMap* qmap, const Para
 }
 
 // ============================================================================ chain
-// seq = b * HV + hv, value columns [32 vt, 32 vt + 32). wait_flags: chunk
-// n's slab is produced in the same launch (wait for its flag before loading
-// it), and the exports are marked for the output items, which the CTA joins
-// (with q by qmap) once its chain is done.
+// seq = b * HV + hv, value columns [32 vt, 32 vt + 32). With maps (the
+// one-launch forward): chunk n's slab is produced in the same launch (wait for
+// its flag before loading it), the CTA first produces chunk vt of its
+// sequence itself, the exports are marked for the output items, and the CTA
+// joins them once its chain is done.
 __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq, int vt,
-                                           bool wait_flags, const CUtensorMap* qmap) {
+                                           const chunk::Maps* maps) {
+  const bool wait_flags = maps != nullptr;
   const int v0 = vt * VC;
   const int N = p.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -409,6 +412,32 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   tc_fence_after();
   const uint32_t tmem = *tslot;
   bool ok = true;
+  if (maps && vt < N) {
+    // The sequence's first chunks come from its own chain CTAs (chunk vt
+    // here, by warps 0-7 in the worker group layout over the rings, which are
+    // idle until the chain starts): their SMs have nothing else in flight, so
+    // the slab is ready and its flag visible sooner than a worker's.
+    if (warp < 8) {
+      if (tid == 0) chunk::init_group_bars(sm);
+      chunk::group_sync(kProduceBar);
+      chunk::produce_chunk(*maps, p, sm, tid, kProduceBar, vt, seq % p.HV, seq / p.HV, 0u, tmem,
+                           nullptr, nullptr);
+      if (tid == 0) {
+        bulk_wait<0>();
+        fence_async_global();
+        st_release_gpu(p.flags + chunk0 + vt, 1u);
+      }
+    }
+    tc_fence_before();
+    nb_sync(1, CHAIN_THREADS);
+    tc_fence_after();
+    if (tid == 0) {
+      uint64_t* gb = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
+      for (int i = 0; i < chunk::kNumBars; ++i)
+        if (i != 2) mbar_inval(gb + i);   // (index 2 holds the TMEM slot word, not a barrier)
+    }
+    nb_sync(1, CHAIN_THREADS);
+  }
   uint8_t* xbase = p.xchg + (size_t)chunk0 * Xchg::BYTES;
   // Mamba2 SSD: W = 0, so D_ws and D_t vanish and r_n = U_n does not depend on
   // the state; the W ring, both products and their waits are skipped, and
@@ -747,7 +776,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
 
   tc_fence_before();
   nb_sync(1, CHAIN_THREADS);
-  if (qmap) {
+  if (maps) {
     // One-launch forward: the CTA joins the output work as two groups of 8
     // warps in the worker group layout, each with 256 of the chain's TMEM
     // columns (the chain's tiles and rings are dead).
@@ -755,7 +784,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     const int grp = warp >> 3;
     uint8_t* gsm = sm + grp * chunk::GROUP_BYTES;
     if ((tid & 255) == 0) chunk::init_group_bars(gsm);
-    output_items(qmap, p, gsm, tid & 255, 1 + grp, tmem + 256 * grp, 0u, 0u);
+    output_items(&maps->q, p, gsm, tid & 255, 1 + grp, tmem + 256 * grp, 0u, 0u);
     // (barrier 0: group 0 may still be on named barrier 1 with 256 threads)
     tc_fence_before();
     __syncthreads();
@@ -770,14 +799,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, false, nullptr);
+  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, nullptr);
 }
 
 
 // =========================================================================== worker
 // Two groups of 8 warps run the chunk-local stage over chunk items in chunk
-// order (item it: chunk it / (B HV) of sequence it % (B HV)); group G of
-// NG takes items G, G + NG, ... Then each group takes output items.
+// order (item it: chunk it / (B HV) of sequence it % (B HV)); group G of NG
+// takes items G, G + NG, ... (the groups 0 of all workers first). Then each
+// group takes output items. (Holding group 1 back until group 0's first chunk
+// was done measured 2 us slower: a worker's first chunk takes ~19 us even
+// alone on its SM, against ~12 us for its later ones.)
 __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Params& p,
                                             uint8_t* sm_base, int worker, int n_workers) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -794,16 +826,18 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
   const uint32_t tmem = *tslot + grp * chunk::TMEM_COLS;
   const int nseq = p.B * p.HV;
   const long items = (long)nseq * p.N;
-  const int G = 2 * worker + grp, NG = 2 * n_workers;
+  const int G = grp * n_workers + worker, NG = 2 * n_workers;
+  // (chunks 0 .. VTILES - 1 of every sequence come from its chain CTAs)
+  const long first = (long)nseq * (p.N < VTILES ? p.N : VTILES);
   unsigned int* pending = nullptr;
   uint32_t ph = 0;
-  for (long it = G; it < items; it += NG) {
+  for (long it = first + G; it < items; it += NG) {
     const int n = (int)(it / nseq), seq = (int)(it % nseq);
     const int b = seq / p.HV, hv = seq % p.HV;
     chunk::produce_chunk(maps, p, sm, gtid, 1 + grp, n, hv, b, ph, tmem, nullptr, pending);
     pending = p.flags + slab_index(p, b, hv, n);
-    if (it < NG) {
-      // The first wave (the chunks the chains start on): published at once
+    if (it < first + NG) {
+      // The first wave (the chunks the chains reach first): published at once
       // rather than at the start of the next item.
       if (gtid == 0) {
         bulk_wait<0>();
@@ -837,7 +871,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   const int cta = blockIdx.x;
   if (cta < n_chain) {
-    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, true, &maps.q);
+    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, &maps);
   } else {
     worker_role(maps, p, sm, cta - n_chain, n_workers);
   }
