@@ -138,8 +138,8 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
     tma_load4(smem_u32(sm + OFF_V0), &maps.v, 0, hv, t0, b, bar_v);
     tma_load4(smem_u32(sm + OFF_V1), &maps.v, 64, hv, t0, b, bar_v);
     // The previous chunk's slab is complete in global memory once this
-    // thread's bulk stores are (its A_qk store completed before its inverse
-    // barrier): publish it.
+    // thread's bulk stores are (every bulk store of a slab is thread 0's; the
+    // row factors, plain stores, came before a group barrier): publish it.
     if (release_flag) {
       bulk_wait<0>();
       fence_async_global();
@@ -331,10 +331,12 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   tc_fence_before();
   group_sync(bar_id);
 
-  // A_qk hi / lo out by TMA and the per-row factors of the state pass, on
-  // warps 2-7 while warps 0-1 run level 0 of the inverse.
+  // A_qk hi / lo out by a bulk copy (thread 0, like every bulk store of the
+  // slab, so that its one completion wait before the flag covers them all),
+  // and the per-row factors of the state pass on warps 2-7 while warps 0-1
+  // run level 0 of the inverse.
   constexpr int kRowTid = 64;          // first thread of the row-factor warps
-  if (tid == kRowTid) {
+  if (tid == 0) {
     bulk_store(slab + Slab::AQ2, smem_u32(sm + OFF_AQS), 16384);
     bulk_commit();
   }
@@ -352,9 +354,9 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
 
   // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
   unit_lower_inverse64<LDL, LDX>(L, X, T, tid, bar_id);
-  // The A_qk store complete (its staging is overwritten next, and the slab is
-  // published only once every store of this chunk is complete).
-  if (tid == kRowTid) bulk_wait<0>();
+  // The A_qk staging read out (it is overwritten next); the store itself
+  // completes before the slab's flag, with the others.
+  if (tid == 0) bulk_wait_read<0>();
   group_sync(bar_id);   // X complete; L and the A_qk staging are dead from here on
 
   // ---- A operands XW = [X' hi/lo], XU = [X hi/lo] (rows interleaved, see stacked_row)
