@@ -108,6 +108,9 @@ constexpr int kMarkTail = 4;
 constexpr int kMarkTailSpan = kMarkEvery;
 constexpr int kMarkLag = 2;
 constexpr int kProduceBar = 4;   // named barrier of a chain CTA's chunk production (warps 0-7)
+// First chunks of a sequence its chain CTAs produce, one each (two each
+// measured 12 us slower per forward).
+constexpr int kChainChunks = VTILES;
 
 // Shared memory of a chain CTA (bytes from a 1024-aligned base). Three rings
 // of two slots, each slot released as soon as its last reader is done:
@@ -413,19 +416,23 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   const uint32_t tmem = *tslot;
   bool ok = true;
   if (maps && vt < N) {
-    // The sequence's first chunks come from its own chain CTAs (chunk vt
-    // here, by warps 0-7 in the worker group layout over the rings, which are
-    // idle until the chain starts): their SMs have nothing else in flight, so
-    // the slab is ready and its flag visible sooner than a worker's.
+    // The sequence's first chunks come from its own chain CTAs (chunks vt,
+    // vt + 4, ... below kChainChunks here, by warps 0-7 in the worker group
+    // layout over the rings, which are idle until the chain starts): their
+    // SMs have nothing else in flight, and a worker's first chunk is slow.
     if (warp < 8) {
       if (tid == 0) chunk::init_group_bars(sm);
       chunk::group_sync(kProduceBar);
-      chunk::produce_chunk(*maps, p, sm, tid, kProduceBar, vt, seq % p.HV, seq / p.HV, 0u, tmem,
-                           nullptr, nullptr);
-      if (tid == 0) {
-        bulk_wait<0>();
-        fence_async_global();
-        st_release_gpu(p.flags + chunk0 + vt, 1u);
+      uint32_t ph = 0;
+      for (int n = vt; n < N && n < kChainChunks; n += VTILES) {
+        chunk::produce_chunk(*maps, p, sm, tid, kProduceBar, n, seq % p.HV, seq / p.HV, ph, tmem,
+                             nullptr, nullptr);
+        if (tid == 0) {
+          bulk_wait<0>();
+          fence_async_global();
+          st_release_gpu(p.flags + chunk0 + n, 1u);
+        }
+        ph ^= 1u;
       }
     }
     tc_fence_before();
@@ -827,8 +834,8 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
   const int nseq = p.B * p.HV;
   const long items = (long)nseq * p.N;
   const int G = grp * n_workers + worker, NG = 2 * n_workers;
-  // (chunks 0 .. VTILES - 1 of every sequence come from its chain CTAs)
-  const long first = (long)nseq * (p.N < VTILES ? p.N : VTILES);
+  // (chunks 0 .. kChainChunks - 1 of every sequence come from its chain CTAs)
+  const long first = (long)nseq * (p.N < kChainChunks ? p.N : kChainChunks);
   unsigned int* pending = nullptr;
   uint32_t ph = 0;
   for (long it = first + G; it < items; it += NG) {
