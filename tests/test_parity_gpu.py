@@ -88,6 +88,30 @@ def test_full_workloads_sampled(name):
     check_against_oracle(w, gin.make_inputs(w), sel=FULL_SAMPLES[name])
 
 
+# The one-launch forward's chunk counts around its own structure: the chain
+# CTAs of a sequence produce its first four chunks, the workers the rest, and
+# the output items wait for export marks every 16 chunks (every 4 in the last
+# 16): one chunk, fewer chunks than chain CTAs, exactly four, one more, a
+# ragged tail past the first mark, and several sequences with a carried state.
+ONE_LAUNCH_SHAPES = [
+    dict(T=1, H=3, HV=3),
+    dict(T=64, H=2, HV=2),
+    dict(T=130, H=2, HV=4),
+    dict(T=256, H=1, HV=3),
+    dict(T=257, H=3, HV=3),
+    dict(T=1100, H=1, HV=2),
+    dict(B=2, T=700, H=2, HV=2, s0_std=0.02),
+]
+
+
+@pytest.mark.parametrize("ov", ONE_LAUNCH_SHAPES, ids=lambda ov: "-".join(f"{k}{v}" for k, v in ov.items()))
+def test_one_launch_chunk_counts(ov):
+    w = gin.shrink(gin.WORKLOADS["gdn_t4096_h12"], **ov)
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    assert gdr.chunk_fwd_path(dims, w.C, 0) == 2          # the one-launch form
+    check_against_oracle(w, gin.make_inputs(w))
+
+
 @pytest.mark.parametrize("name", ["gdn_t4096_h12", "kda_gqa_t8192"])
 def test_bf16_output_is_fp32_output_rounded(name):
     w = gin.shrink(gin.WORKLOADS[name], B=1, T=257, H=1, HV=2)
