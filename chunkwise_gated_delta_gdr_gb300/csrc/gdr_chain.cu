@@ -107,6 +107,8 @@ constexpr int kMarkEvery = 16;
 constexpr int kMarkTail = 4;
 constexpr int kMarkTailSpan = kMarkEvery;
 constexpr int kMarkLag = 2;
+// (Bringing the next four slabs into L2 ahead of the ring loads with bulk
+// prefetches measured 14 us slower per forward.)
 constexpr int kProduceBar = 4;   // named barrier of a chain CTA's chunk production (warps 0-7)
 // First chunks of a sequence its chain CTAs produce, one each (two each
 // measured 12 us slower per forward).
@@ -166,8 +168,10 @@ enum : int {
   B_RP = 17,      // [2] r_n tile published, barrier n % 2 (4 r warps)
   B_ES = 19,      // [3] S_n published, barrier n % 3 (8 state warps; for the exporter)
   B_XR = 22,      // [3] exports of chunk n (S and r tiles) read out, barrier n % 3 (exporter)
-  B_SLOT = 25     // TMEM slot (u32)
+  B_SLOT = 25,    // TMEM slot (u32)
+  B_PP = 26       // [2] SSD: rho_n published, barrier n % 2 (4 r warps; for the D_S issuer)
 };
+static_assert((B_PP + 2) * 8 <= 256, "chain barrier area");
 // A waiter tests an mbarrier phase by parity, so a barrier must never run two
 // phases ahead of one of its waiters. The S, r and export barriers could (S_{n+1}
 // may be published before chunk n is exported, and chunk n - 1 exported before
@@ -401,6 +405,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       mbar_init(&bars[B_WS + i], 1);
       mbar_init(&bars[B_DS + i], 1);
       mbar_init(&bars[B_RP + i], 4);
+      mbar_init(&bars[B_PP + i], 4);
     }
     for (int i = 0; i < S_TILES; ++i) {
       mbar_init(&bars[B_ES + i], 8);
@@ -581,8 +586,15 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       if (lane == 0) mbar_arrive(&bars[B_EMPTYA + sa]);   // U, VEC read; D_t(n) (T_n) done
       tc_fence_before();
       // An arrive: r_{n+1} needs D_t(n + 1), issued only after this phase, so
-      // no r warp can reach the next phase early. Under SSD (no D_t) a sync.
-      if (no_w) nb_sync(3, 160); else nb_arrive(3, 160);
+      // no r warp can reach the next phase early. Under SSD (no D_t) the r
+      // warps do not wait for the issuer at all: they arrive on mbarrier
+      // B_PP n % 2 instead (its next phase needs D_S(n + 1), which the issuer
+      // starts only after this one).
+      if (no_w) {
+        if (lane == 0) mbar_arrive(&bars[B_PP + (n & 1)]);
+      } else {
+        nb_arrive(3, 160);
+      }
       // r into its tile n % 2 once the export of r_{n-2} from it is read out.
       if (n >= 2) ok = warp_wait(&bars[B_XR + (n - 2) % S_TILES], tile_parity(n - 2, S_TILES), ok);
       publish16(sm + OFF_R + sa * 8192, j, 2 * half, r);
@@ -681,9 +693,13 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // alone, for the final state). (D_t first measured slower: S_{n+1}, and
     // with it D_ws(n + 2), comes later.)
     for (int n = 0; n < N; ++n) {
-      nb_sync(3, 160);
+      if (!no_w) nb_sync(3, 160);
       if (lane == 0 && ok) {
         const int sa = n & 1;
+        if (no_w) {
+          ok = mbar_spin(&bars[B_PP + sa], (n >> 1) & 1, kWaitLimit);   // rho_n published
+          tc_fence_after();
+        }
         // (SSD: rho_n does not wait for the state, so D_S buffer n % 2 is
         // free only once the state warps have read D_S(n - 1) for S_{n-1})
         if (no_w && n >= 2)
