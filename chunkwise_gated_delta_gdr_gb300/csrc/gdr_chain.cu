@@ -58,10 +58,12 @@
 // per (chunk, sequence, 64 value columns) on tcgen05.
 //
 // One-launch forward (launch_fused): one cooperative launch of one CTA per SM.
-// The first CTAs are the chains; the other CTAs are workers, two groups of 8
-// warps each, that run the chunk-local stage (gdr_chunk_tc.cuh) over the
-// chunks in chunk order, raising each chunk's flag once its slab is in global
-// memory. A chain's TMA warp waits for chunk n's flag before loading it. Each
+// The first CTAs are the chains; each first runs the chunk-local stage
+// (gdr_chunk_tc.cuh) for one of its sequence's first four chunks. The other
+// CTAs are workers, two groups of 8 warps each, that run the chunk-local stage
+// over the remaining chunks in chunk order. Every chunk's flag is raised once
+// its slab is in global memory, and a chain's TMA warp waits for chunk n's
+// flag before loading it. Each
 // worker group then takes output items (chunk n, sequence, 64 value columns)
 // in chunk order from a counter, and forms o_n once the chains of both value
 // tiles have marked chunk n exported; a chain CTA joins them once its chain
