@@ -123,8 +123,9 @@ gdr_status gdr_chunk_fwd(const void* q, const void* k, const void* v, const floa
  * the decayed dots A_kk / A_qk, the triangular solve for W and U, written into
  * `workspace` (the "chunk 内的 cumsum 与下三角解" section of the notes).
  * gdr_chunk_recur then runs the state recurrence across chunks (the notes'
- * inter-chunk loop) and writes out / final_state. gdr_chunk_fwd is exactly
- * prepare followed by recur on the same stream.
+ * inter-chunk loop) and writes out / final_state. gdr_chunk_fwd computes what
+ * prepare followed by recur on the same stream computes (in one cooperative
+ * launch where it can, see gdr_set_flag_wait_limit).
  *
  * The prepared workspace does not depend on the initial state: after one
  * prepare, recur may run any number of times with different initial states
@@ -180,14 +181,17 @@ gdr_status gdr_stream_status(gdr_stream_t stream, void* workspace);
  * gdr_set_flag_wait_limit -- bound of the device waits of the one-launch forward.
  *
  * With the scalar gate on the tensor-core path, gdr_chunk_fwd runs both stages
- * in one cooperative launch when the problem has few enough chains: worker
- * CTAs produce each chunk's operands and raise a flag for it, chain CTAs of
- * the same launch wait for the flag before they read the chunk. A chain polls
- * a flag at most `polls` times, about 64 ns apart. If the flag is still down,
- * it records GDR_ERR_TIMEOUT in the workspace error word (gdr_stream_status
- * reports it) and runs to its end on whatever the workspace holds: the call
- * then finishes with wrong outputs instead of hanging. The default, 2^24
- * polls (about a second), is far beyond any real wait.
+ * in one cooperative launch when the problem has few enough chains (B HV
+ * value heads x 4 chains at most half the SMs): CTAs produce each chunk's
+ * operands and raise a flag for it, chain CTAs of the same launch wait for
+ * the flag before they read the chunk, and the outputs of each chunk are
+ * formed once its chains have marked it exported. A chain polls a flag, and an
+ * output item a mark, at most `polls` times, about 64 ns apart. If it is still
+ * down, the CTA records GDR_ERR_TIMEOUT in the workspace error word
+ * (gdr_stream_status reports it) and runs to its end on whatever the
+ * workspace holds: the call then finishes with wrong outputs instead of
+ * hanging. The default, 2^24 polls (about a second), is far beyond any real
+ * wait.
  *
  *   polls   >= 0: the new bound, for calls enqueued from now on (all devices,
  *           all threads); < 0: leave the bound as it is.
