@@ -494,7 +494,8 @@ def run_ours(args, rank, local_rank, world):
     # (chunk_tc_kernel, chain_kernel + output_kernel for the scalar gate;
     # chunk_kda_kernel, state_kda_tc_kernel for the per-key gate).
     ck, rk = (("chunk_kda_kernel", "state_kda_tc_kernel") if gate
-              else ("chunk_tc_kernel", "chain_kernel+output_kernel"))
+              else ("chunk_tc_kernel", "chains+outputs (fused_kernel without the chunk stage, "
+                                       "or chain_kernel+output_kernel)"))
     one_launch = path == 2 and segments == 1
     if one_launch:
         kernel_scope = ("fused_kernel (one cooperative launch: chunk producers, chains and "

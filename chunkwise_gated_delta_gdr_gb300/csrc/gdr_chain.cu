@@ -385,10 +385,11 @@ __device__ __forceinline__ void output_items(const CUtensorMap* qmap, const Para
 // one-launch forward): chunk n's slab is produced in the same launch (wait for
 // its flag before loading it), the CTA first produces chunk vt of its
 // sequence itself, the exports are marked for the output items, and the CTA
-// joins them once its chain is done.
+// joins them once its chain is done. With maps but not produce (chains and
+// output items after a finished chunk-local stage) only the last two.
 __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq, int vt,
-                                           const chunk::Maps* maps) {
-  const bool wait_flags = maps != nullptr;
+                                           const chunk::Maps* maps, bool produce) {
+  const bool wait_flags = maps != nullptr && produce;
   const int v0 = vt * VC;
   const int N = p.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -422,7 +423,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   tc_fence_after();
   const uint32_t tmem = *tslot;
   bool ok = true;
-  if (maps && vt < N) {
+  if (wait_flags && vt < N) {
     // The sequence's first chunks come from its own chain CTAs (chunks vt,
     // vt + 4, ... below kChainChunks here, by warps 0-7 in the worker group
     // layout over the rings, which are idle until the chain starts): their
@@ -763,7 +764,10 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     if (lane == 0) {
       // The output pass reads the exchange next: keep it in L2.
       const uint64_t pol_keep = l2_evict_last();
-      unsigned int* mark = wait_flags ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
+      unsigned int* mark = maps ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
+      // (long chains: about 16 marks in all, each holds the exporter up)
+      const int mark_every = N / 16 > kMarkEvery ? ((N / 16 + kMarkTail - 1) / kMarkTail) * kMarkTail
+                                                 : kMarkEvery;
       for (int nx = 0; nx < N && ok; ++nx) {
         ok = mbar_wait(&bars[B_ES + nx % S_TILES], tile_parity(nx, S_TILES), kWaitLimit) &&
              mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
@@ -781,7 +785,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         // kMarkLag groups are.
         const int done = nx + 1 - kMarkLag;
         if (mark && done > 0 && nx + 1 < N &&
-            (done % kMarkEvery == 0 || (done >= N - kMarkTailSpan && done % kMarkTail == 0))) {
+            (done % mark_every == 0 || (done >= N - kMarkTailSpan && done % kMarkTail == 0))) {
           bulk_wait<kMarkLag>();
           fence_async_global();
           st_release_gpu(mark, (unsigned int)done);
@@ -824,7 +828,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, nullptr);
+  chain_role(p, sm, blockIdx.y * p.HV + blockIdx.x / VTILES, blockIdx.x % VTILES, nullptr, false);
 }
 
 
@@ -836,7 +840,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
 // was done measured 2 us slower: a worker's first chunk takes ~19 us even
 // alone on its SM, against ~12 us for its later ones.)
 __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Params& p,
-                                            uint8_t* sm_base, int worker, int n_workers) {
+                                            uint8_t* sm_base, int worker, int n_workers, bool produce) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int grp = warp >> 3, gtid = tid & 255;
   uint8_t* sm = sm_base + grp * chunk::GROUP_BYTES;
@@ -853,7 +857,7 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
   const long items = (long)nseq * p.N;
   const int G = grp * n_workers + worker, NG = 2 * n_workers;
   // (chunks 0 .. kChainChunks - 1 of every sequence come from its chain CTAs)
-  const long first = (long)nseq * (p.N < kChainChunks ? p.N : kChainChunks);
+  const long first = produce ? (long)nseq * (p.N < kChainChunks ? p.N : kChainChunks) : items;
   unsigned int* pending = nullptr;
   uint32_t ph = 0;
   for (long it = first + G; it < items; it += NG) {
@@ -890,15 +894,15 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
 }
 
 __global__ void __launch_bounds__(FUSED_THREADS, 1)
-    fused_kernel(const __grid_constant__ chunk::Maps maps, Params p, int n_chain, int n_workers) {
+    fused_kernel(const __grid_constant__ chunk::Maps maps, Params p, int n_chain, int n_workers, int produce) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   const int cta = blockIdx.x;
   if (cta < n_chain) {
-    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, &maps);
+    if (threadIdx.x < CHAIN_THREADS) chain_role(p, sm, cta / VTILES, cta % VTILES, &maps, produce != 0);
   } else {
-    worker_role(maps, p, sm, cta - n_chain, n_workers);
+    worker_role(maps, p, sm, cta - n_chain, n_workers, produce != 0);
   }
 }
 
@@ -1053,8 +1057,11 @@ bool fused_fits(int B, int HV) {
   return dev.coop && dev.sms > 0 && n_chain * 2 <= dev.sms;
 }
 
-gdr_status launch_fused(const Params& p, cudaStream_t stream) {
-  if (p.gate_mode != 0 || !p.flags || !p.xchg || !fused_fits(p.B, p.HV)) return GDR_ERR_UNSUPPORTED;
+namespace {
+
+// One cooperative launch of fused_kernel: with produce, the whole forward;
+// without, the chains and the output items after a finished chunk-local stage.
+gdr_status launch_one(const Params& p, cudaStream_t stream, bool produce) {
   const DeviceInfo& dev = device_info();
   const int n_chain = p.B * p.HV * VTILES;
   const int n_workers = dev.sms - n_chain;
@@ -1078,12 +1085,27 @@ gdr_status launch_fused(const Params& p, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, m, p, n_chain, n_workers);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, m, p, n_chain, n_workers, produce ? 1 : 0);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return e == cudaErrorCooperativeLaunchTooLarge ? GDR_ERR_UNSUPPORTED : GDR_ERR_CUDA;
   }
   return GDR_OK;
+}
+
+}  // namespace
+
+gdr_status launch_fused(const Params& p, cudaStream_t stream) {
+  if (p.gate_mode != 0 || !p.flags || !p.xchg || !fused_fits(p.B, p.HV)) return GDR_ERR_UNSUPPORTED;
+  return launch_one(p, stream, true);
+}
+
+gdr_status launch_chain_outputs(const Params& p, cudaStream_t stream) {
+  const DeviceInfo& dev = device_info();
+  if (p.gate_mode != 0 || !p.flags || !p.xchg || !dev.coop || dev.sms <= 0 ||
+      (long long)p.B * p.HV * VTILES > dev.sms)
+    return GDR_ERR_UNSUPPORTED;
+  return launch_one(p, stream, false);
 }
 
 }  // namespace fast

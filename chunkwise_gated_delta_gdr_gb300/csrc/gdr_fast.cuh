@@ -133,6 +133,11 @@ gdr_status launch_outputs(const Params& p, cudaStream_t stream);
 // Scalar gate: the whole forward in one cooperative launch (gdr_chain.cu);
 // declines with GDR_ERR_UNSUPPORTED (nothing enqueued) when it does not pay.
 gdr_status launch_fused(const Params& p, cudaStream_t stream);
+// Scalar gate: the chains and the output items in one cooperative launch after
+// a finished chunk-local stage (the outputs of chunks already exported are
+// formed beside the chains); declines with GDR_ERR_UNSUPPORTED (nothing
+// enqueued) when the chains do not fit on the SMs at once.
+gdr_status launch_chain_outputs(const Params& p, cudaStream_t stream);
 // Whether launch_fused runs for B x HV sequences on the current device.
 bool fused_fits(int B, int HV);
 // Per-key gate: the recurrence on tcgen05, 64 value columns per CTA (gdr_state_kda.cu).

@@ -101,6 +101,10 @@ gdr_status launch_tc(const Problem& p, void* ws_body, unsigned int* error_word,
     // output pass, recur_mode 2 is nothing); the scalar-gate chain leaves them
     // to the output pass (recur_mode 1: the states alone).
     if (p.gate_mode) return p.recur_mode == 2 ? GDR_OK : fast::launch_state_kda_tc(f, stream);
+    if (p.recur_mode == 0) {
+      const gdr_status st = fast::launch_chain_outputs(f, stream);
+      if (st != GDR_ERR_UNSUPPORTED) return st;
+    }
     if (p.recur_mode != 2) {
       const gdr_status st = fast::launch_chain(f, stream);
       if (st != GDR_OK || p.recur_mode == 1) return st;
