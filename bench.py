@@ -504,8 +504,8 @@ def run_ours(args, rank, local_rank, world):
         step_traffic = traffic
     elif segments > 1:
         kernel_scope = ("one gdr_chunk_fwd_segmented call: chunk-local kernel, 3 recurrence "
-                        "launches, identity, combine and output kernels")
-        launches = 7 if not gate else 6
+                        "launches (the last with the output items), identity and combine kernels")
+        launches = 6
         step_traffic = None
     else:
         kernel_scope = f"one forward call: {ck} + {rk}"

@@ -402,13 +402,11 @@ gdr_status gdr_chunk_fwd_segmented(const void* q, const void* k, const void* v, 
   st = launch_segment_combine(Ast, Bst, initial_state, Sin, final_state, dims->B, segments,
                               dims->HV, dims->K, s);
   if (st != GDR_OK) return st;
-  // 5. each segment from its true initial state: the states, then the outputs on
-  // every SM (one pass where a kernel writes both)
-  st = run(2, q, k, nullptr, nullptr, nullptr, Sin, chunk_size, scale, use_qk_l2norm, gate_mode,
-           out, nullptr, &d2, workspace, L.inner, stream, 0, 0, 1);
-  if (st != GDR_OK) return st;
-  return run(2, q, k, nullptr, nullptr, nullptr, Sin, chunk_size, scale, use_qk_l2norm,
-             gate_mode, out, nullptr, &d2, workspace, L.inner, stream, 0, 0, 2);
+  // 5. each segment from its true initial state, states and outputs (for the
+  // scalar gate on tensor cores: the chains with their output items beside
+  // them in one launch when they fit on the SMs at once)
+  return run(2, q, k, nullptr, nullptr, nullptr, Sin, chunk_size, scale, use_qk_l2norm, gate_mode,
+             out, nullptr, &d2, workspace, L.inner, stream, 0, 0, 0);
 }
 
 }  // extern "C"
