@@ -641,6 +641,19 @@ def run_decode(args, rank, local_rank, world, kind="decode"):
             pg.destroy_process_group()
         return 0
     hbm, _, peak_kind = load_peaks()
+    if kind == "ssd":
+        # The SSD forward runs the launches of gdr_chunk_fwd: one cooperative
+        # launch when the chains fit beside the producers, else the chunk kernel
+        # and the chains with the output items (or chain and output kernels).
+        dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        if gdr.chunk_fwd_path(dims, w.C, 0) == 2:
+            launches, scope = 1, "one gdr_ssd_chunk_fwd call: fused_kernel (one cooperative launch)"
+        else:
+            launches = 2 if w.B * w.HV * 4 <= sms else 3
+            scope = "one gdr_ssd_chunk_fwd call: chunk_tc_kernel + chains and outputs"
+    else:
+        launches, scope = 1, "one gdr_recurrent_fwd call (one decode kernel)"
     sbytes = 0 if kind == "ssd" else 2 * w.B * w.HV * w.K * w.V * 4   # state read + write
     io = (2 * w.B * w.T * w.H * w.K * 2 + w.B * w.T * w.HV * w.V * 2 + 2 * w.B * w.T * w.HV * 4 +
           w.B * w.T * w.HV * w.V * 4)
@@ -661,12 +674,11 @@ def run_decode(args, rank, local_rank, world, kind="decode"):
                    "parallelism": f"{world} rank(s), value heads sharded, no collective"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,
-                     "scope": ("one gdr_ssd_chunk_fwd call (chunk-local kernel + recurrence kernel)"
-                               if kind == "ssd" else "one gdr_recurrent_fwd call (recurrent_kernel)"),
+                     "scope": scope,
                      "algorithmic_bytes_per_step": bytes_alg, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": (2 if kind == "ssd" else 1) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "median_ms": statistics.median(tot),
         "warm_l2_ms": warm_ms,

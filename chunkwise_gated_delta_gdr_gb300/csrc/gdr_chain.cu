@@ -57,6 +57,11 @@
 //     o_n = qscale (q S_n) + A_qk r_n
 // per (chunk, sequence, 64 value columns) on tcgen05.
 //
+// Mamba2 SSD (W = 0, U = v): r_n = v_n does not depend on the state, so the
+// chunk-local stage forms each chunk's whole increment N_n = k_n^T rho_n and
+// writes the r tiles itself; the chain CTA then runs S_{n+1} = gamma_n S_n +
+// N_n with no product (ssd_chain), exporting S_n as above.
+//
 // One-launch forward (launch_fused): one cooperative launch of one CTA per SM.
 // The first CTAs are the chains; each first runs the chunk-local stage
 // (gdr_chunk_tc.cuh) for one of its sequence's first four chunks. The other
@@ -170,10 +175,9 @@ enum : int {
   B_RP = 17,      // [2] r_n tile published, barrier n % 2 (4 r warps)
   B_ES = 19,      // [3] S_n published, barrier n % 3 (8 state warps; for the exporter)
   B_XR = 22,      // [3] exports of chunk n (S and r tiles) read out, barrier n % 3 (exporter)
-  B_SLOT = 25,    // TMEM slot (u32)
-  B_PP = 26       // [2] SSD: rho_n published, barrier n % 2 (4 r warps; for the D_S issuer)
+  B_SLOT = 25     // TMEM slot (u32)
 };
-static_assert((B_PP + 2) * 8 <= 256, "chain barrier area");
+static_assert((B_SLOT + 1) * 8 <= 256, "chain barrier area");
 // A waiter tests an mbarrier phase by parity, so a barrier must never run two
 // phases ahead of one of its waiters. The S, r and export barriers could (S_{n+1}
 // may be published before chunk n is exported, and chunk n - 1 exported before
@@ -381,6 +385,210 @@ __device__ __forceinline__ void output_items(const CUtensorMap* qmap, const Para
 }
 
 // ============================================================================ chain
+// The next slab flags of a sequence (chunk slabs written by workers of the
+// same launch): kFlagWindow of them read at once, then one acquire for the
+// run of those already set. True when nflag advanced. After p.wait_limit
+// fruitless polls it gives up: records it and sets nflag = N, so that the
+// caller runs to its end on whatever the workspace holds (in bounds) and no
+// other wait runs out too.
+__device__ __forceinline__ bool poll_flags(const Params& p, int chunk0, int N, int& nflag,
+                                           long& polls, bool& flags_ok) {
+  unsigned int f[kFlagWindow];
+#pragma unroll
+  for (int z = 0; z < kFlagWindow; ++z)
+    f[z] = nflag + z < N ? ld_relaxed_gpu(p.flags + chunk0 + nflag + z) : 0u;
+  int m = nflag;
+#pragma unroll
+  for (int z = 0; z < kFlagWindow; ++z)
+    if (m == nflag + z && f[z] != 0u) ++m;
+  if (m > nflag) {
+    fence_acq_rel_gpu();     // acquire the slabs' writes
+    fence_async_global();    // ... for the bulk reads
+    nflag = m;
+    polls = 0;
+    return true;
+  }
+  if (++polls > p.wait_limit) {
+    flags_ok = false;
+    nflag = N;
+    atomicOr(p.error_word, kErrFlagWait);
+  }
+  return false;
+}
+// Chunks between export marks: kMarkEvery, or for long chains about 16 marks
+// in all (each holds the exporter up).
+__device__ __forceinline__ int mark_period(int N) {
+  return N / 16 > kMarkEvery ? ((N / 16 + kMarkTail - 1) / kMarkTail) * kMarkTail : kMarkEvery;
+}
+// After the export of chunk nx (its bulk group committed): chunks 0 .. done - 1
+// are in global memory once all but the newest kMarkLag groups are; announce
+// them every mark_every chunks, and every kMarkTail in the last kMarkTailSpan.
+__device__ __forceinline__ void mark_exports(unsigned int* mark, int nx, int N, int mark_every) {
+  const int done = nx + 1 - kMarkLag;
+  if (mark && done > 0 && nx + 1 < N &&
+      (done % mark_every == 0 || (done >= N - kMarkTailSpan && done % kMarkTail == 0))) {
+    bulk_wait<kMarkLag>();
+    fence_async_global();
+    st_release_gpu(mark, (unsigned int)done);
+  }
+}
+
+// ------------------------------------------------------------------ SSD chain
+// Mamba2 SSD (W = 0): r_n = U_n = v_n does not depend on the state, and the
+// chunk-local stage has formed each chunk's state increment N_n = k_n^T
+// diag(kscale_n) v_n (gdr_chunk_tc.cuh, Slab::ssd_n) and written r_n to the
+// exchange block, so the chain is the fp32 scan
+//     S_{n+1} = gamma_n S_n + N_n
+// without a product. Shared memory (from the chain's 1024-aligned base): a
+// ring of SSD_SLOTS increment boxes (this CTA's 32 value columns, [128 c][32 v]
+// fp32, 128-byte swizzled rows) with gamma_n beside each, then the S tiles.
+// Warps 0-7 hold S as in the delta-rule chain (thread (w, lane): channel
+// 32 (w % 4) + lane, columns [16 (w / 4), 16 (w / 4) + 16)) and publish each
+// S_n for the export; warp 12 loads the ring (waiting for the slab flags in
+// the one-launch forward); warp 13 exports the S tiles and marks them.
+constexpr int SSD_SLOTS = 6;
+constexpr int SSD_SLOT = (int)Slab::SSD_N_BOX;
+constexpr int SSD_OFF_GAM = SSD_SLOTS * SSD_SLOT;   // 16 bytes per slot
+constexpr int SSD_OFF_S = SSD_OFF_GAM + 1024;
+constexpr uint32_t SSD_TX = SSD_SLOT + 16;
+static_assert(SSD_SLOT == 16384 && SSD_OFF_S % 1024 == 0 && SSD_OFF_S + S_TILES * 16384 <= OFF_BARS,
+              "SSD chain shared memory");
+enum : int {
+  SB_FULL = 0,                      // [SSD_SLOTS] ring slot loaded
+  SB_EMPTY = SB_FULL + SSD_SLOTS,   // [SSD_SLOTS] ring slot read (8 state warps)
+  SB_ES = SB_EMPTY + SSD_SLOTS,     // [S_TILES] S_n published, barrier n % S_TILES (8 state warps)
+  SB_XR = SB_ES + S_TILES           // [S_TILES] export of S_n read out (exporter)
+};
+static_assert(SB_XR + S_TILES <= B_SLOT, "SSD barriers below the TMEM slot word");
+
+__device__ __forceinline__ void ssd_init_bars(uint64_t* bars) {
+  for (int i = 0; i < SSD_SLOTS; ++i) {
+    mbar_init(&bars[SB_FULL + i], 1);
+    mbar_init(&bars[SB_EMPTY + i], 8);
+  }
+  for (int i = 0; i < S_TILES; ++i) {
+    mbar_init(&bars[SB_ES + i], 8);
+    mbar_init(&bars[SB_XR + i], 1);
+  }
+}
+
+// All threads of the chain CTA; ok turns false (for the calling thread) when
+// one of its waits gave up.
+__device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq, int vt, bool wait_flags,
+                                          bool marks, uint8_t* xbase, bool& ok) {
+  const int N = p.N, v0 = vt * VC, chunk0 = seq * N;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
+  const uint32_t sb = smem_u32(sm);
+  if (warp < 8) {
+    const int qd = warp & 3, h = warp >> 2;
+    const int c = 32 * qd + lane;
+    float S[16];
+    if (p.s0) {
+      const float4* src =
+          reinterpret_cast<const float4*>(p.s0 + ((size_t)seq * K + c) * V + v0 + 16 * h);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = src[q];
+        S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) S[i] = 0.f;
+    }
+    for (int n = 0; n < N; ++n) {
+      // Chunk n's slab first, although S_n does not need it: its export (and
+      // the mark after it) must come after this CTA acquired chunk n's slab,
+      // whose A_qk, row factors and r tiles the output items read once the
+      // mark is out.
+      const int sl = n % SSD_SLOTS;
+      ok = warp_wait(&bars[SB_FULL + sl], (uint32_t)(n / SSD_SLOTS) & 1u, ok);
+      // S_n into tile n % S_TILES once the export of S_{n - S_TILES} from it is read out.
+      if (n >= S_TILES)
+        ok = warp_wait(&bars[SB_XR + n % S_TILES], tile_parity(n - S_TILES, S_TILES), ok);
+      publish16(sm + SSD_OFF_S + (n % S_TILES) * 16384, c, 2 * h, S);
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[SB_ES + n % S_TILES]);
+      const uint8_t* box = sm + sl * SSD_SLOT;
+      const float gam = *reinterpret_cast<const float*>(sm + SSD_OFF_GAM + sl * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = *reinterpret_cast<const float4*>(box + sw_off(c, 4 * h + q));
+        S[4 * q] = fmaf(gam, S[4 * q], x.x);
+        S[4 * q + 1] = fmaf(gam, S[4 * q + 1], x.y);
+        S[4 * q + 2] = fmaf(gam, S[4 * q + 2], x.z);
+        S[4 * q + 3] = fmaf(gam, S[4 * q + 3], x.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[SB_EMPTY + sl]);
+    }
+    if (p.sT) {
+      float4* dst = reinterpret_cast<float4*>(p.sT + ((size_t)seq * K + c) * V + v0 + 16 * h);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+    }
+  } else if (warp == 12) {
+    if (lane == 0) {
+      // Each increment box is read once, by this CTA.
+      const uint64_t pol = l2_evict_first();
+      int nl = 0, nflag = wait_flags ? 0 : N;
+      bool flags_ok = wait_flags;
+      long idle = 0, flag_polls = 0;
+      while (nl < N && ok) {
+        bool progress = false, polled = false;
+        if (flags_ok && nflag < N && nflag < nl + 2) {
+          polled = true;
+          progress = poll_flags(p, chunk0, N, nflag, flag_polls, flags_ok);
+        }
+        const int sl = nl % SSD_SLOTS;
+        if (nl < nflag &&
+            (nl < SSD_SLOTS || mbar_test(&bars[SB_EMPTY + sl], (uint32_t)(nl / SSD_SLOTS - 1) & 1u))) {
+          const uint8_t* slab = p.slabs + (size_t)(chunk0 + nl) * p.slab_bytes;
+          uint64_t* fb = &bars[SB_FULL + sl];
+          mbar_expect_tx(fb, SSD_TX);
+          bulk_load_hint(sb + sl * SSD_SLOT, slab + Slab::ssd_n(vt), SSD_SLOT, fb, pol);
+          bulk_load(sb + SSD_OFF_GAM + sl * 16, slab + Slab::VEC + 2 * C * 4, 16, fb);
+          ++nl;
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+        } else {
+          if (!polled && ++idle > kTmaIdleLimit) ok = false;
+          __nanosleep(64);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    if (lane == 0) {
+      const uint64_t pol_keep = l2_evict_last();   // the output items read it next
+      unsigned int* mark = marks ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
+      const int mark_every = mark_period(N);
+      for (int nx = 0; nx < N && ok; ++nx) {
+        ok = mbar_wait(&bars[SB_ES + nx % S_TILES], tile_parity(nx, S_TILES), kWaitLimit);
+        if (!ok) break;
+        bulk_store_hint(xbase + (size_t)nx * Xchg::BYTES + Xchg::S + vt * Xchg::S_TILE,
+                        sb + SSD_OFF_S + (nx % S_TILES) * 16384, 16384, pol_keep);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&bars[SB_XR + nx % S_TILES]);
+        mark_exports(mark, nx, N, mark_every);
+      }
+      bulk_wait<0>();
+      // All chunks, also after a wait gave up (recorded): the output items
+      // never wait for exports that will not come.
+      if (mark) {
+        fence_async_global();
+        st_release_gpu(mark, (unsigned int)N);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // seq = b * HV + hv, value columns [32 vt, 32 vt + 32). With maps (the
 // one-launch forward): chunk n's slab is produced in the same launch (wait for
 // its flag before loading it), the CTA first produces chunk vt of its
@@ -397,7 +605,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_SLOT);
 
-  if (tid == 0) {
+  if (tid == 0 && p.ssd) {
+    ssd_init_bars(bars);
+  } else if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_FULLA + i], 1);
       mbar_init(&bars[B_EMPTYA + i], kEmptyA);
@@ -408,7 +618,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       mbar_init(&bars[B_WS + i], 1);
       mbar_init(&bars[B_DS + i], 1);
       mbar_init(&bars[B_RP + i], 4);
-      mbar_init(&bars[B_PP + i], 4);
     }
     for (int i = 0; i < S_TILES; ++i) {
       mbar_init(&bars[B_ES + i], 8);
@@ -454,15 +663,13 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     nb_sync(1, CHAIN_THREADS);
   }
   uint8_t* xbase = p.xchg + (size_t)chunk0 * Xchg::BYTES;
-  // Mamba2 SSD: W = 0, so D_ws and D_t vanish and r_n = U_n does not depend on
-  // the state; the W ring, both products and their waits are skipped, and
-  // only the state update stays serial.
-  const bool no_w = p.ssd != 0;
   const uint32_t sb = smem_u32(sm);
   constexpr uint32_t ID_KMN = idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major
   constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, 1, 1);  // A = k^T read MN-major
 
-  if (warp < 8) {
+  if (p.ssd) {
+    ssd_chain(p, sm, seq, vt, wait_flags, maps != nullptr, xbase, ok);
+  } else if (warp < 8) {
     // ---------------------------------------------------------------- state
     // After publishing S_n the eight warps meet on named barrier 2, which
     // releases the D_ws issuer (warp 15).
@@ -537,20 +744,15 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     for (int n = 0; n < N; ++n) {
       const int sa = n & 1;
       const uint8_t* slot = sm + OFF_A + sa * A_SLOT;
-      if (!no_w) {
-        ok = warp_wait(&bars[B_WS + sa], (n >> 1) & 1, ok);
-        if (lane == 0) mbar_arrive(&bars[B_EMPTYW + sa]);   // D_ws(n) done: W_n read
-      }
+      ok = warp_wait(&bars[B_WS + sa], (n >> 1) & 1, ok);
+      if (lane == 0) mbar_arrive(&bars[B_EMPTYW + sa]);   // D_ws(n) done: W_n read
       ok = warp_wait(&bars[B_FULLA + sa], (n >> 1) & 1, ok);
       tc_fence_after();
       float r[16];
-      if (!no_w) {
+      {
         float d[64];
         tmem_ld64(tmem + lb + T_WS + 64 * sa, d);
         stacked_sum(d, half, r);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0.f;
       }
       const float* vec = reinterpret_cast<const float*>(sm + OFF_V + sa * VEC_BYTES);
       const float ks = vec[j];
@@ -565,7 +767,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         r[4 * q + 2] = fmaf(gam_prev, r[4 * q + 2], uf * u.z);
         r[4 * q + 3] = fmaf(gam_prev, r[4 * q + 3], uf * u.w);
       }
-      if (n > 0 && !no_w) {
+      if (n > 0) {
         ok = warp_wait(&bars[B_T], (n - 1) & 1, ok);
         tc_fence_after();
         float d[64], t[16];
@@ -574,8 +776,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] += t[i];
       }
-      // (no D_t to wait for: D_S(n - 1), the last reader of rho tile n % 2)
-      if (no_w && n >= 2) ok = warp_wait(&bars[B_DS + sa], ((n - 2) >> 1) & 1, ok);
       tc_fence_before();
       // rho into tile n % 2: rho_{n-2} there was read by D_S(n - 1) and
       // D_t(n - 1), issued by the same thread before D_t(n), whose completion
@@ -589,15 +789,8 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       if (lane == 0) mbar_arrive(&bars[B_EMPTYA + sa]);   // U, VEC read; D_t(n) (T_n) done
       tc_fence_before();
       // An arrive: r_{n+1} needs D_t(n + 1), issued only after this phase, so
-      // no r warp can reach the next phase early. Under SSD (no D_t) the r
-      // warps do not wait for the issuer at all: they arrive on mbarrier
-      // B_PP n % 2 instead (its next phase needs D_S(n + 1), which the issuer
-      // starts only after this one).
-      if (no_w) {
-        if (lane == 0) mbar_arrive(&bars[B_PP + (n & 1)]);
-      } else {
-        nb_arrive(3, 160);
-      }
+      // no r warp can reach the next phase early.
+      nb_arrive(3, 160);
       // r into its tile n % 2 once the export of r_{n-2} from it is read out.
       if (n >= 2) ok = warp_wait(&bars[B_XR + (n - 2) % S_TILES], tile_parity(n - 2, S_TILES), ok);
       publish16(sm + OFF_R + sa * 8192, j, 2 * half, r);
@@ -612,7 +805,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // and B likewise; one bulk copy per array.
     if (lane == 0) {
       const uint32_t sb = smem_u32(sm);
-      int nw = no_w ? N : 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
+      int nw = 0, na = 0, nb = 0, nflag = wait_flags ? 0 : N;   // nflag: flags seen
       // This CTA's U columns are read once; -W, -T and k by the four V-tile
       // CTAs of the sequence.
       const uint64_t pol_last_read = l2_evict_first();
@@ -623,30 +816,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         const int lead = nw > na ? (nw > nb ? nw : nb) : (na > nb ? na : nb);
         if (flags_ok && nflag < N && nflag < lead + 2) {
           polled = true;
-          // The next flags (chunk slabs are written by workers of this
-          // launch): kFlagWindow of them read at once, then one acquire for
-          // the run of those already set.
-          unsigned int f[kFlagWindow];
-#pragma unroll
-          for (int z = 0; z < kFlagWindow; ++z)
-            f[z] = nflag + z < N ? ld_relaxed_gpu(p.flags + chunk0 + nflag + z) : 0u;
-          int m = nflag;
-#pragma unroll
-          for (int z = 0; z < kFlagWindow; ++z)
-            if (m == nflag + z && f[z] != 0u) ++m;
-          if (m > nflag) {
-            fence_acq_rel_gpu();                         // acquire the slabs' writes
-            fence_async_global();                        // ... for the bulk reads
-            nflag = m;
-            flag_polls = 0;
-            progress = true;
-          } else if (++flag_polls > p.wait_limit) {
-            // Give up waiting: record it, then run to the end on whatever the
-            // workspace holds (in bounds), so that no other wait runs out too.
-            flags_ok = false;
-            nflag = N;
-            atomicOr(p.error_word, kErrFlagWait);
-          }
+          progress = poll_flags(p, chunk0, N, nflag, flag_polls, flags_ok);
         }
         if (nw < N && nw < nflag &&
             (nw < 2 || mbar_test(&bars[B_EMPTYW + (nw & 1)], ((nw >> 1) - 1) & 1))) {
@@ -696,18 +866,10 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // alone, for the final state). (D_t first measured slower: S_{n+1}, and
     // with it D_ws(n + 2), comes later.)
     for (int n = 0; n < N; ++n) {
-      if (!no_w) nb_sync(3, 160);
+      nb_sync(3, 160);
       if (lane == 0 && ok) {
         const int sa = n & 1;
-        if (no_w) {
-          ok = mbar_spin(&bars[B_PP + sa], (n >> 1) & 1, kWaitLimit);   // rho_n published
-          tc_fence_after();
-        }
-        // (SSD: rho_n does not wait for the state, so D_S buffer n % 2 is
-        // free only once the state warps have read D_S(n - 1) for S_{n-1})
-        if (no_w && n >= 2)
-          ok = mbar_spin(&bars[B_ES + (n - 1) % S_TILES], tile_parity(n - 1, S_TILES), kWaitLimit);
-        if (ok) ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
+        ok = mbar_spin(&bars[B_FULLB + sa], (n >> 1) & 1, kWaitLimit);   // k_n
         if (ok) {
           tc_fence_after();
           const uint32_t kb = sb + OFF_B + sa * KB_SLOT;
@@ -718,7 +880,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
                       sdesc_sw128_lbo(pt + kk * 2048, 8192), ID_MNMN, kk > 0);
           umma_commit(&bars[B_DS + sa]);
         }
-        if (ok && n + 1 < N && !no_w) {
+        if (ok && n + 1 < N) {
           const int m = n + 1;
           ok = mbar_spin(&bars[B_FULLA + (m & 1)], (m >> 1) & 1, kWaitLimit);   // T_{n+1}
           if (ok) {
@@ -752,7 +914,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     };
     for (int n = 0; n < N; ++n) {
       nb_sync(2, 288);
-      if (lane == 0 && ok && !no_w) {
+      if (lane == 0 && ok) {
         tc_fence_after();
         if (n == 0) issue_ws(0);
         if (ok && n + 1 < N) issue_ws(n + 1);
@@ -765,9 +927,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       // The output pass reads the exchange next: keep it in L2.
       const uint64_t pol_keep = l2_evict_last();
       unsigned int* mark = maps ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
-      // (long chains: about 16 marks in all, each holds the exporter up)
-      const int mark_every = N / 16 > kMarkEvery ? ((N / 16 + kMarkTail - 1) / kMarkTail) * kMarkTail
-                                                 : kMarkEvery;
+      const int mark_every = mark_period(N);
       for (int nx = 0; nx < N && ok; ++nx) {
         ok = mbar_wait(&bars[B_ES + nx % S_TILES], tile_parity(nx, S_TILES), kWaitLimit) &&
              mbar_wait(&bars[B_RP + (nx & 1)], (nx >> 1) & 1, kWaitLimit);
@@ -781,15 +941,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(&bars[B_XR + nx % S_TILES]);
-        // Chunks 0 .. done - 1 are in global memory once all but the newest
-        // kMarkLag groups are.
-        const int done = nx + 1 - kMarkLag;
-        if (mark && done > 0 && nx + 1 < N &&
-            (done % mark_every == 0 || (done >= N - kMarkTailSpan && done % kMarkTail == 0))) {
-          bulk_wait<kMarkLag>();
-          fence_async_global();
-          st_release_gpu(mark, (unsigned int)done);
-        }
+        mark_exports(mark, nx, N, mark_every);
       }
       bulk_wait<0>();
       // All chunks, also after a wait gave up (recorded): the output items

@@ -22,6 +22,12 @@
 // swizzled layout without a tensor map). Each per-thread phase is
 // spread over the 8 warps (two per TMEM lane quadrant, one per column half).
 //
+// For the Mamba2 SSD recurrence of the "Chunkwise 并行算法 —— 线性注意力" page
+// (§1.1-1.2: no delta erase, beta = 1) M = I, W = 0 and U = v, so the chunk
+// stops after A_qk and the row factors and forms, instead of W, U and T, its
+// whole state increment N = k^T diag(kscale) v (four tcgen05 products with the
+// raw keys as A), which turns the recurrence into a scan (ssd_increment).
+//
 // The work of one chunk is the device function produce_chunk. It runs in the
 // chunk kernel below (one CTA per chunk, two CTAs per SM) and, for the
 // one-launch forward, in the worker CTAs of gdr_chain.cu (two groups of 8

@@ -89,6 +89,116 @@ __device__ __forceinline__ void group_sync(int bar_id) {
   asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(THREADS) : "memory");
 }
 
+// Shared-memory offset of the B operand tile of value tile t in the SSD
+// increment product (the dead q tiles, then the dead L region).
+__device__ __forceinline__ int ssd_b_tile(int t) { return t < 2 ? OFF_Q0 + t * 16384 : OFF_L + (t - 2) * 8192; }
+static_assert(OFF_Q1 == OFF_Q0 + 16384 && OFF_L + 16384 <= OFF_AQS && OFF_L % 1024 == 0,
+              "SSD operand tiles");
+
+// Mamba2 SSD, the rest of a chunk after its A_qk and row factors. With W = 0
+// the system matrix is I, U = v, and the chunk's whole effect on the state is
+//   S_{n+1} = gamma S_n + N,   N = k^T diag(kscale) v   (K x V, fp32),
+// which does not depend on S: it is formed here, so that the recurrence is a
+// plain scan. Per value tile t (32 columns), on tcgen05:
+//   D_N[t] = k^T [(kscale v_t)_hi | (kscale v_t)_lo]   M = 128 (raw k, MN-major), N = 64, K = 64
+// into TMEM columns 64 t, and N[t] = the hi half + the lo half (v is exact in
+// bf16, kscale v is split). N leaves as four [128 c][32 v] fp32 boxes at
+// Slab::ssd_n(t); r = v goes to the chunk's exchange block as its four r
+// tiles [64 j][v 32 | 0 32] by plain stores (before the slab's flag, like the
+// row factors). The TMA barriers of the previous keys and of T complete this
+// chunk's phase without a transfer, so that every barrier keeps one (the
+// MMA barrier two) phases per chunk.
+__device__ __forceinline__ bool ssd_increment(const Params& p, uint8_t* sm, int tid, int bar_id,
+                                              int idx, uint32_t ph, uint32_t tmem, bool ok) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, colh = warp >> 2;
+  const float* G = reinterpret_cast<const float*>(sm + OFF_SMALL);
+  const float* nk = G + 2 * C;
+  const float* bb = G + 3 * C;
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bar_mma = bar_tma + 1;
+  uint64_t* bar_v = bar_tma + 3;
+  uint64_t* bar_kp = bar_tma + 4;
+  uint64_t* bar_t = bar_tma + 5;
+  uint8_t* slab = p.slabs + (size_t)idx * p.slab_bytes;
+  uint8_t* xr = p.xchg + (size_t)idx * Xchg::BYTES + Xchg::R;
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_v, ph, kWaitLimit));
+  if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
+  if (ok) {
+    // Item (j, cc): row j, 8-column chunk cc of v, i.e. chunk cc % 4 of value tile cc / 4.
+    const float gl = G[C - 1];
+    for (int it = tid; it < C * 16; it += THREADS) {
+      const int j = it >> 4, cc = it & 15, t = cc >> 2, qc = cc & 3;
+      const uint4 raw = *reinterpret_cast<const uint4*>(sm + (cc < 8 ? OFF_V0 : OFF_V1) + box_off(j, cc & 7));
+      const float ks = bb[j] * nk[j] * __expf(gl - G[j]);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int z = 0; z < 4; ++z)
+        split_pair(ks * __uint_as_float(w[z] << 16), ks * __uint_as_float(w[z] & 0xffff0000u), hi[z], lo[z]);
+      uint8_t* bt = sm + ssd_b_tile(t);
+      *reinterpret_cast<uint4*>(bt + box_off(j, qc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(bt + box_off(j, qc + 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      uint8_t* rt = xr + (size_t)t * Xchg::R_TILE;
+      *reinterpret_cast<uint4*>(rt + box_off(j, qc)) = raw;
+      *reinterpret_cast<uint4*>(rt + box_off(j, qc + 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  fence_async_shared();
+  tc_fence_before();
+  group_sync(bar_id);
+  if (tid == 0) {
+    if (ok) {
+      tc_fence_after();
+      constexpr uint32_t id = idesc_bf16(128, 64, 1, 1);
+      const uint32_t kb = smem_u32(sm + OFF_K0);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t bt = smem_u32(sm + ssd_b_tile(t));
+#pragma unroll
+        for (int s = 0; s < C / 16; ++s)
+          umma_bf16(tmem + 64 * t, sdesc_sw128_lbo(kb + s * 2048, 16384),
+                    sdesc_sw128_lbo(bt + s * 2048, 8192), id, s > 0);
+      }
+      umma_commit(bar_mma);
+    }
+    mbar_arrive(bar_kp);
+    mbar_arrive(bar_t);
+  }
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_mma, 1, kWaitLimit));
+  if (!ok && tid == 0) atomicOr(p.error_word, kErrMmaWait);
+  tc_fence_after();
+  // Warp w: key channels c = 32 (w % 4) + lane (its TMEM lanes), value tiles
+  // 2 (w / 4) and 2 (w / 4) + 1, staged as [128][32] fp32 boxes over the dead
+  // key, q, v and L tiles (the products that read them are complete).
+  if (ok) {
+    const int c = 32 * quad + lane;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+#pragma unroll 1
+    for (int u = 0; u < 2; ++u) {
+      const int t = 2 * colh + u;
+      float d[64];
+      tmem_ld64(tmem + lane_base + 64 * t, d);
+      uint8_t* nt = sm + t * 16384;
+#pragma unroll
+      for (int qc = 0; qc < 8; ++qc)
+        *reinterpret_cast<float4*>(nt + box_off(c, qc)) =
+            make_float4(d[4 * qc] + d[32 + 4 * qc], d[4 * qc + 1] + d[33 + 4 * qc],
+                        d[4 * qc + 2] + d[34 + 4 * qc], d[4 * qc + 3] + d[35 + 4 * qc]);
+    }
+  }
+  fence_async_shared();
+  tc_fence_before();
+  group_sync(bar_id);
+  if (tid == 0) {
+    bulk_store(slab + Slab::ssd_n(0), smem_u32(sm), 2 * (uint32_t)Slab::SSD_N_BOX);
+    bulk_store(slab + Slab::ssd_n(2), smem_u32(sm + 2 * Slab::SSD_N_BOX), 2 * (uint32_t)Slab::SSD_N_BOX);
+    bulk_commit();
+  }
+  return ok;
+}
+static_assert(4 * Slab::SSD_N_BOX <= (size_t)OFF_AQS, "SSD increment staging below the A_qk staging");
+
 // One chunk (n, hv, b) by the 256 threads tid = 0 .. 255 of a group that
 // meets on named barrier bar_id, in the group's shared-memory region sm, with
 // its mbarriers (at OFF_BAR, initialised by the caller) in phase ph for this
@@ -168,8 +278,9 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   if (!ok && lane == 0) atomicOr(p.error_word, kErrTmaWait);
   if (tid < C) bb[tid] = bv;   // read after the next group barrier
   // The key tile's image (the recurrence's A operand k^T) goes to the slab as
-  // it is; it must be read out before epilogue 2 overwrites the tile.
-  if (tid == 0) {
+  // it is; it must be read out before epilogue 2 overwrites the tile. (Mamba2
+  // SSD: the recurrence reads no keys.)
+  if (tid == 0 && !p.ssd) {
     bulk_store(slab + Slab::K2, smem_u32(sm + OFF_K0), 8192);
     bulk_store(slab + Slab::K2 + 8192, smem_u32(sm + OFF_K1), 8192);
     bulk_commit();
@@ -351,6 +462,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
     }
     if (e >= 0 && e < K) vec[2 * C + e] = __expf(gl);
   }
+  if (p.ssd) return ssd_increment(p, sm, tid, bar_id, idx, ph, tmem, ok);
 
   // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
   unit_lower_inverse64<LDL, LDX>(L, X, T, tid, bar_id);

@@ -52,6 +52,11 @@ __host__ __device__ constexpr int stacked_row(int i, int lo) { return 32 * (i >>
 // with qscale_i = scale |q_i|^-1 exp(G_i), kscale_j = beta_j |k_j|^-1
 // exp(G_last - G_j), gamma = exp(G_last) on every channel; the recurrence
 // applies them as fp32 row factors to the exact bf16 q and k.
+// Mamba2 SSD (W = 0, U = v): W2, U and T2 are not written; instead the chunk's
+// state increment N = k^T diag(kscale) v (K x V fp32) takes the W2, T2 and K2
+// bytes as four [128 c][32 v] fp32 boxes (128-byte swizzled rows), box t =
+// value columns 32 t .. 32 t + 31 at ssd_n(t), and r = v goes straight to the
+// chunk's exchange block.
 // Per-key gate (plain row-major arrays, read by TMA tensor loads):
 //   W2   [2][C][K] bf16  hi / lo of -W, W = M^-1 (exp(G) k_hat)
 //   AQ2  [2][C][C] bf16  hi / lo of A_qk
@@ -71,7 +76,14 @@ struct Slab {
   static constexpr size_t SCALAR_BYTES = K2 + (size_t)C * K * 2;
   static constexpr size_t PERKEY_BYTES = KB2 + 2ull * C * K * 2;
   static constexpr size_t bytes(int gate_mode) { return gate_mode ? PERKEY_BYTES : SCALAR_BYTES; }
+  static constexpr size_t SSD_N_BOX = (size_t)K * 32 * 4;
+  __host__ __device__ static constexpr size_t ssd_n(int t) {
+    return t < 2 ? W2 + (size_t)t * SSD_N_BOX : T2 + (size_t)(t - 2) * SSD_N_BOX;
+  }
 };
+static_assert(Slab::W2 + 2 * Slab::SSD_N_BOX <= Slab::AQ2 &&
+                  Slab::T2 + 2 * Slab::SSD_N_BOX == Slab::SCALAR_BYTES,
+              "SSD increment boxes in the W2, T2 and K2 bytes");
 static_assert(Slab::AQ2 % 16 == 0 && Slab::U % 16 == 0 && Slab::VEC % 16 == 0 &&
                   Slab::T2 % 16 == 0 && Slab::K2 % 16 == 0 && Slab::QB2 % 16 == 0 &&
                   Slab::KB2 % 16 == 0 && Slab::SCALAR_BYTES % 16 == 0,

@@ -284,8 +284,11 @@ gdr_status gdr_recurrent_fwd(const void* q, const void* k, const void* v, const 
  * i.e. the gated recurrence without the delta erase and without beta. It
  * runs on the same chunk machinery with the triangular solve dropped
  * (M = I, W = 0, U = v): for bf16 inputs with K = V = 128, C = 64 and the
- * scalar gate on the tensor-core path (chunk-local kernel, state chain and
- * output kernel), otherwise on the general fp32 path. Arguments as for
+ * scalar gate on the tensor-core path, where each chunk's state increment
+ * k^T diag(exp(G_last - G) |k|^-1) v is formed with the chunk-local work and
+ * the chain across chunks is a plain fp32 scan (the same launches as
+ * gdr_chunk_fwd: one cooperative launch when the chains fit beside the
+ * producers), otherwise on the general fp32 path. Arguments as for
  * gdr_chunk_fwd, minus beta; the workspace must hold
  * gdr_ssd_chunk_fwd_workspace_size() bytes.
  */

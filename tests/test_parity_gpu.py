@@ -400,15 +400,30 @@ def dataclasses_replace(w, **kw):
 
 # ---- Mamba2 SSD (no delta erase, no beta) on the chunk machinery ------------------
 
-@pytest.mark.parametrize("name,ov", [
+# The scalar-gate bf16 SSD runs the tensor-core path: the chunk-local stage forms
+# each chunk's state increment and the chain is a scan of them. Its shapes: one
+# token, fewer chunks than chain CTAs, batch with GQA and a ragged tail, a tail
+# past the first export mark, and the two multi-launch forms (96 chains: chunk
+# kernel, then chains beside the output items; 160 chains: chunk, chain and
+# output kernels).
+SSD_SHAPES = [
     ("gdn_t4096_h12", dict(T=300, H=2, HV=2)),                 # bf16, scalar gate, C = 64
     ("gdn_long_t65000", dict(T=200, H=2, HV=4)),               # carried state
     ("kda_gqa_t8192", dict(B=1, T=150, H=1, HV=2)),            # per-key gate
     ("tiny_fp32", {}),                                         # fp32, C = 16
     ("gdn_t4096_h12", dict(T=260, H=1, HV=2, K=64, V=64, C=128)),
-])
+    ("ssd_t4096_h12", dict(T=1, H=2, HV=2)),
+    ("ssd_t4096_h12", dict(T=130, H=3, HV=3, s0_std=0.02)),
+    ("ssd_t4096_h12", dict(B=2, T=700, H=2, HV=4, s0_std=0.02)),
+    ("ssd_t4096_h12", dict(T=1100, H=1, HV=2)),
+    ("ssd_t4096_h12", dict(T=200, H=24, HV=24)),
+    ("ssd_t4096_h12", dict(T=130, H=40, HV=40)),
+]
+
+
+@pytest.mark.parametrize("name,ov", SSD_SHAPES)
 def test_ssd_matches_oracle(name, ov):
-    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    w = gin.shrink({**gin.WORKLOADS, **gin.SSD_WORKLOADS}[name], **ov)
     x = gin.make_inputs(w)
     dev = torch.device("cuda:0")
     d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
@@ -419,6 +434,27 @@ def test_ssd_matches_oracle(name, ov):
                                   use_qk_l2norm=w.use_qk_l2norm)
     tol = tol_for(w)
     eo, es = relerr(o.cpu().numpy(), ro), relerr(S.cpu().numpy(), rS)
+    assert eo <= tol and es <= tol, (eo, es)
+
+
+def test_ssd_full_size():
+    """The SSD workload at its full size (12 sequences of 4096 tokens), every
+    sequence against the oracle, in the one-launch form the bench times."""
+    w = gin.SSD_WORKLOADS["ssd_t4096_h12"]
+    dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_F32)
+    assert gdr.chunk_fwd_path(dims, w.C, 0) == 2
+    x = gin.make_inputs(w)
+    dev = torch.device("cuda:0")
+    d = {n: (t.to(dev) if t is not None else None) for n, t in x.items()}
+    o, S = gdr.ssd_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["s0"], chunk_size=w.C,
+                             scale=w.scale, use_qk_l2norm=w.use_qk_l2norm, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rS = oracle.ssd_recurrent(x["q"], x["k"], x["v"], x["g"], x["s0"], scale=w.scale,
+                                  use_qk_l2norm=w.use_qk_l2norm)
+    o, S = o.cpu().numpy(), S.cpu().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    tol = tol_for(w)
+    eo, es = relerr(o, ro), relerr(S, rS)
     assert eo <= tol and es <= tol, (eo, es)
 
 
