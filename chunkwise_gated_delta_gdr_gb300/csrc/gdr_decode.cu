@@ -12,13 +12,15 @@
 // and o, and a call's total is one read and one write of every state.
 //
 // Main kernel (V <= 128 and a multiple of 4, state 16-byte aligned): one
-// persistent CTA per SM walks the heads. A producer warp streams each head's
-// whole state (K x V fp32, one TMA box of up to 512-byte rows) through a
-// three-stage shared-memory ring, so about 190 KB per SM are in flight; 16
-// compute warps each take 8 rows x 4 columns into registers, release the stage
-// at once (the producer refills it while they apply the tokens) and write the
-// finished state back with coalesced 128-byte stores from registers. (Boxes of
-// 128-byte rows were served several times slower.)
+// persistent CTA per SM walks the heads. Each head's whole state (K x V fp32,
+// one TMA box of up to 512-byte rows) streams through a three-stage
+// shared-memory ring, so about 190 KB per SM are in flight. Two groups of 8
+// warps take alternate heads; a warp takes 16 rows x 4 consecutive columns per
+// lane into registers, the group releases the stage at once (its first warp
+// refills it with the head three places on while they apply the tokens) and
+// writes the finished state back from registers, one 512-byte row per warp
+// store. A group's barriers and column sums overlap the other group's work.
+// (Boxes of 128-byte rows were served several times slower.)
 //
 // Fallback kernel (any V, K <= 256): one CTA per (V tile of 32 columns, hv, b),
 // 16 warps: warp w holds state rows [R w, R w + R) of the tile's columns
@@ -166,14 +168,23 @@ __global__ void __launch_bounds__(kThreads, 128 / (8 * kRows)) recurrent_kernel(
 
 // ------------------------------------------------------------ pipelined kernel
 // Whole-head tiles: the K x V state of one (b, hv) is one TMA box of V-element
-// (up to 512-byte) rows, streamed through a three-stage ring.
+// (up to 512-byte) rows, streamed through a three-stage ring. The 16 warps
+// form two groups of 8 that take alternate heads of the CTA's list, each with
+// its own named barriers and token staging, so one group's barriers and
+// column sums overlap the other group's loads, arithmetic and stores. There is
+// no producer warp (a 17th warp would cap every thread at 96 registers): once a
+// group holds head i in registers, its first warp refills that stage with head
+// i + STAGES.
 namespace pipe {
-constexpr int CW = 16, ROWS = 8, CPL = 4;          // compute warps, rows per warp, columns per lane
-constexpr int STAGES = 3, TILE = 128 * 128 * 4;    // 64 KB stage
-constexpr int THREADS = (CW + 1) * 32;
+constexpr int GROUPS = 2, GW = 8, CW = GROUPS * GW;   // warp groups, warps per group, compute warps
+constexpr int ROWS = 16, CPL = 4;                    // rows per warp, consecutive columns per lane
+constexpr int GT = GW * 32;                          // threads per group
+constexpr int STAGES = 3, TILE = 128 * 128 * 4;      // 64 KB stage
+constexpr int THREADS = CW * 32;
 constexpr int OFF_BAR = STAGES * TILE, SMEM = OFF_BAR + 2 * STAGES * 8 + 1024;
 constexpr long kWaitLimit = 1L << 24;
-static_assert(CW * ROWS == 128 && CPL * 32 == 128, "tile covers K, V <= 128");
+static_assert(GW * ROWS == 128 && CPL * 32 == 128, "a group's tile covers K, V <= 128");
+static_assert(GT >= 128, "one group thread per channel and per column");
 __device__ __forceinline__ void nb_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -186,111 +197,126 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(16) float kr[128], qr[128], dec[128];   // zero past K
-  __shared__ float2 red[CW][128];                              // (k^T D S, q^T D S) partials
-  __shared__ float wcol[128];                                  // delta-rule write per column
-  __shared__ float tok[4];
+  // Per warp group: the staged tokens (two buffers, alternating per token;
+  // zero past K) and their beta, the warps' (k^T D S, q^T D S) partials per
+  // column, the delta-rule write per column.
+  __shared__ __align__(16) float kr[GROUPS][2][128], qr[GROUPS][2][128], dec[GROUPS][2][128];
+  __shared__ __align__(16) float2 red[GROUPS][GW][128];
+  __shared__ __align__(16) float wcol[GROUPS][128];
+  __shared__ float tok[GROUPS][2];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* done = full + STAGES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = a.K, V = a.V;
+  // Plane i of this CTA: blockIdx.x + i * gridDim.x (= b * HV + hv).
+  const int my = nplanes > (int)blockIdx.x ? (nplanes - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint32_t tbytes = (uint32_t)K * V * 4;
   if (tid == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&done[i], CW);
+      mbar_init(&done[i], GW);
     }
     mbar_fence_init();
+    // The first STAGES planes; stage s takes plane i + STAGES once the group
+    // holding plane i has it in registers (below).
+    for (int i = 0; i < STAGES && i < my; ++i) {
+      mbar_expect_tx(&full[i], tbytes);
+      tma_load3(smem_u32(sm + i * TILE), &smap, 0, 0, blockIdx.x + i * gridDim.x, &full[i]);
+    }
   }
   __syncthreads();
   bool ok = true;
-  // Plane i of this CTA: blockIdx.x + i * gridDim.x (= b * HV + hv).
-  const int my = nplanes > (int)blockIdx.x ? (nplanes - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-  if (warp == CW) {
-    // ---------------------------------------------------------------- producer
-    // Stage s takes plane i once the compute warps hold plane i - STAGES in
-    // registers (completion i / STAGES - 1 of done[s]).
-    if (lane == 0) {
-      const uint32_t tbytes = (uint32_t)K * V * 4;
-      for (int i = 0; i < my && ok; ++i) {
-        const int s = i % STAGES;
-        if (i >= STAGES) ok = mbar_wait(&done[s], ((i / STAGES) - 1) & 1, kWaitLimit);
-        if (!ok) break;
-        mbar_expect_tx(&full[s], tbytes);
-        tma_load3(smem_u32(sm + s * TILE), &smap, 0, 0, blockIdx.x + i * gridDim.x, &full[s]);
-      }
-    }
-  } else {
+  {
     // ------------------------------------------------------------ compute warps
-    // Warp w holds rows [8 w, 8 w + 8) of columns lane + 32 m (m < 4).
-    // Per token two CTA barriers: C (column partials written) and D (the
-    // delta-rule write per column written, and the next token's inputs staged).
-    // Every warp forms the token's norms itself from the staged k and q.
-    // Threads 0-127 load a token's inputs (channel / column tid) into registers
-    // one token ahead (across heads too) and stage them between C and D: every
-    // read of the staged inputs of a token happens before its barrier C.
-    const int r0 = warp * ROWS;
+    // Group g (warps 8 g .. 8 g + 7) takes planes g, g + 2, ... of the CTA.
+    // Warp gw holds rows [16 gw, 16 gw + 16) of columns [4 lane, 4 lane + 4).
+    // Per token two barriers of the group: C (column partials written) and D
+    // (the delta-rule write per column written, and the next token's inputs
+    // staged). Every warp forms the token's norms itself from the staged k and
+    // q. Group threads 0-127 load a token's inputs (channel / column gt) into
+    // registers one token ahead (across planes too) and stage them between C
+    // and D into the other buffer, whose previous token every warp of the
+    // group finished before C.
+    const int g = warp / GW, gw = warp % GW, gt = tid - g * GT, bar = 1 + g;
+    float* wg = wcol[g];
+    int tb = 0;                                         // buffer of the current token
+    const int r0 = gw * ROWS, c0 = CPL * lane;
     struct Tok {
       float k, q, g, v, beta;
     };
     auto load_tok = [&](int plane, int tk, Tok& x) {
       x.k = x.q = x.g = x.v = x.beta = 0.f;
-      if (tid >= 128) return;
+      if (gt >= 128) return;
       const int b = plane / a.HV, hv = plane % a.HV, h = hv / (a.HV / a.H);
       const size_t bt = (size_t)b * a.T + tk;
-      if (tid < K) {
-        const size_t qk = (bt * a.H + h) * K + tid;
+      if (gt < K) {
+        const size_t qk = (bt * a.H + h) * K + gt;
         x.k = ld_x(a.k, qk, a.in_bf16);
         x.q = ld_x(a.q, qk, a.in_bf16);
-        if (a.g) x.g = a.per_key ? a.g[(bt * a.HV + hv) * K + tid] : a.g[bt * a.HV + hv];
+        if (a.g) x.g = a.per_key ? a.g[(bt * a.HV + hv) * K + gt] : a.g[bt * a.HV + hv];
       }
-      if (tid < V) x.v = ld_x(a.v, (bt * a.HV + hv) * V + tid, a.in_bf16);
-      if (tid == 0) x.beta = a.beta[bt * a.HV + hv];
+      if (gt < V) x.v = ld_x(a.v, (bt * a.HV + hv) * V + gt, a.in_bf16);
+      if (gt == 0) x.beta = a.beta[bt * a.HV + hv];
     };
-    auto stage_tok = [&](const Tok& x) {
-      if (tid < 128) {
-        kr[tid] = x.k;
-        qr[tid] = x.q;
-        dec[tid] = tid < K ? expf(x.g) : 0.f;
-        if (tid == 0) tok[0] = x.beta;
+    auto stage_tok = [&](const Tok& x, int buf) {
+      if (gt < 128) {
+        kr[g][buf][gt] = x.k;
+        qr[g][buf][gt] = x.q;
+        dec[g][buf][gt] = gt < K ? expf(x.g) : 0.f;
+        if (gt == 0) tok[g][buf] = x.beta;
       }
     };
     Tok nx;
-    if (my > 0) {
-      load_tok(blockIdx.x, 0, nx);
-      stage_tok(nx);
+    if (g < my) {
+      load_tok(blockIdx.x + g * gridDim.x, 0, nx);
+      stage_tok(nx, 0);
     }
-    nb_sync(1, CW * 32);                               // the first token is staged
-    for (int i = 0; i < my; ++i) {
+    nb_sync(bar, GT);                                   // the first token is staged
+    for (int i = g; i < my; i += GROUPS) {
       const int s = i % STAGES;
       const int plane = blockIdx.x + i * gridDim.x;
       const int b = plane / a.HV, hv = plane % a.HV;
       const float* tile = reinterpret_cast<const float*>(sm + s * TILE);   // [K][V] fp32
       ok = ok && mbar_wait(&full[s], (i / STAGES) & 1, kWaitLimit);
+      const bool cok = c0 < V;                          // V % 4 == 0: all four columns or none
       float S[ROWS][CPL];
 #pragma unroll
-      for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-        for (int m = 0; m < CPL; ++m) {
-          const int c = lane + 32 * m;
-          S[r][m] = (r0 + r < K && c < V) ? tile[(r0 + r) * V + c] : 0.f;
-        }
-      // The head is in registers: stage s may be refilled.
+      for (int r = 0; r < ROWS; ++r) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + r < K && cok) x = *reinterpret_cast<const float4*>(tile + (r0 + r) * V + c0);
+        S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
+      }
+      // The head is in registers: stage s may be refilled, with plane
+      // i + STAGES, once all 8 warps of the group are done with it.
       __syncwarp();
-      if (lane == 0) mbar_arrive(&done[s]);
+      if (lane == 0) {
+        mbar_arrive(&done[s]);
+        if (gw == 0 && i + STAGES < my) {
+          ok = ok && mbar_wait(&done[s], (i / STAGES) & 1, kWaitLimit);
+          if (ok) {
+            mbar_expect_tx(&full[s], tbytes);
+            tma_load3(smem_u32(sm + s * TILE), &smap, 0, 0, blockIdx.x + (i + STAGES) * gridDim.x,
+                      &full[s]);
+          }
+        }
+      }
+      __syncwarp();
       for (int tk = 0; tk < a.T; ++tk) {
         const size_t bt = (size_t)b * a.T + tk;
-        const Tok x = nx;                              // this token (staged)
-        const bool more = tk + 1 < a.T || i + 1 < my;
+        const float xv = nx.v;                          // this token's v (the rest is staged)
+        const float* kg = kr[g][tb];
+        const float* qg = qr[g][tb];
+        const float* dg = dec[g][tb];
+        const bool more = tk + 1 < a.T || i + GROUPS < my;
         if (tk + 1 < a.T)
           load_tok(plane, tk + 1, nx);
-        else if (i + 1 < my)
-          load_tok(plane + gridDim.x, 0, nx);
+        else if (i + GROUPS < my)
+          load_tok(plane + GROUPS * gridDim.x, 0, nx);
         // Norms of the staged k and q (zero past K), every warp for itself.
         float sk = 0.f, sq = 0.f, sqk = 0.f;
 #pragma unroll
         for (int c = lane; c < 128; c += 32) {
-          const float kc = kr[c], qc = qr[c];
+          const float kc = kg[c], qc = qg[c];
           sk = fmaf(kc, kc, sk);
           sq = fmaf(qc, qc, sq);
           sqk = fmaf(qc, kc, sqk);
@@ -303,67 +329,76 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
         }
         const float nk = a.use_l2 ? 1.f / sqrtf(sk + 1e-6f) : 1.f;
         const float nq = a.scale * (a.use_l2 ? 1.f / sqrtf(sq + 1e-6f) : 1.f);
-        const float qk = nq * nk * sqk, beta = tok[0];
-        // Decay, then this warp's share of k^T (D S) and q^T (D S) per column.
-        const float4 kk0 = *reinterpret_cast<const float4*>(kr + r0);
-        const float4 kk1 = *reinterpret_cast<const float4*>(kr + r0 + 4);
-        const float4 qq0 = *reinterpret_cast<const float4*>(qr + r0);
-        const float4 qq1 = *reinterpret_cast<const float4*>(qr + r0 + 4);
-        const float4 dd0 = *reinterpret_cast<const float4*>(dec + r0);
-        const float4 dd1 = *reinterpret_cast<const float4*>(dec + r0 + 4);
-        const float kv[ROWS] = {kk0.x, kk0.y, kk0.z, kk0.w, kk1.x, kk1.y, kk1.z, kk1.w};
-        const float qv[ROWS] = {qq0.x, qq0.y, qq0.z, qq0.w, qq1.x, qq1.y, qq1.z, qq1.w};
-        const float dv[ROWS] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
+        const float qk = nq * nk * sqk, beta = tok[g][tb];
+        // Decay, then this warp's share of k^T (D S) and q^T (D S) per column
+        // (the row factors are shared-memory broadcasts).
+        float pu[CPL] = {0.f, 0.f, 0.f, 0.f}, po[CPL] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < CPL; ++m) {
-          float pu = 0.f, po = 0.f;
+        for (int r = 0; r < ROWS; r += 4) {
+          // (four rows' factors at a time: the compiler would otherwise hold
+          // all 48 at once beside the 64 state values)
+          asm volatile("" ::: "memory");
+          const float4 d4 = *reinterpret_cast<const float4*>(dg + r0 + r);
+          const float4 k4 = *reinterpret_cast<const float4*>(kg + r0 + r);
+          const float4 q4 = *reinterpret_cast<const float4*>(qg + r0 + r);
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w},
+                      qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-          for (int r = 0; r < ROWS; ++r) {
-            S[r][m] *= dv[r];
-            pu = fmaf(kv[r], S[r][m], pu);
-            po = fmaf(qv[r], S[r][m], po);
-          }
-          red[warp][lane + 32 * m] = make_float2(pu, po);
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+              S[r + e][m] *= dd[e];
+              pu[m] = fmaf(kk[e], S[r + e][m], pu[m]);
+              po[m] = fmaf(qq[e], S[r + e][m], po[m]);
+            }
         }
-        nb_sync(1, CW * 32);                           // C: partials written
-        if (tid < 128) {
-          // Column tid: sum the warps' partials, form the write and the output.
+        float4* rp = reinterpret_cast<float4*>(&red[g][gw][c0]);
+        rp[0] = make_float4(pu[0], po[0], pu[1], po[1]);
+        rp[1] = make_float4(pu[2], po[2], pu[3], po[3]);
+        nb_sync(bar, GT);                               // C: partials written
+        if (gt < 128) {
+          // Column gt: sum the group's partials, form the write and the output.
           float u = 0.f, oq = 0.f;
 #pragma unroll
-          for (int w = 0; w < CW; ++w) {
-            const float2 pr = red[w][tid];
+          for (int w = 0; w < GW; ++w) {
+            const float2 pr = red[g][w][gt];
             u += pr.x;
             oq += pr.y;
           }
-          const float wv = beta * (x.v - nk * u);
-          wcol[tid] = nk * wv;                              // times k^ = nk k
-          if (tid < V) {
-            const float o = fmaf(qk, wv, nq * oq);         // S'^T q~ = (D S)^T q~ + (q~ . k^) w
-            const size_t off = (bt * a.HV + hv) * V + tid;
+          const float wv = beta * (xv - nk * u);
+          wg[gt] = nk * wv;                             // times k^ = nk k
+          if (gt < V) {
+            const float o = fmaf(qk, wv, nq * oq);      // S'^T q~ = (D S)^T q~ + (q~ . k^) w
+            const size_t off = (bt * a.HV + hv) * V + gt;
             if (a.out_bf16)
               static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(o);
             else
               static_cast<float*>(a.out)[off] = o;
           }
-          if (more) stage_tok(nx);                     // the next token's inputs
+          if (more) stage_tok(nx, tb ^ 1);              // the next token's inputs
         }
-        nb_sync(1, CW * 32);                           // D: writes and next inputs visible
+        nb_sync(bar, GT);                               // D: writes and next inputs visible
+        const float4 wk4 = *reinterpret_cast<const float4*>(wg + c0);
+        const float wk[CPL] = {wk4.x, wk4.y, wk4.z, wk4.w};
 #pragma unroll
-        for (int m = 0; m < CPL; ++m) {
-          const float wk = wcol[lane + 32 * m];
+        for (int r = 0; r < ROWS; r += 4) {
+          asm volatile("" ::: "memory");
+          const float4 k4 = *reinterpret_cast<const float4*>(kg + r0 + r);
+          const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-          for (int r = 0; r < ROWS; ++r) S[r][m] = fmaf(kv[r], wk, S[r][m]);
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) S[r + e][m] = fmaf(kk[e], wk[m], S[r + e][m]);
         }
+        tb ^= 1;
       }
-      // Row r0 + r of the head: each warp store is one 128-byte segment.
+      // Row r0 + r of the head: each warp store is one contiguous 512-byte row.
       float* dst = a.state + (size_t)plane * K * V;
 #pragma unroll
       for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-        for (int m = 0; m < CPL; ++m) {
-          const int c = lane + 32 * m;
-          if (r0 + r < K && c < V) dst[(size_t)(r0 + r) * V + c] = S[r][m];
-        }
+        if (r0 + r < K && cok)
+          *reinterpret_cast<float4*>(dst + (size_t)(r0 + r) * V + c0) =
+              make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
     }
   }
   if (!ok && a.error_word) atomicOr(a.error_word, 16u);
