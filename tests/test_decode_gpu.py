@@ -126,3 +126,15 @@ def test_steps_compose():
                                       S2, scale=w.scale, out_dtype=torch.float32))
     torch.cuda.synchronize()
     assert torch.equal(o1, torch.cat(outs, dim=1)) and torch.equal(S1, S2)
+
+
+# Many heads: several per CTA (1024 heads on 152 CTAs), both warp groups of the
+# streaming kernel busy, its three-stage ring wrapping, also with several
+# tokens per head; and fewer heads than CTAs (the second group idle).
+@pytest.mark.parametrize("B,T,H,HV", [(64, 1, 16, 16), (40, 3, 8, 16), (7, 2, 3, 3)])
+def test_many_heads_per_cta(B, T, H, HV):
+    w = gin.shrink(gin.DECODE_WORKLOADS["decode_b64_h16"], B=B, T=T, H=H, HV=HV)
+    x = gin.make_inputs(w)
+    o, S = run_gpu(w, x)
+    ro, rS = oracle_run(w, x)
+    assert relerr(o, ro) <= 2e-3 and relerr(S, rS) <= 2e-3, (relerr(o, ro), relerr(S, rS))
