@@ -46,8 +46,9 @@
 //              published S_n. Each is released by a named barrier (the r
 //              warps arrive on theirs without waiting, the state warps sync).
 //   warp 13    TMEM owner and exporter: once S_n and r_n are published it copies both tiles
-//              to the exchange block (bulk copies, one group per chunk) and
-//              announces them read out (the tiles are double buffered). In
+//              to the exchange block (bulk copies, one group per chunk, one
+//              group in flight) and announces the previous chunk's tiles read
+//              out (three S tiles, two r tiles). In
 //              the one-launch forward it also marks the chunks exported so
 //              far, every kMarkEvery chunks and a little behind the copies.
 // The S_n and r_n tiles of every chunk leave by bulk copies (a plain store of a
@@ -573,8 +574,13 @@ __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq,
         bulk_store_hint(xbase + (size_t)nx * Xchg::BYTES + Xchg::S + vt * Xchg::S_TILE,
                         sb + SSD_OFF_S + (nx % S_TILES) * 16384, 16384, pol_keep);
         bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(&bars[SB_XR + nx % S_TILES]);
+        // One export in flight: the previous chunk's tile is read out once all
+        // but the newest group are (the state warps rewrite a tile three
+        // chunks on; two in flight measured the same).
+        if (nx > 0) {
+          bulk_wait_read<1>();
+          mbar_arrive(&bars[SB_XR + (nx - 1) % S_TILES]);
+        }
         mark_exports(mark, nx, N, mark_every);
       }
       bulk_wait<0>();
@@ -939,8 +945,13 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
                         pol_keep);
         bulk_store_hint(xb + Xchg::R + vt * Xchg::R_TILE, sb + OFF_R + (nx & 1) * 8192, 8192, pol_keep);
         bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(&bars[B_XR + nx % S_TILES]);
+        // One export in flight: the previous chunk's tiles are read out once
+        // all but the newest group are (an S tile is rewritten three chunks
+        // on, an r tile two).
+        if (nx > 0) {
+          bulk_wait_read<1>();
+          mbar_arrive(&bars[B_XR + (nx - 1) % S_TILES]);
+        }
         mark_exports(mark, nx, N, mark_every);
       }
       bulk_wait<0>();
