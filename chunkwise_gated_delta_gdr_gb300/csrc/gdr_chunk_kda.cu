@@ -58,6 +58,21 @@ static_assert(SMEM_BYTES <= 113 * 1024, "two CTAs per SM");
 __device__ __forceinline__ uint32_t box_off(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
+// The slab arrays are stored as the byte images of the 128-byte swizzled
+// boxes the recurrence loads them into (one bulk copy per array, no tensor
+// map): byte offset of element (plane, row i, column col) of a [2][C][K] bf16
+// array (boxes of 64 columns, plane-major: hi c0-63, hi c64-127, lo c0-63,
+// lo c64-127), of a [2][C][C] bf16 array (one box per plane), and of the
+// [C][V] fp32 array U (boxes of 32 columns).
+__device__ __forceinline__ uint32_t img_k(int plane, int i, int col) {
+  return (uint32_t)((2 * plane + (col >> 6)) * 8192) + box_off(i, (col & 63) >> 3) + (col & 7) * 2;
+}
+__device__ __forceinline__ uint32_t img_c(int plane, int i, int col) {
+  return (uint32_t)(plane * 8192) + box_off(i, col >> 3) + (col & 7) * 2;
+}
+__device__ __forceinline__ uint32_t img_u(int i, int col) {
+  return (uint32_t)((col >> 5) * 8192) + box_off(i, (col & 31) >> 2) + (col & 3) * 4;
+}
 
 __device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
@@ -247,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
       }
     }
     // A_qk (beta on the columns, zero above the diagonal) -> slab; A_kk beta -> L.
-    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
+    uint8_t* aq = slab + Slab::AQ2;
 #pragma unroll
     for (int u = 0; u < 3; ++u) {
       if (u < ntn) {
@@ -259,8 +274,8 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
           uint32_t hi, lo;
           split_pair((j <= i) ? accq[u][2 * hr] * b0 : 0.f, (j + 1 <= i) ? accq[u][2 * hr + 1] * b1 : 0.f,
                      hi, lo);
-          *reinterpret_cast<uint32_t*>(aq + i * C + j) = hi;
-          *reinterpret_cast<uint32_t*>(aq + C * C + i * C + j) = lo;
+          *reinterpret_cast<uint32_t*>(aq + img_c(0, i, j)) = hi;
+          *reinterpret_cast<uint32_t*>(aq + img_c(1, i, j)) = lo;
           *reinterpret_cast<float2*>(L + i * LDL + j) =
               make_float2((j < i) ? acck[u][2 * hr] * b0 : 0.f, (j + 1 < i) ? acck[u][2 * hr + 1] * b1 : 0.f);
         }
@@ -276,8 +291,8 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
     inverse_level0<LDL>(L, xd, tid);
   } else {
     const float* Gl = G + (C - 1) * LDG;
-    __nv_bfloat16* qb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::QB2);
-    __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(slab + Slab::KB2);
+    uint8_t* qb = slab + Slab::QB2;
+    uint8_t* kb = slab + Slab::KB2;
     constexpr int EW = THREADS - 64;
     for (int idx = tid - 64; idx < C * 16; idx += EW) {
       const int i = idx >> 4, c = (idx & 15) * 8;
@@ -299,11 +314,11 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
       }
       uint4 hi, lo;
       split8(xq, hi, lo);
-      *reinterpret_cast<uint4*>(qb + i * K + c) = hi;
-      *reinterpret_cast<uint4*>(qb + C * K + i * K + c) = lo;
+      *reinterpret_cast<uint4*>(qb + img_k(0, i, c)) = hi;
+      *reinterpret_cast<uint4*>(qb + img_k(1, i, c)) = lo;
       split8(xk, hi, lo);
-      *reinterpret_cast<uint4*>(kb + i * K + c) = hi;
-      *reinterpret_cast<uint4*>(kb + C * K + i * K + c) = lo;
+      *reinterpret_cast<uint4*>(kb + img_k(0, i, c)) = hi;
+      *reinterpret_cast<uint4*>(kb + img_k(1, i, c)) = lo;
       split8(xe, hi, lo);
       *reinterpret_cast<uint4*>(ks + i * LDB + c) = hi;   // same thread read these bytes above
       *reinterpret_cast<uint4*>(qs + i * LDB + c) = lo;
@@ -314,12 +329,12 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
       else vec[e - K] = 1.f;   // qscale = kscale = 1
     }
     // A_qk blocks above the diagonal: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3).
-    __nv_bfloat16* aq = reinterpret_cast<__nv_bfloat16*>(slab + Slab::AQ2);
+    uint8_t* aq = slab + Slab::AQ2;
     for (int idx = tid - 64; idx < 6 * 16 * 4; idx += EW) {
       const int plane = idx & 1, half = (idx >> 1) & 1, rr = (idx >> 2) & 15, blk = idx >> 6;
       const int Ib = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int Jb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      *reinterpret_cast<uint4*>(aq + plane * C * C + (16 * Ib + rr) * C + 16 * Jb + 8 * half) =
+      *reinterpret_cast<uint4*>(aq + img_c(plane, 16 * Ib + rr, 16 * Jb + 8 * half)) =
           make_uint4(0u, 0u, 0u, 0u);
     }
   }
@@ -383,8 +398,8 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
         }
       }
     }
-    __nv_bfloat16* w2 = reinterpret_cast<__nv_bfloat16*>(slab + Slab::W2);
-    float* uo = reinterpret_cast<float*>(slab + Slab::U);
+    uint8_t* w2 = slab + Slab::W2;
+    uint8_t* uo = slab + Slab::U;
 #pragma unroll
     for (int Ib = 0; Ib < 4; ++Ib) {
 #pragma unroll
@@ -395,9 +410,9 @@ __global__ void __launch_bounds__(THREADS, 2) chunk_kda_kernel(Params p) {
           const int i = 16 * Ib + r8 + 8 * hr;
           uint32_t hi, lo;
           split_pair(-aw[Ib][u][2 * hr], -aw[Ib][u][2 * hr + 1], hi, lo);
-          *reinterpret_cast<uint32_t*>(w2 + i * K + col) = hi;
-          *reinterpret_cast<uint32_t*>(w2 + C * K + i * K + col) = lo;
-          *reinterpret_cast<float2*>(uo + i * V + col) = make_float2(au[Ib][u][2 * hr], au[Ib][u][2 * hr + 1]);
+          *reinterpret_cast<uint32_t*>(w2 + img_k(0, i, col)) = hi;
+          *reinterpret_cast<uint32_t*>(w2 + img_k(1, i, col)) = lo;
+          *reinterpret_cast<float2*>(uo + img_u(i, col)) = make_float2(au[Ib][u][2 * hr], au[Ib][u][2 * hr + 1]);
         }
       }
     }

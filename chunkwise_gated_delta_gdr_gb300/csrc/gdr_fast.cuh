@@ -57,7 +57,10 @@ __host__ __device__ constexpr int stacked_row(int i, int lo) { return 32 * (i >>
 // bytes as four [128 c][32 v] fp32 boxes (128-byte swizzled rows), box t =
 // value columns 32 t .. 32 t + 31 at ssd_n(t), and r = v goes straight to the
 // chunk's exchange block.
-// Per-key gate (plain row-major arrays, read by TMA tensor loads):
+// Per-key gate (the byte images of the 128-byte swizzled boxes the recurrence
+// loads with one bulk copy per array: [2][C][K] bf16 arrays as four [C][64]
+// boxes, plane-major (hi columns 0-63, hi 64-127, lo 0-63, lo 64-127); [2][C][C]
+// as two; U as four [C][32] fp32 boxes):
 //   W2   [2][C][K] bf16  hi / lo of -W, W = M^-1 (exp(G) k_hat)
 //   AQ2  [2][C][C] bf16  hi / lo of A_qk
 //   U    [C][V]    fp32

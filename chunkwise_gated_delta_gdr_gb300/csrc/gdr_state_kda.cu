@@ -39,7 +39,6 @@
 
 #include "gdr_fast.cuh"
 #include "gdr_ptx.cuh"
-#include "gdr_tmap.cuh"
 
 namespace gdr {
 namespace fast {
@@ -72,10 +71,6 @@ constexpr uint32_t kUBytes = 16384 + 512;
 // (even and odd K steps, two independent MMA chains), dS, o.
 constexpr uint32_t T_R = 0, T_R2 = 128, T_DS = 256, T_O = 384, TMEM_COLS = 512;
 
-struct Maps {
-  CUtensorMap w2, qb2, kb2, aq2, u;
-};
-
 __device__ __forceinline__ void nb_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -99,8 +94,7 @@ __device__ __forceinline__ void publish(uint8_t* hi, uint8_t* lo, int r, int q0,
     *reinterpret_cast<uint4*>(lo + sw_off(r, q)) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
-__global__ void __launch_bounds__(THREADS, 1)
-    state_kda_tc_kernel(const __grid_constant__ Maps maps, Params p) {
+__global__ void __launch_bounds__(THREADS, 1) state_kda_tc_kernel(Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -268,44 +262,31 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint32_t sb = smem_u32(sm);
       auto slab = [&](int n) { return p.slabs + (size_t)(chunk0 + n) * p.slab_bytes; };
+      // One bulk copy per array: the chunk-local stage stores each as the
+      // byte image of the 128-byte swizzled boxes it takes here.
       auto issue_w = [&](int n) {
-        const int s = n & 1, idx = chunk0 + n;
-        const uint32_t wb = sb + W_BASE + s * 32768;
+        const int s = n & 1;
         mbar_expect_tx(&w_full[s], 32768);
-        tma_load3(wb, &maps.w2, 0, 0, idx, &w_full[s]);
-        tma_load3(wb + 8192, &maps.w2, 64, 0, idx, &w_full[s]);
-        tma_load3(wb + 16384, &maps.w2, 0, 64, idx, &w_full[s]);
-        tma_load3(wb + 24576, &maps.w2, 64, 64, idx, &w_full[s]);
+        bulk_load(sb + W_BASE + s * 32768, slab(n) + Slab::W2, 32768, &w_full[s]);
       };
       auto issue_u = [&](int n) {
-        const int s = n & 1, idx = chunk0 + n;
+        const int s = n & 1;
         mbar_expect_tx(&u_full[s], kUBytes);
-        tma_load3(sb + U_BASE + s * 16384, &maps.u, v0, 0, idx, &u_full[s]);
-        tma_load3(sb + U_BASE + s * 16384 + 8192, &maps.u, v0 + 32, 0, idx, &u_full[s]);
+        bulk_load(sb + U_BASE + s * 16384, slab(n) + Slab::U + (size_t)vt * 16384, 16384, &u_full[s]);
         bulk_load(sb + GAM_BASE + s * 512, slab(n) + Slab::VEC + 2 * C * sizeof(float), 512,
                   &u_full[s]);
       };
       auto issue_kb = [&](int n) {
-        const int idx = chunk0 + n;
         mbar_expect_tx(kb_full, 32768);
-        tma_load3(sb + KB_BASE, &maps.kb2, 0, 0, idx, kb_full);
-        tma_load3(sb + KB_BASE + 8192, &maps.kb2, 64, 0, idx, kb_full);
-        tma_load3(sb + KB_BASE + 16384, &maps.kb2, 0, 64, idx, kb_full);
-        tma_load3(sb + KB_BASE + 24576, &maps.kb2, 64, 64, idx, kb_full);
+        bulk_load(sb + KB_BASE, slab(n) + Slab::KB2, 32768, kb_full);
       };
       auto issue_qb = [&](int n) {
-        const int idx = chunk0 + n;
         mbar_expect_tx(qb_full, 32768);
-        tma_load3(sb + QB_BASE, &maps.qb2, 0, 0, idx, qb_full);
-        tma_load3(sb + QB_BASE + 8192, &maps.qb2, 64, 0, idx, qb_full);
-        tma_load3(sb + QB_BASE + 16384, &maps.qb2, 0, 64, idx, qb_full);
-        tma_load3(sb + QB_BASE + 24576, &maps.qb2, 64, 64, idx, qb_full);
+        bulk_load(sb + QB_BASE, slab(n) + Slab::QB2, 32768, qb_full);
       };
       auto issue_aq = [&](int n) {
-        const int idx = chunk0 + n;
         mbar_expect_tx(aq_full, 16384);
-        tma_load3(sb + AQ_BASE, &maps.aq2, 0, 0, idx, aq_full);
-        tma_load3(sb + AQ_BASE + 8192, &maps.aq2, 0, 64, idx, aq_full);
+        bulk_load(sb + AQ_BASE, slab(n) + Slab::AQ2, 16384, aq_full);
       };
       issue_w(0);
       issue_qb(0);
@@ -430,23 +411,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 gdr_status launch_state_kda_tc(const Params& p, cudaStream_t stream) {
-  Maps m;
-  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  const size_t nch = (size_t)p.B * p.HV * p.N;
-  const bool ok =
-      tmap_blocks(&m.w2, p.slabs + Slab::W2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 64, SW) &&
-      tmap_blocks(&m.qb2, p.slabs + Slab::QB2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 64, SW) &&
-      tmap_blocks(&m.kb2, p.slabs + Slab::KB2, BF, 2, K, 2 * C, nch, p.slab_bytes, 64, 64, SW) &&
-      tmap_blocks(&m.aq2, p.slabs + Slab::AQ2, BF, 2, C, 2 * C, nch, p.slab_bytes, 64, 64, SW) &&
-      tmap_blocks(&m.u, p.slabs + Slab::U, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, V, C, nch,
-                  p.slab_bytes, 32, 64, SW);
-  if (!ok) return GDR_ERR_CUDA;
+  static_assert(Slab::W2 % 16 == 0 && Slab::U % 16 == 0 && Slab::QB2 % 16 == 0 &&
+                    Slab::KB2 % 16 == 0 && Slab::AQ2 % 16 == 0,
+                "bulk copies from the slab need 16-byte alignment");
+  if (p.slab_bytes % 16 != 0) return GDR_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(state_kda_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES) != cudaSuccess)
     return GDR_ERR_CUDA;
   dim3 grid(V / VC, p.HV, p.B);
-  state_kda_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(m, p);
+  state_kda_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
