@@ -71,6 +71,8 @@ def workload(name):
         return gin.SSD_WORKLOADS[name]
     if name in gin.SEGMENTED_WORKLOADS:
         return gin.SEGMENTED_WORKLOADS[name]
+    if name in gin.GENERAL_WORKLOADS:
+        return gin.GENERAL_WORKLOADS[name]
     return gin.WORKLOADS[name or gin.HEADLINE]
 
 
@@ -493,9 +495,12 @@ def run_ours(args, rank, local_rank, world):
     # and output items), or the chunk-local kernel and the recurrence
     # (chunk_tc_kernel, chain_kernel + output_kernel for the scalar gate;
     # chunk_kda_kernel, state_kda_tc_kernel for the per-key gate).
-    ck, rk = (("chunk_kda_kernel", "state_kda_tc_kernel") if gate
-              else ("chunk_tc_kernel", "chains+outputs (fused_kernel without the chunk stage, "
-                                       "or chain_kernel+output_kernel)"))
+    if path == 0:
+        ck, rk = "general_prep_kernel", "general_state_kernel"
+    else:
+        ck, rk = (("chunk_kda_kernel", "state_kda_tc_kernel") if gate
+                  else ("chunk_tc_kernel", "chains+outputs (fused_kernel without the chunk stage, "
+                                           "or chain_kernel+output_kernel)"))
     one_launch = path == 2 and segments == 1
     if one_launch:
         kernel_scope = ("fused_kernel (one cooperative launch: chunk producers, chains and "
@@ -509,7 +514,11 @@ def run_ours(args, rank, local_rank, world):
         step_traffic = None
     else:
         kernel_scope = f"one forward call: {ck} + {rk}"
-        launches = 2 if gate else 3
+        # Scalar gate on tensor cores: the chunk kernel, then the chains with the
+        # output items in one launch when they fit on the SMs at once, else the
+        # chain and output kernels.
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        launches = 2 if (gate or path == 0 or w.B * w.HV * 4 <= sms) else 3
         step_traffic = traffic
     tokens = world * w.B * w.T
     line = {

@@ -275,10 +275,28 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   }
 }
 
-// Shared memory of the state kernel: S and the next S [K][kVt], r [C][kVt],
-// exp(G_last) [K]. The chunk operands are read from the workspace (L2).
+// State kernel: per chunk three phases over the CTA's kVt = 32 value columns
+// (lane = column j; warp w of 8 takes rows i = w + 8 m of the chunk and
+// channels c = w + 8 m of the state, accumulating in registers):
+//   r  = U - W S            rows i
+//   o  = QE S + A_qk r      rows i
+//   S' = GM S + KD^T r      channels c
+// Each phase streams its per-chunk matrix through shared memory in tiles of
+// 32 channels (or 32 chunk rows for KD^T and A_qk), staged with coalesced
+// loads, so every term of the inner products comes from shared memory (the
+// matrix element is a broadcast within the warp). S is padded to a multiple
+// of 32 channels and r to a multiple of 32 rows, with zeros.
+constexpr int kSt = 32;                 // channel / row tile of the state kernel
+constexpr int kRowAcc = 128 / 8;        // rows per thread (C <= 128)
+constexpr int kChAcc = 256 / 8;         // channels per thread (K <= 256)
+
+__host__ __device__ inline int round32(int x) { return (x + 31) & ~31; }
+
+// Shared memory: S [Kp][kVt], r [Cp][kVt], exp(G_last) [Kp], one tile of
+// max(Cp, Kp) x 32 floats.
 size_t state_smem_bytes(const Problem& p) {
-  return sizeof(float) * ((size_t)p.K * kVt * 2 + (size_t)p.C * kVt + (size_t)p.K);
+  const size_t Kp = round32(p.K), Cp = round32(p.C);
+  return sizeof(float) * (Kp * kVt + Cp * kVt + Kp + (Kp > Cp ? Kp : Cp) * kSt);
 }
 
 __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
@@ -286,20 +304,22 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
   const Problem& p = a.p;
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
   const int C = p.C, K = p.K, V = p.V;
+  const int Kp = round32(K), Cp = round32(C);
   const int v0 = vt * kVt;
   const int vw = min(kVt, V - v0);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
 
-  float* S = sm;                  // [K][kVt]
-  float* S2 = S + K * kVt;        // [K][kVt] next state
-  float* r = S2 + K * kVt;        // [C][kVt]
-  float* gm = r + C * kVt;        // [K]
+  float* S = sm;                  // [Kp][kVt]
+  float* r = S + Kp * kVt;        // [Cp][kVt]
+  float* gm = r + Cp * kVt;       // [Kp]
+  float* tile = gm + Kp;          // [max(Cp, Kp)][kSt] or [kSt][Kp]
 
   const long seq = (long)b * p.HV + hv;
-  for (int idx = tid; idx < K * kVt; idx += kThreads) {
-    const int c = idx / kVt, j = idx % kVt;
-    S[idx] = (p.s0 && j < vw) ? p.s0[(seq * K + c) * V + v0 + j] : 0.f;
+  for (int idx = tid; idx < Kp * kVt; idx += kThreads) {
+    const int c = idx / kVt, jj = idx % kVt;
+    S[idx] = (p.s0 && c < K && jj < vw) ? p.s0[(seq * K + c) * V + v0 + jj] : 0.f;
   }
+  for (int idx = tid; idx < Cp * kVt; idx += kThreads) r[idx] = 0.f;
 
   for (int n = 0; n < p.N; ++n) {
     const long chunk = seq * p.N + n;
@@ -308,44 +328,107 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
     const float* KD = a.s.KD + chunk * (long)C * K;
     const float* U = a.s.U + chunk * (long)C * V;
     const float* AQ = a.s.AQ + chunk * (long)C * C;
-    __syncthreads();
-    for (int c = tid; c < K; c += kThreads) gm[c] = a.s.GM[chunk * K + (p.gate_mode ? c : 0)];
-    // r = U - W S (a warp shares its row i: the W loads are broadcasts)
-    for (int idx = tid; idx < C * kVt; idx += kThreads) {
-      const int i = idx / kVt, j = idx % kVt;
-      float acc = (j < vw && !p.zero_u) ? U[(long)i * V + v0 + j] : 0.f;
-      for (int c = 0; c < K; ++c) acc = fmaf(-W[(long)i * K + c], S[c * kVt + j], acc);
-      r[idx] = acc;
+    __syncthreads();   // the previous chunk's S and r are written
+    for (int c = tid; c < Kp; c += kThreads)
+      gm[c] = c < K ? a.s.GM[chunk * K + (p.gate_mode ? c : 0)] : 0.f;
+    // [C rows][32 columns c0 ..] of a row-major [C][ld] matrix into the tile.
+    // (unrolled, so that a thread has several loads in flight: one at a time
+    // each would wait for its own round trip to L2)
+    auto stage_rows = [&](const float* M, int ld, int cols, int c0) {
+      __syncthreads();   // the tile's previous readers are done
+#pragma unroll 8
+      for (int idx = tid; idx < C * kSt; idx += kThreads) {
+        const int i = idx >> 5, cc = idx & 31;
+        tile[idx] = c0 + cc < cols ? M[(long)i * ld + c0 + cc] : 0.f;
+      }
+      __syncthreads();
+    };
+    // ---- r = U - W S
+    float acc[kRowAcc];
+#pragma unroll
+    for (int m = 0; m < kRowAcc; ++m) {
+      const int i = w + 8 * m;
+      acc[m] = (i < C && j < vw && !p.zero_u) ? U[(long)i * V + v0 + j] : 0.f;
     }
-    __syncthreads();
-    // o = (q exp(G)) S + A_qk r, and the next state into S2.
-    for (int idx = tid; idx < C * kVt; idx += kThreads) {
-      const int i = idx / kVt, j = idx % kVt;
-      const int t = n * C + i;
-      if (j >= vw || t >= p.T) continue;
-      float acc = 0.f;
-      for (int c = 0; c < K; ++c) acc = fmaf(QE[(long)i * K + c], S[c * kVt + j], acc);
-      for (int m = 0; m <= i; ++m) acc = fmaf(AQ[i * C + m], r[m * kVt + j], acc);
+    for (int c0 = 0; c0 < K; c0 += kSt) {
+      stage_rows(W, K, K, c0);
+#pragma unroll 4
+      for (int cc = 0; cc < kSt; ++cc) {
+        const float sv = S[(c0 + cc) * kVt + j];
+#pragma unroll
+        for (int m = 0; m < kRowAcc; ++m)
+          if (w + 8 * m < C) acc[m] = fmaf(-tile[(w + 8 * m) * kSt + cc], sv, acc[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kRowAcc; ++m)
+      if (w + 8 * m < C) r[(w + 8 * m) * kVt + j] = acc[m];
+    // ---- o = QE S + A_qk r
+#pragma unroll
+    for (int m = 0; m < kRowAcc; ++m) acc[m] = 0.f;
+    for (int c0 = 0; c0 < K; c0 += kSt) {
+      stage_rows(QE, K, K, c0);
+#pragma unroll 4
+      for (int cc = 0; cc < kSt; ++cc) {
+        const float sv = S[(c0 + cc) * kVt + j];
+#pragma unroll
+        for (int m = 0; m < kRowAcc; ++m)
+          if (w + 8 * m < C) acc[m] = fmaf(tile[(w + 8 * m) * kSt + cc], sv, acc[m]);
+      }
+    }
+    for (int m0 = 0; m0 < C; m0 += kSt) {
+      stage_rows(AQ, C, C, m0);   // (the barrier in it also makes r visible)
+#pragma unroll 4
+      for (int mm = 0; mm < kSt; ++mm) {
+        const float rv = r[(m0 + mm) * kVt + j];
+#pragma unroll
+        for (int m = 0; m < kRowAcc; ++m)
+          if (w + 8 * m < C) acc[m] = fmaf(tile[(w + 8 * m) * kSt + mm], rv, acc[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kRowAcc; ++m) {
+      const int i = w + 8 * m, t = n * C + i;
+      if (i >= C || j >= vw || t >= p.T) continue;
       const long off = (((long)b * p.T + t) * p.HV + hv) * V + v0 + j;
       if (p.out_bf16)
-        static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(acc);
+        static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(acc[m]);
       else
-        static_cast<float*>(p.out)[off] = acc;
+        static_cast<float*>(p.out)[off] = acc[m];
     }
-    for (int idx = tid; idx < K * kVt; idx += kThreads) {
-      const int c = idx / kVt, j = idx % kVt;
-      float acc = gm[c] * S[idx];
-      for (int m = 0; m < C; ++m) acc = fmaf(KD[(long)m * K + c], r[m * kVt + j], acc);
-      S2[idx] = acc;
+    // ---- S' = GM S + KD^T r: the tile holds KD rows m0 .. m0 + 31, all K channels.
+    float acc2[kChAcc];
+#pragma unroll
+    for (int m = 0; m < kChAcc; ++m) {
+      const int c = w + 8 * m;
+      acc2[m] = c < K ? gm[c] * S[c * kVt + j] : 0.f;
     }
-    __syncthreads();
-    for (int idx = tid; idx < K * kVt; idx += kThreads) S[idx] = S2[idx];
+    for (int m0 = 0; m0 < C; m0 += kSt) {
+      __syncthreads();
+#pragma unroll 8
+      for (int idx = tid; idx < kSt * K; idx += kThreads) {
+        const int mm = idx / K, c = idx % K;
+        tile[idx] = m0 + mm < C ? KD[(long)(m0 + mm) * K + c] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll 4
+      for (int mm = 0; mm < kSt; ++mm) {
+        const float rv = r[(m0 + mm) * kVt + j];
+#pragma unroll
+        for (int m = 0; m < kChAcc; ++m)
+          if (w + 8 * m < K) acc2[m] = fmaf(tile[mm * K + w + 8 * m], rv, acc2[m]);
+      }
+    }
+    __syncthreads();   // every read of this chunk's S is done
+#pragma unroll
+    for (int m = 0; m < kChAcc; ++m)
+      if (w + 8 * m < K) S[(w + 8 * m) * kVt + j] = acc2[m];
   }
   __syncthreads();
   if (p.sT) {
     for (int idx = tid; idx < K * kVt; idx += kThreads) {
-      const int c = idx / kVt, j = idx % kVt;
-      if (j < vw) p.sT[(seq * K + c) * V + v0 + j] = S[idx];
+      const int c = idx / kVt, jj = idx % kVt;
+      if (jj < vw) p.sT[(seq * K + c) * V + v0 + jj] = S[idx];
     }
   }
 }

@@ -111,6 +111,19 @@ SSD_WORKLOADS = {
         description="Mamba2 SSD forward on the headline shape"),
 }
 
+# The headline shape with a chunk size or head dims outside the tensor-core
+# path (C = 128; K = V = 64): the general fp32 path.
+GENERAL_WORKLOADS = {
+    "gdn_c128_t4096_h12": Workload(
+        "gdn_c128_t4096_h12", B=1, T=4096, H=12, HV=12, K=128, V=128, C=128, dtype=torch.bfloat16,
+        gate_mode=0, g_mean=0.0, g_std=1.0, s0_std=None, seed=1,
+        description="the headline shape with chunk size 128"),
+    "gdn_k64_t4096_h12": Workload(
+        "gdn_k64_t4096_h12", B=1, T=4096, H=12, HV=12, K=64, V=64, C=64, dtype=torch.bfloat16,
+        gate_mode=0, g_mean=0.0, g_std=1.0, s0_std=None, seed=1,
+        description="the headline shape with head dims K = V = 64"),
+}
+
 HEADLINE = "gdn_t4096_h12"
 
 
