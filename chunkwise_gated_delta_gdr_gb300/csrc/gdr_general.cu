@@ -275,29 +275,33 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
   }
 }
 
-// State kernel: per chunk three phases over the CTA's kVt = 32 value columns
-// (lane = column j; warp w of 8 takes rows i = w + 8 m of the chunk and
-// channels c = w + 8 m of the state, accumulating in registers):
-//   r  = U - W S            rows i
+// State kernel: per chunk three phases over the CTA's kVt = 32 value columns,
+// each thread accumulating a 4 x 4 block in registers (column group cg =
+// tid % 8: columns 4 cg .. 4 cg + 3; row group rg = tid / 8: rows, or state
+// channels, 4 rg .. 4 rg + 3, and 4 rg + 128 .. for K > 128):
+//   r  = U - W S            rows i of the chunk
 //   o  = QE S + A_qk r      rows i
-//   S' = GM S + KD^T r      channels c
+//   S' = GM S + KD^T r      state channels c
 // Each phase streams its per-chunk matrix through shared memory in tiles of
 // 32 channels (or 32 chunk rows for KD^T and A_qk), staged with coalesced
-// loads, so every term of the inner products comes from shared memory (the
-// matrix element is a broadcast within the warp). S is padded to a multiple
-// of 32 channels and r to a multiple of 32 rows, with zeros.
+// loads (W, QE and A_qk transposed, so that a thread's four rows are one
+// 16-byte read); every step of an inner product then takes one 16-byte read
+// of each operand for 16 FMAs. S is padded to a multiple of 32 channels and r
+// to a multiple of 32 rows, with zeros.
 constexpr int kSt = 32;                 // channel / row tile of the state kernel
-constexpr int kRowAcc = 128 / 8;        // rows per thread (C <= 128)
-constexpr int kChAcc = 256 / 8;         // channels per thread (K <= 256)
+constexpr int kChPass = 2;              // passes of 128 state channels (K <= 256)
+constexpr int kStageRegs = 256 * kSt / 256;   // a thread's share of one tile (K <= 256)
 
 __host__ __device__ inline int round32(int x) { return (x + 31) & ~31; }
 
-// Shared memory: S [Kp][kVt], r [Cp][kVt], exp(G_last) [Kp], one tile of
-// max(Cp, Kp) x 32 floats.
+// Shared memory: S [Kp][kVt], r [Cp][kVt], exp(G_last) [Kp], and one tile:
+// transposed [kSt][Cp + 4] or [kSt][Kp + 4].
 size_t state_smem_bytes(const Problem& p) {
   const size_t Kp = round32(p.K), Cp = round32(p.C);
-  return sizeof(float) * (Kp * kVt + Cp * kVt + Kp + (Kp > Cp ? Kp : Cp) * kSt);
+  return sizeof(float) * (Kp * kVt + Cp * kVt + Kp + kSt * ((Kp > Cp ? Kp : Cp) + 4));
 }
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
   extern __shared__ float sm[];
@@ -305,14 +309,16 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
   const int vt = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
   const int C = p.C, K = p.K, V = p.V;
   const int Kp = round32(K), Cp = round32(C);
+  const int LC = Cp + 4, LK = Kp + 4;     // tile row strides (16-byte multiples)
   const int v0 = vt * kVt;
   const int vw = min(kVt, V - v0);
-  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int tid = threadIdx.x, cg = tid & 7, rg = tid >> 3;
+  const int j0 = 4 * cg;                  // this thread's first column
 
   float* S = sm;                  // [Kp][kVt]
   float* r = S + Kp * kVt;        // [Cp][kVt]
   float* gm = r + Cp * kVt;       // [Kp]
-  float* tile = gm + Kp;          // [max(Cp, Kp)][kSt] or [kSt][Kp]
+  float* tile = gm + Kp;          // [kSt][LC] (transposed rows) or [kSt][LK]
 
   const long seq = (long)b * p.HV + hv;
   for (int idx = tid; idx < Kp * kVt; idx += kThreads) {
@@ -320,109 +326,177 @@ __global__ void __launch_bounds__(kThreads) general_state_kernel(Args a) {
     S[idx] = (p.s0 && c < K && jj < vw) ? p.s0[(seq * K + c) * V + v0 + jj] : 0.f;
   }
   for (int idx = tid; idx < Cp * kVt; idx += kThreads) r[idx] = 0.f;
+  const int i0 = 4 * rg;                  // this thread's first row (r and o phases)
+  const bool rows_ok = i0 < C;            // (C is a multiple of 16)
 
-  for (int n = 0; n < p.N; ++n) {
-    const long chunk = seq * p.N + n;
-    const float* W = a.s.W + chunk * (long)C * K;
-    const float* QE = a.s.QE + chunk * (long)C * K;
-    const float* KD = a.s.KD + chunk * (long)C * K;
-    const float* U = a.s.U + chunk * (long)C * V;
-    const float* AQ = a.s.AQ + chunk * (long)C * C;
-    __syncthreads();   // the previous chunk's S and r are written
-    for (int c = tid; c < Kp; c += kThreads)
-      gm[c] = c < K ? a.s.GM[chunk * K + (p.gate_mode ? c : 0)] : 0.f;
-    // [C rows][32 columns c0 ..] of a row-major [C][ld] matrix into the tile.
-    // (unrolled, so that a thread has several loads in flight: one at a time
-    // each would wait for its own round trip to L2)
-    auto stage_rows = [&](const float* M, int ld, int cols, int c0) {
-      __syncthreads();   // the tile's previous readers are done
-#pragma unroll 8
-      for (int idx = tid; idx < C * kSt; idx += kThreads) {
+  // acc += tile^T x X over the 32 staged steps: this thread's 4 rows
+  // (tile[cc][i0 ..]) times 4 columns of X (rows x0 + cc of [.][kVt]).
+  auto tile_product = [&](float (&acc)[4][4], const float* X, int x0, float sign) {
+#pragma unroll 4
+    for (int cc = 0; cc < kSt; ++cc) {
+      const float4 xv = ld4(X + (x0 + cc) * kVt + j0);
+      const float4 tv = ld4(tile + cc * LC + i0);
+      const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float ts[4] = {sign * tv.x, sign * tv.y, sign * tv.z, sign * tv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] = fmaf(ts[e], xs[f], acc[e][f]);
+    }
+  };
+  // The chunks' tiles form one sequence of stages: per chunk nK tiles of W,
+  // nK of QE, nC of A_qk, nC of KD. The values of stage q + 1 are loaded into
+  // registers (a thread's share, at most kStageRegs) while stage q is
+  // computed, so that the round trip to L2 or DRAM overlaps the arithmetic.
+  const int nK = (K + kSt - 1) / kSt, nC = (C + kSt - 1) / kSt;
+  const int per_chunk = 2 * nK + 2 * nC;
+  const long nstages = (long)p.N * per_chunk;
+  float nxt[kStageRegs];
+  // Source of stage q: which matrix, its leading dimension, column count and
+  // first column (or first KD row).
+  auto load_stage = [&](long q) {
+    const long chunk = seq * p.N + q / per_chunk;
+    const int s = (int)(q % per_chunk);
+    if (s < 2 * nK + nC) {   // W, QE or A_qk columns, read along the row
+      const float* M;
+      int ld, cols, c0;
+      if (s < nK) { M = a.s.W + chunk * (long)C * K; ld = K; cols = K; c0 = kSt * s; }
+      else if (s < 2 * nK) { M = a.s.QE + chunk * (long)C * K; ld = K; cols = K; c0 = kSt * (s - nK); }
+      else { M = a.s.AQ + chunk * (long)C * C; ld = C; cols = C; c0 = kSt * (s - 2 * nK); }
+#pragma unroll
+      for (int kk = 0; kk < kStageRegs; ++kk) {
+        const int idx = tid + kThreads * kk;
         const int i = idx >> 5, cc = idx & 31;
-        tile[idx] = c0 + cc < cols ? M[(long)i * ld + c0 + cc] : 0.f;
+        nxt[kk] = (i < C && c0 + cc < cols) ? M[(long)i * ld + c0 + cc] : 0.f;
       }
-      __syncthreads();
-    };
-    // ---- r = U - W S
-    float acc[kRowAcc];
+    } else {                 // KD rows m0 .. m0 + 31, all K channels
+      const float* KD = a.s.KD + chunk * (long)C * K;
+      const int m0 = kSt * (s - 2 * nK - nC);
 #pragma unroll
-    for (int m = 0; m < kRowAcc; ++m) {
-      const int i = w + 8 * m;
-      acc[m] = (i < C && j < vw && !p.zero_u) ? U[(long)i * V + v0 + j] : 0.f;
-    }
-    for (int c0 = 0; c0 < K; c0 += kSt) {
-      stage_rows(W, K, K, c0);
-#pragma unroll 4
-      for (int cc = 0; cc < kSt; ++cc) {
-        const float sv = S[(c0 + cc) * kVt + j];
-#pragma unroll
-        for (int m = 0; m < kRowAcc; ++m)
-          if (w + 8 * m < C) acc[m] = fmaf(-tile[(w + 8 * m) * kSt + cc], sv, acc[m]);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < kRowAcc; ++m)
-      if (w + 8 * m < C) r[(w + 8 * m) * kVt + j] = acc[m];
-    // ---- o = QE S + A_qk r
-#pragma unroll
-    for (int m = 0; m < kRowAcc; ++m) acc[m] = 0.f;
-    for (int c0 = 0; c0 < K; c0 += kSt) {
-      stage_rows(QE, K, K, c0);
-#pragma unroll 4
-      for (int cc = 0; cc < kSt; ++cc) {
-        const float sv = S[(c0 + cc) * kVt + j];
-#pragma unroll
-        for (int m = 0; m < kRowAcc; ++m)
-          if (w + 8 * m < C) acc[m] = fmaf(tile[(w + 8 * m) * kSt + cc], sv, acc[m]);
-      }
-    }
-    for (int m0 = 0; m0 < C; m0 += kSt) {
-      stage_rows(AQ, C, C, m0);   // (the barrier in it also makes r visible)
-#pragma unroll 4
-      for (int mm = 0; mm < kSt; ++mm) {
-        const float rv = r[(m0 + mm) * kVt + j];
-#pragma unroll
-        for (int m = 0; m < kRowAcc; ++m)
-          if (w + 8 * m < C) acc[m] = fmaf(tile[(w + 8 * m) * kSt + mm], rv, acc[m]);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < kRowAcc; ++m) {
-      const int i = w + 8 * m, t = n * C + i;
-      if (i >= C || j >= vw || t >= p.T) continue;
-      const long off = (((long)b * p.T + t) * p.HV + hv) * V + v0 + j;
-      if (p.out_bf16)
-        static_cast<__nv_bfloat16*>(p.out)[off] = __float2bfloat16_rn(acc[m]);
-      else
-        static_cast<float*>(p.out)[off] = acc[m];
-    }
-    // ---- S' = GM S + KD^T r: the tile holds KD rows m0 .. m0 + 31, all K channels.
-    float acc2[kChAcc];
-#pragma unroll
-    for (int m = 0; m < kChAcc; ++m) {
-      const int c = w + 8 * m;
-      acc2[m] = c < K ? gm[c] * S[c * kVt + j] : 0.f;
-    }
-    for (int m0 = 0; m0 < C; m0 += kSt) {
-      __syncthreads();
-#pragma unroll 8
-      for (int idx = tid; idx < kSt * K; idx += kThreads) {
+      for (int kk = 0; kk < kStageRegs; ++kk) {
+        const int idx = tid + kThreads * kk;
         const int mm = idx / K, c = idx % K;
-        tile[idx] = m0 + mm < C ? KD[(long)(m0 + mm) * K + c] : 0.f;
-      }
-      __syncthreads();
-#pragma unroll 4
-      for (int mm = 0; mm < kSt; ++mm) {
-        const float rv = r[(m0 + mm) * kVt + j];
-#pragma unroll
-        for (int m = 0; m < kChAcc; ++m)
-          if (w + 8 * m < K) acc2[m] = fmaf(tile[mm * K + w + 8 * m], rv, acc2[m]);
+        nxt[kk] = (mm < kSt && m0 + mm < C) ? KD[(long)(m0 + mm) * K + c] : 0.f;
       }
     }
-    __syncthreads();   // every read of this chunk's S is done
+  };
+  // The loaded values into the tile: W, QE and A_qk transposed ([cc][i]), KD
+  // as is ([mm][c], channels K .. Kp + 3 zero).
+  auto store_stage = [&](long q) {
+    const int s = (int)(q % per_chunk);
+    if (s < 2 * nK + nC) {
 #pragma unroll
-    for (int m = 0; m < kChAcc; ++m)
-      if (w + 8 * m < K) S[(w + 8 * m) * kVt + j] = acc2[m];
+      for (int kk = 0; kk < kStageRegs; ++kk) {
+        const int idx = tid + kThreads * kk;
+        const int i = idx >> 5, cc = idx & 31;
+        if (i < C) tile[cc * LC + i] = nxt[kk];
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < kStageRegs; ++kk) {
+        const int idx = tid + kThreads * kk;
+        const int mm = idx / K, c = idx % K;
+        if (mm < kSt) tile[mm * LK + c] = nxt[kk];
+      }
+      for (int idx = tid; idx < kSt * (LK - K); idx += kThreads) {
+        const int mm = idx / (LK - K), c = K + idx % (LK - K);
+        tile[mm * LK + c] = 0.f;
+      }
+    }
+  };
+  float acc[4][4], acc2[kChPass][4][4];
+  if (nstages > 0) load_stage(0);
+  for (long q = 0; q < nstages; ++q) {
+    const int n = (int)(q / per_chunk), s = (int)(q % per_chunk);
+    const long chunk = seq * p.N + n;
+    __syncthreads();   // the tile's previous readers (and S and r writers) are done
+    store_stage(q);
+    if (s == 0)
+      for (int c = tid; c < Kp; c += kThreads)
+        gm[c] = c < K ? a.s.GM[chunk * K + (p.gate_mode ? c : 0)] : 0.f;
+    __syncthreads();
+    if (q + 1 < nstages) load_stage(q + 1);
+    if (s == 0 || s == nK) {
+      // r = U - W S starts from U; o = QE S + A_qk r from zero.
+      const float* U = a.s.U + chunk * (long)C * V;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f)
+          acc[e][f] = (s == 0 && rows_ok && j0 + f < vw && !p.zero_u)
+                          ? U[(long)(i0 + e) * V + v0 + j0 + f] : 0.f;
+    }
+    if (s < nK) {
+      if (rows_ok) tile_product(acc, S, kSt * s, -1.f);
+      if (s == nK - 1 && rows_ok) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<float4*>(r + (i0 + e) * kVt + j0) =
+              make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
+      }
+    } else if (s < 2 * nK) {
+      if (rows_ok) tile_product(acc, S, kSt * (s - nK), 1.f);
+    } else if (s < 2 * nK + nC) {
+      if (rows_ok) tile_product(acc, r, kSt * (s - 2 * nK), 1.f);
+      if (s == 2 * nK + nC - 1 && rows_ok) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = n * C + i0 + e;
+          if (t >= p.T) continue;
+          const long off = (((long)b * p.T + t) * p.HV + hv) * V + v0 + j0;
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            if (j0 + f >= vw) continue;
+            if (p.out_bf16)
+              static_cast<__nv_bfloat16*>(p.out)[off + f] = __float2bfloat16_rn(acc[e][f]);
+            else
+              static_cast<float*>(p.out)[off + f] = acc[e][f];
+          }
+        }
+      }
+    } else {
+      const int m0 = kSt * (s - 2 * nK - nC);
+      if (m0 == 0) {
+        // S' = GM S + KD^T r: this thread's channels c = 4 rg + 128 q' + e.
+#pragma unroll
+        for (int qq = 0; qq < kChPass; ++qq)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * rg + 128 * qq + e;
+#pragma unroll
+            for (int f = 0; f < 4; ++f)
+              acc2[qq][e][f] = c < Kp ? gm[c] * S[c * kVt + j0 + f] : 0.f;
+          }
+      }
+#pragma unroll 4
+      for (int mm = 0; mm < kSt; ++mm) {
+        const float4 rv = ld4(r + (m0 + mm) * kVt + j0);
+        const float rs[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+        for (int qq = 0; qq < kChPass; ++qq) {
+          const int c = 4 * rg + 128 * qq;
+          if (c >= Kp) continue;
+          const float4 kv = ld4(tile + mm * LK + c);
+          const float ks[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) acc2[qq][e][f] = fmaf(ks[e], rs[f], acc2[qq][e][f]);
+        }
+      }
+      if (s == per_chunk - 1) {
+        __syncthreads();   // every read of this chunk's S is done
+#pragma unroll
+        for (int qq = 0; qq < kChPass; ++qq) {
+          const int c = 4 * rg + 128 * qq;
+          if (c >= Kp) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<float4*>(S + (c + e) * kVt + j0) =
+                make_float4(acc2[qq][e][0], acc2[qq][e][1], acc2[qq][e][2], acc2[qq][e][3]);
+        }
+      }
+    }
   }
   __syncthreads();
   if (p.sT) {
