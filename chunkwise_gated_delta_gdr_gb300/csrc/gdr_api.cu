@@ -25,7 +25,7 @@ gdr_status check_dims(const gdr_dims* d, int chunk_size, int gate_mode) {
   if (chunk_size != 16 && chunk_size != 32 && chunk_size != 64 && chunk_size != 128)
     return GDR_ERR_UNSUPPORTED;
   // The general path streams K and V in tiles; its state kernel keeps a K x 32
-  // state tile (and the next one) in shared memory.
+  // state tile in shared memory.
   if (d->K > 256 || d->V > 256) return GDR_ERR_UNSUPPORTED;
   if (d->HV > 65535 || d->B > 65535) return GDR_ERR_UNSUPPORTED;
   // Element counts must fit the kernels' 64-bit indexing and the grid limits.

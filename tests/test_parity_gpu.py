@@ -377,6 +377,23 @@ LARGE_HEADS = [
 ]
 
 
+# Head dims that are not multiples of the general state kernel's 32-channel
+# tiles or of its 4-wide register blocks in the value columns.
+ODD_HEADS = [
+    ("tiny_fp32", dict(T=77, K=20, V=36, C=16)),
+    ("gdn_t4096_h12", dict(T=150, H=1, HV=2, K=100, V=60)),
+    ("kda_gqa_t8192", dict(B=1, T=90, H=1, HV=2, K=36, V=50, C=32)),
+]
+
+
+@pytest.mark.parametrize("name,ov", ODD_HEADS)
+def test_odd_head_dims(name, ov):
+    w = gin.shrink(gin.WORKLOADS[name], **ov)
+    assert gdr.chunk_fwd_path(gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, 1, 0), w.C,
+                              w.gate_mode) == 0
+    check_against_oracle(w, gin.make_inputs(w))
+
+
 @pytest.mark.parametrize("name,ov", LARGE_HEADS)
 def test_large_head_dims(name, ov):
     w = gin.shrink(gin.WORKLOADS[name], **ov)
