@@ -9,8 +9,9 @@
 //
 //  general_prep_kernel   one CTA per chunk (n, hv, b): L2 norm and scale of q/k,
 //                        gate cumsum G, decayed dots A_kk / A_qk, the unit
-//                        lower-triangular inverse X = M^-1 (substitution on the
-//                        unit columns), W = X (exp(G) k) and U = X v, and the
+//                        lower-triangular inverse X = M^-1 (blocked: 16 x 16
+//                        diagonal blocks by substitution, the rest by doubling),
+//                        W = X (exp(G) k) and U = X v, and the
 //                        per-chunk factors the state pass needs ("分块并行计算（Chunkwise）" notes, section
 //                        "chunk 内的 cumsum 与下三角解" and listing naive_chunk_kda).
 //  general_state_kernel  one CTA per (V tile, hv, b), serial over chunks: the
@@ -219,12 +220,42 @@ __global__ void __launch_bounds__(kThreads) general_prep_kernel(Args a) {
     Lm[idx] = (j < i && !p.ssd) ? Lm[idx] * nk[i] * f : 0.f;   // SSD: no erase, M = I
   }
   __syncthreads();
-  // X = M^-1 by forward substitution on the unit columns, one column per thread.
+  // X = M^-1, M = I + L (L strictly lower, in Lm), blocked: the 16 x 16
+  // diagonal blocks by forward substitution on their unit columns (one column
+  // per thread), then the blocks below them by doubling. For adjacent s-blocks
+  // J (rows and columns [2 k s, 2 k s + s)) and I (the next s), the inverse of
+  // [[M_JJ, 0], [L_IJ, M_II]] has the lower block X_IJ = -X_II (L_IJ X_JJ), both
+  // products in fp32 (T = L_IJ X_JJ in the dead q tile).
+  for (int idx = tid; idx < C * C; idx += kThreads) Aq[idx] = 0.f;
+  __syncthreads();
   for (int col = tid; col < C; col += kThreads) {
-    for (int i = 0; i < C; ++i) {
+    const int o = col & ~15;
+    for (int i = col; i < o + 16; ++i) {
       float acc = (i == col) ? 1.f : 0.f;
       for (int m = col; m < i; ++m) acc = fmaf(-Lm[i * C + m], Aq[m * C + col], acc);
       Aq[i * C + col] = acc;
+    }
+  }
+  float* Tm = tq;   // pairs x s x s <= C s / 2 <= C (kTk + 1) floats
+  for (int sz = 16; sz < C; sz *= 2) {
+    const int pairs = C / (2 * sz), ss = sz * sz;
+    __syncthreads();
+    for (int idx = tid; idx < pairs * ss; idx += kThreads) {
+      const int pr = idx / ss, e = idx % ss, i = e / sz, j = e % sz;
+      const int rI = 2 * pr * sz + sz, cJ = 2 * pr * sz;
+      float acc = 0.f;
+      for (int m = j; m < sz; ++m)   // X_JJ is lower triangular
+        acc = fmaf(Lm[(rI + i) * C + cJ + m], Aq[(cJ + m) * C + cJ + j], acc);
+      Tm[idx] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < pairs * ss; idx += kThreads) {
+      const int pr = idx / ss, e = idx % ss, i = e / sz, j = e % sz;
+      const int rI = 2 * pr * sz + sz, cJ = 2 * pr * sz;
+      float acc = 0.f;
+      for (int m = 0; m <= i; ++m)   // X_II is lower triangular
+        acc = fmaf(Aq[(rI + i) * C + rI + m], Tm[pr * ss + m * sz + j], acc);
+      Aq[(rI + i) * C + cJ + j] = -acc;
     }
   }
   // Per-chunk factors of the state pass and W = X (exp(G) k_hat), tile by tile.
