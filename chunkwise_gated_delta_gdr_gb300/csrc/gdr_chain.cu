@@ -442,27 +442,22 @@ __device__ __forceinline__ void mark_exports(unsigned int* mark, int nx, int N, 
 //     S_{n+1} = gamma_n S_n + N_n
 // without a product. Shared memory (from the chain's 1024-aligned base): a
 // ring of SSD_SLOTS increment boxes (this CTA's 32 value columns, [128 c][32 v]
-// fp32, 128-byte swizzled rows) with gamma_n beside each, then the S tiles,
-// all inside the first worker group region: with output items to form, warps
-// 8-15 form them in the second region while the scan runs (kSsdStateWarps
-// warps hold S, thread (w, lane) channel 32 w + lane and all 32 columns, and
-// publish each S_n for the export; warp kSsdStateWarps loads the ring, waiting
-// for the slab flags in the one-launch forward; the warp after it exports the
-// S tiles and marks them).
-constexpr int kSsdStateWarps = 4;
-constexpr int kSsdRingWarp = kSsdStateWarps, kSsdExportWarp = kSsdStateWarps + 1;
-constexpr int SSD_SLOTS = 3;
+// fp32, 128-byte swizzled rows) with gamma_n beside each, then the S tiles.
+// Warps 0-7 hold S as in the delta-rule chain (thread (w, lane): channel
+// 32 (w % 4) + lane, columns [16 (w / 4), 16 (w / 4) + 16)) and publish each
+// S_n for the export; warp 12 loads the ring (waiting for the slab flags in
+// the one-launch forward); warp 13 exports the S tiles and marks them.
+constexpr int SSD_SLOTS = 6;
 constexpr int SSD_SLOT = (int)Slab::SSD_N_BOX;
 constexpr int SSD_OFF_GAM = SSD_SLOTS * SSD_SLOT;   // 16 bytes per slot
 constexpr int SSD_OFF_S = SSD_OFF_GAM + 1024;
 constexpr uint32_t SSD_TX = SSD_SLOT + 16;
-static_assert(SSD_SLOT == 16384 && SSD_OFF_S % 1024 == 0 && SSD_OFF_S + S_TILES * 16384 <= chunk::GROUP_BYTES &&
-                  2 * chunk::GROUP_BYTES <= OFF_BARS && kSsdStateWarps * 32 == K,
-              "SSD chain shared memory: the scan in group region 0, output items in region 1");
+static_assert(SSD_SLOT == 16384 && SSD_OFF_S % 1024 == 0 && SSD_OFF_S + S_TILES * 16384 <= OFF_BARS,
+              "SSD chain shared memory");
 enum : int {
   SB_FULL = 0,                      // [SSD_SLOTS] ring slot loaded
-  SB_EMPTY = SB_FULL + SSD_SLOTS,   // [SSD_SLOTS] ring slot read (the state warps)
-  SB_ES = SB_EMPTY + SSD_SLOTS,     // [S_TILES] S_n published, barrier n % S_TILES (the state warps)
+  SB_EMPTY = SB_FULL + SSD_SLOTS,   // [SSD_SLOTS] ring slot read (8 state warps)
+  SB_ES = SB_EMPTY + SSD_SLOTS,     // [S_TILES] S_n published, barrier n % S_TILES (8 state warps)
   SB_XR = SB_ES + S_TILES           // [S_TILES] export of S_n read out (exporter)
 };
 static_assert(SB_XR + S_TILES <= B_SLOT, "SSD barriers below the TMEM slot word");
@@ -470,35 +465,37 @@ static_assert(SB_XR + S_TILES <= B_SLOT, "SSD barriers below the TMEM slot word"
 __device__ __forceinline__ void ssd_init_bars(uint64_t* bars) {
   for (int i = 0; i < SSD_SLOTS; ++i) {
     mbar_init(&bars[SB_FULL + i], 1);
-    mbar_init(&bars[SB_EMPTY + i], kSsdStateWarps);
+    mbar_init(&bars[SB_EMPTY + i], 8);
   }
   for (int i = 0; i < S_TILES; ++i) {
-    mbar_init(&bars[SB_ES + i], kSsdStateWarps);
+    mbar_init(&bars[SB_ES + i], 8);
     mbar_init(&bars[SB_XR + i], 1);
   }
 }
 
-// Warps 0 .. kSsdExportWarp of the chain CTA (the others return at once); ok
-// turns false (for the calling thread) when one of its waits gave up.
+// All threads of the chain CTA; ok turns false (for the calling thread) when
+// one of its waits gave up.
 __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq, int vt, bool wait_flags,
                                           bool marks, uint8_t* xbase, bool& ok) {
   const int N = p.N, v0 = vt * VC, chunk0 = seq * N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
   const uint32_t sb = smem_u32(sm);
-  if (warp < kSsdStateWarps) {
-    const int c = 32 * warp + lane;
-    float S[VC];
+  if (warp < 8) {
+    const int qd = warp & 3, h = warp >> 2;
+    const int c = 32 * qd + lane;
+    float S[16];
     if (p.s0) {
-      const float4* src = reinterpret_cast<const float4*>(p.s0 + ((size_t)seq * K + c) * V + v0);
+      const float4* src =
+          reinterpret_cast<const float4*>(p.s0 + ((size_t)seq * K + c) * V + v0 + 16 * h);
 #pragma unroll
-      for (int q = 0; q < VC / 4; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const float4 x = src[q];
         S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < VC; ++i) S[i] = 0.f;
+      for (int i = 0; i < 16; ++i) S[i] = 0.f;
     }
     for (int n = 0; n < N; ++n) {
       // Chunk n's slab first, although S_n does not need it: its export (and
@@ -510,17 +507,15 @@ __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq,
       // S_n into tile n % S_TILES once the export of S_{n - S_TILES} from it is read out.
       if (n >= S_TILES)
         ok = warp_wait(&bars[SB_XR + n % S_TILES], tile_parity(n - S_TILES, S_TILES), ok);
-      uint8_t* tile = sm + SSD_OFF_S + (n % S_TILES) * 16384;
-      publish16(tile, c, 0, S);
-      publish16(tile, c, 2, S + 16);
+      publish16(sm + SSD_OFF_S + (n % S_TILES) * 16384, c, 2 * h, S);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SB_ES + n % S_TILES]);
       const uint8_t* box = sm + sl * SSD_SLOT;
       const float gam = *reinterpret_cast<const float*>(sm + SSD_OFF_GAM + sl * 16);
 #pragma unroll
-      for (int q = 0; q < VC / 4; ++q) {
-        const float4 x = *reinterpret_cast<const float4*>(box + sw_off(c, q));
+      for (int q = 0; q < 4; ++q) {
+        const float4 x = *reinterpret_cast<const float4*>(box + sw_off(c, 4 * h + q));
         S[4 * q] = fmaf(gam, S[4 * q], x.x);
         S[4 * q + 1] = fmaf(gam, S[4 * q + 1], x.y);
         S[4 * q + 2] = fmaf(gam, S[4 * q + 2], x.z);
@@ -530,12 +525,12 @@ __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq,
       if (lane == 0) mbar_arrive(&bars[SB_EMPTY + sl]);
     }
     if (p.sT) {
-      float4* dst = reinterpret_cast<float4*>(p.sT + ((size_t)seq * K + c) * V + v0);
+      float4* dst = reinterpret_cast<float4*>(p.sT + ((size_t)seq * K + c) * V + v0 + 16 * h);
 #pragma unroll
-      for (int q = 0; q < VC / 4; ++q)
+      for (int q = 0; q < 4; ++q)
         dst[q] = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
-  } else if (warp == kSsdRingWarp) {
+  } else if (warp == 12) {
     if (lane == 0) {
       // Each increment box is read once, by this CTA.
       const uint64_t pol = l2_evict_first();
@@ -568,7 +563,7 @@ __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq,
       }
     }
     __syncwarp();
-  } else if (warp == kSsdExportWarp) {
+  } else if (warp == 13) {
     if (lane == 0) {
       const uint64_t pol_keep = l2_evict_last();   // the output items read it next
       unsigned int* mark = marks ? p.xmark + (size_t)seq * VTILES + vt : nullptr;
@@ -600,83 +595,6 @@ __device__ __forceinline__ void ssd_chain(const Params& p, uint8_t* sm, int seq,
   }
 }
 
-// Chunks vt, vt + VTILES, ... below kChainChunks of sequence seq, produced
-// by warps 0-7 of a chain CTA (named barrier kProduceBar) in the worker group
-// layout at sm with TMEM columns tmem .. tmem + 255, each slab flagged once
-// stored.
-__device__ __forceinline__ void produce_first_chunks(const chunk::Maps& maps, const Params& p, uint8_t* sm,
-                                                     int seq, int vt, uint32_t tmem) {
-  const int tid = threadIdx.x, N = p.N, chunk0 = seq * N;
-  if (tid == 0) chunk::init_group_bars(sm);
-  chunk::group_sync(kProduceBar);
-  uint32_t ph = 0;
-  for (int n = vt; n < N && n < kChainChunks; n += VTILES) {
-    chunk::produce_chunk(maps, p, sm, tid, kProduceBar, n, seq % p.HV, seq / p.HV, ph, tmem, nullptr,
-                         nullptr);
-    if (tid == 0) {
-      bulk_wait<0>();
-      fence_async_global();
-      st_release_gpu(p.flags + chunk0 + n, 1u);
-    }
-    ph ^= 1u;
-  }
-}
-// The worker group barriers at sm, before the region is reused.
-__device__ __forceinline__ void inval_group_bars(uint8_t* sm) {
-  uint64_t* gb = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
-  for (int i = 0; i < chunk::kNumBars; ++i)
-    if (i != 2) mbar_inval(gb + i);   // (index 2 holds the TMEM slot word, not a barrier)
-}
-
-// A Mamba2 SSD chain CTA of the one-launch forward (or of chains with output
-// items after a finished chunk-local stage, without produce). Warps 0-7
-// produce the sequence's first chunk (with produce) and run the scan in the
-// first worker group region with TMEM columns 0-255, then form output items
-// there; warps 8-15 form output items from the start, in the second region
-// with columns 256-511, so that these SMs do output work while the scan waits
-// for the workers' slabs.
-__device__ __forceinline__ void ssd_role(const Params& p, uint8_t* sm, int seq, int vt,
-                                         const chunk::Maps& maps, bool produce) {
-  const int N = p.N, chunk0 = seq * N;
-  const int tid = threadIdx.x, warp = tid >> 5, grp = warp >> 3;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + B_SLOT);
-  if (tid == 0) {
-    ssd_init_bars(bars);
-    mbar_fence_init();
-  }
-  if (warp == 13) tmem_alloc(tslot, CHAIN_TMEM);
-  tc_fence_before();
-  nb_sync(1, CHAIN_THREADS);
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  if (grp == 0) {
-    if (produce && vt < N) {
-      produce_first_chunks(maps, p, sm, seq, vt, tmem);
-      tc_fence_before();
-      chunk::group_sync(kProduceBar);
-      tc_fence_after();
-      if (tid == 0) inval_group_bars(sm);
-      chunk::group_sync(kProduceBar);
-    }
-    bool ok = true;
-    ssd_chain(p, sm, seq, vt, produce, true, p.xchg + (size_t)chunk0 * Xchg::BYTES, ok);
-    if (!ok) atomicOr(p.error_word, kErrChainWait);
-    tc_fence_before();
-    chunk::group_sync(kProduceBar);   // the ring and the S tiles are dead
-    tc_fence_after();
-  }
-  uint8_t* gsm = sm + grp * chunk::GROUP_BYTES;
-  if ((tid & 255) == 0) chunk::init_group_bars(gsm);
-  output_items(&maps.q, p, gsm, tid & 255, 1 + grp, tmem + 256 * grp, 0u, 0u);
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 13) {
-    tc_fence_after();
-    tmem_dealloc(tmem, CHAIN_TMEM);
-  }
-}
-
 // seq = b * HV + hv, value columns [32 vt, 32 vt + 32). With maps (the
 // one-launch forward): chunk n's slab is produced in the same launch (wait for
 // its flag before loading it), the CTA first produces chunk vt of its
@@ -684,14 +602,11 @@ __device__ __forceinline__ void ssd_role(const Params& p, uint8_t* sm, int seq, 
 // joins them once its chain is done. With maps but not produce (chains and
 // output items after a finished chunk-local stage) only the last two.
 // kSsd = p.ssd (Mamba2 SSD), a template argument so that the delta-rule
-// chain is compiled without the scan's code and the other way round.
+// chain is compiled without the scan's code and the other way round (one
+// kernel with both measured 1-2 us slower on the delta rule).
 template <bool kSsd>
 __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq, int vt,
                                            const chunk::Maps* maps, bool produce) {
-  if (kSsd && maps) {
-    ssd_role(p, sm, seq, vt, *maps, produce);
-    return;
-  }
   const bool wait_flags = maps != nullptr && produce;
   const int v0 = vt * VC;
   const int N = p.N;
@@ -733,11 +648,29 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
     // vt + 4, ... below kChainChunks here, by warps 0-7 in the worker group
     // layout over the rings, which are idle until the chain starts): their
     // SMs have nothing else in flight, and a worker's first chunk is slow.
-    if (warp < 8) produce_first_chunks(*maps, p, sm, seq, vt, tmem);
+    if (warp < 8) {
+      if (tid == 0) chunk::init_group_bars(sm);
+      chunk::group_sync(kProduceBar);
+      uint32_t ph = 0;
+      for (int n = vt; n < N && n < kChainChunks; n += VTILES) {
+        chunk::produce_chunk(*maps, p, sm, tid, kProduceBar, n, seq % p.HV, seq / p.HV, ph, tmem,
+                             nullptr, nullptr);
+        if (tid == 0) {
+          bulk_wait<0>();
+          fence_async_global();
+          st_release_gpu(p.flags + chunk0 + n, 1u);
+        }
+        ph ^= 1u;
+      }
+    }
     tc_fence_before();
     nb_sync(1, CHAIN_THREADS);
     tc_fence_after();
-    if (tid == 0) inval_group_bars(sm);
+    if (tid == 0) {
+      uint64_t* gb = reinterpret_cast<uint64_t*>(sm + chunk::OFF_BAR);
+      for (int i = 0; i < chunk::kNumBars; ++i)
+        if (i != 2) mbar_inval(gb + i);   // (index 2 holds the TMEM slot word, not a barrier)
+    }
     nb_sync(1, CHAIN_THREADS);
   }
   uint8_t* xbase = p.xchg + (size_t)chunk0 * Xchg::BYTES;
