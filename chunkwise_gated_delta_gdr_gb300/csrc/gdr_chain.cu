@@ -653,7 +653,7 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, int seq
       chunk::group_sync(kProduceBar);
       uint32_t ph = 0;
       for (int n = vt; n < N && n < kChainChunks; n += VTILES) {
-        chunk::produce_chunk(*maps, p, sm, tid, kProduceBar, n, seq % p.HV, seq / p.HV, ph, tmem,
+        chunk::produce_chunk<kSsd>(*maps, p, sm, tid, kProduceBar, n, seq % p.HV, seq / p.HV, ph, tmem,
                              nullptr, nullptr);
         if (tid == 0) {
           bulk_wait<0>();
@@ -1008,6 +1008,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1) chain_kernel(Params p) {
 // group takes output items. (Holding group 1 back until group 0's first chunk
 // was done measured 2 us slower: a worker's first chunk takes ~19 us even
 // alone on its SM, against ~12 us for its later ones.)
+template <bool kSsd>
 __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Params& p,
                                             uint8_t* sm_base, int worker, int n_workers, bool produce) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -1032,7 +1033,7 @@ __device__ __forceinline__ void worker_role(const chunk::Maps& maps, const Param
   for (long it = first + G; it < items; it += NG) {
     const int n = (int)(it / nseq), seq = (int)(it % nseq);
     const int b = seq / p.HV, hv = seq % p.HV;
-    chunk::produce_chunk(maps, p, sm, gtid, 1 + grp, n, hv, b, ph, tmem, nullptr, pending);
+    chunk::produce_chunk<kSsd>(maps, p, sm, gtid, 1 + grp, n, hv, b, ph, tmem, nullptr, pending);
     pending = p.flags + slab_index(p, b, hv, n);
     if (it < first + NG) {
       // The first wave (the chunks the chains reach first): published at once
@@ -1072,7 +1073,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   if (cta < n_chain) {
     if (threadIdx.x < CHAIN_THREADS) chain_role<kSsd>(p, sm, cta / VTILES, cta % VTILES, &maps, produce != 0);
   } else {
-    worker_role(maps, p, sm, cta - n_chain, n_workers, produce != 0);
+    worker_role<kSsd>(maps, p, sm, cta - n_chain, n_workers, produce != 0);
   }
 }
 

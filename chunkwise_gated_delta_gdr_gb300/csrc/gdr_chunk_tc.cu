@@ -49,6 +49,7 @@ bool make_maps(Maps* m, const Params& p) {
 
 namespace {
 
+template <bool kSsd>
 __global__ void __launch_bounds__(chunk::THREADS, 2) chunk_tc_kernel(
     const __grid_constant__ chunk::Maps maps, Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(chunk::THREADS, 2) chunk_tc_kernel(
   // (the first barrier inside produce_chunk orders the initialisation before
   // any wait; only thread 0 uses the barriers before it)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  chunk::produce_chunk(maps, p, sm, threadIdx.x, 1, blockIdx.x, blockIdx.y, blockIdx.z, 0, 0,
+  chunk::produce_chunk<kSsd>(maps, p, sm, threadIdx.x, 1, blockIdx.x, blockIdx.y, blockIdx.z, 0, 0,
                        tslot, nullptr);
   if (threadIdx.x == 0) ptx::bulk_wait_read<0>();   // staging read before the smem is released
   if ((threadIdx.x >> 5) == 1) {
@@ -74,11 +75,12 @@ gdr_status launch_chunk_tc(const Params& p, cudaStream_t stream) {
   if (p.gate_mode != 0) return launch_chunk_kda(p, stream);
   chunk::Maps m;
   if (!chunk::make_maps(&m, p)) return GDR_ERR_CUDA;
-  if (cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto kern = p.ssd ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            chunk::SMEM_BYTES) != cudaSuccess)
     return GDR_ERR_CUDA;
   dim3 grid(p.N, p.HV, p.B);
-  chunk_tc_kernel<<<grid, chunk::THREADS, chunk::SMEM_BYTES, stream>>>(m, p);
+  kern<<<grid, chunk::THREADS, chunk::SMEM_BYTES, stream>>>(m, p);
   return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

@@ -206,6 +206,10 @@ static_assert(4 * Slab::SSD_N_BOX <= (size_t)OFF_AQS, "SSD increment staging bel
 // alloc_slot when that is not null. Thread 0 publishes release_flag (the
 // previous chunk of the group) once that chunk's stores are complete, and
 // leaves this chunk's stores in flight. Returns false if a wait gave up.
+// kSsd = p.ssd (Mamba2 SSD: no erase, the state increment instead of W, U
+// and T), a template argument so that each form is compiled without the
+// other's code.
+template <bool kSsd>
 __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p, uint8_t* sm, int tid, int bar_id,
                               int n, int hv, int b, uint32_t ph, uint32_t tmem_given,
                               uint32_t* alloc_slot, unsigned int* release_flag) {
@@ -267,7 +271,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   if (tid < C) {
     const int t = t0 + tid;
     // SSD: beta = 1 on real rows.
-    bv = (t < p.T) ? (p.ssd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
+    bv = (t < p.T) ? (kSsd ? 1.f : p.beta[((size_t)b * p.T + t) * p.HV + hv]) : 0.f;
   }
   if (alloc_slot && warp == 1) tmem_alloc(alloc_slot, TMEM_COLS);   // warp 0 is issuing the loads
   tc_fence_before();
@@ -280,7 +284,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
   // The key tile's image (the recurrence's A operand k^T) goes to the slab as
   // it is; it must be read out before epilogue 2 overwrites the tile. (Mamba2
   // SSD: the recurrence reads no keys.)
-  if (tid == 0 && !p.ssd) {
+  if (tid == 0 && !kSsd) {
     bulk_store(slab + Slab::K2, smem_u32(sm + OFF_K0), 8192);
     bulk_store(slab + Slab::K2 + 8192, smem_u32(sm + OFF_K1), 8192);
     bulk_commit();
@@ -375,7 +379,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
         float a4[4];
 #pragma unroll
         for (int z = 0; z < 4; ++z)
-          a4[z] = (jb + e + z < rr && !p.ssd) ? v[e + z] * (rowe * cs[z]) : 0.f;
+          a4[z] = (jb + e + z < rr && !kSsd) ? v[e + z] * (rowe * cs[z]) : 0.f;
         *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     } else {
@@ -413,7 +417,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
 #pragma unroll
         for (int z = 0; z < 4; ++z) {
           const int j = jb + e + z;
-          a4[z] = (j < rr && !p.ssd) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
+          a4[z] = (j < rr && !kSsd) ? v[e + z] * rowf * nk[j] * __expf(Gi - G[j]) * bb[j] : 0.f;
         }
         *reinterpret_cast<float4*>(L + rr * LDL + jb + e) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
@@ -462,7 +466,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
     }
     if (e >= 0 && e < K) vec[2 * C + e] = __expf(gl);
   }
-  if (p.ssd) return ssd_increment(p, sm, tid, bar_id, idx, ph, tmem, ok);
+  if (kSsd) return ssd_increment(p, sm, tid, bar_id, idx, ph, tmem, ok);
 
   // ---- X = (I + L)^-1, blocked (gdr_trinv.cuh) ---------------------------------
   unit_lower_inverse64<LDL, LDX>(L, X, T, tid, bar_id);
@@ -565,7 +569,7 @@ __device__ __forceinline__ bool produce_chunk(const Maps& maps, const Params& p,
       if (!is_u) {
         uint32_t hi[8], lo[8];
         // SSD keeps no erase term: W = 0 (then X = I and U = v).
-        const float ws = p.ssd ? 0.f : -1.f;
+        const float ws = kSsd ? 0.f : -1.f;
 #pragma unroll
         for (int e = 0; e < 16; e += 2) split_pair(ws * s[e], ws * s[e + 1], hi[e / 2], lo[e / 2]);
         const int bx = c0 >> 6, c = (c0 & 63) >> 3;
