@@ -234,9 +234,10 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
     // (the delta-rule write per column written, and the next token's inputs
     // staged). Every warp forms the token's norms itself from the staged k and
     // q. Group threads 0-127 load a token's inputs (channel / column gt) into
-    // registers one token ahead (across planes too) and stage them between C
-    // and D into the other buffer, whose previous token every warp of the
-    // group finished before C.
+    // registers two tokens ahead (across planes too), so that a load has a
+    // whole token's work to arrive in, and stage the next token between C and
+    // D into the other buffer, whose previous token every warp of the group
+    // finished before C.
     const int g = warp / GW, gw = warp % GW, gt = tid - g * GT, bar = 1 + g;
     float* wg = wcol[g];
     int tb = 0;                                         // buffer of the current token
@@ -266,12 +267,21 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
         if (gt == 0) tok[g][buf] = x.beta;
       }
     };
-    Tok nx;
+    // Token j of the group: plane g + GROUPS (j / T) of the CTA, token j % T.
+    auto load_nth = [&](int j, Tok& x) {
+      const int ij = g + GROUPS * (j / a.T);
+      if (ij < my) load_tok(blockIdx.x + ij * gridDim.x, j % a.T, x);
+    };
+    Tok nx, nn;                                         // the next token, the one after it
+    float cv = 0.f;                                     // this token's v (the rest is staged)
     if (g < my) {
-      load_tok(blockIdx.x + g * gridDim.x, 0, nx);
+      load_nth(0, nx);
       stage_tok(nx, 0);
+      cv = nx.v;
+      load_nth(1, nx);
     }
     nb_sync(bar, GT);                                   // the first token is staged
+    int jt = 0;                                         // the group's token index
     for (int i = g; i < my; i += GROUPS) {
       const int s = i % STAGES;
       const int plane = blockIdx.x + i * gridDim.x;
@@ -303,15 +313,12 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
       __syncwarp();
       for (int tk = 0; tk < a.T; ++tk) {
         const size_t bt = (size_t)b * a.T + tk;
-        const float xv = nx.v;                          // this token's v (the rest is staged)
+        const float xv = cv;
         const float* kg = kr[g][tb];
         const float* qg = qr[g][tb];
         const float* dg = dec[g][tb];
         const bool more = tk + 1 < a.T || i + GROUPS < my;
-        if (tk + 1 < a.T)
-          load_tok(plane, tk + 1, nx);
-        else if (i + GROUPS < my)
-          load_tok(plane + GROUPS * gridDim.x, 0, nx);
+        load_nth(jt + 2, nn);
         // Norms of the staged k and q (zero past K), every warp for itself.
         float sk = 0.f, sq = 0.f, sqk = 0.f;
 #pragma unroll
@@ -378,6 +385,9 @@ __global__ void __launch_bounds__(pipe::THREADS, 1)
           if (more) stage_tok(nx, tb ^ 1);              // the next token's inputs
         }
         nb_sync(bar, GT);                               // D: writes and next inputs visible
+        cv = nx.v;
+        nx = nn;
+        ++jt;
         const float4 wk4 = *reinterpret_cast<const float4*>(wg + c0);
         const float wk[CPL] = {wk4.x, wk4.y, wk4.z, wk4.w};
 #pragma unroll
