@@ -16,7 +16,10 @@ With N > 1 (launched by torch.distributed.run) every rank runs the same
 workload on its own GPU as a shard of 12 value heads of a 12N-head layer
 (independent sequences, no collective on the data path): weak scaling. Rank 0
 prints one JSON line. ``--impl reference`` times the float64 CPU oracle on the
-host cores instead (rank 0 only).
+host cores instead (rank 0 only). The default headline run at N = 1 also times
+the other workloads' forwards the same way (device-resident inputs, L2 flushed,
+CUDA events) and adds them to its line as ``other_workloads``
+(``--skip-other-workloads`` leaves them out).
 """
 from __future__ import annotations
 
@@ -53,6 +56,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
+    ap.add_argument("--skip-other-workloads", action="store_true",
+                    help="headline run only: leave out the timings of the other workloads")
     ap.add_argument("--out-dtype", choices=["bf16", "fp32"], default="bf16",
                     help="dtype of o in the timed forward (the other is timed beside it)")
     return ap.parse_args()
@@ -311,6 +316,82 @@ def timed(fn, stream, n, flush):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+OTHER_WORKLOADS = ("kda_gqa_t8192", "gdn_long_t65000", "kda_many_b64", "ssd_t4096_h12",
+                   "gdn_h2_t65536", "decode_b64_h16", "gdn_c128_t4096_h12", "gdn_k64_t4096_h12")
+
+
+def other_workloads(dev, stream, flush, hbm, steps=10, warmup=3):
+    """The other workloads' forwards, timed as the headline is (device-resident
+    inputs, L2 flushed before each call, CUDA events on the launching stream),
+    so that their figures sit in the headline's JSON line: per workload the mean
+    time per call, tokens/s and the fraction of the measured HBM copy rate for
+    its compulsory bytes. A workload that fails reports its error instead."""
+    import torch
+    import chunkwise_gated_delta_gdr_gb300 as gdr
+    from chunkwise_gated_delta_gdr_gb300 import inputs as gin
+    res = {}
+    for name in OTHER_WORKLOADS:
+        try:
+            w = workload(name)
+            x = {n: (t.to(dev) if t is not None else None) for n, t in gin.make_inputs(w).items()}
+            if name in gin.DECODE_WORKLOADS or name in gin.SSD_WORKLOADS:
+                ssd = name in gin.SSD_WORKLOADS
+                out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.float32, device=dev)
+                state = None if ssd else x["s0"].clone()
+
+                def step():
+                    if ssd:
+                        gdr.ssd_chunk_fwd(x["q"], x["k"], x["v"], x["g"], None, chunk_size=w.C,
+                                          scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                                          out_dtype=torch.float32, output_final_state=False,
+                                          stream=stream)
+                    else:
+                        gdr.recurrent_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], state,
+                                          scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                                          out=out, stream=stream)
+                sbytes = 0 if ssd else 2 * w.B * w.HV * w.K * w.V * 4
+                nbytes = sbytes + (2 * w.B * w.T * w.H * w.K * 2 + w.B * w.T * w.HV * w.V * 2 +
+                                   2 * w.B * w.T * w.HV * 4 + w.B * w.T * w.HV * w.V * 4)
+                odt = "fp32"
+            else:
+                segments = getattr(w, "segments", 1)
+                dims = gdr.make_dims(w.B, w.T, w.H, w.HV, w.K, w.V, gdr.GDR_BF16, gdr.GDR_BF16)
+                nws = (gdr.chunk_fwd_segmented_workspace_size(dims, w.C, w.gate_mode, segments)
+                       if segments > 1 else gdr.chunk_fwd_workspace_size(dims, w.C, w.gate_mode))
+                ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+                out = torch.empty(w.B, w.T, w.HV, w.V, dtype=torch.bfloat16, device=dev)
+                fin = torch.empty(w.B, w.HV, w.K, w.V, dtype=torch.float32, device=dev)
+
+                def step():
+                    if segments > 1:
+                        gdr.chunk_fwd_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"],
+                                                segments=segments, chunk_size=w.C, scale=w.scale,
+                                                use_qk_l2norm=w.use_qk_l2norm,
+                                                out_dtype=torch.bfloat16, workspace=ws, out=out,
+                                                final_state=fin, stream=stream)
+                    else:
+                        gdr.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["s0"],
+                                      chunk_size=w.C, scale=w.scale, use_qk_l2norm=w.use_qk_l2norm,
+                                      out_dtype=torch.bfloat16, workspace=ws, out=out,
+                                      final_state=fin, stream=stream)
+                nbytes = algorithmic_bytes(w, 2)
+                odt = "bf16"
+            for _ in range(warmup):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+            ms = statistics.mean(timed(step, stream, steps, flush))
+            assert torch.isfinite(out.float()).all()
+            res[name] = {"ms_per_step": ms, "tokens_per_s": w.B * w.T / (ms * 1e-3),
+                         "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                         "algorithmic_bytes_per_step": nbytes, "out_dtype": odt, "steps": steps}
+            del x, out
+        except Exception as e:   # reported, so that the headline line still prints
+            res[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
     import chunkwise_gated_delta_gdr_gb300 as gdr
@@ -553,6 +634,8 @@ def run_ours(args, rank, local_rank, world):
         "warm_l2_ms": warm_ms,
     }
     line["cpu_baseline"] = cpu_baseline(w, x_cpu)
+    if world == 1 and w.name == gin.HEADLINE and not args.skip_other_workloads:
+        line["other_workloads"] = other_workloads(dev, stream, flush, hbm)
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
